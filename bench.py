@@ -1,0 +1,510 @@
+#!/usr/bin/env python
+"""Benchmark: the routed-MoE FFN decode step on a 43-layer Q8_0 stack (GB300).
+
+Workload (``decode_stack43``): 43 resident decode MoE layers, each H=2048,
+I=1024, 64 routed experts (top-6) + 1 shared expert, Q8_0 weights (18.7 GB
+in HBM), 1 token per step, router logits skewed by a Zipf(1.1) per-expert
+offset; the step ends with the greedy argmax over 129,280 vocabulary logits.
+One step = one token through all 43 layers (route, quantize, group, gate/up
+pair + SwiGLU, down + combine per layer) + the argmax: every kernel of the
+path.  Inputs are pre-drawn for 64 steps (x and logits per layer) and cycle.
+
+Prints one JSON line.  ``--impl reference`` times the CPU oracle instead, on
+a bounded sample (one layer of one token per step), on the host cores.
+
+Timing: W warm-up steps, then K steps bracketed by a barrier and a device
+synchronize, timed with CUDA events on the launch stream; max over ranks.
+L2: every step reads ~2.0 GB of distinct expert weights (> 129 MB L2).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from quantized_moe_decode_luce_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MoE-FFN layer µs, tokens/s and expert-weight HBM GB/s vs GB300 peak"
+UNIT = "tokens/s"
+VOCAB = 129280
+SPEC_HBM_GBS = 8000.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying CUDA graphs")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--layers", type=int, default=None, help="(debug) fewer layers; invalid as a bench number")
+    return p.parse_args()
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def config_dict(wl, layers, graph):
+    return {"workload": "decode_stack43", "tokens_per_step": wl.T, "layers": layers, "hidden": wl.H,
+            "expert_intermediate": wl.I, "routed_experts": wl.E, "top_k": wl.k, "shared_experts": 1,
+            "weights": "Q8_0 (34 B / 32 values)", "activations": "q8_1", "argmax_vocab": VOCAB,
+            "input_steps": wl.steps, "graph": graph,
+            "l2": "inputs larger than L2: each step reads ~2.0 GB of distinct expert weights (18.7 GB resident)"}
+
+
+# ----------------------------------------------------------------------------- inputs
+def draw_inputs(wl, layers, rank):
+    """Per layer bias, per (step, layer) x and logits, per step vocab logits."""
+    seed = wl.seed * 1000 + rank
+    xs = np.empty((wl.steps, layers, wl.T, wl.H), np.float32)
+    lg = np.empty((wl.steps, layers, wl.T, wl.E), np.float32)
+    biases = []
+    for l in range(layers):
+        g = W.rng(seed, 10_000 + l)
+        wl_l = W.Workload(**{**wl.__dict__})
+        # one Zipf ranking and bias per layer; fresh N(0, 1) draws per step
+        logits_all, bias = W.router_logits(g, wl_l, T=wl.T * wl.steps)
+        biases.append(bias)
+        lg[:, l] = logits_all.reshape(wl.steps, wl.T, wl.E)
+        xs[:, l] = W.activations(W.rng(seed, 20_000 + l), wl.T * wl.steps, wl.H).reshape(wl.steps, wl.T, wl.H)
+    vocab = W.vocab_logits(W.rng(seed, 30_000), wl.steps, VOCAB).reshape(wl.steps, 1, VOCAB)
+    return xs, lg, np.stack(biases), vocab
+
+
+def layer_bytes(wl, n_active):
+    """Algorithmic bytes of one layer: touched expert weights + activations."""
+    wts = W.touched_weight_bytes(wl, n_active)
+    rows = wl.T * wl.k + wl.T
+    act = (wl.T * wl.H * 4 + wl.T * wl.E * 4 + wl.T * wl.H // 32 * 36 * 2 + rows * wl.I * 4 * 2
+           + rows * wl.I // 32 * 36 * 2 + wl.T * wl.H * 4)
+    return wts + act
+
+
+def glu_bytes(wl, n_active):
+    """Algorithmic bytes of one gate/up launch: gate+up rows of the touched
+    experts, the q8_1 input, h and hq written."""
+    n = n_active + 1
+    rows = wl.T * wl.k + wl.T
+    return (n * 2 * wl.I * wl.H // 32 * 34 + wl.T * wl.H // 32 * 36 + rows * wl.I * 4
+            + rows * wl.I // 32 * 36)
+
+
+def down_bytes(wl, n_active):
+    n = n_active + 1
+    rows = wl.T * wl.k + wl.T
+    return n * wl.H * wl.I // 32 * 34 + rows * wl.I // 32 * 36 + wl.T * wl.H * 4 + wl.T * wl.k * 8
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            p = [s.strip() for s in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) timing
+def oracle_layer_times(wl, n_layers, budget_s, host_layer_fn):
+    """Time the CPU oracle on up to n_layers decode layers (one token each),
+    stopping after budget_s seconds of oracle work."""
+    import oracle
+    times = []
+    spent = 0.0
+    for l in range(n_layers):
+        args = host_layer_fn(l)
+        t = time.perf_counter()
+        oracle.moe_layer(*args)
+        dt = time.perf_counter() - t
+        times.append(dt)
+        spent += dt
+        if spent >= budget_s:
+            break
+    return times
+
+
+def host_layer_sampler(wl, layers, seed):
+    """Host-drawn layer inputs for the oracle: only the experts the router
+    selects are drawn (the oracle never reads the others)."""
+    xs, lg, biases, _ = draw_inputs(wl, layers, 0)
+
+    def make(l):
+        import oracle
+        ids, _ = oracle.route_topk(lg[0, l], biases[l], wl.k)
+        used = sorted(set(ids.reshape(-1).tolist()))
+        g = W.rng(seed, 40_000 + l)
+        E = wl.E
+        nb_h, nb_i = wl.H // 32, wl.I // 32
+        wg = np.zeros((E, wl.I, nb_h, 34), np.uint8)
+        wu = np.zeros_like(wg)
+        wd = np.zeros((E, wl.H, nb_i, 34), np.uint8)
+        for e in used:
+            wg[e] = W.q8_0_blocks(g, wl.I, wl.H)
+            wu[e] = W.q8_0_blocks(g, wl.I, wl.H)
+            wd[e] = W.q8_0_blocks(g, wl.H, wl.I)
+        wsg, wsu, wsd = W.q8_0_blocks(g, wl.I, wl.H), W.q8_0_blocks(g, wl.I, wl.H), W.q8_0_blocks(g, wl.H, wl.I)
+        return (wg, wu, wd, wsg, wsu, wsd, xs[0, l], lg[0, l], biases[l], wl.k, wl.clamp)
+
+    return make
+
+
+def run_reference(args, wl, layers):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    make = host_layer_sampler(wl, layers, wl.seed)
+    steps = max(1, args.steps)
+    warm = max(0, args.warmup)
+    # each step: one decode layer of one token (a bounded sample of the token)
+    per = []
+    budget = 150.0
+    t_all = time.perf_counter()
+    prepared = {}
+    for i in range(warm + steps):
+        l = i % layers
+        if l not in prepared:
+            prepared[l] = make(l)
+        t = time.perf_counter()
+        oracle.moe_layer(*prepared[l])
+        dt = time.perf_counter() - t
+        if i >= warm:
+            per.append(dt)
+        if time.perf_counter() - t_all > budget and len(per) >= 1:
+            break
+    layer_s = float(np.mean(per))
+    value = 1.0 / (layer_s * layers)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": len(per), "warmup": warm, "ms_per_step": layer_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "i8 codes, f64 accumulation", "data": "synthetic",
+            "config": config_dict(wl, layers, False),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{len(per)} steps, each one decode layer of one token "
+                                       f"(x {layers} layers = 1 token); single-threaded C oracle"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "layer_us": layer_s * 1e6}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_files):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("source_hash") == source_hash(kernel_files):
+            return d.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def run_ours(args, wl, layers):
+    import torch
+    import torch.distributed as dist
+
+    from quantized_moe_decode_luce_gb300 import binding as Bd
+    from quantized_moe_decode_luce_gb300 import build as Bl
+    from quantized_moe_decode_luce_gb300.layer import Argmax, MoEStep
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    Bl.build()
+    Bd.lib()
+
+    # resident weights: 43 layers x (64 routed + 1 shared) experts
+    wls = W.Workload(**{**wl.__dict__, "layers": 1})
+    t_gen = time.time()
+    dls = [W.device_layer(wls, wl.seed * 1000 + l, dev) for l in range(layers)]
+    torch.cuda.synchronize()
+    t_gen = time.time() - t_gen
+    xs, lg, biases, vocab = draw_inputs(wl, layers, rank)
+    # active experts per (step, layer): the router's selection (T=1: always k)
+    n_active = wl.k
+    xs_d = torch.from_numpy(xs).to(dev)
+    lg_d = torch.from_numpy(lg).to(dev)
+    b_d = torch.from_numpy(biases).to(dev)
+    vocab_d = torch.from_numpy(vocab).to(dev)
+    outs = torch.empty((layers, wl.T, wl.H), dtype=torch.float32, device=dev)
+    step_bufs = MoEStep(wl.T, wl.H, wl.I, wl.E, wl.k, wl.shared, wl.clamp, device=dev)
+    am = Argmax(1, VOCAB, device=dev)
+    graph = not args.no_graph
+
+    # per-kernel timing events (recorded inside the graphs as external events)
+    ev_kind = {"glu": [], "down": []}
+
+    def make_events():
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            return torch.cuda.Event(enable_timing=True)
+
+    def run_step(s, x_src, lg_src, v_src, out_dst, record):
+        for l in range(layers):
+            bufs = step_bufs
+            lay = dls[l]
+            B = Bd
+            B.luce_route_topk(lg_src[s, l], b_d[l], wl.k, bufs.ids, bufs.weights)
+            B.luce_quantize_q8_1(x_src[s, l], bufs.xq)
+            B.luce_moe_group(bufs.ids, wl.E, bufs.counts, bufs.offsets, bufs.routes)
+            if record is not None:
+                e0, e1, e2 = record[l]
+                e0.record()
+            B.luce_moe_glu_pair(lay.wg, lay.wu, lay.wsg, lay.wsu, bufs.xq, bufs.offsets, bufs.routes, wl.T,
+                                wl.k, wl.E, wl.H, wl.I, wl.clamp, bufs.h, bufs.hq)
+            if record is not None:
+                e1.record()
+            B.luce_moe_down_combine(lay.wd, lay.wsd, bufs.hq, bufs.ids, bufs.weights, bufs.offsets,
+                                    bufs.routes, wl.T, wl.k, wl.E, wl.H, wl.I, out_dst[l])
+            if record is not None:
+                e2.record()
+        am.run(v_src[s])
+
+    launches_per_step = layers * 5 + 1
+    S = wl.steps
+    stream = torch.cuda.Stream(device=dev)
+    records = [[(make_events(), make_events(), make_events()) for _ in range(layers)] for _ in range(S)]
+    graphs = []
+    with torch.cuda.stream(stream):
+        for s in range(S):  # eager once: sets kernel attributes, checks every call
+            run_step(s, xs_d, lg_d, vocab_d, outs, None)
+        torch.cuda.synchronize()
+        if graph:
+            for s in range(S):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    run_step(s, xs_d, lg_d, vocab_d, outs, records[s])
+                graphs.append(g)
+        torch.cuda.synchronize()
+
+    def step(i):
+        if graph:
+            graphs[i % S].replay()
+        else:
+            run_step(i % S, xs_d, lg_d, vocab_d, outs, records[i % S])
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+        barrier()
+        clocks = ClockSampler(dev.index)
+        time.sleep(0.3)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        barrier()
+        start.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i)
+        end.record(stream)
+        barrier()
+        clk = clocks.stop()
+    ms = start.elapsed_time(end)
+    # per-kernel durations: the last execution of every recorded pair
+    glu_ms, down_ms = [], []
+    for s in range(S):
+        for (e0, e1, e2) in records[s]:
+            try:
+                glu_ms.append(e0.elapsed_time(e1))
+                down_ms.append(e1.elapsed_time(e2))
+            except Exception:
+                pass
+    tmax = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+    ms = float(tmax.item())
+    ms_per_step = ms / args.steps
+    tokens = args.steps * wl.T * world
+    value = tokens / (ms / 1e3)
+    lb = layer_bytes(wl, n_active)
+    step_bytes = layers * lb + VOCAB * 4
+    peak, peak_kind = measured_peaks()
+    glu_avg = float(np.mean(glu_ms)) if glu_ms else None
+    down_avg = float(np.mean(down_ms)) if down_ms else None
+    gb = glu_bytes(wl, n_active)
+    kernel_files = ["quantized_moe_decode_luce_gb300/csrc/glu_pair.cu", "quantized_moe_decode_luce_gb300/csrc/common.cuh"]
+    roofline = None
+    if glu_avg:
+        ach = gb / (glu_avg * 1e-3) / 1e9
+        roofline = {"kernel": "k_glu_pair", "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                    "frac": ach / peak, "peak_kind": f"{peak_kind} (STREAM-style copy)",
+                    "frac_of_8TBps_spec": ach / SPEC_HBM_GBS, "bytes_per_launch": gb,
+                    "avg_launch_us": glu_avg * 1e3, "traffic": profiled_traffic(kernel_files)}
+    kernels = {}
+    if down_avg:
+        db = down_bytes(wl, n_active)
+        kernels["k_down_combine"] = {"avg_launch_us": down_avg * 1e3, "bytes_per_launch": db,
+                                     "GBps": db / (down_avg * 1e-3) / 1e9}
+
+    # e2e: host inputs -> device, the same step, result back to the host
+    e2e = None
+    if rank == 0 or world > 1:
+        pin_x = torch.from_numpy(xs).pin_memory()
+        pin_l = torch.from_numpy(lg).pin_memory()
+        pin_v = torch.from_numpy(vocab).pin_memory()
+        host_out = torch.empty((layers, wl.T, wl.H), dtype=torch.float32).pin_memory()
+        host_idx = torch.empty(1, dtype=torch.int32).pin_memory()
+        stage_x = torch.empty_like(xs_d[0:1])
+        stage_l = torch.empty_like(lg_d[0:1])
+        stage_v = torch.empty_like(vocab_d[0:1])
+        e2e_graphs = []
+        with torch.cuda.stream(stream):
+            run_step(0, stage_x, stage_l, stage_v, outs, None)
+            torch.cuda.synchronize()
+            if graph:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    run_step(0, stage_x, stage_l, stage_v, outs, None)
+                e2e_graphs.append(g)
+            K2 = max(10, min(args.steps, 500))
+            h2d = (xs[0].nbytes + lg[0].nbytes + vocab[0].nbytes)
+            d2h = host_out.numel() * 4 + 4
+
+            def e2e_step(i):
+                s = i % S
+                stage_x.copy_(pin_x[s:s + 1], non_blocking=True)
+                stage_l.copy_(pin_l[s:s + 1], non_blocking=True)
+                stage_v.copy_(pin_v[s:s + 1], non_blocking=True)
+                if graph:
+                    e2e_graphs[0].replay()
+                else:
+                    run_step(0, stage_x, stage_l, stage_v, outs, None)
+                host_out.copy_(outs, non_blocking=True)
+                host_idx.copy_(am.idx, non_blocking=True)
+
+            for i in range(3):
+                e2e_step(i)
+            barrier()
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            for i in range(K2):
+                e2e_step(i)
+            s1.record(stream)
+            barrier()
+        e_ms = s0.elapsed_time(s1)
+        et = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(et, op=dist.ReduceOp.MAX)
+        e2e = {"value": K2 * wl.T * world / (float(et.item()) / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": K2,
+               "path": "pinned host x/logits/vocab -> device copies -> C-ABI step -> outputs + token to pinned host"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        try:
+            make = host_layer_sampler(wl, layers, wl.seed)
+            times = oracle_layer_times(wl, layers, 12.0, make)
+            layer_s = float(np.mean(times))
+            cpu = {"value": 1.0 / (layer_s * layers), "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "sample": f"{len(times)} decode layers of one token (T=1, H=2048, I=1024, E=64, top-6 + shared); "
+                             f"tokens/s = 1 / (mean layer time x {layers})",
+                   "layer_us": layer_s * 1e6}
+        except Exception as exc:  # the baseline is a report, never a reason to fail the bench
+            cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {exc}"}
+
+    fault = Bd.luce_get_fault()
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "i8 codes (dp4a int32 block sums), f32 scales/accumulation",
+                "data": "synthetic (seeded Q8_0 weights, N(0,1) activations, Zipf-skewed router logits)",
+                "config": config_dict(wl, layers, graph),
+                "layer_us": ms_per_step * 1e3 / layers,
+                "stack_weight_GBps": step_bytes / (ms_per_step * 1e-3) / 1e9,
+                "stack_frac_of_measured_hbm": step_bytes / (ms_per_step * 1e-3) / 1e9 / peak,
+                "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches_per_step * args.steps, "clocks": clk,
+                "device_faults": fault, "weights_gen_s": round(t_gen, 2)}
+        if layers != 43:
+            line["invalid"] = f"debug run with {layers} layers"
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    wl = W.WORKLOADS["decode_stack43"]
+    layers = args.layers or wl.layers
+    if args.impl == "reference":
+        run_reference(args, wl, layers)
+    else:
+        run_ours(args, wl, layers)
+
+
+if __name__ == "__main__":
+    main()

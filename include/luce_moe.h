@@ -1,0 +1,231 @@
+/*
+ * luce_moe.h -- C ABI of the GB300 (sm_103a) routed-MoE FFN decode library.
+ *
+ * The library computes the routed mixture-of-experts FFN step of an LLM
+ * decode or speculative-verify pass on Q8_0-quantized experts, plus the
+ * exact greedy argmax over a vocabulary of logits.  It is a from-scratch
+ * design of the operations described on the page Lucebox PR #826
+ * "feat(ds41): two-box expert-parallel serving" (cited below as [PR826],
+ * with the section of the page: a commit subject, a code review, or a part
+ * of the PR description).
+ *
+ * Conventions shared by every entry point:
+ *   - All array pointers are DEVICE pointers, owned by the caller.  The
+ *     library never allocates, frees or retains memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Calls are asynchronous on that stream: LUCE_OK means the
+ *     work was validated and enqueued, nothing more.  Outputs are ready when
+ *     the stream reaches that point.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     bad argument returns LUCE_ERR_INVALID_ARG (or LUCE_ERR_UNSUPPORTED for
+ *     a valid shape this build has no kernel for) with nothing enqueued.
+ *     A launch failure returns LUCE_ERR_CUDA.  No C++ exception crosses the
+ *     ABI.  T == 0 (or R == 0) is a valid empty call that enqueues nothing.
+ *   - Route ids < 0 are masked routes ([PR826], review "moe_combine_masked_
+ *     kernel indexes valid with an unchecked (possibly -1) route id"): they
+ *     are skipped by grouping, products and combine.  Ids >= E are invalid
+ *     data; kernels skip them and raise LUCE_FAULT_BAD_ID (luce_get_fault).
+ *   - Outputs never alias inputs.
+ *
+ * Data layouts (row-major, little-endian):
+ *   luce_block_q8_0  32 int8 codes q and an fp16 scale d; value = d*q.
+ *                    34 bytes.  The ggml block_q8_0 layout the page names
+ *                    (review of the commit "whole-row-lane slice").
+ *   luce_block_q8_1  fp16 d, fp16 s = d*sum(q), 32 int8 codes; 36 bytes.
+ *                    The q8_1 activation rows of [PR826], commit "fused
+ *                    DS4.1 decode kernels" ("a q8_1 activation memo").
+ *   A Q8_0 matrix [rows][K] is rows*K/32 blocks, row after row.
+ *   Expert weights: w_gate, w_up [E][I][H/32] blocks; w_down [E][H][I/32].
+ *   The shared expert's weights have the same shapes without the E axis.
+ */
+#ifndef LUCE_MOE_H
+#define LUCE_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LUCE_API __attribute__((visibility("default")))
+#else
+#define LUCE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LUCE_OK = 0,
+    LUCE_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or shape     */
+    LUCE_ERR_UNSUPPORTED = 2, /* valid but not supported by this build     */
+    LUCE_ERR_CUDA = 3         /* a CUDA runtime call or launch failed      */
+} luce_status;
+
+typedef struct {
+    uint16_t d;    /* fp16 scale */
+    int8_t qs[32]; /* codes      */
+} luce_block_q8_0;
+
+typedef struct {
+    uint16_t d;    /* fp16 scale d = max|x| / 127 */
+    uint16_t s;    /* fp16 d * sum(qs)            */
+    int8_t qs[32]; /* codes round(x / d)          */
+} luce_block_q8_1;
+
+/* Device fault bits (luce_get_fault). */
+#define LUCE_FAULT_BAD_ID 0x1u  /* a route id >= E was seen and skipped          */
+#define LUCE_FAULT_TIMEOUT 0x2u /* a bounded device wait gave up (never expected) */
+
+/* ------------------------------------------------------------------------
+ * luce_route_topk -- router select + weights in one launch.
+ * [PR826], commit "fused DS4.1 decode kernels": "one launch ... for the
+ * router's select and weights over the same logits".
+ *
+ * Per token t: score_e = logits[t][e] + bias[e] (fp32 add).  The k largest
+ * scores are selected, best first; equal scores go to the lower index.
+ * weights[t][j] = softmax over the k selected UNBIASED logits (max-
+ * subtracted, fp32 expf).  The bias only steers selection.
+ *
+ *   logits  [T][E] fp32          bias [E] fp32, or NULL for none
+ *   ids     [T][k] int32 out     weights [T][k] fp32 out
+ * Requires 1 <= E <= 1024, 1 <= k <= min(E, 64), T >= 0, 4-byte alignment.
+ */
+LUCE_API luce_status luce_route_topk(const float *logits, const float *bias, int T, int E, int k, int32_t *ids,
+                            float *weights, void *stream);
+
+/* ------------------------------------------------------------------------
+ * luce_quantize_q8_1 -- quantize fp32 rows to q8_1 blocks, once per layer.
+ * [PR826], commit "fused DS4.1 decode kernels" ("a q8_1 activation memo
+ * shared across reshapes") and commit "fused routed combine and q8_1 inputs
+ * for the hybrid owners" (the FFN input "as the q8_1 rows its MMVQ reads,
+ * quantized once").
+ *
+ * Per 32-value block: amax = max|x|, d = amax / 127 (fp32 IEEE division),
+ * q = roundf(x / d) (half away from zero; 0 when amax == 0), stored
+ * d16 = fp16(d) and s16 = fp16(d * sum(q)), fp16 round to nearest even.
+ *
+ *   x   [T][K] fp32 (4-byte aligned)      xq [T][K/32] luce_block_q8_1 out
+ * Requires K % 32 == 0, K > 0, xq 4-byte aligned.
+ */
+LUCE_API luce_status luce_quantize_q8_1(const float *x, int T, int K, luce_block_q8_1 *xq, void *stream);
+
+/* ------------------------------------------------------------------------
+ * luce_moe_group -- group the T*k routes by expert (one counting sort per
+ * layer, shared by gate, up and down).  [PR826], commit "fused DS4.1 decode
+ * kernels": "one expert grouping per MoE layer for gate, up and down".
+ *
+ * Route r = t*k + j has expert ids[r].  Outputs:
+ *   counts  [E]    number of routes of expert e (masked routes excluded)
+ *   offsets [E+1]  offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e]
+ *   routes  [T*k]  routes[offsets[e] .. offsets[e+1]) = the route indices
+ *                  r of expert e in increasing r; the tail after
+ *                  offsets[E] is filled with -1.
+ * One CTA, no atomics on the order: the result is unique and deterministic.
+ * Requires 1 <= E <= 1024, 1 <= k <= 64, T*k <= 2^20, 4-byte alignment.
+ */
+LUCE_API luce_status luce_moe_group(const int32_t *ids, int T, int k, int E, int32_t *counts, int32_t *offsets,
+                           int32_t *routes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * luce_moe_glu_pair -- the Q8_0 gate/up products of every routed token and
+ * of the shared expert, fused with the (clamped) SwiGLU and the q8_1
+ * quantization of its result.  [PR826], commit "RDNA4 Q8_0 gate/up pair"
+ * (both matrices read with one load of each activation fragment, the GLU
+ * written in the epilogue) and commit "fused routed combine ..." (the
+ * clamped routed SwiGLU).
+ *
+ * For each expert e with routes (from luce_moe_group), for each of its
+ * routes r = t*k + j and each row i < I:
+ *   g = W_gate[e][i] . xq[t],  u = W_up[e][i] . xq[t]
+ *   h[r][i] = silu(g) * u                                  (clamp <= 0)
+ *   h[r][i] = silu(min(g, clamp)) * min(max(u, -clamp), clamp)   (clamp > 0)
+ * where a row dot is sum_b d_w[b] * d_x[b] * isum[b] with exact int32 block
+ * sums isum[b] (dp4a) accumulated in fp32.  If ws_gate/ws_up are given, the
+ * shared expert is computed for every token t into row T*k + t.
+ * hq[r] = q8_1(h[r]) with the rule of luce_quantize_q8_1, from exactly the
+ * fp32 h values stored.  Rows of masked routes are not written.
+ *
+ *   w_gate, w_up   [E][I][H/32] Q8_0        ws_gate, ws_up [I][H/32] or NULL
+ *   xq             [T][H/32] q8_1           offsets [E+1], routes [T*k]
+ *   h              [T*k + T][I] fp32 out    hq [T*k + T][I/32] q8_1 out
+ *   variant        0 = automatic (only one kernel exists in this build)
+ * Requires H % 256 == 0, I % 256 == 0, H/32 <= 1024; w_*, xq, hq 16-byte
+ * aligned; ws_gate and ws_up both given or both NULL.
+ */
+LUCE_API luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const luce_block_q8_0 *w_up,
+                              const luce_block_q8_0 *ws_gate, const luce_block_q8_0 *ws_up,
+                              const luce_block_q8_1 *xq, const int32_t *offsets, const int32_t *routes, int T, int k,
+                              int E, int H, int I, float clamp, float *h, luce_block_q8_1 *hq, int variant,
+                              void *stream);
+
+/* ------------------------------------------------------------------------
+ * luce_moe_down_combine -- the Q8_0 down product of every route and of the
+ * shared expert, fused with the masked, route-weighted combine.  [PR826],
+ * commit "fused routed combine and q8_1 inputs for the hybrid owners": "the
+ * owner route mask, the route weighting and the route sum run in one
+ * launch; the masked combine rounds its products and its sums separately".
+ *
+ *   y[r][n]  = W_down[ids[r]][n] . hq[r]        (fp32, as in luce_moe_glu_pair)
+ *   yS[t][n] = Ws_down[n] . hq[T*k + t]         (if ws_down is given)
+ *   out[t][n] = 0; for j = 0..k-1 with ids[t*k+j] >= 0:
+ *                    out = out + w[t][j] * y[t*k+j][n]   (product rounded,
+ *                                                         then sum rounded)
+ *               then out = out + yS[t][n]
+ * No floating-point atomics: each out element is summed by one thread in
+ * slot order, so the result is deterministic.
+ *
+ *   w_down [E][H][I/32] Q8_0    ws_down [H][I/32] or NULL
+ *   hq [T*k + T][I/32] q8_1     ids, weights [T][k]   offsets, routes as above
+ *   out [T][H] fp32 out         variant 0 = automatic
+ * Requires H % 256 == 0 (H >= 256), I % 256 == 0, I/32 <= 1024; w_*, hq
+ * 16-byte aligned.
+ */
+LUCE_API luce_status luce_moe_down_combine(const luce_block_q8_0 *w_down, const luce_block_q8_0 *ws_down,
+                                  const luce_block_q8_1 *hq, const int32_t *ids, const float *weights,
+                                  const int32_t *offsets, const int32_t *routes, int T, int k, int E, int H, int I,
+                                  float *out, int variant, void *stream);
+
+/* ------------------------------------------------------------------------
+ * luce_argmax -- exact greedy argmax per row, as a "pair/pick": each CTA
+ * reduces a chunk of a row to a (value, index) pair; the last CTA of the
+ * row picks among the pairs.  [PR826], commit "fused DS4.1 decode kernels":
+ * "an argmax pair/pick that finds the greedy token of a vocabulary ...
+ * exactly".
+ *
+ * idx[r] = the lowest index of the maximum of logits[r][0..V) (float
+ * comparison: -0 == +0 is a tie; inputs must hold no NaN); val[r] = that
+ * maximum (val may be NULL).
+ *
+ *   logits [R][V] fp32          idx [R] int32 out      val [R] fp32 out or NULL
+ *   workspace, workspace_bytes  device scratch of at least
+ *                               luce_argmax_workspace_bytes(R, V) bytes,
+ *                               8-byte aligned, ZERO-FILLED before its first
+ *                               use.  Each call leaves it zero-filled again,
+ *                               so one buffer serves any number of calls on
+ *                               one stream; calls that overlap on the GPU
+ *                               must not share it.
+ * Requires 1 <= V < 2^31, R >= 0, logits 4-byte aligned.
+ */
+LUCE_API luce_status luce_argmax(const float *logits, int R, int64_t V, int32_t *idx, float *val, void *workspace,
+                        size_t workspace_bytes, void *stream);
+LUCE_API size_t luce_argmax_workspace_bytes(int R, int64_t V);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics. */
+
+/* Short English name of a status code (static storage). */
+LUCE_API const char *luce_status_string(luce_status s);
+
+/* Read and clear the device fault bits (LUCE_FAULT_*) raised by kernels on
+ * the current device.  Synchronizes the device.  Returns LUCE_OK or
+ * LUCE_ERR_CUDA; *bits receives the OR of all faults since the last call. */
+LUCE_API luce_status luce_get_fault(unsigned int *bits);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+LUCE_API int luce_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LUCE_MOE_H */

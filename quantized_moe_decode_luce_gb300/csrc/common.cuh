@@ -1,0 +1,266 @@
+// common.cuh -- device helpers shared by the kernels of libluce_moe.
+//
+// Q8_0 / q8_1 block access, the q8_1 quantization rule, the warp reductions,
+// and the Blackwell asynchronous-copy machinery (mbarrier + cp.async.bulk)
+// used to stream expert weights into shared memory.  Host-side argument
+// checks live here too.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/luce_moe.h"
+
+namespace luce {
+
+constexpr int QK = 32;
+constexpr int Q8_0_BYTES = 34;
+constexpr int Q8_1_BYTES = 36;
+constexpr int Q8_1_WORDS = 9;
+// A bounded device wait gives up after this many nanoseconds and raises
+// LUCE_FAULT_TIMEOUT.  Nothing in a correct run waits longer than a few
+// microseconds; the bound only keeps a defect from hanging the GPU.
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+
+// ---------------------------------------------------------------------------
+// Fault word: one per translation unit (no relocatable device code).  Each
+// .cu file defines it through LUCE_DEFINE_FAULT_WORD and exposes a host
+// reader; luce_get_fault ORs them.
+#define LUCE_DEFINE_FAULT_WORD(name)                                                    \
+    static __device__ unsigned int g_fault_word;                                        \
+    extern "C" __attribute__((visibility("hidden"))) cudaError_t name(unsigned int *bits) \
+    {                                                                                   \
+        unsigned int v = 0, zero = 0;                                                   \
+        cudaError_t e = cudaMemcpyFromSymbol(&v, g_fault_word, sizeof(v));              \
+        if (e == cudaSuccess)                                                           \
+            e = cudaMemcpyToSymbol(g_fault_word, &zero, sizeof(zero));                  \
+        *bits |= v;                                                                     \
+        return e;                                                                       \
+    }
+
+// ---------------------------------------------------------------------------
+// Small device helpers.
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ int warp_sum_i(int v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t bits16)
+{
+    return __half2float(__ushort_as_half((unsigned short)(bits16 & 0xffffu)));
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------------------
+// q8_1 rule for one block held by a warp (lane i holds x[i]):
+// amax = max|x|, d = amax / 127 (IEEE), q = roundf(x / d) (0 if amax == 0),
+// d16 = fp16(d), s16 = fp16(d * sum(q)) (round to nearest even).  The block
+// is written as 9 little-endian 32-bit words: d16 | s16 << 16, then the
+// codes four to a word.
+__device__ __forceinline__ void quantize_q8_1_warp(float x, uint32_t *__restrict__ out_words, int lane)
+{
+    const float amax = warp_max(fabsf(x));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const int q = (amax == 0.0f) ? 0 : (int)roundf(__fdiv_rn(x, d));
+    const int sum = warp_sum_i(q);
+    uint32_t byte = (uint32_t)(q & 0xff);
+    uint32_t w = byte;
+    w |= __shfl_down_sync(0xffffffffu, byte, 1) << 8;
+    w |= __shfl_down_sync(0xffffffffu, byte, 2) << 16;
+    w |= __shfl_down_sync(0xffffffffu, byte, 3) << 24;
+    if (lane == 0) {
+        const uint32_t d16 = __half_as_ushort(__float2half_rn(d));
+        const uint32_t s16 = __half_as_ushort(__float2half_rn(__fmul_rn(d, (float)sum)));
+        out_words[0] = d16 | (s16 << 16);
+    }
+    if ((lane & 3) == 0)
+        out_words[1 + (lane >> 2)] = w;
+}
+
+// ---------------------------------------------------------------------------
+// A Q8_0 block b of a row that starts 16-byte aligned sits at byte 34*b:
+// 4-byte aligned for even b, 2 bytes off for odd b.  Nine aligned words
+// starting at (34*b) & ~3 hold the whole block either way; a funnel shift
+// by 16 (even b) or 32 (odd b) extracts the scale and the eight code words.
+struct Q80Block {
+    float d;
+    uint32_t q[8];
+};
+
+__device__ __forceinline__ void load_q8_0_smem(const uint8_t *row, int b, Q80Block &blk)
+{
+    const uint32_t *p = reinterpret_cast<const uint32_t *>(row + ((34 * b) & ~3));
+    uint32_t w[9];
+#pragma unroll
+    for (int i = 0; i < 9; i++)
+        w[i] = p[i];
+    const uint32_t sh = (b & 1) ? 32u : 16u;
+    blk.d = half_bits_to_float(__funnelshift_rc(w[0], w[1], sh - 16u));
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        blk.q[i] = __funnelshift_rc(w[i], w[i + 1], sh);
+}
+
+// q8_1 block from global memory (read-only path, L1-cached): scale + codes.
+struct Q81Block {
+    float d;
+    int q[8];
+};
+
+__device__ __forceinline__ void load_q8_1_global(const uint32_t *__restrict__ words, Q81Block &blk)
+{
+    blk.d = half_bits_to_float(__ldg(words));
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        blk.q[i] = (int)__ldg(words + 1 + i);
+}
+
+__device__ __forceinline__ int dot_q8_block(const uint32_t (&w)[8], const int (&x)[8])
+{
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        s = __dp4a((int)w[i], x[i], s);
+    return s;
+}
+
+// SwiGLU of the pages: silu(g) * u, optionally silu(min(g, L)) * clamp(u, -L, L).
+__device__ __forceinline__ float swiglu(float g, float u, float clamp)
+{
+    if (clamp > 0.0f) {
+        g = fminf(g, clamp);
+        u = fminf(fmaxf(u, -clamp), clamp);
+    }
+    const float s = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
+    return __fmul_rn(s, u);
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier + bulk asynchronous copy (global -> shared), sm_90+ PTX.
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete, for at most WAIT_LIMIT_NS.
+// Returns false (and the caller raises LUCE_FAULT_TIMEOUT) if it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const unsigned long long t0 = global_timer_ns();
+    for (uint32_t i = 1;; i++) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((i & 31u) == 0u && global_timer_ns() - t0 > WAIT_LIMIT_NS)
+            return false;
+    }
+}
+
+// L2 policy for weights that are streamed once per step.
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global to shared memory, completing `bytes` of transaction on `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                              uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// Named barrier among `nthreads` threads (id 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+} // namespace luce
+
+// ---------------------------------------------------------------------------
+// Host-side helpers.
+namespace luce_host {
+
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Maps the last launch error to a status (and clears it).
+inline luce_status launch_status()
+{
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? LUCE_OK : LUCE_ERR_CUDA;
+}
+
+} // namespace luce_host

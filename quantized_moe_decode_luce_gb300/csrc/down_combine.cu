@@ -1,0 +1,358 @@
+// down_combine.cu -- the Q8_0 x q8_1 down product of every route and of the
+// shared expert, fused with the masked route-weighted combine, and its C-ABI
+// entry point.
+//
+// Pages cited by title: [PR826] = Lucebox PR #826 "feat(ds41): two-box
+// expert-parallel serving", commit "fused routed combine and q8_1 inputs for
+// the hybrid owners": the route mask, the route weighting and the route sum
+// in one launch, "the masked combine rounds its products and its sums
+// separately, as the unfused ops do".
+//
+// GB300 shape (our own): a CTA owns a slab of RN output rows n for a tile of
+// tokens, and streams those RN rows of EVERY active expert (one bulk copy
+// per expert and column chunk) through a shared-memory ring; each weight row
+// still crosses HBM once per token tile (once per step for decode and verify,
+// where one tile holds every token).  Each route's product y is kept in
+// shared memory, so the combine of a token needs no second pass and no
+// atomics: one thread sums out[t][n] over the k slots in slot order with
+// separately rounded products and sums (__fmul_rn / __fadd_rn), then adds
+// the shared expert.  Deterministic; no global scratch.
+#include <algorithm>
+#include <climits>
+
+#include "common.cuh"
+
+LUCE_DEFINE_FAULT_WORD(luce_internal_fault_down)
+
+namespace {
+
+using namespace luce;
+
+constexpr int NCU_MAX = 32; // columns per virtual expert
+constexpr int CW = 4;       // consumer warps
+constexpr int RN = 8;       // output rows per CTA
+constexpr int RPW = RN / CW;
+
+struct DownArgs {
+    const uint8_t *wd;     // [E][H][rowbytes]
+    const uint8_t *wsd;    // [H][rowbytes] or null
+    const uint32_t *hq;    // [T*k+T][nbI] q8_1 blocks (9 words)
+    const int32_t *ids;    // [T][k]
+    const float *weights;  // [T][k]
+    const int32_t *offsets, *routes;
+    float *out;            // [T][H]
+    int T, k, E, H, I;
+    int nbI, rowbytes;
+    int TT;                // tokens per tile
+    int NS;                // ring stages
+    int ncu;
+};
+
+struct VUnit {
+    const uint8_t *w; // RN rows of this expert
+    int e;            // expert (E = shared)
+    int first;        // index into routes[] of the first column (routed)
+    int col0, ncols;
+};
+
+template <int NC>
+__global__ void __launch_bounds__((CW + 1) * 32)
+    k_down_combine(const DownArgs a)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int stage_bytes = RN * a.rowbytes;
+    uint8_t *ring = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.NS * stage_bytes);
+    uint64_t *empty = full + a.NS;
+    int *vpre = reinterpret_cast<int *>(empty + a.NS); // [E + 1]
+    int *vlo = vpre + a.E + 1;                        // [E]: first route of the tile
+    int *vcnt = vlo + a.E;                            // [E]: routes of the tile
+    float *ybuf = reinterpret_cast<float *>(vcnt + a.E);
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = blockIdx.x * a.TT, t1 = min(a.T, t0 + a.TT);
+    const int n0 = blockIdx.y * RN;
+    const int ntok = t1 - t0;
+    if (tid == 0) {
+        for (int s = 0; s < a.NS; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], CW);
+        }
+        fence_mbar_init();
+        s_abort = 0;
+    }
+    // routes of expert e that belong to tokens [t0, t1): a sub-range, since
+    // an expert's routes are sorted by r = t*k + j
+    for (int e = tid; e < a.E; e += blockDim.x) {
+        int lo = a.offsets[e], hi = a.offsets[e + 1];
+        const int rlo = t0 * a.k, rhi = t1 * a.k;
+        int b = lo, c = hi;
+        while (b < c) { // first route >= rlo
+            const int m = (b + c) >> 1;
+            if (a.routes[m] < rlo)
+                b = m + 1;
+            else
+                c = m;
+        }
+        const int first = b;
+        c = hi;
+        while (b < c) { // first route >= rhi
+            const int m = (b + c) >> 1;
+            if (a.routes[m] < rhi)
+                b = m + 1;
+            else
+                c = m;
+        }
+        vlo[e] = first;
+        vcnt[e] = b - first;
+        vpre[e + 1] = (b - first + a.ncu - 1) / a.ncu;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base < a.E; base += 32) {
+            const int e = base + lane;
+            int inc = e < a.E ? vpre[e + 1] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o)
+                    inc += v;
+            }
+            if (e < a.E)
+                vpre[e + 1] = carry + inc;
+            carry += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0)
+            vpre[0] = 0;
+    }
+    __syncthreads();
+    const int NVr = vpre[a.E];
+    const int NV = NVr + (a.wsd ? (ntok + a.ncu - 1) / a.ncu : 0);
+
+    auto decode = [&](int v) {
+        VUnit r;
+        if (v < NVr) {
+            int lo = 0, hi = a.E - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (vpre[mid] <= v)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            r.e = lo;
+            r.first = vlo[lo];
+            r.col0 = (v - vpre[lo]) * a.ncu;
+            r.ncols = min(a.ncu, vcnt[lo] - r.col0);
+            r.w = a.wd + ((size_t)lo * a.H + n0) * a.rowbytes;
+        } else {
+            r.e = a.E;
+            r.first = 0;
+            r.col0 = (v - NVr) * a.ncu;
+            r.ncols = min(a.ncu, ntok - r.col0);
+            r.w = a.wsd + (size_t)n0 * a.rowbytes;
+        }
+        return r;
+    };
+
+    if (warp == CW) {
+        if (lane != 0)
+            return;
+        const uint64_t pol = l2_evict_first_policy();
+        uint32_t q = 0;
+        for (int v = 0; v < NV; v++, q++) {
+            const VUnit un = decode(v);
+            const uint32_t slot = q % a.NS, use = q / a.NS;
+            if (use > 0 && !mbar_wait_bounded(&empty[slot], (use - 1) & 1u)) {
+                atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
+                *(volatile int *)&s_abort = 1;
+                break;
+            }
+            if (*(volatile int *)&s_abort)
+                break;
+            mbar_arrive_expect_tx(&full[slot], (uint32_t)stage_bytes);
+            bulk_copy_g2s(ring + (size_t)slot * stage_bytes, un.w, (uint32_t)stage_bytes, &full[slot], pol);
+        }
+        const uint32_t n_slots = (q < (uint32_t)a.NS ? q : (uint32_t)a.NS);
+        for (uint32_t slot = 0; slot < n_slots; slot++) {
+            const uint32_t last_use = (q - 1 - slot) / a.NS;
+            if (!mbar_wait_bounded(&full[slot], last_use & 1u))
+                atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    bool dead = false;
+    for (int v = 0; v < NV; v++) {
+        const VUnit un = decode(v);
+        int my_r = 0, my_slot = 0; // column `lane`: its hq row and its y slot
+        if (lane < un.ncols) {
+            if (un.e < a.E) {
+                my_r = a.routes[un.first + un.col0 + lane];
+                my_slot = my_r - t0 * a.k;
+            } else {
+                const int t = t0 + un.col0 + lane;
+                my_r = a.T * a.k + t;
+                my_slot = ntok * a.k + (t - t0);
+            }
+        }
+        const uint32_t slot = (uint32_t)v % a.NS, use = (uint32_t)v / a.NS;
+        if (!dead && *(volatile int *)&s_abort)
+            dead = true;
+        if (!dead) {
+            const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], use & 1u));
+            if (!got) {
+                if (lane == 0) {
+                    atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
+                    *(volatile int *)&s_abort = 1;
+                }
+                dead = true;
+            }
+        }
+        if (!dead) {
+            const uint8_t *st = ring + (size_t)slot * stage_bytes;
+            for (int c0 = 0; c0 < un.ncols; c0 += NC) {
+                const int nc = min(NC, un.ncols - c0);
+                int rr[NC];
+#pragma unroll
+                for (int c = 0; c < NC; c++)
+                    rr[c] = __shfl_sync(0xffffffffu, my_r, c0 + (c < nc ? c : 0));
+                float acc[RPW][NC];
+#pragma unroll
+                for (int m = 0; m < RPW; m++)
+#pragma unroll
+                    for (int c = 0; c < NC; c++)
+                        acc[m][c] = 0.0f;
+                for (int b = lane; b < a.nbI; b += 32) {
+                    Q80Block wb[RPW];
+#pragma unroll
+                    for (int m = 0; m < RPW; m++)
+                        load_q8_0_smem(st + (size_t)(warp + CW * m) * a.rowbytes, b, wb[m]);
+#pragma unroll
+                    for (int c = 0; c < NC; c++) {
+                        if (c < nc) {
+                            Q81Block xb;
+                            load_q8_1_global(a.hq + ((size_t)rr[c] * a.nbI + b) * Q8_1_WORDS, xb);
+#pragma unroll
+                            for (int m = 0; m < RPW; m++)
+                                acc[m][c] = fmaf(wb[m].d * xb.d, (float)dot_q8_block(wb[m].q, xb.q), acc[m][c]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < NC; c++) {
+                    if (c < nc) {
+                        const int ys = __shfl_sync(0xffffffffu, my_slot, c0 + c);
+#pragma unroll
+                        for (int m = 0; m < RPW; m++) {
+                            const float y = warp_sum(acc[m][c]);
+                            if (lane == 0)
+                                ybuf[ys * RN + warp + CW * m] = y;
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && !dead)
+            mbar_arrive(&empty[slot]);
+    }
+    named_barrier(1, CW * 32);
+    if (dead || *(volatile int *)&s_abort)
+        return;
+    // combine: out[t][n] = sum_j fl(w * y) in slot order, then + shared
+    for (int idx = tid; idx < ntok * RN; idx += CW * 32) {
+        const int tl = idx / RN, i = idx % RN;
+        const int t = t0 + tl;
+        float acc = 0.0f;
+        for (int j = 0; j < a.k; j++) {
+            const int e = a.ids[(size_t)t * a.k + j];
+            if (e >= 0 && e < a.E)
+                acc = __fadd_rn(acc, __fmul_rn(a.weights[(size_t)t * a.k + j], ybuf[(tl * a.k + j) * RN + i]));
+        }
+        if (a.wsd)
+            acc = __fadd_rn(acc, ybuf[(ntok * a.k + tl) * RN + i]);
+        a.out[(size_t)t * a.H + n0 + i] = acc;
+    }
+}
+
+template <int NC>
+luce_status launch_down(const DownArgs &a, dim3 grid, size_t smem, cudaStream_t stream)
+{
+    static size_t smem_set[64] = {0}; // per device: the attribute value in force
+    auto kern = k_down_combine<NC>;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return LUCE_ERR_CUDA;
+    if (smem_set[dev] < smem) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return LUCE_ERR_CUDA;
+        smem_set[dev] = smem;
+    }
+    kern<<<grid, (CW + 1) * 32, smem, stream>>>(a);
+    return luce_host::launch_status();
+}
+
+} // namespace
+
+using namespace luce_host;
+
+extern "C" luce_status luce_moe_down_combine(const luce_block_q8_0 *w_down, const luce_block_q8_0 *ws_down,
+                                             const luce_block_q8_1 *hq, const int32_t *ids, const float *weights,
+                                             const int32_t *offsets, const int32_t *routes, int T, int k, int E,
+                                             int H, int I, float *out, int variant, void *stream)
+{
+    if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 64 || (int64_t)T * k > (1 << 20))
+        return LUCE_ERR_INVALID_ARG;
+    if (H <= 0 || I <= 0 || H % 256 != 0 || I % 256 != 0 || I / 32 > 1024 || H > (1 << 20))
+        return LUCE_ERR_INVALID_ARG;
+    if (variant != 0)
+        return LUCE_ERR_INVALID_ARG;
+    if (T == 0)
+        return LUCE_OK;
+    if (!w_down || !hq || !ids || !weights || !offsets || !routes || !out)
+        return LUCE_ERR_INVALID_ARG;
+    if (!aligned(w_down, 16) || (ws_down && !aligned(ws_down, 16)) || !aligned(hq, 16) || !aligned(ids, 4) ||
+        !aligned(weights, 4) || !aligned(offsets, 4) || !aligned(routes, 4) || !aligned(out, 4))
+        return LUCE_ERR_INVALID_ARG;
+    DownArgs a;
+    a.wd = reinterpret_cast<const uint8_t *>(w_down);
+    a.wsd = reinterpret_cast<const uint8_t *>(ws_down);
+    a.hq = reinterpret_cast<const uint32_t *>(hq);
+    a.ids = ids;
+    a.weights = weights;
+    a.offsets = offsets;
+    a.routes = routes;
+    a.out = out;
+    a.T = T;
+    a.k = k;
+    a.E = E;
+    a.H = H;
+    a.I = I;
+    a.nbI = I / 32;
+    a.rowbytes = a.nbI * Q8_0_BYTES;
+    a.ncu = NCU_MAX;
+    const int stage = RN * a.rowbytes;
+    a.NS = std::max(2, std::min(8, (64 * 1024) / stage));
+    // y buffer: (TT*k + TT) slots x RN floats, at most 32 KB
+    const int per_tok = (k + 1) * RN * (int)sizeof(float);
+    a.TT = std::max(1, std::min(T, (32 * 1024) / per_tok));
+    const size_t smem = (size_t)a.NS * stage + (size_t)2 * a.NS * sizeof(uint64_t) +
+                        (size_t)(3 * E + 1) * sizeof(int) + (size_t)(a.TT * k + a.TT) * RN * sizeof(float);
+    const int tiles = (T + a.TT - 1) / a.TT;
+    if (H / RN > 65535)
+        return LUCE_ERR_UNSUPPORTED;
+    dim3 grid((unsigned)tiles, (unsigned)(H / RN));
+    const int maxcols = std::min(std::min(T, a.TT), NCU_MAX);
+    cudaStream_t st = as_stream(stream);
+    if (maxcols <= 1)
+        return launch_down<1>(a, grid, smem, st);
+    if (maxcols <= 2)
+        return launch_down<2>(a, grid, smem, st);
+    if (maxcols <= 4)
+        return launch_down<4>(a, grid, smem, st);
+    return launch_down<8>(a, grid, smem, st);
+}

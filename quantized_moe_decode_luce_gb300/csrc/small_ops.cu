@@ -1,0 +1,455 @@
+// small_ops.cu -- router select + weights, q8_1 quantization, expert
+// grouping and the argmax pair/pick, with their C-ABI entry points.
+//
+// Pages cited by title: [PR826] = Lucebox PR #826 "feat(ds41): two-box
+// expert-parallel serving" (section named at each use).
+#include <algorithm>
+#include <climits>
+#include <cmath>
+
+#include "common.cuh"
+
+LUCE_DEFINE_FAULT_WORD(luce_internal_fault_small_ops)
+
+namespace {
+
+using namespace luce;
+
+// ---------------------------------------------------------------------------
+// Router select + weights ([PR826], commit "fused DS4.1 decode kernels").
+// One warp per token.  The E scores (logit + bias, one fp32 add) are staged in
+// shared memory; k rounds of a warp arg-max pick the best untaken score,
+// ties to the lower expert index (the (value, index) order is total, so the
+// butterfly reduction gives every lane the same winner).  The weights are a
+// softmax over the selected, unbiased logits.
+constexpr int ROUTE_WARPS = 4;
+
+__global__ void __launch_bounds__(ROUTE_WARPS * 32)
+    k_route_topk(const float *__restrict__ logits, const float *__restrict__ bias, int T, int E, int k,
+                 int32_t *__restrict__ ids, float *__restrict__ weights)
+{
+    extern __shared__ float s_scores[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * ROUTE_WARPS + warp;
+    if (t >= T)
+        return;
+    float *s = s_scores + warp * E;
+    const float *l = logits + (size_t)t * E;
+    for (int e = lane; e < E; e += 32)
+        s[e] = bias ? __fadd_rn(l[e], bias[e]) : l[e];
+    __syncwarp();
+
+    const int n_i = (E + 31) >> 5;
+    uint32_t taken = 0;
+    float sel0 = 0.0f, sel1 = 0.0f; // unbiased logit of slot lane and lane + 32
+    for (int j = 0; j < k; j++) {
+        float bv = 0.0f;
+        int bi = INT_MAX;
+        for (int i = 0; i < n_i; i++) {
+            const int e = lane + 32 * i;
+            if (e < E && !((taken >> i) & 1u)) {
+                const float v = s[e];
+                if (bi == INT_MAX || v > bv) {
+                    bv = v;
+                    bi = e;
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (oi != INT_MAX && (bi == INT_MAX || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane)
+            taken |= 1u << (bi >> 5);
+        if (lane == 0)
+            ids[(size_t)t * k + j] = bi;
+        if (j == lane)
+            sel0 = l[bi];
+        else if (j == lane + 32)
+            sel1 = l[bi];
+    }
+    const bool has0 = lane < k, has1 = lane + 32 < k;
+    float m = has0 ? sel0 : -INFINITY;
+    if (has1)
+        m = fmaxf(m, sel1);
+    m = warp_max(m);
+    const float e0 = has0 ? expf(__fsub_rn(sel0, m)) : 0.0f;
+    const float e1 = has1 ? expf(__fsub_rn(sel1, m)) : 0.0f;
+    const float den = warp_sum(__fadd_rn(e0, e1));
+    if (has0)
+        weights[(size_t)t * k + lane] = __fdiv_rn(e0, den);
+    if (has1)
+        weights[(size_t)t * k + lane + 32] = __fdiv_rn(e1, den);
+}
+
+// ---------------------------------------------------------------------------
+// q8_1 quantization ([PR826], commit "fused DS4.1 decode kernels": the q8_1
+// activation memo).  One warp per 32-value block; a row of K values is K/32
+// consecutive blocks, so the whole [T][K] input is one flat run of blocks.
+constexpr int QUANT_WARPS = 8;
+
+__global__ void __launch_bounds__(QUANT_WARPS * 32)
+    k_quantize_q8_1(const float *__restrict__ x, int64_t n_blocks, uint32_t *__restrict__ out)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t b = (int64_t)blockIdx.x * QUANT_WARPS + (threadIdx.x >> 5);
+    if (b >= n_blocks)
+        return;
+    const float v = x[b * QK + lane];
+    quantize_q8_1_warp(v, out + b * Q8_1_WORDS, lane);
+}
+
+// ---------------------------------------------------------------------------
+// Expert grouping ([PR826], commit "fused DS4.1 decode kernels").  One CTA.
+// Warp w owns a contiguous segment of routes and counts it into its own
+// histogram row; the exclusive scan of the totals gives the offsets, and a
+// per-(warp, expert) running base makes the scatter stable in r: within a
+// 32-route chunk, lanes with the same expert take consecutive slots in lane
+// order (match + popcount), then the group's last lane advances the base.
+constexpr int GROUP_THREADS = 1024;
+
+__global__ void __launch_bounds__(GROUP_THREADS)
+    k_moe_group(const int32_t *__restrict__ ids, int R, int E, int nw, int32_t *__restrict__ counts,
+                int32_t *__restrict__ offsets, int32_t *__restrict__ routes)
+{
+    extern __shared__ int s_mem[];
+    int *hist = s_mem;           // [nw][E]: counts, then running bases
+    int *excl = s_mem + nw * E;  // [E + 1]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int i = tid; i < nw * E; i += blockDim.x)
+        hist[i] = 0;
+    __syncthreads();
+    const int seg = (R + nw - 1) / nw;
+    const int r0 = warp * seg, r1 = min(R, r0 + seg);
+    if (warp < nw) {
+        for (int r = r0 + lane; r < r1; r += 32) {
+            const int e = ids[r];
+            if (e >= 0 && e < E)
+                atomicAdd(&hist[warp * E + e], 1);
+            else if (e >= E)
+                atomicOr(&g_fault_word, LUCE_FAULT_BAD_ID);
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) {
+        int c = 0;
+        for (int w = 0; w < nw; w++)
+            c += hist[w * E + e];
+        excl[e] = c;
+        counts[e] = c;
+    }
+    __syncthreads();
+    if (warp == 0) { // exclusive scan of the counts, 32 at a time
+        int carry = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int e = base + lane;
+            const int c = e < E ? excl[e] : 0;
+            int inc = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o)
+                    inc += v;
+            }
+            if (e < E)
+                excl[e] = carry + inc - c;
+            carry += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0)
+            excl[E] = carry;
+    }
+    __syncthreads();
+    for (int e = tid; e <= E; e += blockDim.x)
+        offsets[e] = excl[e];
+    for (int e = tid; e < E; e += blockDim.x) {
+        int run = excl[e];
+        for (int w = 0; w < nw; w++) {
+            const int c = hist[w * E + e];
+            hist[w * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    if (warp < nw) {
+        const unsigned lt = (1u << lane) - 1u;
+        for (int base = r0; base < r1; base += 32) {
+            const int r = base + lane;
+            const int e = r < r1 ? ids[r] : -1;
+            const bool ok = e >= 0 && e < E;
+            const unsigned m = __match_any_sync(0xffffffffu, ok ? e : -1);
+            int pos = 0;
+            if (ok)
+                pos = hist[warp * E + e] + __popc(m & lt);
+            __syncwarp();
+            if (ok) {
+                routes[pos] = r;
+                if (lane == 31 - __clz(m))
+                    hist[warp * E + e] += __popc(m);
+            }
+            __syncwarp();
+        }
+    }
+    const int total = excl[E];
+    for (int r = total + tid; r < R; r += blockDim.x)
+        routes[r] = -1;
+}
+
+// ---------------------------------------------------------------------------
+// Argmax pair/pick ([PR826], commit "fused DS4.1 decode kernels").  CTA
+// (c, r) reduces chunk c of row r to a (value, index) pair; the CTA that
+// arrives last on the row's counter picks among the C pairs and resets the
+// counter.  The (greater value, then lower index) order is total, so the
+// result does not depend on which CTA finishes last.
+constexpr int ARGMAX_THREADS = 256;
+
+struct ArgPair {
+    float v;
+    int i;
+};
+
+__device__ __forceinline__ void better(float &bv, int &bi, float ov, int oi)
+{
+    if (oi != INT_MAX && (bi == INT_MAX || ov > bv || (ov == bv && oi < bi))) {
+        bv = ov;
+        bi = oi;
+    }
+}
+
+__device__ __forceinline__ void block_argmax(float &bv, int &bi)
+{
+    __shared__ float sv[ARGMAX_THREADS / 32];
+    __shared__ int si[ARGMAX_THREADS / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        better(bv, bi, ov, oi);
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        sv[warp] = bv;
+        si[warp] = bi;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        bv = lane < ARGMAX_THREADS / 32 ? sv[lane] : 0.0f;
+        bi = lane < ARGMAX_THREADS / 32 ? si[lane] : INT_MAX;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            better(bv, bi, ov, oi);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(ARGMAX_THREADS)
+    k_argmax(const float *__restrict__ logits, int64_t V, int64_t L, int C, bool vec4, ArgPair *__restrict__ pairs,
+             unsigned int *__restrict__ counters, int32_t *__restrict__ idx, float *__restrict__ val)
+{
+    const int c = blockIdx.x, r = blockIdx.y;
+    const int64_t lo = (int64_t)c * L, hi = min(V, lo + L);
+    const float *row = logits + (int64_t)r * V;
+    float bv = 0.0f;
+    int bi = INT_MAX;
+    if (vec4) {
+        const float4 *p = reinterpret_cast<const float4 *>(row + lo);
+        const int64_t n4 = (hi - lo) >> 2;
+        for (int64_t i = threadIdx.x; i < n4; i += ARGMAX_THREADS) {
+            const float4 q = __ldcs(p + i);
+            const int base = (int)(lo + 4 * i);
+            better(bv, bi, q.x, base);
+            better(bv, bi, q.y, base + 1);
+            better(bv, bi, q.z, base + 2);
+            better(bv, bi, q.w, base + 3);
+        }
+        for (int64_t i = lo + 4 * n4 + threadIdx.x; i < hi; i += ARGMAX_THREADS)
+            better(bv, bi, row[i], (int)i);
+    } else {
+        for (int64_t i = lo + threadIdx.x; i < hi; i += ARGMAX_THREADS)
+            better(bv, bi, __ldcs(row + i), (int)i);
+    }
+    block_argmax(bv, bi);
+    __shared__ bool s_last;
+    if (threadIdx.x == 0) {
+        pairs[(size_t)r * C + c] = ArgPair{bv, bi};
+        __threadfence();
+        const unsigned ticket = atomicAdd(&counters[r], 1u);
+        s_last = (ticket == (unsigned)(C - 1));
+    }
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+    bv = 0.0f;
+    bi = INT_MAX;
+    for (int i = threadIdx.x; i < C; i += ARGMAX_THREADS) {
+        const float ov = __ldcg(&pairs[(size_t)r * C + i].v);
+        const int oi = __ldcg(&pairs[(size_t)r * C + i].i);
+        better(bv, bi, ov, oi);
+    }
+    block_argmax(bv, bi);
+    if (threadIdx.x == 0) {
+        idx[r] = bi;
+        if (val)
+            val[r] = bv;
+        counters[r] = 0u;
+    }
+}
+
+// Chunking of an argmax row: a pure function of (R, V), so the workspace size
+// does not depend on the device.
+void argmax_chunks(int R, int64_t V, int64_t &L, int &C)
+{
+    const int64_t want = R > 0 ? std::max<int64_t>(1, 320 / R) : 1;
+    L = std::max<int64_t>(2048, (V + want - 1) / want);
+    L = (L + 3) & ~int64_t(3);
+    C = (int)((V + L - 1) / L);
+}
+
+size_t argmax_pairs_bytes(int R, int C) { return ((size_t)R * C * sizeof(ArgPair) + 15) & ~size_t(15); }
+
+} // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault_glu(unsigned int *bits);
+extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault_down(unsigned int *bits);
+
+namespace luce_host {
+int sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 148;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+} // namespace luce_host
+
+using namespace luce_host;
+
+extern "C" const char *luce_status_string(luce_status s)
+{
+    switch (s) {
+    case LUCE_OK:
+        return "ok";
+    case LUCE_ERR_INVALID_ARG:
+        return "invalid argument";
+    case LUCE_ERR_UNSUPPORTED:
+        return "unsupported shape";
+    case LUCE_ERR_CUDA:
+        return "CUDA error";
+    }
+    return "unknown status";
+}
+
+extern "C" int luce_version(void) { return 100; }
+
+extern "C" luce_status luce_get_fault(unsigned int *bits)
+{
+    if (!bits)
+        return LUCE_ERR_INVALID_ARG;
+    *bits = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess)
+        return LUCE_ERR_CUDA;
+    cudaError_t e1 = luce_internal_fault_small_ops(bits);
+    cudaError_t e2 = luce_internal_fault_glu(bits);
+    cudaError_t e3 = luce_internal_fault_down(bits);
+    return (e1 == cudaSuccess && e2 == cudaSuccess && e3 == cudaSuccess) ? LUCE_OK : LUCE_ERR_CUDA;
+}
+
+extern "C" luce_status luce_route_topk(const float *logits, const float *bias, int T, int E, int k, int32_t *ids,
+                                       float *weights, void *stream)
+{
+    if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E || k > 64)
+        return LUCE_ERR_INVALID_ARG;
+    if (T == 0)
+        return LUCE_OK;
+    if (!logits || !ids || !weights || !aligned(logits, 4) || !aligned(ids, 4) || !aligned(weights, 4) ||
+        (bias && !aligned(bias, 4)))
+        return LUCE_ERR_INVALID_ARG;
+    const int blocks = (T + ROUTE_WARPS - 1) / ROUTE_WARPS;
+    const size_t smem = (size_t)ROUTE_WARPS * E * sizeof(float);
+    k_route_topk<<<blocks, ROUTE_WARPS * 32, smem, as_stream(stream)>>>(logits, bias, T, E, k, ids, weights);
+    return launch_status();
+}
+
+extern "C" luce_status luce_quantize_q8_1(const float *x, int T, int K, luce_block_q8_1 *xq, void *stream)
+{
+    if (T < 0 || K <= 0 || K % QK != 0)
+        return LUCE_ERR_INVALID_ARG;
+    if (T == 0)
+        return LUCE_OK;
+    if (!x || !xq || !aligned(x, 4) || !aligned(xq, 4))
+        return LUCE_ERR_INVALID_ARG;
+    const int64_t nb = (int64_t)T * (K / QK);
+    const int64_t blocks = (nb + QUANT_WARPS - 1) / QUANT_WARPS;
+    if (blocks > INT_MAX)
+        return LUCE_ERR_INVALID_ARG;
+    k_quantize_q8_1<<<(unsigned)blocks, QUANT_WARPS * 32, 0, as_stream(stream)>>>(
+        x, nb, reinterpret_cast<uint32_t *>(xq));
+    return launch_status();
+}
+
+extern "C" luce_status luce_moe_group(const int32_t *ids, int T, int k, int E, int32_t *counts, int32_t *offsets,
+                                      int32_t *routes, void *stream)
+{
+    if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 64 || (int64_t)T * k > (1 << 20))
+        return LUCE_ERR_INVALID_ARG;
+    if (!counts || !offsets || !aligned(counts, 4) || !aligned(offsets, 4))
+        return LUCE_ERR_INVALID_ARG;
+    if (T > 0 && (!ids || !routes || !aligned(ids, 4) || !aligned(routes, 4)))
+        return LUCE_ERR_INVALID_ARG;
+    const int R = T * k;
+    const int nw = std::max(1, std::min(32, 8192 / E));
+    const size_t smem = ((size_t)nw * E + E + 1) * sizeof(int);
+    k_moe_group<<<1, GROUP_THREADS, smem, as_stream(stream)>>>(ids, R, E, nw, counts, offsets, routes);
+    return launch_status();
+}
+
+extern "C" size_t luce_argmax_workspace_bytes(int R, int64_t V)
+{
+    if (R <= 0 || V <= 0)
+        return 0;
+    int64_t L;
+    int C;
+    argmax_chunks(R, V, L, C);
+    return argmax_pairs_bytes(R, C) + (((size_t)R * sizeof(unsigned int) + 15) & ~size_t(15));
+}
+
+extern "C" luce_status luce_argmax(const float *logits, int R, int64_t V, int32_t *idx, float *val,
+                                   void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (R < 0 || V < 1 || V >= ((int64_t)1 << 31) || R > 65535)
+        return LUCE_ERR_INVALID_ARG;
+    if (R == 0)
+        return LUCE_OK;
+    if (!logits || !idx || !workspace || !aligned(logits, 4) || !aligned(idx, 4) || !aligned(workspace, 8) ||
+        (val && !aligned(val, 4)))
+        return LUCE_ERR_INVALID_ARG;
+    if (workspace_bytes < luce_argmax_workspace_bytes(R, V))
+        return LUCE_ERR_INVALID_ARG;
+    int64_t L;
+    int C;
+    argmax_chunks(R, V, L, C);
+    ArgPair *pairs = reinterpret_cast<ArgPair *>(workspace);
+    unsigned int *counters =
+        reinterpret_cast<unsigned int *>(reinterpret_cast<uint8_t *>(workspace) + argmax_pairs_bytes(R, C));
+    const bool vec4 = (V % 4 == 0) && aligned(logits, 16);
+    dim3 grid((unsigned)C, (unsigned)R);
+    k_argmax<<<grid, ARGMAX_THREADS, 0, as_stream(stream)>>>(logits, V, L, C, vec4, pairs, counters, idx, val);
+    return launch_status();
+}
