@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying CUDA graphs")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--layers", type=int, default=None, help="(debug) fewer layers; invalid as a bench number")
+    p.add_argument("--input-steps", type=int, default=None,
+                   help="pre-drawn input steps to cycle (default 64; fewer keeps profiling runs short)")
     return p.parse_args()
 
 
@@ -499,6 +501,8 @@ def run_ours(args, wl, layers):
 def main():
     args = parse()
     wl = W.WORKLOADS["decode_stack43"]
+    if args.input_steps:
+        wl = W.Workload(**{**wl.__dict__, "steps": args.input_steps})
     layers = args.layers or wl.layers
     if args.impl == "reference":
         run_reference(args, wl, layers)

@@ -14,3 +14,4 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: long-running case")
+    config.addinivalue_line("markers", "allow_fault: the test reads and clears the library's device fault bits")
