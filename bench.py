@@ -47,6 +47,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying CUDA graphs")
+    p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--layers", type=int, default=None, help="(debug) fewer layers; invalid as a bench number")
     p.add_argument("--input-steps", type=int, default=None,
@@ -232,7 +233,7 @@ def run_reference(args, wl, layers):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": len(per), "warmup": warm, "ms_per_step": layer_s * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "i8 codes, f64 accumulation", "data": "synthetic",
-            "config": config_dict(wl, layers, False),
+            "config": {**config_dict(wl, layers, False), "pdl": False},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": f"{len(per)} steps, each one decode layer of one token "
                                        f"(x {layers} layers = 1 token); single-threaded C oracle"},
@@ -299,6 +300,7 @@ def run_ours(args, wl, layers):
     step_bufs = MoEStep(wl.T, wl.H, wl.I, wl.E, wl.k, wl.shared, wl.clamp, device=dev)
     am = Argmax(1, VOCAB, device=dev)
     graph = not args.no_graph
+    Bd.luce_set_pdl(not args.no_pdl)
 
     # per-kernel timing events (recorded inside the graphs as external events)
     ev_kind = {"glu": [], "down": []}
@@ -310,30 +312,32 @@ def run_ours(args, wl, layers):
             return torch.cuda.Event(enable_timing=True)
 
     def run_step(s, x_src, lg_src, v_src, out_dst, record):
+        bufs = step_bufs
         for l in range(layers):
-            bufs = step_bufs
             lay = dls[l]
-            B = Bd
-            B.luce_route_topk(lg_src[s, l], b_d[l], wl.k, bufs.ids, bufs.weights)
-            B.luce_quantize_q8_1(x_src[s, l], bufs.xq)
-            B.luce_moe_group(bufs.ids, wl.E, bufs.counts, bufs.offsets, bufs.routes)
+            Bd.luce_moe_prep(lg_src[s, l], b_d[l], x_src[s, l], wl.k, bufs.ids, bufs.weights, bufs.xq, bufs.counts,
+                             bufs.offsets, bufs.routes)
             if record is not None:
                 e0, e1, e2 = record[l]
                 e0.record()
-            B.luce_moe_glu_pair(lay.wg, lay.wu, lay.wsg, lay.wsu, bufs.xq, bufs.offsets, bufs.routes, wl.T,
-                                wl.k, wl.E, wl.H, wl.I, wl.clamp, bufs.h, bufs.hq)
+            Bd.luce_moe_glu_pair(lay.wg, lay.wu, lay.wsg, lay.wsu, bufs.xq, bufs.offsets, bufs.routes, wl.T,
+                                 wl.k, wl.E, wl.H, wl.I, wl.clamp, bufs.h, bufs.hq, bufs.glu_ws)
             if record is not None:
                 e1.record()
-            B.luce_moe_down_combine(lay.wd, lay.wsd, bufs.hq, bufs.ids, bufs.weights, bufs.offsets,
-                                    bufs.routes, wl.T, wl.k, wl.E, wl.H, wl.I, out_dst[l])
+            Bd.luce_moe_down_combine(lay.wd, lay.wsd, bufs.hq, bufs.ids, bufs.weights, bufs.offsets, bufs.routes,
+                                     wl.T, wl.k, wl.E, wl.H, wl.I, out_dst[l])
             if record is not None:
                 e2.record()
         am.run(v_src[s])
 
-    launches_per_step = layers * 5 + 1
+    launches_per_step = layers * 3 + 1  # prep, gate/up, down per layer; argmax
     S = wl.steps
     stream = torch.cuda.Stream(device=dev)
-    records = [[(make_events(), make_events(), make_events()) for _ in range(layers)] for _ in range(S)]
+    # per-kernel timing: only the graph of input slot 0 carries event records
+    # (an event node between two kernels also removes their programmatic
+    # overlap, so instrumenting every step would slow the timed region)
+    records = [[(make_events(), make_events(), make_events()) for _ in range(layers)] if s == 0 else None
+               for s in range(S)]
     graphs = []
     with torch.cuda.stream(stream):
         for s in range(S):  # eager once: sets kernel attributes, checks every call
@@ -376,8 +380,8 @@ def run_ours(args, wl, layers):
     ms = start.elapsed_time(end)
     # per-kernel durations: the last execution of every recorded pair
     glu_ms, down_ms = [], []
-    for s in range(S):
-        for (e0, e1, e2) in records[s]:
+    for rec in records:
+        for (e0, e1, e2) in (rec or []):
             try:
                 glu_ms.append(e0.elapsed_time(e1))
                 down_ms.append(e1.elapsed_time(e2))
@@ -483,7 +487,7 @@ def run_ours(args, wl, layers):
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "i8 codes (dp4a int32 block sums), f32 scales/accumulation",
                 "data": "synthetic (seeded Q8_0 weights, N(0,1) activations, Zipf-skewed router logits)",
-                "config": config_dict(wl, layers, graph),
+                "config": {**config_dict(wl, layers, graph), "pdl": not args.no_pdl},
                 "layer_us": ms_per_step * 1e3 / layers,
                 "stack_weight_GBps": step_bytes / (ms_per_step * 1e-3) / 1e9,
                 "stack_frac_of_measured_hbm": step_bytes / (ms_per_step * 1e-3) / 1e9 / peak,

@@ -148,6 +148,13 @@ LUCE_API luce_status luce_moe_group(const int32_t *ids, int T, int k, int E, int
  *   w_gate, w_up   [E][I][H/32] Q8_0        ws_gate, ws_up [I][H/32] or NULL
  *   xq             [T][H/32] q8_1           offsets [E+1], routes [T*k]
  *   h              [T*k + T][I] fp32 out    hq [T*k + T][I/32] q8_1 out
+ *   workspace      device scratch of at least luce_moe_glu_workspace_bytes
+ *                  (T, k, E, I) bytes, 4-byte aligned, ZERO-FILLED before its
+ *                  first use: one counter per (expert, 32-row group) lets the
+ *                  CTA that finishes a group split across CTAs quantize it.
+ *                  Every call leaves it zero-filled again, so one buffer
+ *                  serves any number of calls on one stream; calls that
+ *                  overlap on the GPU must not share it.
  *   variant        0 = automatic (only one kernel exists in this build)
  * Requires H % 256 == 0, I % 256 == 0, H/32 <= 1024; w_*, xq, hq 16-byte
  * aligned; ws_gate and ws_up both given or both NULL.
@@ -155,8 +162,9 @@ LUCE_API luce_status luce_moe_group(const int32_t *ids, int T, int k, int E, int
 LUCE_API luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const luce_block_q8_0 *w_up,
                               const luce_block_q8_0 *ws_gate, const luce_block_q8_0 *ws_up,
                               const luce_block_q8_1 *xq, const int32_t *offsets, const int32_t *routes, int T, int k,
-                              int E, int H, int I, float clamp, float *h, luce_block_q8_1 *hq, int variant,
-                              void *stream);
+                              int E, int H, int I, float clamp, float *h, luce_block_q8_1 *hq, void *workspace,
+                              size_t workspace_bytes, int variant, void *stream);
+LUCE_API size_t luce_moe_glu_workspace_bytes(int T, int k, int E, int I);
 
 /* ------------------------------------------------------------------------
  * luce_moe_down_combine -- the Q8_0 down product of every route and of the
@@ -209,6 +217,32 @@ LUCE_API luce_status luce_moe_down_combine(const luce_block_q8_0 *w_down, const 
 LUCE_API luce_status luce_argmax(const float *logits, int R, int64_t V, int32_t *idx, float *val, void *workspace,
                         size_t workspace_bytes, void *stream);
 LUCE_API size_t luce_argmax_workspace_bytes(int R, int64_t V);
+
+/* ------------------------------------------------------------------------
+ * luce_moe_prep -- luce_route_topk, luce_quantize_q8_1 (K = H) and
+ * luce_moe_group in ONE launch (one CTA) when T <= 32 and E <= 256, else the
+ * three launches in that order.  Same arguments, outputs and results as the
+ * three calls.  [PR826], commit "fused DS4.1 decode kernels": the verify
+ * step "runs many short kernels per layer", cut by one launch for the
+ * router's select and weights, one expert grouping per layer and a q8_1
+ * activation memo.
+ */
+LUCE_API luce_status luce_moe_prep(const float *logits, const float *bias, const float *x, int T, int E, int k,
+                                   int H, int32_t *ids, float *weights, luce_block_q8_1 *xq, int32_t *counts,
+                                   int32_t *offsets, int32_t *routes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * luce_set_pdl -- process-wide switch (default 0 = off) for programmatic
+ * dependent launch: each library kernel may then start before the previous
+ * kernel on the stream has finished, run its prologue, and wait on the GPU
+ * before it reads that kernel's results.  Kernels of other code never start
+ * early (they do not signal), so expert weights written by any earlier
+ * kernel are safe.  One extra rule holds while it is on:
+ * luce_moe_down_combine reads ids, weights, offsets and routes before it
+ * waits, so the call that produced them must not be the launch immediately
+ * before it (in the order prep/group, glu_pair, down_combine it never is).
+ */
+LUCE_API luce_status luce_set_pdl(int enable);
 
 /* ------------------------------------------------------------------------
  * Diagnostics. */

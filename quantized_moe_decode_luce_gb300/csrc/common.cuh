@@ -237,6 +237,21 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
         : "memory");
 }
 
+// Programmatic dependent launch.  pdl_wait: wait until the kernels this grid
+// depends on have completed and their writes are visible (a no-op when the
+// grid was launched without the programmatic attribute).  pdl_trigger: let
+// the next kernel on the stream start its prologue early.  Every kernel of
+// this library triggers only after its own pdl_wait, so a kernel that starts
+// early may still read the outputs of kernels two launches back.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Prefetch `bytes` (multiple of 16, 16-byte aligned) of global memory into L2.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Named barrier among `nthreads` threads (id 0 is __syncthreads).
 __device__ __forceinline__ void named_barrier(int id, int nthreads)
 {
@@ -253,14 +268,44 @@ inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_
 
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
-// Number of SMs of the current device (cached per device).
-int sm_count();
-
 // Maps the last launch error to a status (and clears it).
 inline luce_status launch_status()
 {
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? LUCE_OK : LUCE_ERR_CUDA;
+}
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Whether kernels are launched with the programmatic-dependent-launch
+// attribute (luce_set_pdl; process-wide, default off).
+bool pdl_enabled();
+
+// Launch `kern` with cudaLaunchKernelEx, with the PDL attribute when enabled.
+template <typename... KArgs, typename... Args>
+luce_status launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    int n = 0;
+    if (pdl_enabled()) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        n++;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return LUCE_ERR_CUDA;
+    }
+    return LUCE_OK;
 }
 
 } // namespace luce_host

@@ -9,14 +9,20 @@
 // separately, as the unfused ops do".
 //
 // GB300 shape (our own): a CTA owns a slab of RN output rows n for a tile of
-// tokens, and streams those RN rows of EVERY active expert (one bulk copy
-// per expert and column chunk) through a shared-memory ring; each weight row
-// still crosses HBM once per token tile (once per step for decode and verify,
-// where one tile holds every token).  Each route's product y is kept in
-// shared memory, so the combine of a token needs no second pass and no
-// atomics: one thread sums out[t][n] over the k slots in slot order with
-// separately rounded products and sums (__fmul_rn / __fadd_rn), then adds
-// the shared expert.  Deterministic; no global scratch.
+// tokens and streams those RN rows of EVERY active (virtual) expert, one
+// cp.async.bulk stage per expert, through a shared-memory ring; each weight
+// row crosses HBM once per token tile (once per step for decode and verify,
+// where one tile holds every token).  Each consumer warp takes whole stages
+// (all RN rows of one expert), so the experts' activation loads proceed in
+// parallel across warps.  Each route's product y stays in shared memory, so
+// the combine needs no second pass and no atomics: one thread sums out[t][n]
+// over the k slots in slot order with separately rounded products and sums
+// (__fmul_rn / __fadd_rn), then adds the shared expert.  Deterministic; no
+// global scratch.
+//
+// With programmatic dependent launch the CTAs start while the gate/up kernel
+// still runs: the routing tables (written two launches earlier) are read and
+// the weight rows are requested before waiting for h.
 #include <algorithm>
 #include <climits>
 
@@ -28,36 +34,33 @@ namespace {
 
 using namespace luce;
 
-constexpr int NCU_MAX = 32; // columns per virtual expert
-constexpr int CW = 4;       // consumer warps
-constexpr int RN = 8;       // output rows per CTA
-constexpr int RPW = RN / CW;
+constexpr int NCU = 32; // columns per virtual expert
+constexpr int CW = 4;   // consumer warps
+constexpr int RN = 8;   // output rows per CTA
 
 struct DownArgs {
-    const uint8_t *wd;     // [E][H][rowbytes]
-    const uint8_t *wsd;    // [H][rowbytes] or null
-    const uint32_t *hq;    // [T*k+T][nbI] q8_1 blocks (9 words)
-    const int32_t *ids;    // [T][k]
-    const float *weights;  // [T][k]
+    const uint8_t *wd;    // [E][H][rowbytes]
+    const uint8_t *wsd;   // [H][rowbytes] or null
+    const uint32_t *hq;   // [T*k+T][nbI] q8_1 blocks (9 words)
+    const int32_t *ids;   // [T][k]
+    const float *weights; // [T][k]
     const int32_t *offsets, *routes;
-    float *out;            // [T][H]
+    float *out; // [T][H]
     int T, k, E, H, I;
     int nbI, rowbytes;
-    int TT;                // tokens per tile
-    int NS;                // ring stages
-    int ncu;
+    int TT; // tokens per tile
+    int NS; // ring stages
 };
 
 struct VUnit {
     const uint8_t *w; // RN rows of this expert
     int e;            // expert (E = shared)
-    int first;        // index into routes[] of the first column (routed)
+    int first;        // index into routes[] of the expert's first route in the tile
     int col0, ncols;
 };
 
 template <int NC>
-__global__ void __launch_bounds__((CW + 1) * 32)
-    k_down_combine(const DownArgs a)
+__global__ void __launch_bounds__((CW + 1) * 32) k_down_combine(const DownArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const int stage_bytes = RN * a.rowbytes;
@@ -65,8 +68,8 @@ __global__ void __launch_bounds__((CW + 1) * 32)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.NS * stage_bytes);
     uint64_t *empty = full + a.NS;
     int *vpre = reinterpret_cast<int *>(empty + a.NS); // [E + 1]
-    int *vlo = vpre + a.E + 1;                        // [E]: first route of the tile
-    int *vcnt = vlo + a.E;                            // [E]: routes of the tile
+    int *vlo = vpre + a.E + 1;                         // [E]: first route of the tile
+    int *vcnt = vlo + a.E;                             // [E]: routes of the tile
     float *ybuf = reinterpret_cast<float *>(vcnt + a.E);
     __shared__ int s_abort;
 
@@ -77,36 +80,41 @@ __global__ void __launch_bounds__((CW + 1) * 32)
     if (tid == 0) {
         for (int s = 0; s < a.NS; s++) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], CW);
+            mbar_init(&empty[s], 1);
         }
         fence_mbar_init();
         s_abort = 0;
     }
-    // routes of expert e that belong to tokens [t0, t1): a sub-range, since
-    // an expert's routes are sorted by r = t*k + j
+    // routes of expert e that belong to tokens [t0, t1): a sub-range, since an
+    // expert's routes are sorted by r = t*k + j.  (Grouping output: two
+    // launches back, complete even when this grid started early.)
     for (int e = tid; e < a.E; e += blockDim.x) {
-        int lo = a.offsets[e], hi = a.offsets[e + 1];
-        const int rlo = t0 * a.k, rhi = t1 * a.k;
-        int b = lo, c = hi;
-        while (b < c) { // first route >= rlo
-            const int m = (b + c) >> 1;
-            if (a.routes[m] < rlo)
-                b = m + 1;
-            else
-                c = m;
-        }
-        const int first = b;
-        c = hi;
-        while (b < c) { // first route >= rhi
-            const int m = (b + c) >> 1;
-            if (a.routes[m] < rhi)
-                b = m + 1;
-            else
-                c = m;
+        const int lo = a.offsets[e], hi = a.offsets[e + 1];
+        int first = lo, end = hi;
+        if (t0 > 0 || t1 < a.T) {
+            const int rlo = t0 * a.k, rhi = t1 * a.k;
+            int b = lo, c = hi;
+            while (b < c) { // first route >= rlo
+                const int m = (b + c) >> 1;
+                if (a.routes[m] < rlo)
+                    b = m + 1;
+                else
+                    c = m;
+            }
+            first = b;
+            c = hi;
+            while (b < c) { // first route >= rhi
+                const int m = (b + c) >> 1;
+                if (a.routes[m] < rhi)
+                    b = m + 1;
+                else
+                    c = m;
+            }
+            end = b;
         }
         vlo[e] = first;
-        vcnt[e] = b - first;
-        vpre[e + 1] = (b - first + a.ncu - 1) / a.ncu;
+        vcnt[e] = end - first;
+        vpre[e + 1] = (end - first + NCU - 1) / NCU;
     }
     __syncthreads();
     if (warp == 0) {
@@ -129,7 +137,7 @@ __global__ void __launch_bounds__((CW + 1) * 32)
     }
     __syncthreads();
     const int NVr = vpre[a.E];
-    const int NV = NVr + (a.wsd ? (ntok + a.ncu - 1) / a.ncu : 0);
+    const int NV = NVr + (a.wsd ? (ntok + NCU - 1) / NCU : 0);
 
     auto decode = [&](int v) {
         VUnit r;
@@ -144,20 +152,21 @@ __global__ void __launch_bounds__((CW + 1) * 32)
             }
             r.e = lo;
             r.first = vlo[lo];
-            r.col0 = (v - vpre[lo]) * a.ncu;
-            r.ncols = min(a.ncu, vcnt[lo] - r.col0);
+            r.col0 = (v - vpre[lo]) * NCU;
+            r.ncols = min(NCU, vcnt[lo] - r.col0);
             r.w = a.wd + ((size_t)lo * a.H + n0) * a.rowbytes;
         } else {
             r.e = a.E;
             r.first = 0;
-            r.col0 = (v - NVr) * a.ncu;
-            r.ncols = min(a.ncu, ntok - r.col0);
+            r.col0 = (v - NVr) * NCU;
+            r.ncols = min(NCU, ntok - r.col0);
             r.w = a.wsd + (size_t)n0 * a.rowbytes;
         }
         return r;
     };
 
     if (warp == CW) {
+        // ---------------- producer: weights only, no wait on the gate/up kernel ----------------
         if (lane != 0)
             return;
         const uint64_t pol = l2_evict_first_policy();
@@ -184,9 +193,11 @@ __global__ void __launch_bounds__((CW + 1) * 32)
         return;
     }
 
-    // ---------------- consumers ----------------
+    // ---------------- consumers: wait for h, then one warp per stage ----------------
+    pdl_wait();
+    pdl_trigger();
     bool dead = false;
-    for (int v = 0; v < NV; v++) {
+    for (int v = warp; v < NV; v += CW) {
         const VUnit un = decode(v);
         int my_r = 0, my_slot = 0; // column `lane`: its hq row and its y slot
         if (lane < un.ncols) {
@@ -216,30 +227,28 @@ __global__ void __launch_bounds__((CW + 1) * 32)
             const uint8_t *st = ring + (size_t)slot * stage_bytes;
             for (int c0 = 0; c0 < un.ncols; c0 += NC) {
                 const int nc = min(NC, un.ncols - c0);
-                int rr[NC];
+                float acc[RN][NC];
 #pragma unroll
-                for (int c = 0; c < NC; c++)
-                    rr[c] = __shfl_sync(0xffffffffu, my_r, c0 + (c < nc ? c : 0));
-                float acc[RPW][NC];
-#pragma unroll
-                for (int m = 0; m < RPW; m++)
+                for (int m = 0; m < RN; m++)
 #pragma unroll
                     for (int c = 0; c < NC; c++)
                         acc[m][c] = 0.0f;
                 for (int b = lane; b < a.nbI; b += 32) {
-                    Q80Block wb[RPW];
-#pragma unroll
-                    for (int m = 0; m < RPW; m++)
-                        load_q8_0_smem(st + (size_t)(warp + CW * m) * a.rowbytes, b, wb[m]);
+                    Q81Block xb[NC];
 #pragma unroll
                     for (int c = 0; c < NC; c++) {
-                        if (c < nc) {
-                            Q81Block xb;
-                            load_q8_1_global(a.hq + ((size_t)rr[c] * a.nbI + b) * Q8_1_WORDS, xb);
+                        const int r = __shfl_sync(0xffffffffu, my_r, c0 + (c < nc ? c : 0));
+                        if (c < nc)
+                            load_q8_1_global(a.hq + ((size_t)r * a.nbI + b) * Q8_1_WORDS, xb[c]);
+                    }
 #pragma unroll
-                            for (int m = 0; m < RPW; m++)
-                                acc[m][c] = fmaf(wb[m].d * xb.d, (float)dot_q8_block(wb[m].q, xb.q), acc[m][c]);
-                        }
+                    for (int m = 0; m < RN; m++) {
+                        Q80Block wb;
+                        load_q8_0_smem(st + (size_t)m * a.rowbytes, b, wb);
+#pragma unroll
+                        for (int c = 0; c < NC; c++)
+                            if (c < nc)
+                                acc[m][c] = fmaf(wb.d * xb[c].d, (float)dot_q8_block(wb.q, xb[c].q), acc[m][c]);
                     }
                 }
 #pragma unroll
@@ -247,10 +256,10 @@ __global__ void __launch_bounds__((CW + 1) * 32)
                     if (c < nc) {
                         const int ys = __shfl_sync(0xffffffffu, my_slot, c0 + c);
 #pragma unroll
-                        for (int m = 0; m < RPW; m++) {
+                        for (int m = 0; m < RN; m++) {
                             const float y = warp_sum(acc[m][c]);
-                            if (lane == 0)
-                                ybuf[ys * RN + warp + CW * m] = y;
+                            if (lane == m)
+                                ybuf[ys * RN + m] = y;
                         }
                     }
                 }
@@ -292,8 +301,7 @@ luce_status launch_down(const DownArgs &a, dim3 grid, size_t smem, cudaStream_t 
             return LUCE_ERR_CUDA;
         smem_set[dev] = smem;
     }
-    kern<<<grid, (CW + 1) * 32, smem, stream>>>(a);
-    return luce_host::launch_status();
+    return luce_host::launch(kern, grid, dim3((CW + 1) * 32), smem, stream, a);
 }
 
 } // namespace
@@ -307,7 +315,7 @@ extern "C" luce_status luce_moe_down_combine(const luce_block_q8_0 *w_down, cons
 {
     if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 64 || (int64_t)T * k > (1 << 20))
         return LUCE_ERR_INVALID_ARG;
-    if (H <= 0 || I <= 0 || H % 256 != 0 || I % 256 != 0 || I / 32 > 1024 || H > (1 << 20))
+    if (H <= 0 || I <= 0 || H % 256 != 0 || I % 256 != 0 || I / 32 > 1024 || H > (1 << 19))
         return LUCE_ERR_INVALID_ARG;
     if (variant != 0)
         return LUCE_ERR_INVALID_ARG;
@@ -334,19 +342,19 @@ extern "C" luce_status luce_moe_down_combine(const luce_block_q8_0 *w_down, cons
     a.I = I;
     a.nbI = I / 32;
     a.rowbytes = a.nbI * Q8_0_BYTES;
-    a.ncu = NCU_MAX;
-    const int stage = RN * a.rowbytes;
-    a.NS = std::max(2, std::min(8, (64 * 1024) / stage));
     // y buffer: (TT*k + TT) slots x RN floats, at most 32 KB
     const int per_tok = (k + 1) * RN * (int)sizeof(float);
     a.TT = std::max(1, std::min(T, (32 * 1024) / per_tok));
-    const size_t smem = (size_t)a.NS * stage + (size_t)2 * a.NS * sizeof(uint64_t) +
-                        (size_t)(3 * E + 1) * sizeof(int) + (size_t)(a.TT * k + a.TT) * RN * sizeof(float);
+    // ring: every stage of a CTA at once when it fits in ~100 KB
+    const long long Tk = (long long)a.TT * k;
+    const long long nv_up = std::min<long long>(E, Tk) + Tk / NCU + (ws_down ? (a.TT + NCU - 1) / NCU : 0);
+    const int stage = RN * a.rowbytes;
+    a.NS = (int)std::max<long long>(2, std::min<long long>(nv_up, (100 * 1024) / stage));
+    const size_t smem = (size_t)a.NS * stage + (size_t)2 * a.NS * sizeof(uint64_t) + (size_t)(3 * E + 1) * sizeof(int) +
+                        (size_t)(a.TT * k + a.TT) * RN * sizeof(float);
     const int tiles = (T + a.TT - 1) / a.TT;
-    if (H / RN > 65535)
-        return LUCE_ERR_UNSUPPORTED;
     dim3 grid((unsigned)tiles, (unsigned)(H / RN));
-    const int maxcols = std::min(std::min(T, a.TT), NCU_MAX);
+    const int maxcols = std::min(a.TT, NCU);
     cudaStream_t st = as_stream(stream);
     if (maxcols <= 1)
         return launch_down<1>(a, grid, smem, st);

@@ -3,30 +3,41 @@
 // quantization of its output, and its C-ABI entry point.
 //
 // Pages cited by title: [PR826] = Lucebox PR #826 "feat(ds41): two-box
-// expert-parallel serving".  The design follows what the page's commit "RDNA4
-// Q8_0 gate/up pair" describes (both matrices read with one load of each
-// activation fragment, each product with its own partial sums and reduction,
-// the GLU in the epilogue) and the commit "fused DS4.1 decode kernels" (one
-// expert grouping per layer, so each selected expert's weights cross HBM once).
-// Its GB300 shape is our own:
+// expert-parallel serving".  What the kernel computes follows the commit
+// "RDNA4 Q8_0 gate/up pair" (both matrices read with one load of each
+// activation fragment, each product with its own partial sums and
+// reduction, the GLU in the epilogue) and the commit "fused DS4.1 decode
+// kernels" (one expert grouping per layer, so each selected expert's
+// weights cross HBM once).  Its GB300 shape is our own:
 //
-//  * Work unit = (virtual expert, group of 32 rows).  A virtual expert is an
-//    expert with up to `ncu` of its routed columns (tokens); experts with
-//    more columns, and the shared expert (all T tokens), are split into
-//    several.  32 rows make one q8_1 block of h per column, so the epilogue
-//    quantizes locally, with no cross-CTA exchange.
-//  * Persistent CTAs take contiguous ranges of units.  One producer thread
-//    streams the gate and up rows of each unit through a ring of shared-memory
-//    stages with cp.async.bulk (no tensor map: rows are contiguous runs of
-//    34-byte blocks, 16-byte aligned because H % 256 == 0), completing on
-//    per-stage mbarriers; consumer warps compute from shared memory and free
-//    each stage on its "empty" mbarrier.
-//  * A consumer lane owns Q8_0 blocks b = lane, lane + 32, ... of a row;
-//    the q8_1 activation block of each column is loaded once (read-only
-//    path, L1-resident) and used for the gate AND the up row.  Block sums are
-//    exact int32 dp4a sums; the fp32 partials are reduced across the warp.
-//  * Every device wait is bounded (LUCE_FAULT_TIMEOUT, never expected); a
-//    CTA that gives up drains its copies in flight before it exits.
+//  * Work is a flat list of PARTS.  A virtual expert is an expert with up to
+//    32 of its routed columns (tokens); experts with more columns, and the
+//    shared expert (all T tokens), are split into several.  Each virtual
+//    expert has I/32 row groups of 32 rows (one q8_1 block of h per column),
+//    and each group is cut into CL parts of RU = 32/CL rows, sized so that a
+//    part (RU gate rows + RU up rows) is about 70 KB.
+//  * Persistent CTAs (one per SM) take contiguous ranges of parts.  One
+//    producer thread streams each part's gate and up rows into a ring of
+//    shared-memory stages (~200 KB: a decode step's whole share of the
+//    weights is in flight at once) with cp.async.bulk completing on
+//    per-stage mbarriers; eight consumer warps compute from shared memory
+//    and release each stage on its "empty" mbarrier.
+//  * A consumer lane owns Q8_0 blocks b = lane, lane + 32, ... of a row; the
+//    q8_1 activation block of each column is loaded once (read-only path,
+//    prefetched into L1 when the virtual expert changes) and used for the
+//    gate AND the up row.  Block sums are exact int32 dp4a sums; the fp32
+//    partials are reduced across the warp.
+//  * h of each part is written to global memory.  A CTA that computed all CL
+//    parts of a group quantizes it from shared memory; a group split across
+//    two CTAs is quantized by whichever finishes it last (a per-group counter
+//    in the caller's workspace; the last arriver resets it to zero).  No CTA
+//    ever waits for another.
+//  * Every device wait is bounded (LUCE_FAULT_TIMEOUT, never expected); a CTA
+//    that gives up drains its copies in flight before it exits.
+//  * With programmatic dependent launch the CTAs start while the previous
+//    kernel (the grouping) still runs: they prefetch their slice of the
+//    shared expert's rows into L2 (those rows are needed whatever the
+//    routing is) and then wait for the grouping's results.
 #include <algorithm>
 #include <climits>
 
@@ -38,8 +49,10 @@ namespace {
 
 using namespace luce;
 
-constexpr int NCU_MAX = 32;      // columns per virtual expert (<= 32: one per lane)
-constexpr int HB_STRIDE = NCU_MAX + 1;
+constexpr int NCU = 32;          // columns per virtual expert (<= 32: one per lane)
+constexpr int HB_STRIDE = NCU + 1;
+constexpr int CW = 8;            // consumer warps
+constexpr int THREADS = (CW + 1) * 32;
 
 struct GluArgs {
     const uint8_t *wg, *wu;   // [E][I][rowbytes]
@@ -49,79 +62,98 @@ struct GluArgs {
     const int32_t *routes;    // [T*k]
     float *h;                 // [T*k+T][I]
     uint32_t *hq;             // [T*k+T][I/32] q8_1 blocks
+    unsigned int *group_cnt;  // [nv_max * I/32] zero-initialized counters
     int T, k, E, H, I;
     float clamp;
     int nb, rowbytes;
-    int S;   // row pairs per stage (divides 32)
-    int NS;  // stages in the ring
-    int ncu; // columns per virtual expert
+    int RU; // rows per part (divides 32)
+    int CL; // parts per 32-row group
+    int NS; // stages (one part each) in the ring
 };
 
-struct Unit {
+struct Part {
     const uint8_t *g, *u; // gate / up rows of this virtual expert
+    int v;                // virtual expert
     int e;                // expert (E = shared)
     int col0, ncols;      // column range within the expert's routes / tokens
-    int grp;              // 32-row group
+    int grp, p;           // 32-row group, part within the group
 };
 
-__device__ __forceinline__ Unit decode_unit(const GluArgs &a, const int *vpre, int NVr, long long u)
+__device__ __forceinline__ Part decode_part(const GluArgs &a, const int *vpre, int NVr, long long u)
 {
     const int G = a.I / 32;
-    const int v = (int)(u / G);
-    Unit r;
-    r.grp = (int)(u % G);
-    if (v < NVr) {
-        // the largest e with vpre[e] <= v is the expert owning virtual expert v
+    const long long per_v = (long long)G * a.CL;
+    Part r;
+    r.v = (int)(u / per_v);
+    const int rem = (int)(u % per_v);
+    r.grp = rem / a.CL;
+    r.p = rem % a.CL;
+    if (r.v < NVr) {
+        // the largest e with vpre[e] <= v owns virtual expert v
         int lo = 0, hi = a.E - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (vpre[mid] <= v)
+            if (vpre[mid] <= r.v)
                 lo = mid;
             else
                 hi = mid - 1;
         }
         r.e = lo;
-        r.col0 = (v - vpre[lo]) * a.ncu;
-        const int cnt = a.offsets[lo + 1] - a.offsets[lo];
-        r.ncols = min(a.ncu, cnt - r.col0);
+        r.col0 = (r.v - vpre[lo]) * NCU;
+        r.ncols = min(NCU, a.offsets[lo + 1] - a.offsets[lo] - r.col0);
         r.g = a.wg + (size_t)lo * a.I * a.rowbytes;
         r.u = a.wu + (size_t)lo * a.I * a.rowbytes;
     } else {
         r.e = a.E;
-        r.col0 = (v - NVr) * a.ncu;
-        r.ncols = min(a.ncu, a.T - r.col0);
+        r.col0 = (r.v - NVr) * NCU;
+        r.ncols = min(NCU, a.T - r.col0);
         r.g = a.wsg;
         r.u = a.wsu;
     }
     return r;
 }
 
-template <int CW, int NC>
-__global__ void __launch_bounds__((CW + 1) * 32) k_glu_pair(const GluArgs a)
+template <int NC>
+__global__ void __launch_bounds__(THREADS, 1) k_glu_pair(const GluArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    const int stage_bytes = 2 * a.S * a.rowbytes;
+    const int half_bytes = a.RU * a.rowbytes;
+    const int stage_bytes = 2 * half_bytes;
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.NS * stage_bytes);
     uint64_t *empty = full + a.NS;
-    int *vpre = reinterpret_cast<int *>(empty + a.NS); // [E + 1]
-    float *hbuf = reinterpret_cast<float *>(vpre + a.E + 1 + 1);
-    __shared__ int s_abort;
+    int *vpre = reinterpret_cast<int *>(empty + a.NS);    // [E + 1]
+    int *col_r = vpre + a.E + 1;                          // [NCU]: h row of each column
+    float *hbuf = reinterpret_cast<float *>(col_r + NCU); // [32][HB_STRIDE]
+    __shared__ int s_abort, s_last;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wpart = min(a.S, CW); // consumer warps that touch one stage
     if (tid == 0) {
         for (int s = 0; s < a.NS; s++) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], wpart);
+            mbar_init(&empty[s], CW);
         }
         fence_mbar_init();
         s_abort = 0;
     }
+    // Before the grouping has finished: warm L2 with this CTA's slice of the
+    // shared expert (needed whatever the routing), then wait for it.
+    if (a.wsg && warp == CW && lane == 0) {
+        const size_t total = (size_t)a.I * a.rowbytes; // multiple of 16
+        const size_t chunk = ((total / gridDim.x) + 15) & ~size_t(15);
+        const size_t off = chunk * blockIdx.x;
+        if (off < total) {
+            const uint32_t n = (uint32_t)min(chunk, total - off);
+            prefetch_l2(a.wsg + off, n);
+            prefetch_l2(a.wsu + off, n);
+        }
+    }
+    pdl_wait();
+    pdl_trigger();
     // virtual experts per expert, then an inclusive scan: vpre[e] = first v of e
     for (int e = tid; e < a.E; e += blockDim.x) {
         const int cnt = a.offsets[e + 1] - a.offsets[e];
-        vpre[e + 1] = (cnt + a.ncu - 1) / a.ncu;
+        vpre[e + 1] = (cnt + NCU - 1) / NCU;
     }
     __syncthreads();
     if (warp == 0) {
@@ -145,39 +177,32 @@ __global__ void __launch_bounds__((CW + 1) * 32) k_glu_pair(const GluArgs a)
     __syncthreads();
 
     const int NVr = vpre[a.E];
-    const int NV = NVr + (a.wsg ? (a.T + a.ncu - 1) / a.ncu : 0);
-    const long long N = (long long)NV * (a.I / 32);
+    const int NV = NVr + (a.wsg ? (a.T + NCU - 1) / NCU : 0);
+    const int G = a.I / 32;
+    const long long N = (long long)NV * G * a.CL;
     const long long u0 = N * blockIdx.x / gridDim.x, u1 = N * (blockIdx.x + 1) / gridDim.x;
-    const int STG = 32 / a.S;
 
     if (warp == CW) {
-        // ---------------- producer: one thread streams the rows ----------------
+        // ---------------- producer: one thread streams the parts ----------------
         if (lane != 0)
             return;
         const uint64_t pol = l2_evict_first_policy();
-        const uint32_t half = (uint32_t)(a.S * a.rowbytes);
         uint32_t q = 0;
-        bool ok = true;
-        for (long long u = u0; u < u1 && ok; u++) {
-            const Unit un = decode_unit(a, vpre, NVr, u);
-            for (int s = 0; s < STG; s++, q++) {
-                const uint32_t slot = q % a.NS, use = q / a.NS;
-                if (use > 0 && !mbar_wait_bounded(&empty[slot], (use - 1) & 1u)) {
-                    atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
-                    *(volatile int *)&s_abort = 1;
-                    ok = false;
-                    break;
-                }
-                if (*(volatile int *)&s_abort) {
-                    ok = false;
-                    break;
-                }
-                const size_t row0 = (size_t)un.grp * 32 + (size_t)s * a.S;
-                uint8_t *dst = ring + (size_t)slot * stage_bytes;
-                mbar_arrive_expect_tx(&full[slot], 2 * half);
-                bulk_copy_g2s(dst, un.g + row0 * a.rowbytes, half, &full[slot], pol);
-                bulk_copy_g2s(dst + half, un.u + row0 * a.rowbytes, half, &full[slot], pol);
+        for (long long u = u0; u < u1; u++, q++) {
+            const Part pt = decode_part(a, vpre, NVr, u);
+            const uint32_t slot = q % a.NS, use = q / a.NS;
+            if (use > 0 && !mbar_wait_bounded(&empty[slot], (use - 1) & 1u)) {
+                atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
+                *(volatile int *)&s_abort = 1;
+                break;
             }
+            if (*(volatile int *)&s_abort)
+                break;
+            const size_t row0 = (size_t)pt.grp * 32 + (size_t)pt.p * a.RU;
+            uint8_t *dst = ring + (size_t)slot * stage_bytes;
+            mbar_arrive_expect_tx(&full[slot], (uint32_t)stage_bytes);
+            bulk_copy_g2s(dst, pt.g + row0 * a.rowbytes, (uint32_t)half_bytes, &full[slot], pol);
+            bulk_copy_g2s(dst + half_bytes, pt.u + row0 * a.rowbytes, (uint32_t)half_bytes, &full[slot], pol);
         }
         // no bulk copy may still be writing shared memory when the CTA exits
         const uint32_t n_slots = (q < (uint32_t)a.NS ? q : (uint32_t)a.NS);
@@ -192,94 +217,137 @@ __global__ void __launch_bounds__((CW + 1) * 32) k_glu_pair(const GluArgs a)
     // ---------------- consumers ----------------
     const int cthreads = CW * 32;
     bool dead = false;
+    int cur_v = -1;
+    int my_t = 0; // lane c holds column c's token
     uint32_t q = 0;
-    for (long long u = u0; u < u1; u++) {
-        const Unit un = decode_unit(a, vpre, NVr, u);
-        // lane c holds column c: its token t and its h row r
-        int my_t = 0, my_r = 0;
-        if (lane < un.ncols) {
-            if (un.e < a.E) {
-                my_r = a.routes[a.offsets[un.e] + un.col0 + lane];
-                my_t = my_r / a.k;
-            } else {
-                my_t = un.col0 + lane;
-                my_r = a.T * a.k + my_t;
-            }
-        }
-        for (int s = 0; s < STG; s++, q++) {
-            const uint32_t slot = q % a.NS, use = q / a.NS;
-            // this warp's row pairs in the stage: p = s*S + i with p % CW == warp
-            const int first = ((warp - s * a.S) % CW + CW) % CW;
-            if (first >= a.S)
-                continue;
-            if (!dead && *(volatile int *)&s_abort)
-                dead = true;
-            if (!dead) {
-                const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], use & 1u));
-                if (!got) {
-                    if (lane == 0) {
-                        atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
-                        *(volatile int *)&s_abort = 1;
-                    }
-                    dead = true;
+    for (long long u = u0; u < u1; u++, q++) {
+        const Part pt = decode_part(a, vpre, NVr, u);
+        if (pt.v != cur_v) {
+            cur_v = pt.v;
+            int my_r = 0;
+            my_t = 0;
+            if (lane < pt.ncols) {
+                if (pt.e < a.E) {
+                    my_r = a.routes[a.offsets[pt.e] + pt.col0 + lane];
+                    my_t = my_r / a.k;
+                } else {
+                    my_t = pt.col0 + lane;
+                    my_r = a.T * a.k + my_t;
                 }
             }
-            if (!dead) {
-                const uint8_t *st = ring + (size_t)slot * stage_bytes;
-                for (int i = first; i < a.S; i += CW) {
-                    const int p = s * a.S + i; // row within the 32-row group
-                    const uint8_t *grow = st + (size_t)i * a.rowbytes;
-                    const uint8_t *urow = st + (size_t)(a.S + i) * a.rowbytes;
-                    for (int c0 = 0; c0 < un.ncols; c0 += NC) {
-                        const int nc = min(NC, un.ncols - c0);
-                        int tcol[NC];
+            if (warp == 0 && lane < pt.ncols)
+                col_r[lane] = my_r;
+            // warm L1 with the activation blocks this lane will read
+            for (int c = 0; c < pt.ncols; c++) {
+                const int t = __shfl_sync(0xffffffffu, my_t, c);
+                for (int b = lane; b < a.nb; b += 32) {
+                    const uint32_t *w = a.xq + ((size_t)t * a.nb + b) * Q8_1_WORDS;
+                    asm volatile("prefetch.global.L1 [%0];" ::"l"(w));
+                    asm volatile("prefetch.global.L1 [%0];" ::"l"(w + 8));
+                }
+            }
+            named_barrier(1, cthreads); // col_r visible to every consumer warp
+        }
+        const uint32_t slot = q % a.NS, use = q / a.NS;
+        if (!dead && *(volatile int *)&s_abort)
+            dead = true;
+        if (!dead) {
+            const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], use & 1u));
+            if (!got) {
+                if (lane == 0) {
+                    atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
+                    *(volatile int *)&s_abort = 1;
+                }
+                dead = true;
+            }
+        }
+        if (!dead) {
+            const uint8_t *st = ring + (size_t)slot * stage_bytes;
+            for (int i = warp; i < a.RU; i += CW) {
+                const int prow = pt.p * a.RU + i; // row within the 32-row group
+                const uint8_t *grow = st + (size_t)i * a.rowbytes;
+                const uint8_t *urow = st + half_bytes + (size_t)i * a.rowbytes;
+                for (int c0 = 0; c0 < pt.ncols; c0 += NC) {
+                    const int nc = min(NC, pt.ncols - c0);
+                    int tcol[NC];
 #pragma unroll
-                        for (int c = 0; c < NC; c++)
-                            tcol[c] = __shfl_sync(0xffffffffu, my_t, c0 + (c < nc ? c : 0));
-                        float ag[NC], au[NC];
+                    for (int c = 0; c < NC; c++)
+                        tcol[c] = __shfl_sync(0xffffffffu, my_t, c0 + (c < nc ? c : 0));
+                    float ag[NC], au[NC];
 #pragma unroll
-                        for (int c = 0; c < NC; c++)
-                            ag[c] = au[c] = 0.0f;
-                        for (int b = lane; b < a.nb; b += 32) {
-                            Q80Block gb, ub;
-                            load_q8_0_smem(grow, b, gb);
-                            load_q8_0_smem(urow, b, ub);
-#pragma unroll
-                            for (int c = 0; c < NC; c++) {
-                                if (c < nc) {
-                                    Q81Block xb;
-                                    load_q8_1_global(a.xq + ((size_t)tcol[c] * a.nb + b) * Q8_1_WORDS, xb);
-                                    const int sg = dot_q8_block(gb.q, xb.q);
-                                    const int su = dot_q8_block(ub.q, xb.q);
-                                    ag[c] = fmaf(gb.d * xb.d, (float)sg, ag[c]);
-                                    au[c] = fmaf(ub.d * xb.d, (float)su, au[c]);
-                                }
-                            }
-                        }
+                    for (int c = 0; c < NC; c++)
+                        ag[c] = au[c] = 0.0f;
+                    for (int b = lane; b < a.nb; b += 32) {
+                        Q80Block gb, ub;
+                        load_q8_0_smem(grow, b, gb);
+                        load_q8_0_smem(urow, b, ub);
 #pragma unroll
                         for (int c = 0; c < NC; c++) {
                             if (c < nc) {
-                                const float g = warp_sum(ag[c]);
-                                const float uu = warp_sum(au[c]);
-                                if (lane == 0)
-                                    hbuf[p * HB_STRIDE + c0 + c] = swiglu(g, uu, a.clamp);
+                                Q81Block xb;
+                                load_q8_1_global(a.xq + ((size_t)tcol[c] * a.nb + b) * Q8_1_WORDS, xb);
+                                const int sg = dot_q8_block(gb.q, xb.q);
+                                const int su = dot_q8_block(ub.q, xb.q);
+                                ag[c] = fmaf(gb.d * xb.d, (float)sg, ag[c]);
+                                au[c] = fmaf(ub.d * xb.d, (float)su, au[c]);
                             }
+                        }
+                    }
+#pragma unroll
+                    for (int c = 0; c < NC; c++) {
+                        if (c < nc) {
+                            const float g = warp_sum(ag[c]);
+                            const float uu = warp_sum(au[c]);
+                            if (lane == 0)
+                                hbuf[prow * HB_STRIDE + c0 + c] = swiglu(g, uu, a.clamp);
                         }
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0 && !dead)
-                mbar_arrive(&empty[slot]);
         }
+        __syncwarp();
+        if (lane == 0 && !dead)
+            mbar_arrive(&empty[slot]);
         named_barrier(1, cthreads);
-        if (!dead && !*(volatile int *)&s_abort) {
-            // epilogue: per column, the 32 h values of this row group -> h, hq
-            for (int c = warp; c < un.ncols; c += CW) {
-                const int r = __shfl_sync(0xffffffffu, my_r, c);
-                const float v = hbuf[lane * HB_STRIDE + c];
-                a.h[(size_t)r * a.I + (size_t)un.grp * 32 + lane] = v;
-                quantize_q8_1_warp(v, a.hq + ((size_t)r * (a.I / 32) + un.grp) * Q8_1_WORDS, lane);
+        const bool ok = !dead && !*(volatile int *)&s_abort;
+        // h rows of this part -> global memory
+        if (ok) {
+            for (int idx = tid; idx < a.RU * pt.ncols; idx += cthreads) {
+                const int i = idx % a.RU, c = idx / a.RU;
+                const int prow = pt.p * a.RU + i;
+                a.h[(size_t)col_r[c] * a.I + (size_t)pt.grp * 32 + prow] = hbuf[prow * HB_STRIDE + c];
+            }
+        }
+        // quantize the group once all its parts are done
+        const long long gfirst = u - pt.p;
+        const bool whole = gfirst >= u0 && gfirst + a.CL <= u1;
+        if (whole) {
+            if (pt.p == a.CL - 1 && ok) {
+                for (int c = warp; c < pt.ncols; c += CW) {
+                    const int r = col_r[c];
+                    const float v = hbuf[lane * HB_STRIDE + c];
+                    quantize_q8_1_warp(v, a.hq + ((size_t)r * G + pt.grp) * Q8_1_WORDS, lane);
+                }
+            }
+        } else {
+            __threadfence();
+            named_barrier(1, cthreads);
+            if (tid == 0) {
+                unsigned int *cnt = a.group_cnt + (size_t)pt.v * G + pt.grp;
+                const unsigned int old = ok ? atomicAdd(cnt, 1u) : 0u;
+                const bool last = ok && old == (unsigned)(a.CL - 1);
+                if (last)
+                    *cnt = 0u; // every part has arrived: reset for the next call
+                s_last = last ? 1 : 0;
+            }
+            named_barrier(1, cthreads);
+            if (s_last) {
+                __threadfence();
+                for (int c = warp; c < pt.ncols; c += CW) {
+                    const int r = col_r[c];
+                    const float v = __ldcg(&a.h[(size_t)r * a.I + (size_t)pt.grp * 32 + lane]);
+                    quantize_q8_1_warp(v, a.hq + ((size_t)r * G + pt.grp) * Q8_1_WORDS, lane);
+                }
             }
         }
         named_barrier(1, cthreads);
@@ -287,48 +355,48 @@ __global__ void __launch_bounds__((CW + 1) * 32) k_glu_pair(const GluArgs a)
 }
 
 // Per template instance and device: the dynamic shared memory the kernel may
-// use and its occupancy at that size (cached, so that steady-state calls make
-// no attribute or occupancy queries).
-struct LaunchCache {
-    size_t smem = 0;
-    int occ = 0;
-};
-
-template <int CW, int NC>
-luce_status launch_glu(const GluArgs &a, cudaStream_t stream, int grid_cap)
+// use (cached, so that steady-state calls make no attribute calls).
+template <int NC>
+luce_status launch_glu(const GluArgs &a, cudaStream_t stream, size_t smem)
 {
-    static LaunchCache cache[64];
-    auto kern = k_glu_pair<CW, NC>;
-    const size_t smem = (size_t)a.NS * 2 * a.S * a.rowbytes + (size_t)2 * a.NS * sizeof(uint64_t) +
-                        (size_t)(a.E + 2) * sizeof(int) + (size_t)32 * HB_STRIDE * sizeof(float);
+    static size_t smem_set[64] = {0};
+    auto kern = k_glu_pair<NC>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return LUCE_ERR_CUDA;
-    LaunchCache &c = cache[dev];
-    if (c.smem != smem) {
+    if (smem_set[dev] < smem) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return LUCE_ERR_CUDA;
-        int occ = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, (CW + 1) * 32, smem) != cudaSuccess ||
-            occ < 1)
-            return LUCE_ERR_CUDA;
-        c.smem = smem;
-        c.occ = occ;
+        smem_set[dev] = smem;
     }
-    const int grid = std::max(1, std::min(grid_cap, luce_host::sm_count() * c.occ));
-    kern<<<grid, (CW + 1) * 32, smem, stream>>>(a);
-    return luce_host::launch_status();
+    return luce_host::launch(kern, dim3(luce_host::sm_count()), dim3(THREADS), smem, stream, a);
+}
+
+// Upper bound of the number of virtual experts of a call.
+long long max_virtual_experts(int T, int k, int E, bool shared)
+{
+    const long long Tk = (long long)T * k;
+    return std::min<long long>(E, Tk) + Tk / NCU + (shared ? (T + NCU - 1) / NCU : 0);
 }
 
 } // namespace
 
 using namespace luce_host;
 
+extern "C" size_t luce_moe_glu_workspace_bytes(int T, int k, int E, int I)
+{
+    if (T <= 0 || k <= 0 || E <= 0 || I <= 0)
+        return 0;
+    // counters per (virtual expert, 32-row group), with or without the shared expert
+    return (size_t)max_virtual_experts(T, k, E, true) * (size_t)(I / 32) * sizeof(unsigned int);
+}
+
 extern "C" luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const luce_block_q8_0 *w_up,
                                          const luce_block_q8_0 *ws_gate, const luce_block_q8_0 *ws_up,
                                          const luce_block_q8_1 *xq, const int32_t *offsets, const int32_t *routes,
                                          int T, int k, int E, int H, int I, float clamp, float *h,
-                                         luce_block_q8_1 *hq, int variant, void *stream)
+                                         luce_block_q8_1 *hq, void *workspace, size_t workspace_bytes, int variant,
+                                         void *stream)
 {
     if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 64 || (int64_t)T * k > (1 << 20))
         return LUCE_ERR_INVALID_ARG;
@@ -338,10 +406,13 @@ extern "C" luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const lu
         return LUCE_ERR_INVALID_ARG;
     if (T == 0)
         return LUCE_OK;
-    if (!w_gate || !w_up || !xq || !offsets || !routes || !h || !hq)
+    if (!w_gate || !w_up || !xq || !offsets || !routes || !h || !hq || !workspace)
         return LUCE_ERR_INVALID_ARG;
     if (!aligned(w_gate, 16) || !aligned(w_up, 16) || (ws_gate && (!aligned(ws_gate, 16) || !aligned(ws_up, 16))) ||
-        !aligned(xq, 16) || !aligned(hq, 16) || !aligned(h, 4) || !aligned(offsets, 4) || !aligned(routes, 4))
+        !aligned(xq, 16) || !aligned(hq, 16) || !aligned(h, 4) || !aligned(offsets, 4) || !aligned(routes, 4) ||
+        !aligned(workspace, 4))
+        return LUCE_ERR_INVALID_ARG;
+    if (workspace_bytes < luce_moe_glu_workspace_bytes(T, k, E, I))
         return LUCE_ERR_INVALID_ARG;
 
     GluArgs a;
@@ -354,6 +425,7 @@ extern "C" luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const lu
     a.routes = routes;
     a.h = h;
     a.hq = reinterpret_cast<uint32_t *>(hq);
+    a.group_cnt = reinterpret_cast<unsigned int *>(workspace);
     a.T = T;
     a.k = k;
     a.E = E;
@@ -362,26 +434,26 @@ extern "C" luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const lu
     a.clamp = clamp;
     a.nb = H / 32;
     a.rowbytes = a.nb * Q8_0_BYTES;
-    a.ncu = NCU_MAX;
-    // stage = S gate rows + S up rows, about 16-32 KB; ring of about 96 KB
-    int S = 1;
-    while (S < 32 && 2 * (2 * S) * a.rowbytes <= 36 * 1024)
-        S *= 2;
-    a.S = S;
-    const int stage = 2 * S * a.rowbytes;
-    a.NS = std::max(2, std::min(8, (96 * 1024) / stage));
-    // an upper bound on the number of units, to size the grid
-    const long long Tk = (long long)T * k;
-    const long long nv_up = std::min<long long>(E, Tk) + Tk / NCU_MAX + (ws_gate ? (T + NCU_MAX - 1) / NCU_MAX : 0);
-    const long long units = nv_up * (I / 32);
-    const int cap = (int)std::min<long long>(units, INT_MAX);
-    const int maxcols = std::min(T, NCU_MAX);
+    // a part (RU gate rows + RU up rows) of about 70 KB; three of them in flight
+    int RU = 32;
+    while (RU > 1 && 2 * RU * a.rowbytes > 72 * 1024)
+        RU /= 2;
+    a.RU = RU;
+    a.CL = 32 / RU;
+    const size_t stage = (size_t)2 * RU * a.rowbytes;
+    const size_t fixed = (size_t)(E + 1 + NCU) * sizeof(int) + (size_t)32 * HB_STRIDE * sizeof(float) + 64;
+    const size_t budget = 220 * 1024;
+    int NS = (int)std::min<size_t>(8, (budget - fixed) / (stage + 16));
+    NS = std::max(NS, 2);
+    a.NS = NS;
+    const size_t smem = (size_t)NS * stage + (size_t)2 * NS * sizeof(uint64_t) + fixed;
+    const int maxcols = std::min(T, NCU);
     cudaStream_t st = as_stream(stream);
     if (maxcols <= 1)
-        return launch_glu<4, 1>(a, st, cap);
+        return launch_glu<1>(a, st, smem);
     if (maxcols <= 2)
-        return launch_glu<4, 2>(a, st, cap);
+        return launch_glu<2>(a, st, smem);
     if (maxcols <= 4)
-        return launch_glu<4, 4>(a, st, cap);
-    return launch_glu<4, 8>(a, st, cap);
+        return launch_glu<4>(a, st, smem);
+    return launch_glu<8>(a, st, smem);
 }

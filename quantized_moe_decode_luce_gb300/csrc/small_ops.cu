@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(ROUTE_WARPS * 32)
                  int32_t *__restrict__ ids, float *__restrict__ weights)
 {
     extern __shared__ float s_scores[];
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * ROUTE_WARPS + warp;
     if (t >= T)
@@ -96,6 +98,8 @@ constexpr int QUANT_WARPS = 8;
 __global__ void __launch_bounds__(QUANT_WARPS * 32)
     k_quantize_q8_1(const float *__restrict__ x, int64_t n_blocks, uint32_t *__restrict__ out)
 {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t b = (int64_t)blockIdx.x * QUANT_WARPS + (threadIdx.x >> 5);
     if (b >= n_blocks)
@@ -113,13 +117,11 @@ __global__ void __launch_bounds__(QUANT_WARPS * 32)
 // order (match + popcount), then the group's last lane advances the base.
 constexpr int GROUP_THREADS = 1024;
 
-__global__ void __launch_bounds__(GROUP_THREADS)
-    k_moe_group(const int32_t *__restrict__ ids, int R, int E, int nw, int32_t *__restrict__ counts,
-                int32_t *__restrict__ offsets, int32_t *__restrict__ routes)
+// The grouping by one CTA of GROUP_THREADS threads.  ids_src may be global or
+// shared memory; hist [nw*E] and excl [E+1] are shared scratch.
+__device__ void group_body(const int32_t *ids_src, int R, int E, int nw, int *hist, int *excl,
+                           int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ routes)
 {
-    extern __shared__ int s_mem[];
-    int *hist = s_mem;           // [nw][E]: counts, then running bases
-    int *excl = s_mem + nw * E;  // [E + 1]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int i = tid; i < nw * E; i += blockDim.x)
         hist[i] = 0;
@@ -128,7 +130,7 @@ __global__ void __launch_bounds__(GROUP_THREADS)
     const int r0 = warp * seg, r1 = min(R, r0 + seg);
     if (warp < nw) {
         for (int r = r0 + lane; r < r1; r += 32) {
-            const int e = ids[r];
+            const int e = ids_src[r];
             if (e >= 0 && e < E)
                 atomicAdd(&hist[warp * E + e], 1);
             else if (e >= E)
@@ -179,7 +181,7 @@ __global__ void __launch_bounds__(GROUP_THREADS)
         const unsigned lt = (1u << lane) - 1u;
         for (int base = r0; base < r1; base += 32) {
             const int r = base + lane;
-            const int e = r < r1 ? ids[r] : -1;
+            const int e = r < r1 ? ids_src[r] : -1;
             const bool ok = e >= 0 && e < E;
             const unsigned m = __match_any_sync(0xffffffffu, ok ? e : -1);
             int pos = 0;
@@ -197,6 +199,116 @@ __global__ void __launch_bounds__(GROUP_THREADS)
     const int total = excl[E];
     for (int r = total + tid; r < R; r += blockDim.x)
         routes[r] = -1;
+}
+
+__global__ void __launch_bounds__(GROUP_THREADS)
+    k_moe_group(const int32_t *__restrict__ ids, int R, int E, int nw, int32_t *__restrict__ counts,
+                int32_t *__restrict__ offsets, int32_t *__restrict__ routes)
+{
+    extern __shared__ int s_mem[];
+    pdl_wait();
+    pdl_trigger();
+    group_body(ids, R, E, nw, s_mem, s_mem + nw * E, counts, offsets, routes);
+}
+
+// ---------------------------------------------------------------------------
+// Fused prep: router select + weights, q8_1 quantization of the FFN input
+// and expert grouping in ONE launch of one CTA ([PR826], commit "fused DS4.1
+// decode kernels": the router's select and weights in one launch, one
+// expert grouping per layer, the q8_1 activation memo).  For T <= 32 tokens
+// and E <= 256 experts: warp t routes token t with its scores in registers
+// (EPL per lane), all 32 warps then quantize the T*H/32 blocks, and after a
+// CTA barrier the same CTA groups the routes from shared memory.
+struct PrepArgs {
+    const float *logits, *bias, *x;
+    int T, E, k, H;
+    int32_t *ids;
+    float *weights;
+    uint32_t *xq;
+    int32_t *counts, *offsets, *routes;
+};
+
+template <int EPL>
+__device__ __forceinline__ void route_token_regs(const float *__restrict__ l, const float *__restrict__ bias, int E,
+                                                 int k, int32_t *ids_s, int32_t *ids_g, float *w_g, int lane)
+{
+    float sc[EPL];
+    uint32_t taken = 0;
+#pragma unroll
+    for (int i = 0; i < EPL; i++) {
+        const int e = lane + 32 * i;
+        if (e < E)
+            sc[i] = bias ? __fadd_rn(l[e], bias[e]) : l[e];
+        else {
+            sc[i] = 0.0f;
+            taken |= 1u << i;
+        }
+    }
+    float sel0 = 0.0f, sel1 = 0.0f;
+    for (int j = 0; j < k; j++) {
+        float bv = 0.0f;
+        int bi = INT_MAX;
+#pragma unroll
+        for (int i = 0; i < EPL; i++) {
+            if (!((taken >> i) & 1u) && (bi == INT_MAX || sc[i] > bv)) {
+                bv = sc[i];
+                bi = lane + 32 * i;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (oi != INT_MAX && (bi == INT_MAX || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane)
+            taken |= 1u << (bi >> 5);
+        if (lane == 0) {
+            ids_s[j] = bi;
+            ids_g[j] = bi;
+        }
+        if (j == lane)
+            sel0 = l[bi];
+        else if (j == lane + 32)
+            sel1 = l[bi];
+    }
+    const bool has0 = lane < k, has1 = lane + 32 < k;
+    float m = has0 ? sel0 : -INFINITY;
+    if (has1)
+        m = fmaxf(m, sel1);
+    m = warp_max(m);
+    const float e0 = has0 ? expf(__fsub_rn(sel0, m)) : 0.0f;
+    const float e1 = has1 ? expf(__fsub_rn(sel1, m)) : 0.0f;
+    const float den = warp_sum(__fadd_rn(e0, e1));
+    if (has0)
+        w_g[lane] = __fdiv_rn(e0, den);
+    if (has1)
+        w_g[lane + 32] = __fdiv_rn(e1, den);
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(GROUP_THREADS) k_moe_prep(const PrepArgs a)
+{
+    extern __shared__ int s_mem[];
+    int *ids_s = s_mem;                  // [T*k]
+    int *hist = ids_s + a.T * a.k;       // [32*E]
+    int *excl = hist + 32 * a.E;         // [E+1]
+    pdl_wait();
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < a.T) {
+        const size_t o = (size_t)warp * a.k;
+        route_token_regs<EPL>(a.logits + (size_t)warp * a.E, a.bias, a.E, a.k, ids_s + o, a.ids + o,
+                              a.weights + o, lane);
+    }
+    const int nbl = a.T * (a.H / QK);
+    for (int b = warp; b < nbl; b += 32)
+        quantize_q8_1_warp(a.x[(size_t)b * QK + lane], a.xq + (size_t)b * Q8_1_WORDS, lane);
+    __syncthreads();
+    group_body(ids_s, a.T * a.k, a.E, 32, hist, excl, a.counts, a.offsets, a.routes);
 }
 
 // ---------------------------------------------------------------------------
@@ -252,6 +364,8 @@ __global__ void __launch_bounds__(ARGMAX_THREADS)
     k_argmax(const float *__restrict__ logits, int64_t V, int64_t L, int C, bool vec4, ArgPair *__restrict__ pairs,
              unsigned int *__restrict__ counters, int32_t *__restrict__ idx, float *__restrict__ val)
 {
+    pdl_wait();
+    pdl_trigger();
     const int c = blockIdx.x, r = blockIdx.y;
     const int64_t lo = (int64_t)c * L, hi = min(V, lo + L);
     const float *row = logits + (int64_t)r * V;
@@ -323,6 +437,9 @@ extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault
 extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault_down(unsigned int *bits);
 
 namespace luce_host {
+static int g_pdl = 0;
+bool pdl_enabled() { return __atomic_load_n(&g_pdl, __ATOMIC_RELAXED) != 0; }
+
 int sm_count()
 {
     static int cached[64] = {0};
@@ -356,7 +473,13 @@ extern "C" const char *luce_status_string(luce_status s)
     return "unknown status";
 }
 
-extern "C" int luce_version(void) { return 100; }
+extern "C" int luce_version(void) { return 200; }
+
+extern "C" luce_status luce_set_pdl(int enable)
+{
+    __atomic_store_n(&luce_host::g_pdl, enable ? 1 : 0, __ATOMIC_RELAXED);
+    return LUCE_OK;
+}
 
 extern "C" luce_status luce_get_fault(unsigned int *bits)
 {
@@ -383,8 +506,8 @@ extern "C" luce_status luce_route_topk(const float *logits, const float *bias, i
         return LUCE_ERR_INVALID_ARG;
     const int blocks = (T + ROUTE_WARPS - 1) / ROUTE_WARPS;
     const size_t smem = (size_t)ROUTE_WARPS * E * sizeof(float);
-    k_route_topk<<<blocks, ROUTE_WARPS * 32, smem, as_stream(stream)>>>(logits, bias, T, E, k, ids, weights);
-    return launch_status();
+    return launch(k_route_topk, dim3(blocks), dim3(ROUTE_WARPS * 32), smem, as_stream(stream), logits, bias, T, E,
+                  k, ids, weights);
 }
 
 extern "C" luce_status luce_quantize_q8_1(const float *x, int T, int K, luce_block_q8_1 *xq, void *stream)
@@ -399,9 +522,8 @@ extern "C" luce_status luce_quantize_q8_1(const float *x, int T, int K, luce_blo
     const int64_t blocks = (nb + QUANT_WARPS - 1) / QUANT_WARPS;
     if (blocks > INT_MAX)
         return LUCE_ERR_INVALID_ARG;
-    k_quantize_q8_1<<<(unsigned)blocks, QUANT_WARPS * 32, 0, as_stream(stream)>>>(
-        x, nb, reinterpret_cast<uint32_t *>(xq));
-    return launch_status();
+    return launch(k_quantize_q8_1, dim3((unsigned)blocks), dim3(QUANT_WARPS * 32), 0, as_stream(stream), x, nb,
+                  reinterpret_cast<uint32_t *>(xq));
 }
 
 extern "C" luce_status luce_moe_group(const int32_t *ids, int T, int k, int E, int32_t *counts, int32_t *offsets,
@@ -416,8 +538,8 @@ extern "C" luce_status luce_moe_group(const int32_t *ids, int T, int k, int E, i
     const int R = T * k;
     const int nw = std::max(1, std::min(32, 8192 / E));
     const size_t smem = ((size_t)nw * E + E + 1) * sizeof(int);
-    k_moe_group<<<1, GROUP_THREADS, smem, as_stream(stream)>>>(ids, R, E, nw, counts, offsets, routes);
-    return launch_status();
+    return launch(k_moe_group, dim3(1), dim3(GROUP_THREADS), smem, as_stream(stream), ids, R, E, nw, counts, offsets,
+                  routes);
 }
 
 extern "C" size_t luce_argmax_workspace_bytes(int R, int64_t V)
@@ -450,6 +572,41 @@ extern "C" luce_status luce_argmax(const float *logits, int R, int64_t V, int32_
         reinterpret_cast<unsigned int *>(reinterpret_cast<uint8_t *>(workspace) + argmax_pairs_bytes(R, C));
     const bool vec4 = (V % 4 == 0) && aligned(logits, 16);
     dim3 grid((unsigned)C, (unsigned)R);
-    k_argmax<<<grid, ARGMAX_THREADS, 0, as_stream(stream)>>>(logits, V, L, C, vec4, pairs, counters, idx, val);
-    return launch_status();
+    return launch(k_argmax, grid, dim3(ARGMAX_THREADS), 0, as_stream(stream), logits, V, L, C, vec4, pairs, counters,
+                  idx, val);
+}
+
+extern "C" luce_status luce_moe_prep(const float *logits, const float *bias, const float *x, int T, int E, int k, int H,
+                                     int32_t *ids, float *weights, luce_block_q8_1 *xq, int32_t *counts,
+                                     int32_t *offsets, int32_t *routes, void *stream)
+{
+    if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E || k > 64 || H <= 0 || H % QK != 0 ||
+        (int64_t)T * k > (1 << 20))
+        return LUCE_ERR_INVALID_ARG;
+    if (!counts || !offsets || !aligned(counts, 4) || !aligned(offsets, 4))
+        return LUCE_ERR_INVALID_ARG;
+    if (T > 0 && (!logits || !x || !ids || !weights || !xq || !routes || !aligned(logits, 4) || !aligned(x, 4) ||
+                  !aligned(ids, 4) || !aligned(weights, 4) || !aligned(xq, 4) || !aligned(routes, 4) ||
+                  (bias && !aligned(bias, 4))))
+        return LUCE_ERR_INVALID_ARG;
+    if (T == 0 || T > 32 || E > 256) {
+        // the general path: three launches
+        luce_status st = luce_route_topk(logits, bias, T, E, k, ids, weights, stream);
+        if (st == LUCE_OK)
+            st = luce_quantize_q8_1(x, T, H, xq, stream);
+        if (st == LUCE_OK)
+            st = luce_moe_group(ids, T, k, E, counts, offsets, routes, stream);
+        return st;
+    }
+    PrepArgs a{logits, bias, x, T, E, k, H, ids, weights, reinterpret_cast<uint32_t *>(xq), counts, offsets, routes};
+    const size_t smem = ((size_t)T * k + 32 * (size_t)E + E + 1) * sizeof(int);
+    const int epl = (E + 31) / 32;
+    cudaStream_t st = as_stream(stream);
+    if (epl <= 1)
+        return launch(k_moe_prep<1>, dim3(1), dim3(GROUP_THREADS), smem, st, a);
+    if (epl <= 2)
+        return launch(k_moe_prep<2>, dim3(1), dim3(GROUP_THREADS), smem, st, a);
+    if (epl <= 4)
+        return launch(k_moe_prep<4>, dim3(1), dim3(GROUP_THREADS), smem, st, a);
+    return launch(k_moe_prep<8>, dim3(1), dim3(GROUP_THREADS), smem, st, a);
 }

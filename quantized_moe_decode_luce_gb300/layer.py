@@ -3,7 +3,8 @@
 :class:`MoEStep` allocates (once, with torch) every intermediate buffer of
 the step for a fixed token count and runs the five calls of the step in the
 pages' order on one stream: route select + weights, q8_1 quantization of
-the FFN input, expert grouping, gate/up pair + SwiGLU, down + combine.
+the FFN input, expert grouping (one fused launch for the first three when
+it fits one CTA), gate/up pair + SwiGLU, down + combine.
 Allocation is torch's; all arithmetic is in libluce_moe's kernels.
 """
 from __future__ import annotations
@@ -29,20 +30,26 @@ class MoEStep:
         self.h = torch.empty((max(1, rows), I), dtype=torch.float32, device=dev)
         self.hq = torch.empty((max(1, rows), I // QK, Q8_1_BYTES), dtype=torch.uint8, device=dev)
         self.out = torch.empty((T, H), dtype=torch.float32, device=dev)
+        self.glu_ws = torch.zeros(max(16, B.luce_moe_glu_workspace_bytes(T, k, E, I)), dtype=torch.uint8, device=dev)
+        self.fused_prep = True
 
     def run(self, layer, x, logits, bias=None, stream=None, out=None) -> torch.Tensor:
         """layer: object with wg, wu, wd (+ wsg, wsu, wsd) uint8 CUDA tensors.
         Writes the layer output into `out` (default: this step's own buffer)."""
         out = self.out if out is None else out
         T, H, I, E, k = self.T, self.H, self.I, self.E, self.k
-        B.luce_route_topk(logits, bias, k, self.ids, self.weights, stream)
-        B.luce_quantize_q8_1(x, self.xq, stream)
-        B.luce_moe_group(self.ids, E, self.counts, self.offsets, self.routes, stream)
+        if self.fused_prep:
+            B.luce_moe_prep(logits, bias, x, k, self.ids, self.weights, self.xq, self.counts, self.offsets,
+                            self.routes, stream)
+        else:
+            B.luce_route_topk(logits, bias, k, self.ids, self.weights, stream)
+            B.luce_quantize_q8_1(x, self.xq, stream)
+            B.luce_moe_group(self.ids, E, self.counts, self.offsets, self.routes, stream)
         wsg = layer.wsg if self.shared else None
         wsu = layer.wsu if self.shared else None
         wsd = layer.wsd if self.shared else None
         B.luce_moe_glu_pair(layer.wg, layer.wu, wsg, wsu, self.xq, self.offsets, self.routes, T, k, E, H, I,
-                            self.clamp, self.h, self.hq, 0, stream)
+                            self.clamp, self.h, self.hq, self.glu_ws, 0, stream)
         B.luce_moe_down_combine(layer.wd, wsd, self.hq, self.ids, self.weights, self.offsets, self.routes,
                                 T, k, E, H, I, out, 0, stream)
         return out

@@ -144,6 +144,8 @@ GLU_CASES = [
     ("masked", 4, 3, 8, 256, 256, True, 10.0, 0.3),
     ("shared_only", 3, 2, 8, 256, 512, True, 0.0, 1.0),
     ("decode_shape", 1, 6, 64, 2048, 1024, True, 0.0, 0.0),
+    ("verify_shape_small_E", 5, 8, 12, 4096, 512, True, 10.0, 0.0),
+    ("h1024_many_groups", 3, 4, 40, 1024, 2048, False, 0.0, 0.1),
 ]
 
 
@@ -166,9 +168,12 @@ def test_glu_pair(case):
     rows = T * k + (T if shared else 0)
     h = torch.full((rows, I), float("nan"), dtype=torch.float32, device="cuda")
     hq = torch.zeros((rows, I // 32, 36), dtype=torch.uint8, device="cuda")
-    B.luce_moe_glu_pair(dev(L.wg), dev(L.wu), dev(L.wsg) if shared else None, dev(L.wsu) if shared else None,
-                        dev(xq), dev(offsets), dev(routes), T, k, E, H, I, clamp, h, hq)
-    torch.cuda.synchronize()
+    ws = torch.zeros(B.luce_moe_glu_workspace_bytes(T, k, E, I), dtype=torch.uint8, device="cuda")
+    for _ in range(2):  # the second call checks that the workspace reset itself
+        B.luce_moe_glu_pair(dev(L.wg), dev(L.wu), dev(L.wsg) if shared else None, dev(L.wsu) if shared else None,
+                            dev(xq), dev(offsets), dev(routes), T, k, E, H, I, clamp, h, hq, ws)
+        torch.cuda.synchronize()
+        assert int(ws.count_nonzero()) == 0
     hg = host(h)
     valid = ~np.isnan(h_ref[:, 0])
     assert np.isnan(hg[~valid]).all(), "rows of masked routes must not be written"
@@ -380,3 +385,61 @@ def test_argmax_bit_exact(R, V, kind):
         assert np.array_equal(host(idx), ref_i)
         assert np.array_equal(host(val).view(np.uint32), ref_v.view(np.uint32))
     assert int(am.workspace[-64:].sum()) == 0 or True
+
+
+# ----------------------------------------------------------------------------- fused prep
+@pytest.mark.parametrize("T,E,k,H,bias", [(1, 64, 6, 2048, True), (5, 128, 8, 4096, False), (32, 256, 8, 512, True),
+                                          (3, 16, 16, 256, False), (1, 1, 1, 512, False), (33, 64, 6, 256, True),
+                                          (4, 300, 7, 256, True)])
+def test_moe_prep_matches_the_three_calls(T, E, k, H, bias):
+    g = W.rng(700, T * E + k)
+    logits = g.standard_normal((T, E)).astype(np.float32)
+    x = g.standard_normal((T, H)).astype(np.float32)
+    b = (g.standard_normal(E) * 0.1).astype(np.float32) if bias else None
+    ids_ref, w_ref = oracle.route_topk(logits, b, k)
+    c_ref, o_ref, r_ref = oracle.moe_group(ids_ref, E)
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    xq = torch.empty((T, H // 32, 36), dtype=torch.uint8, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    routes = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    B.luce_moe_prep(dev(logits), dev(b) if b is not None else None, dev(x), k, ids, w, xq, counts, offsets, routes)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(ids), ids_ref)
+    assert np.abs(host(w) - w_ref).max() < 2e-6
+    assert np.array_equal(host(xq), oracle.quantize_q8_1(x))
+    assert np.array_equal(host(counts), c_ref) and np.array_equal(host(offsets), o_ref)
+    assert np.array_equal(host(routes), r_ref)
+
+
+@pytest.mark.parametrize("name", ["decode_layer", "tiny"])
+def test_layer_chain_with_programmatic_launch(name):
+    wl = W.WORKLOADS[name]
+    L = W.host_layer(wl)
+    B.luce_set_pdl(True)
+    try:
+        step, _ = _run_chain(wl, L)
+        _check_chain(wl, L, step)
+        # back-to-back steps on one stream: each one's early start must not
+        # read the previous step's buffers before they are complete
+        layer = W.DeviceLayer(dev(L.wg), dev(L.wu), dev(L.wd), dev(L.wsg) if wl.shared else None,
+                              dev(L.wsu) if wl.shared else None, dev(L.wsd) if wl.shared else None)
+        ref_out = step.out.clone()
+        for _ in range(5):
+            step.run(layer, dev(L.x), dev(L.logits), dev(L.bias) if L.bias is not None else None)
+        torch.cuda.synchronize()
+        assert torch.equal(step.out, ref_out)
+    finally:
+        B.luce_set_pdl(False)
+
+
+def test_layer_chain_unfused_prep_path():
+    wl = W.WORKLOADS["decode_layer"]
+    L = W.host_layer(wl)
+    step = MoEStep(wl.T, wl.H, wl.I, wl.E, wl.k, wl.shared, wl.clamp)
+    step.fused_prep = False
+    layer = W.DeviceLayer(dev(L.wg), dev(L.wu), dev(L.wd), dev(L.wsg), dev(L.wsu), dev(L.wsd))
+    step.run(layer, dev(L.x), dev(L.logits), dev(L.bias))
+    torch.cuda.synchronize()
+    _check_chain(wl, L, step)
