@@ -233,14 +233,17 @@ __global__ void __launch_bounds__((CW + 1) * 32) k_down_combine(const DownArgs a
 #pragma unroll
                     for (int c = 0; c < NC; c++)
                         acc[m][c] = 0.0f;
+                // warp-collective shuffles stay outside the lane-dependent block loop
+                int rr[NC];
+#pragma unroll
+                for (int c = 0; c < NC; c++)
+                    rr[c] = __shfl_sync(0xffffffffu, my_r, c0 + (c < nc ? c : 0));
                 for (int b = lane; b < a.nbI; b += 32) {
                     Q81Block xb[NC];
 #pragma unroll
-                    for (int c = 0; c < NC; c++) {
-                        const int r = __shfl_sync(0xffffffffu, my_r, c0 + (c < nc ? c : 0));
+                    for (int c = 0; c < NC; c++)
                         if (c < nc)
-                            load_q8_1_global(a.hq + ((size_t)r * a.nbI + b) * Q8_1_WORDS, xb[c]);
-                    }
+                            load_q8_1_global(a.hq + ((size_t)rr[c] * a.nbI + b) * Q8_1_WORDS, xb[c]);
 #pragma unroll
                     for (int m = 0; m < RN; m++) {
                         Q80Block wb;
