@@ -141,6 +141,15 @@ __device__ __forceinline__ void load_q8_1_global(const uint32_t *__restrict__ wo
         blk.q[i] = (int)__ldg(words + 1 + i);
 }
 
+// q8_1 block through a generic pointer (shared or global memory).
+__device__ __forceinline__ void load_q8_1_any(const uint32_t *words, Q81Block &blk)
+{
+    blk.d = half_bits_to_float(words[0]);
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        blk.q[i] = (int)words[1 + i];
+}
+
 __device__ __forceinline__ int dot_q8_block(const uint32_t (&w)[8], const int (&x)[8])
 {
     int s = 0;

@@ -50,6 +50,7 @@ struct DownArgs {
     int nbI, rowbytes;
     int TT; // tokens per tile
     int NS; // ring stages
+    int hs_rows; // activation rows staged in shared memory (0: read through L1)
 };
 
 struct VUnit {
@@ -70,7 +71,8 @@ __global__ void __launch_bounds__((CW + 1) * 32) k_down_combine(const DownArgs a
     int *vpre = reinterpret_cast<int *>(empty + a.NS); // [E + 1]
     int *vlo = vpre + a.E + 1;                         // [E]: first route of the tile
     int *vcnt = vlo + a.E;                             // [E]: routes of the tile
-    float *ybuf = reinterpret_cast<float *>(vcnt + a.E);
+    float *ybuf = reinterpret_cast<float *>(vcnt + a.E); // [TT*k + TT][RN]
+    uint32_t *hs = reinterpret_cast<uint32_t *>(ybuf + (size_t)(a.TT * a.k + a.TT) * RN); // [hs_rows][nbI][9]
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -196,6 +198,27 @@ __global__ void __launch_bounds__((CW + 1) * 32) k_down_combine(const DownArgs a
     // ---------------- consumers: wait for h, then one warp per stage ----------------
     pdl_wait();
     pdl_trigger();
+    const int xstride = a.nbI * Q8_1_WORDS; // words per activation row
+    const bool hs_on = a.hs_rows > 0;
+    if (hs_on) {
+        // stage the activation row of every y slot of the tile (routed slots of
+        // kept routes, then the shared expert's tokens) in one parallel pass
+        const int nslots = ntok * a.k + (a.wsd ? ntok : 0);
+        for (int i = tid; i < nslots * xstride; i += CW * 32) {
+            const int ys = i / xstride, w = i - ys * xstride;
+            int row;
+            if (ys < ntok * a.k) {
+                row = t0 * a.k + ys;
+                const int e = a.ids[row];
+                if (e < 0 || e >= a.E)
+                    continue;
+            } else {
+                row = a.T * a.k + t0 + (ys - ntok * a.k);
+            }
+            hs[(size_t)ys * xstride + w] = __ldg(a.hq + (size_t)row * xstride + w);
+        }
+        named_barrier(1, CW * 32);
+    }
     bool dead = false;
     for (int v = warp; v < NV; v += CW) {
         const VUnit un = decode(v);
@@ -234,16 +257,20 @@ __global__ void __launch_bounds__((CW + 1) * 32) k_down_combine(const DownArgs a
                     for (int c = 0; c < NC; c++)
                         acc[m][c] = 0.0f;
                 // warp-collective shuffles stay outside the lane-dependent block loop
-                int rr[NC];
+                const uint32_t *xc[NC]; // activation row of each column (shared or global)
 #pragma unroll
-                for (int c = 0; c < NC; c++)
-                    rr[c] = __shfl_sync(0xffffffffu, my_r, c0 + (c < nc ? c : 0));
+                for (int c = 0; c < NC; c++) {
+                    const int cc = c0 + (c < nc ? c : 0);
+                    const int r = __shfl_sync(0xffffffffu, my_r, cc);
+                    const int ys = __shfl_sync(0xffffffffu, my_slot, cc);
+                    xc[c] = hs_on ? hs + (size_t)ys * xstride : a.hq + (size_t)r * xstride;
+                }
                 for (int b = lane; b < a.nbI; b += 32) {
                     Q81Block xb[NC];
 #pragma unroll
                     for (int c = 0; c < NC; c++)
                         if (c < nc)
-                            load_q8_1_global(a.hq + ((size_t)rr[c] * a.nbI + b) * Q8_1_WORDS, xb[c]);
+                            load_q8_1_any(xc[c] + (size_t)b * Q8_1_WORDS, xb[c]);
 #pragma unroll
                     for (int m = 0; m < RN; m++) {
                         Q80Block wb;
@@ -353,8 +380,12 @@ extern "C" luce_status luce_moe_down_combine(const luce_block_q8_0 *w_down, cons
     const long long nv_up = std::min<long long>(E, Tk) + Tk / NCU + (ws_down ? (a.TT + NCU - 1) / NCU : 0);
     const int stage = RN * a.rowbytes;
     a.NS = (int)std::max<long long>(2, std::min<long long>(nv_up, (100 * 1024) / stage));
+    // activation rows of a tile in shared memory when they fit in 24 KB
+    const size_t xrow = (size_t)a.nbI * Q8_1_BYTES;
+    const int slots = a.TT * k + (ws_down ? a.TT : 0);
+    a.hs_rows = ((size_t)slots * xrow <= 24 * 1024) ? slots : 0;
     const size_t smem = (size_t)a.NS * stage + (size_t)2 * a.NS * sizeof(uint64_t) + (size_t)(3 * E + 1) * sizeof(int) +
-                        (size_t)(a.TT * k + a.TT) * RN * sizeof(float);
+                        (size_t)(a.TT * k + a.TT) * RN * sizeof(float) + (size_t)a.hs_rows * xrow;
     const int tiles = (T + a.TT - 1) / a.TT;
     dim3 grid((unsigned)tiles, (unsigned)(H / RN));
     const int maxcols = std::min(a.TT, NCU);

@@ -10,28 +10,27 @@
 // kernels" (one expert grouping per layer, so each selected expert's
 // weights cross HBM once).  Its GB300 shape is our own:
 //
-//  * Work is a flat list of PARTS.  A virtual expert is an expert with up to
-//    32 of its routed columns (tokens); experts with more columns, and the
-//    shared expert (all T tokens), are split into several.  Each virtual
-//    expert has I/32 row groups of 32 rows (one q8_1 block of h per column),
-//    and each group is cut into CL parts of RU = 32/CL rows, sized so that a
-//    part (RU gate rows + RU up rows) is about 70 KB.
-//  * Persistent CTAs (one per SM) take contiguous ranges of parts.  One
-//    producer thread streams each part's gate and up rows into a ring of
-//    shared-memory stages (~200 KB: a decode step's whole share of the
-//    weights is in flight at once) with cp.async.bulk completing on
-//    per-stage mbarriers; eight consumer warps compute from shared memory
-//    and release each stage on its "empty" mbarrier.
-//  * A consumer lane owns Q8_0 blocks b = lane, lane + 32, ... of a row; the
-//    q8_1 activation block of each column is loaded once (read-only path,
-//    prefetched into L1 when the virtual expert changes) and used for the
+//  * Work is a flat list of 32-row GROUPS.  A virtual expert is an expert with
+//    up to 32 of its routed columns (tokens); experts with more columns, and
+//    the shared expert (all T tokens), are split into several.  Each virtual
+//    expert has I/32 groups (one q8_1 block of h per column and group).
+//  * Persistent CTAs (one per SM) take contiguous ranges of whole groups, so
+//    every group is quantized from shared memory by the CTA that computed it
+//    and no CTA ever waits for another.  Whole groups are a coarse unit, but
+//    one SM can pull several times its even share of HBM bandwidth, so the
+//    bytes per CTA need not be balanced finely: what matters is that every
+//    SM keeps enough requests in flight.
+//  * One producer thread streams each group as parts of RU gate rows + RU up
+//    rows (~35 KB) into a ring of shared-memory stages (~175 KB: a decode
+//    step's whole share of the weights is requested at once) with
+//    cp.async.bulk completing on per-stage mbarriers; eight consumer warps
+//    compute from shared memory and release each stage on its "empty"
+//    mbarrier.
+//  * A consumer lane owns Q8_0 blocks b = lane, lane + 32, ... of a row.  The
+//    q8_1 activation rows of the current virtual expert's columns are staged
+//    in shared memory (when they fit) and each block is loaded once for the
 //    gate AND the up row.  Block sums are exact int32 dp4a sums; the fp32
 //    partials are reduced across the warp.
-//  * h of each part is written to global memory.  A CTA that computed all CL
-//    parts of a group quantizes it from shared memory; a group split across
-//    two CTAs is quantized by whichever finishes it last (a per-group counter
-//    in the caller's workspace; the last arriver resets it to zero).  No CTA
-//    ever waits for another.
 //  * Every device wait is bounded (LUCE_FAULT_TIMEOUT, never expected); a CTA
 //    that gives up drains its copies in flight before it exits.
 //  * With programmatic dependent launch the CTAs start while the previous
@@ -62,13 +61,13 @@ struct GluArgs {
     const int32_t *routes;    // [T*k]
     float *h;                 // [T*k+T][I]
     uint32_t *hq;             // [T*k+T][I/32] q8_1 blocks
-    unsigned int *group_cnt;  // [nv_max * I/32] zero-initialized counters
     int T, k, E, H, I;
     float clamp;
     int nb, rowbytes;
-    int RU; // rows per part (divides 32)
-    int CL; // parts per 32-row group
-    int NS; // stages (one part each) in the ring
+    int RU;     // rows per part (divides 32)
+    int CL;     // parts per 32-row group
+    int NS;     // stages (one part each) in the ring
+    int xs_cols; // activation columns staged in shared memory (0: read through L1)
 };
 
 struct Part {
@@ -122,10 +121,10 @@ __global__ void __launch_bounds__(THREADS, 1) k_glu_pair(const GluArgs a)
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.NS * stage_bytes);
     uint64_t *empty = full + a.NS;
-    int *vpre = reinterpret_cast<int *>(empty + a.NS);    // [E + 1]
-    int *col_r = vpre + a.E + 1;                          // [NCU]: h row of each column
-    float *hbuf = reinterpret_cast<float *>(col_r + NCU); // [32][HB_STRIDE]
-    __shared__ int s_abort, s_last;
+    uint32_t *xs = reinterpret_cast<uint32_t *>(empty + a.NS); // [xs_cols][nb][9]
+    int *vpre = reinterpret_cast<int *>(xs + (size_t)a.xs_cols * a.nb * Q8_1_WORDS); // [E + 1]
+    float *hbuf = reinterpret_cast<float *>(vpre + a.E + 1); // [2][32][HB_STRIDE]
+    __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
@@ -179,8 +178,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_glu_pair(const GluArgs a)
     const int NVr = vpre[a.E];
     const int NV = NVr + (a.wsg ? (a.T + NCU - 1) / NCU : 0);
     const int G = a.I / 32;
-    const long long N = (long long)NV * G * a.CL;
-    const long long u0 = N * blockIdx.x / gridDim.x, u1 = N * (blockIdx.x + 1) / gridDim.x;
+    const long long NG = (long long)NV * G; // groups
+    const long long g0 = NG * blockIdx.x / gridDim.x, g1 = NG * (blockIdx.x + 1) / gridDim.x;
 
     if (warp == CW) {
         // ---------------- producer: one thread streams the parts ----------------
@@ -188,21 +187,27 @@ __global__ void __launch_bounds__(THREADS, 1) k_glu_pair(const GluArgs a)
             return;
         const uint64_t pol = l2_evict_first_policy();
         uint32_t q = 0;
-        for (long long u = u0; u < u1; u++, q++) {
-            const Part pt = decode_part(a, vpre, NVr, u);
-            const uint32_t slot = q % a.NS, use = q / a.NS;
-            if (use > 0 && !mbar_wait_bounded(&empty[slot], (use - 1) & 1u)) {
-                atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
-                *(volatile int *)&s_abort = 1;
-                break;
+        bool stop = false;
+        for (long long gi = g0; gi < g1 && !stop; gi++) {
+            const Part pt = decode_part(a, vpre, NVr, gi * a.CL);
+            for (int p = 0; p < a.CL; p++, q++) {
+                const uint32_t slot = q % a.NS, use = q / a.NS;
+                if (use > 0 && !mbar_wait_bounded(&empty[slot], (use - 1) & 1u)) {
+                    atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
+                    *(volatile int *)&s_abort = 1;
+                    stop = true;
+                    break;
+                }
+                if (*(volatile int *)&s_abort) {
+                    stop = true;
+                    break;
+                }
+                const size_t row0 = (size_t)pt.grp * 32 + (size_t)p * a.RU;
+                uint8_t *dst = ring + (size_t)slot * stage_bytes;
+                mbar_arrive_expect_tx(&full[slot], (uint32_t)stage_bytes);
+                bulk_copy_g2s(dst, pt.g + row0 * a.rowbytes, (uint32_t)half_bytes, &full[slot], pol);
+                bulk_copy_g2s(dst + half_bytes, pt.u + row0 * a.rowbytes, (uint32_t)half_bytes, &full[slot], pol);
             }
-            if (*(volatile int *)&s_abort)
-                break;
-            const size_t row0 = (size_t)pt.grp * 32 + (size_t)pt.p * a.RU;
-            uint8_t *dst = ring + (size_t)slot * stage_bytes;
-            mbar_arrive_expect_tx(&full[slot], (uint32_t)stage_bytes);
-            bulk_copy_g2s(dst, pt.g + row0 * a.rowbytes, (uint32_t)half_bytes, &full[slot], pol);
-            bulk_copy_g2s(dst + half_bytes, pt.u + row0 * a.rowbytes, (uint32_t)half_bytes, &full[slot], pol);
         }
         // no bulk copy may still be writing shared memory when the CTA exits
         const uint32_t n_slots = (q < (uint32_t)a.NS ? q : (uint32_t)a.NS);
@@ -216,16 +221,19 @@ __global__ void __launch_bounds__(THREADS, 1) k_glu_pair(const GluArgs a)
 
     // ---------------- consumers ----------------
     const int cthreads = CW * 32;
+    const int xstride = a.nb * Q8_1_WORDS; // words per activation row
     bool dead = false;
     int cur_v = -1;
-    int my_t = 0; // lane c holds column c's token
+    int my_t = 0, my_r = 0; // lane c holds column c's token and h row
+    bool x_in_smem = false;
     uint32_t q = 0;
-    for (long long u = u0; u < u1; u++, q++) {
-        const Part pt = decode_part(a, vpre, NVr, u);
+    int par = 0;
+    for (long long gi = g0; gi < g1; gi++, par ^= 1) {
+        const Part pt = decode_part(a, vpre, NVr, gi * a.CL);
         if (pt.v != cur_v) {
             cur_v = pt.v;
-            int my_r = 0;
             my_t = 0;
+            my_r = 0;
             if (lane < pt.ncols) {
                 if (pt.e < a.E) {
                     my_r = a.routes[a.offsets[pt.e] + pt.col0 + lane];
@@ -235,122 +243,97 @@ __global__ void __launch_bounds__(THREADS, 1) k_glu_pair(const GluArgs a)
                     my_r = a.T * a.k + my_t;
                 }
             }
-            if (warp == 0 && lane < pt.ncols)
-                col_r[lane] = my_r;
-            // warm L1 with the activation blocks this lane will read
-            for (int c = 0; c < pt.ncols; c++) {
-                const int t = __shfl_sync(0xffffffffu, my_t, c);
-                for (int b = lane; b < a.nb; b += 32) {
-                    const uint32_t *w = a.xq + ((size_t)t * a.nb + b) * Q8_1_WORDS;
-                    asm volatile("prefetch.global.L1 [%0];" ::"l"(w));
-                    asm volatile("prefetch.global.L1 [%0];" ::"l"(w + 8));
+            x_in_smem = pt.ncols <= a.xs_cols;
+            if (x_in_smem) {
+                // stage the columns' q8_1 rows: warp w copies columns w, w+CW, ...
+                // (every warp is past the previous group's products: the group
+                // barrier below; the epilogue does not read xs)
+                for (int c = warp; c < pt.ncols; c += CW) {
+                    const int t = __shfl_sync(0xffffffffu, my_t, c);
+                    const uint32_t *src = a.xq + (size_t)t * xstride;
+                    uint32_t *dst = xs + (size_t)c * xstride;
+                    for (int w = lane; w < xstride; w += 32)
+                        dst[w] = __ldg(src + w);
                 }
+                named_barrier(1, cthreads);
             }
-            named_barrier(1, cthreads); // col_r visible to every consumer warp
         }
-        const uint32_t slot = q % a.NS, use = q / a.NS;
-        if (!dead && *(volatile int *)&s_abort)
-            dead = true;
-        if (!dead) {
-            const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], use & 1u));
-            if (!got) {
-                if (lane == 0) {
-                    atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
-                    *(volatile int *)&s_abort = 1;
-                }
+        float *hb = hbuf + par * 32 * HB_STRIDE;
+        for (int p = 0; p < a.CL; p++, q++) {
+            const uint32_t slot = q % a.NS, use = q / a.NS;
+            if (!dead && *(volatile int *)&s_abort)
                 dead = true;
+            if (!dead) {
+                const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], use & 1u));
+                if (!got) {
+                    if (lane == 0) {
+                        atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
+                        *(volatile int *)&s_abort = 1;
+                    }
+                    dead = true;
+                }
             }
-        }
-        if (!dead) {
-            const uint8_t *st = ring + (size_t)slot * stage_bytes;
-            for (int i = warp; i < a.RU; i += CW) {
-                const int prow = pt.p * a.RU + i; // row within the 32-row group
-                const uint8_t *grow = st + (size_t)i * a.rowbytes;
-                const uint8_t *urow = st + half_bytes + (size_t)i * a.rowbytes;
-                for (int c0 = 0; c0 < pt.ncols; c0 += NC) {
-                    const int nc = min(NC, pt.ncols - c0);
-                    int tcol[NC];
+            if (!dead) {
+                const uint8_t *st = ring + (size_t)slot * stage_bytes;
+                for (int i = warp; i < a.RU; i += CW) {
+                    const int prow = p * a.RU + i; // row within the 32-row group
+                    const uint8_t *grow = st + (size_t)i * a.rowbytes;
+                    const uint8_t *urow = st + half_bytes + (size_t)i * a.rowbytes;
+                    for (int c0 = 0; c0 < pt.ncols; c0 += NC) {
+                        const int nc = min(NC, pt.ncols - c0);
+                        const uint32_t *xc[NC]; // activation row of each column (shared or global)
 #pragma unroll
-                    for (int c = 0; c < NC; c++)
-                        tcol[c] = __shfl_sync(0xffffffffu, my_t, c0 + (c < nc ? c : 0));
-                    float ag[NC], au[NC];
+                        for (int c = 0; c < NC; c++) {
+                            const int cc = c0 + (c < nc ? c : 0);
+                            const int t = __shfl_sync(0xffffffffu, my_t, cc);
+                            xc[c] = x_in_smem ? xs + (size_t)cc * xstride : a.xq + (size_t)t * xstride;
+                        }
+                        float ag[NC], au[NC];
 #pragma unroll
-                    for (int c = 0; c < NC; c++)
-                        ag[c] = au[c] = 0.0f;
-                    for (int b = lane; b < a.nb; b += 32) {
-                        Q80Block gb, ub;
-                        load_q8_0_smem(grow, b, gb);
-                        load_q8_0_smem(urow, b, ub);
+                        for (int c = 0; c < NC; c++)
+                            ag[c] = au[c] = 0.0f;
+                        for (int b = lane; b < a.nb; b += 32) {
+                            Q80Block gb, ub;
+                            load_q8_0_smem(grow, b, gb);
+                            load_q8_0_smem(urow, b, ub);
+#pragma unroll
+                            for (int c = 0; c < NC; c++) {
+                                if (c < nc) {
+                                    Q81Block xb;
+                                    load_q8_1_any(xc[c] + (size_t)b * Q8_1_WORDS, xb);
+                                    const int sg = dot_q8_block(gb.q, xb.q);
+                                    const int su = dot_q8_block(ub.q, xb.q);
+                                    ag[c] = fmaf(gb.d * xb.d, (float)sg, ag[c]);
+                                    au[c] = fmaf(ub.d * xb.d, (float)su, au[c]);
+                                }
+                            }
+                        }
 #pragma unroll
                         for (int c = 0; c < NC; c++) {
                             if (c < nc) {
-                                Q81Block xb;
-                                load_q8_1_global(a.xq + ((size_t)tcol[c] * a.nb + b) * Q8_1_WORDS, xb);
-                                const int sg = dot_q8_block(gb.q, xb.q);
-                                const int su = dot_q8_block(ub.q, xb.q);
-                                ag[c] = fmaf(gb.d * xb.d, (float)sg, ag[c]);
-                                au[c] = fmaf(ub.d * xb.d, (float)su, au[c]);
+                                const float g = warp_sum(ag[c]);
+                                const float uu = warp_sum(au[c]);
+                                if (lane == 0)
+                                    hb[prow * HB_STRIDE + c0 + c] = swiglu(g, uu, a.clamp);
                             }
                         }
                     }
-#pragma unroll
-                    for (int c = 0; c < NC; c++) {
-                        if (c < nc) {
-                            const float g = warp_sum(ag[c]);
-                            const float uu = warp_sum(au[c]);
-                            if (lane == 0)
-                                hbuf[prow * HB_STRIDE + c0 + c] = swiglu(g, uu, a.clamp);
-                        }
-                    }
                 }
             }
+            __syncwarp();
+            if (lane == 0 && !dead)
+                mbar_arrive(&empty[slot]);
         }
-        __syncwarp();
-        if (lane == 0 && !dead)
-            mbar_arrive(&empty[slot]);
+        // the group is complete: h and its q8_1 block per column
         named_barrier(1, cthreads);
-        const bool ok = !dead && !*(volatile int *)&s_abort;
-        // h rows of this part -> global memory
-        if (ok) {
-            for (int idx = tid; idx < a.RU * pt.ncols; idx += cthreads) {
-                const int i = idx % a.RU, c = idx / a.RU;
-                const int prow = pt.p * a.RU + i;
-                a.h[(size_t)col_r[c] * a.I + (size_t)pt.grp * 32 + prow] = hbuf[prow * HB_STRIDE + c];
+        if (!dead && !*(volatile int *)&s_abort) {
+            for (int c = warp; c < pt.ncols; c += CW) {
+                const int r = __shfl_sync(0xffffffffu, my_r, c);
+                const float v = hb[lane * HB_STRIDE + c];
+                a.h[(size_t)r * a.I + (size_t)pt.grp * 32 + lane] = v;
+                quantize_q8_1_warp(v, a.hq + ((size_t)r * G + pt.grp) * Q8_1_WORDS, lane);
             }
         }
-        // quantize the group once all its parts are done
-        const long long gfirst = u - pt.p;
-        const bool whole = gfirst >= u0 && gfirst + a.CL <= u1;
-        if (whole) {
-            if (pt.p == a.CL - 1 && ok) {
-                for (int c = warp; c < pt.ncols; c += CW) {
-                    const int r = col_r[c];
-                    const float v = hbuf[lane * HB_STRIDE + c];
-                    quantize_q8_1_warp(v, a.hq + ((size_t)r * G + pt.grp) * Q8_1_WORDS, lane);
-                }
-            }
-        } else {
-            __threadfence();
-            named_barrier(1, cthreads);
-            if (tid == 0) {
-                unsigned int *cnt = a.group_cnt + (size_t)pt.v * G + pt.grp;
-                const unsigned int old = ok ? atomicAdd(cnt, 1u) : 0u;
-                const bool last = ok && old == (unsigned)(a.CL - 1);
-                if (last)
-                    *cnt = 0u; // every part has arrived: reset for the next call
-                s_last = last ? 1 : 0;
-            }
-            named_barrier(1, cthreads);
-            if (s_last) {
-                __threadfence();
-                for (int c = warp; c < pt.ncols; c += CW) {
-                    const int r = col_r[c];
-                    const float v = __ldcg(&a.h[(size_t)r * a.I + (size_t)pt.grp * 32 + lane]);
-                    quantize_q8_1_warp(v, a.hq + ((size_t)r * G + pt.grp) * Q8_1_WORDS, lane);
-                }
-            }
-        }
-        named_barrier(1, cthreads);
     }
 }
 
@@ -372,31 +355,15 @@ luce_status launch_glu(const GluArgs &a, cudaStream_t stream, size_t smem)
     return luce_host::launch(kern, dim3(luce_host::sm_count()), dim3(THREADS), smem, stream, a);
 }
 
-// Upper bound of the number of virtual experts of a call.
-long long max_virtual_experts(int T, int k, int E, bool shared)
-{
-    const long long Tk = (long long)T * k;
-    return std::min<long long>(E, Tk) + Tk / NCU + (shared ? (T + NCU - 1) / NCU : 0);
-}
-
 } // namespace
 
 using namespace luce_host;
-
-extern "C" size_t luce_moe_glu_workspace_bytes(int T, int k, int E, int I)
-{
-    if (T <= 0 || k <= 0 || E <= 0 || I <= 0)
-        return 0;
-    // counters per (virtual expert, 32-row group), with or without the shared expert
-    return (size_t)max_virtual_experts(T, k, E, true) * (size_t)(I / 32) * sizeof(unsigned int);
-}
 
 extern "C" luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const luce_block_q8_0 *w_up,
                                          const luce_block_q8_0 *ws_gate, const luce_block_q8_0 *ws_up,
                                          const luce_block_q8_1 *xq, const int32_t *offsets, const int32_t *routes,
                                          int T, int k, int E, int H, int I, float clamp, float *h,
-                                         luce_block_q8_1 *hq, void *workspace, size_t workspace_bytes, int variant,
-                                         void *stream)
+                                         luce_block_q8_1 *hq, int variant, void *stream)
 {
     if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 64 || (int64_t)T * k > (1 << 20))
         return LUCE_ERR_INVALID_ARG;
@@ -406,13 +373,10 @@ extern "C" luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const lu
         return LUCE_ERR_INVALID_ARG;
     if (T == 0)
         return LUCE_OK;
-    if (!w_gate || !w_up || !xq || !offsets || !routes || !h || !hq || !workspace)
+    if (!w_gate || !w_up || !xq || !offsets || !routes || !h || !hq)
         return LUCE_ERR_INVALID_ARG;
     if (!aligned(w_gate, 16) || !aligned(w_up, 16) || (ws_gate && (!aligned(ws_gate, 16) || !aligned(ws_up, 16))) ||
-        !aligned(xq, 16) || !aligned(hq, 16) || !aligned(h, 4) || !aligned(offsets, 4) || !aligned(routes, 4) ||
-        !aligned(workspace, 4))
-        return LUCE_ERR_INVALID_ARG;
-    if (workspace_bytes < luce_moe_glu_workspace_bytes(T, k, E, I))
+        !aligned(xq, 16) || !aligned(hq, 16) || !aligned(h, 4) || !aligned(offsets, 4) || !aligned(routes, 4))
         return LUCE_ERR_INVALID_ARG;
 
     GluArgs a;
@@ -425,7 +389,6 @@ extern "C" luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const lu
     a.routes = routes;
     a.h = h;
     a.hq = reinterpret_cast<uint32_t *>(hq);
-    a.group_cnt = reinterpret_cast<unsigned int *>(workspace);
     a.T = T;
     a.k = k;
     a.E = E;
@@ -434,20 +397,25 @@ extern "C" luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const lu
     a.clamp = clamp;
     a.nb = H / 32;
     a.rowbytes = a.nb * Q8_0_BYTES;
-    // a part (RU gate rows + RU up rows) of about 70 KB; three of them in flight
+    // a part (RU gate rows + RU up rows) of about 35 KB, but at least one row
+    // per consumer warp while a part stays under 72 KB
     int RU = 32;
-    while (RU > 1 && 2 * RU * a.rowbytes > 72 * 1024)
+    while (RU > 1 && 2 * RU * a.rowbytes > 36 * 1024 && !(RU <= CW && 2 * RU * a.rowbytes <= 72 * 1024))
         RU /= 2;
     a.RU = RU;
     a.CL = 32 / RU;
+    // activation rows in shared memory when up to 32 columns fit in 40 KB
+    const int maxcols = std::min(T, NCU);
+    const size_t xrow = (size_t)a.nb * Q8_1_BYTES;
+    a.xs_cols = (maxcols * xrow <= 40 * 1024) ? maxcols : 0;
     const size_t stage = (size_t)2 * RU * a.rowbytes;
-    const size_t fixed = (size_t)(E + 1 + NCU) * sizeof(int) + (size_t)32 * HB_STRIDE * sizeof(float) + 64;
-    const size_t budget = 220 * 1024;
-    int NS = (int)std::min<size_t>(8, (budget - fixed) / (stage + 16));
+    const size_t fixed = (size_t)a.xs_cols * xrow + (size_t)(E + 1) * sizeof(int) +
+                         (size_t)2 * 32 * HB_STRIDE * sizeof(float) + 64;
+    const size_t budget = 216 * 1024;
+    int NS = (int)std::min<size_t>(16, (budget - fixed) / (stage + 16));
     NS = std::max(NS, 2);
     a.NS = NS;
     const size_t smem = (size_t)NS * stage + (size_t)2 * NS * sizeof(uint64_t) + fixed;
-    const int maxcols = std::min(T, NCU);
     cudaStream_t st = as_stream(stream);
     if (maxcols <= 1)
         return launch_glu<1>(a, st, smem);
