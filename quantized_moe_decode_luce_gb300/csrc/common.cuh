@@ -291,24 +291,57 @@ int sm_count();
 // attribute (luce_set_pdl; process-wide, default off).
 bool pdl_enabled();
 
-// Launch `kern` with cudaLaunchKernelEx, with the PDL attribute when enabled.
-template <typename... KArgs, typename... Args>
-luce_status launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args)
+// Launch configuration: the PDL attribute when enabled and, if cluster > 1, a
+// 1-D thread-block cluster of that size.  `attr` must hold two entries.
+inline void make_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, dim3 grid, dim3 block, size_t smem,
+                        cudaStream_t stream, int cluster)
 {
-    cudaLaunchConfig_t cfg = {};
+    cfg = cudaLaunchConfig_t{};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
     int n = 0;
     if (pdl_enabled()) {
         attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[n].val.programmaticStreamSerializationAllowed = 1;
         n++;
     }
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        n++;
+    }
     cfg.attrs = attr;
     cfg.numAttrs = n;
+}
+
+// Launch `kern` with cudaLaunchKernelEx (PDL attribute when enabled, optional
+// cluster size).
+template <typename... KArgs, typename... Args>
+luce_status launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, int cluster,
+                      Args... args)
+{
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    make_config(cfg, attr, grid, block, smem, stream, cluster);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return LUCE_ERR_CUDA;
+    }
+    return LUCE_OK;
+}
+
+// Launch `kern` with cudaLaunchKernelEx, with the PDL attribute when enabled.
+template <typename... KArgs, typename... Args>
+luce_status launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    make_config(cfg, attr, grid, block, smem, stream, 1);
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();

@@ -68,11 +68,12 @@ __global__ void __launch_bounds__((CW + 1) * 32) k_down_combine(const DownArgs a
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.NS * stage_bytes);
     uint64_t *empty = full + a.NS;
-    int *vpre = reinterpret_cast<int *>(empty + a.NS); // [E + 1]
+    uint64_t *hs_bar = empty + a.NS;                            // staged activation rows landed
+    uint32_t *hs = reinterpret_cast<uint32_t *>(hs_bar + 2);    // [hs_rows][nbI][9], 16-byte aligned
+    float *ybuf = reinterpret_cast<float *>(hs + (size_t)a.hs_rows * a.nbI * Q8_1_WORDS); // [TT*k + TT][RN]
+    int *vpre = reinterpret_cast<int *>(ybuf + (size_t)(a.TT * a.k + a.TT) * RN); // [E + 1]
     int *vlo = vpre + a.E + 1;                         // [E]: first route of the tile
     int *vcnt = vlo + a.E;                             // [E]: routes of the tile
-    float *ybuf = reinterpret_cast<float *>(vcnt + a.E); // [TT*k + TT][RN]
-    uint32_t *hs = reinterpret_cast<uint32_t *>(ybuf + (size_t)(a.TT * a.k + a.TT) * RN); // [hs_rows][nbI][9]
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__((CW + 1) * 32) k_down_combine(const DownArgs a
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
+        mbar_init(hs_bar, 1);
         fence_mbar_init();
         s_abort = 0;
     }
@@ -200,26 +202,46 @@ __global__ void __launch_bounds__((CW + 1) * 32) k_down_combine(const DownArgs a
     pdl_trigger();
     const int xstride = a.nbI * Q8_1_WORDS; // words per activation row
     const bool hs_on = a.hs_rows > 0;
-    if (hs_on) {
-        // stage the activation row of every y slot of the tile (routed slots of
-        // kept routes, then the shared expert's tokens) in one parallel pass
-        const int nslots = ntok * a.k + (a.wsd ? ntok : 0);
-        for (int i = tid; i < nslots * xstride; i += CW * 32) {
-            const int ys = i / xstride, w = i - ys * xstride;
-            int row;
-            if (ys < ntok * a.k) {
-                row = t0 * a.k + ys;
-                const int e = a.ids[row];
-                if (e < 0 || e >= a.E)
-                    continue;
-            } else {
-                row = a.T * a.k + t0 + (ys - ntok * a.k);
-            }
-            hs[(size_t)ys * xstride + w] = __ldg(a.hq + (size_t)row * xstride + w);
-        }
-        named_barrier(1, CW * 32);
-    }
     bool dead = false;
+    if (hs_on) {
+        // one bulk copy per activation row of the tile: the routed slots of
+        // kept routes, then the shared expert's tokens
+        if (tid == 0) {
+            const int nslots = ntok * a.k + (a.wsd ? ntok : 0);
+            const uint32_t xrow = (uint32_t)(xstride * 4);
+            uint32_t bytes = 0;
+            for (int ys = 0; ys < nslots; ys++) {
+                if (ys < ntok * a.k) {
+                    const int e = a.ids[t0 * a.k + ys];
+                    if (e >= 0 && e < a.E)
+                        bytes += xrow;
+                } else {
+                    bytes += xrow;
+                }
+            }
+            mbar_arrive_expect_tx(hs_bar, bytes);
+            for (int ys = 0; ys < nslots; ys++) {
+                int row;
+                if (ys < ntok * a.k) {
+                    row = t0 * a.k + ys;
+                    const int e = a.ids[row];
+                    if (e < 0 || e >= a.E)
+                        continue;
+                } else {
+                    row = a.T * a.k + t0 + (ys - ntok * a.k);
+                }
+                bulk_copy_g2s(hs + (size_t)ys * xstride, a.hq + (size_t)row * xstride, xrow, hs_bar,
+                              l2_evict_first_policy());
+            }
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(hs_bar, 0))) {
+            if (lane == 0) {
+                atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
+                *(volatile int *)&s_abort = 1;
+            }
+            dead = true;
+        }
+    }
     for (int v = warp; v < NV; v += CW) {
         const VUnit un = decode(v);
         int my_r = 0, my_slot = 0; // column `lane`: its hq row and its y slot
@@ -380,12 +402,13 @@ extern "C" luce_status luce_moe_down_combine(const luce_block_q8_0 *w_down, cons
     const long long nv_up = std::min<long long>(E, Tk) + Tk / NCU + (ws_down ? (a.TT + NCU - 1) / NCU : 0);
     const int stage = RN * a.rowbytes;
     a.NS = (int)std::max<long long>(2, std::min<long long>(nv_up, (100 * 1024) / stage));
-    // activation rows of a tile in shared memory when they fit in 24 KB
+    // activation rows of a tile in shared memory when they fit in 24 KB (a row
+    // is a multiple of 16 bytes since I % 256 == 0)
     const size_t xrow = (size_t)a.nbI * Q8_1_BYTES;
     const int slots = a.TT * k + (ws_down ? a.TT : 0);
     a.hs_rows = ((size_t)slots * xrow <= 24 * 1024) ? slots : 0;
-    const size_t smem = (size_t)a.NS * stage + (size_t)2 * a.NS * sizeof(uint64_t) + (size_t)(3 * E + 1) * sizeof(int) +
-                        (size_t)(a.TT * k + a.TT) * RN * sizeof(float) + (size_t)a.hs_rows * xrow;
+    const size_t smem = (size_t)a.NS * stage + (size_t)(2 * a.NS + 2) * sizeof(uint64_t) + (size_t)a.hs_rows * xrow +
+                        (size_t)(a.TT * k + a.TT) * RN * sizeof(float) + (size_t)(3 * E + 1) * sizeof(int);
     const int tiles = (T + a.TT - 1) / a.TT;
     dim3 grid((unsigned)tiles, (unsigned)(H / RN));
     const int maxcols = std::min(a.TT, NCU);

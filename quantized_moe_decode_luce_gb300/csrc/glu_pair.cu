@@ -14,31 +14,33 @@
 //    up to 32 of its routed columns (tokens); experts with more columns, and
 //    the shared expert (all T tokens), are split into several.  Each virtual
 //    expert has I/32 groups (one q8_1 block of h per column and group).
-//  * Persistent CTAs (one per SM) take contiguous ranges of whole groups, so
-//    every group is quantized from shared memory by the CTA that computed it
-//    and no CTA ever waits for another.  Whole groups are a coarse unit, but
-//    one SM can pull several times its even share of HBM bandwidth, so the
-//    bytes per CTA need not be balanced finely: what matters is that every
-//    SM keeps enough requests in flight.
-//  * One producer thread streams each group as parts of RU gate rows + RU up
-//    rows (~35 KB) into a ring of shared-memory stages (~175 KB: a decode
-//    step's whole share of the weights is requested at once) with
-//    cp.async.bulk completing on per-stage mbarriers; eight consumer warps
-//    compute from shared memory and release each stage on its "empty"
-//    mbarrier.
-//  * A consumer lane owns Q8_0 blocks b = lane, lane + 32, ... of a row.  The
-//    q8_1 activation rows of the current virtual expert's columns are staged
-//    in shared memory (when they fit) and each block is loaded once for the
-//    gate AND the up row.  Block sums are exact int32 dp4a sums; the fp32
-//    partials are reduced across the warp.
-//  * Every device wait is bounded (LUCE_FAULT_TIMEOUT, never expected); a CTA
-//    that gives up drains its copies in flight before it exits.
+//  * The grid is one CTA per SM, in thread-block clusters of one or two CTAs.
+//    A cluster takes a contiguous range of groups; with two CTAs each streams
+//    16 of the 32 rows of every group, so that a decode step's few hundred
+//    groups spread evenly over the SMs.  The rows' SwiGLU values meet in the
+//    cluster leader's shared memory (distributed shared memory stores, one
+//    cluster barrier per group) and the leader writes h and its q8_1 block.
+//  * Thread 0 streams each CTA's parts (RU gate rows + RU up rows, ~35-70 KB)
+//    into a ring of shared-memory stages (~175-210 KB: a decode step's whole
+//    share of the weights is requested at once) with cp.async.bulk
+//    completing on per-stage mbarriers, and refills a stage once every warp
+//    has passed the CTA barrier that ends its part.
+//  * A lane owns Q8_0 blocks b = lane, lane + 32, ... of a row.  The q8_1
+//    activation rows of the current virtual expert's columns are staged in
+//    shared memory (when they fit) and each block is loaded once for the gate
+//    AND the up row.  Block sums are exact int32 dp4a sums; the fp32 partials
+//    are reduced across the warp.
+//  * Every mbarrier wait is bounded (LUCE_FAULT_TIMEOUT, never expected); a
+//    CTA that gives up keeps every CTA and cluster barrier in step, skips the
+//    arithmetic, and drains its copies in flight before it exits.
 //  * With programmatic dependent launch the CTAs start while the previous
 //    kernel (the grouping) still runs: they prefetch their slice of the
 //    shared expert's rows into L2 (those rows are needed whatever the
 //    routing is) and then wait for the grouping's results.
 #include <algorithm>
 #include <climits>
+
+#include <cooperative_groups.h>
 
 #include "common.cuh"
 
@@ -50,8 +52,8 @@ using namespace luce;
 
 constexpr int NCU = 32;          // columns per virtual expert (<= 32: one per lane)
 constexpr int HB_STRIDE = NCU + 1;
-constexpr int CW = 8;            // consumer warps
-constexpr int THREADS = (CW + 1) * 32;
+constexpr int CW = 8;            // warps per CTA
+constexpr int THREADS = CW * 32;
 
 struct GluArgs {
     const uint8_t *wg, *wu;   // [E][I][rowbytes]
@@ -64,29 +66,25 @@ struct GluArgs {
     int T, k, E, H, I;
     float clamp;
     int nb, rowbytes;
-    int RU;     // rows per part (divides 32)
-    int CL;     // parts per 32-row group
-    int NS;     // stages (one part each) in the ring
+    int RU;      // rows per part (divides 32 / cluster size)
+    int NS;      // stages (one part each) in the ring
     int xs_cols; // activation columns staged in shared memory (0: read through L1)
 };
 
-struct Part {
+struct Group {
     const uint8_t *g, *u; // gate / up rows of this virtual expert
     int v;                // virtual expert
     int e;                // expert (E = shared)
     int col0, ncols;      // column range within the expert's routes / tokens
-    int grp, p;           // 32-row group, part within the group
+    int grp;              // 32-row group
 };
 
-__device__ __forceinline__ Part decode_part(const GluArgs &a, const int *vpre, int NVr, long long u)
+__device__ __forceinline__ Group decode_group(const GluArgs &a, const int *vpre, int NVr, long long gi)
 {
     const int G = a.I / 32;
-    const long long per_v = (long long)G * a.CL;
-    Part r;
-    r.v = (int)(u / per_v);
-    const int rem = (int)(u % per_v);
-    r.grp = rem / a.CL;
-    r.p = rem % a.CL;
+    Group r;
+    r.v = (int)(gi / G);
+    r.grp = (int)(gi % G);
     if (r.v < NVr) {
         // the largest e with vpre[e] <= v owns virtual expert v
         int lo = 0, hi = a.E - 1;
@@ -115,36 +113,38 @@ __device__ __forceinline__ Part decode_part(const GluArgs &a, const int *vpre, i
 template <int NC>
 __global__ void __launch_bounds__(THREADS, 1) k_glu_pair(const GluArgs a)
 {
+    namespace cg = cooperative_groups;
     extern __shared__ __align__(128) uint8_t smem[];
     const int half_bytes = a.RU * a.rowbytes;
     const int stage_bytes = 2 * half_bytes;
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.NS * stage_bytes);
-    uint64_t *empty = full + a.NS;
-    uint32_t *xs = reinterpret_cast<uint32_t *>(empty + a.NS); // [xs_cols][nb][9]
+    uint32_t *xs = reinterpret_cast<uint32_t *>(full + a.NS); // [xs_cols][nb][9]
     int *vpre = reinterpret_cast<int *>(xs + (size_t)a.xs_cols * a.nb * Q8_1_WORDS); // [E + 1]
-    float *hbuf = reinterpret_cast<float *>(vpre + a.E + 1); // [2][32][HB_STRIDE]
+    float *hbuf = reinterpret_cast<float *>(vpre + a.E + 1); // [2][32][HB_STRIDE], used by the leader
     __shared__ int s_abort;
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int crank = (int)cluster.block_rank(), csize = (int)cluster.num_blocks();
+    float *hlead = cluster.map_shared_rank(hbuf, 0); // the leader's h buffer
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
-        for (int s = 0; s < a.NS; s++) {
+        for (int s = 0; s < a.NS; s++)
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], CW);
-        }
         fence_mbar_init();
         s_abort = 0;
-    }
-    // Before the grouping has finished: warm L2 with this CTA's slice of the
-    // shared expert (needed whatever the routing), then wait for it.
-    if (a.wsg && warp == CW && lane == 0) {
-        const size_t total = (size_t)a.I * a.rowbytes; // multiple of 16
-        const size_t chunk = ((total / gridDim.x) + 15) & ~size_t(15);
-        const size_t off = chunk * blockIdx.x;
-        if (off < total) {
-            const uint32_t n = (uint32_t)min(chunk, total - off);
-            prefetch_l2(a.wsg + off, n);
-            prefetch_l2(a.wsu + off, n);
+        // before the grouping has finished: warm L2 with this CTA's slice of
+        // the shared expert (needed whatever the routing)
+        if (a.wsg) {
+            const size_t total = (size_t)a.I * a.rowbytes; // multiple of 16
+            const size_t chunk = ((total / gridDim.x) + 15) & ~size_t(15);
+            const size_t off = chunk * blockIdx.x;
+            if (off < total) {
+                const uint32_t n = (uint32_t)min(chunk, total - off);
+                prefetch_l2(a.wsg + off, n);
+                prefetch_l2(a.wsu + off, n);
+            }
         }
     }
     pdl_wait();
@@ -179,88 +179,72 @@ __global__ void __launch_bounds__(THREADS, 1) k_glu_pair(const GluArgs a)
     const int NV = NVr + (a.wsg ? (a.T + NCU - 1) / NCU : 0);
     const int G = a.I / 32;
     const long long NG = (long long)NV * G; // groups
-    const long long g0 = NG * blockIdx.x / gridDim.x, g1 = NG * (blockIdx.x + 1) / gridDim.x;
+    const int ncl = gridDim.x / csize, cid = blockIdx.x / csize;
+    const long long g0 = NG * cid / ncl, g1 = NG * (cid + 1) / ncl;
+    const int RPC = 32 / csize;   // rows of each group this CTA streams
+    const int PPG = RPC / a.RU;   // parts per group
+    const long long NP = (g1 - g0) * PPG;
+    const uint64_t pol = l2_evict_first_policy();
 
-    if (warp == CW) {
-        // ---------------- producer: one thread streams the parts ----------------
-        if (lane != 0)
-            return;
-        const uint64_t pol = l2_evict_first_policy();
-        uint32_t q = 0;
-        bool stop = false;
-        for (long long gi = g0; gi < g1 && !stop; gi++) {
-            const Part pt = decode_part(a, vpre, NVr, gi * a.CL);
-            for (int p = 0; p < a.CL; p++, q++) {
-                const uint32_t slot = q % a.NS, use = q / a.NS;
-                if (use > 0 && !mbar_wait_bounded(&empty[slot], (use - 1) & 1u)) {
-                    atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
-                    *(volatile int *)&s_abort = 1;
-                    stop = true;
-                    break;
-                }
-                if (*(volatile int *)&s_abort) {
-                    stop = true;
-                    break;
-                }
-                const size_t row0 = (size_t)pt.grp * 32 + (size_t)p * a.RU;
-                uint8_t *dst = ring + (size_t)slot * stage_bytes;
-                mbar_arrive_expect_tx(&full[slot], (uint32_t)stage_bytes);
-                bulk_copy_g2s(dst, pt.g + row0 * a.rowbytes, (uint32_t)half_bytes, &full[slot], pol);
-                bulk_copy_g2s(dst + half_bytes, pt.u + row0 * a.rowbytes, (uint32_t)half_bytes, &full[slot], pol);
-            }
-        }
-        // no bulk copy may still be writing shared memory when the CTA exits
-        const uint32_t n_slots = (q < (uint32_t)a.NS ? q : (uint32_t)a.NS);
-        for (uint32_t slot = 0; slot < n_slots; slot++) {
-            const uint32_t last_use = (q - 1 - slot) / a.NS;
-            if (!mbar_wait_bounded(&full[slot], last_use & 1u))
-                atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
-        }
-        return;
+    // thread 0 requests part q (of this CTA's NP) into stage q % NS
+    auto issue = [&](long long q) {
+        const Group gr = decode_group(a, vpre, NVr, g0 + q / PPG);
+        const int p = (int)(q % PPG);
+        const size_t row0 = (size_t)gr.grp * 32 + (size_t)crank * RPC + (size_t)p * a.RU;
+        const uint32_t slot = (uint32_t)(q % a.NS);
+        uint8_t *dst = ring + (size_t)slot * stage_bytes;
+        mbar_arrive_expect_tx(&full[slot], (uint32_t)stage_bytes);
+        bulk_copy_g2s(dst, gr.g + row0 * a.rowbytes, (uint32_t)half_bytes, &full[slot], pol);
+        bulk_copy_g2s(dst + half_bytes, gr.u + row0 * a.rowbytes, (uint32_t)half_bytes, &full[slot], pol);
+    };
+    long long issued = 0, waited = 0; // thread 0: parts requested / seen complete
+    if (tid == 0) {
+        for (; issued < NP && issued < a.NS; issued++)
+            issue(issued);
     }
+    // every CTA of the cluster has started before any distributed shared
+    // memory access
+    cluster.sync();
 
-    // ---------------- consumers ----------------
-    const int cthreads = CW * 32;
     const int xstride = a.nb * Q8_1_WORDS; // words per activation row
     bool dead = false;
     int cur_v = -1;
     int my_t = 0, my_r = 0; // lane c holds column c's token and h row
     bool x_in_smem = false;
-    uint32_t q = 0;
+    long long q = 0;
     int par = 0;
     for (long long gi = g0; gi < g1; gi++, par ^= 1) {
-        const Part pt = decode_part(a, vpre, NVr, gi * a.CL);
-        if (pt.v != cur_v) {
-            cur_v = pt.v;
+        const Group gr = decode_group(a, vpre, NVr, gi);
+        if (gr.v != cur_v) {
+            cur_v = gr.v;
             my_t = 0;
             my_r = 0;
-            if (lane < pt.ncols) {
-                if (pt.e < a.E) {
-                    my_r = a.routes[a.offsets[pt.e] + pt.col0 + lane];
+            if (lane < gr.ncols) {
+                if (gr.e < a.E) {
+                    my_r = a.routes[a.offsets[gr.e] + gr.col0 + lane];
                     my_t = my_r / a.k;
                 } else {
-                    my_t = pt.col0 + lane;
+                    my_t = gr.col0 + lane;
                     my_r = a.T * a.k + my_t;
                 }
             }
-            x_in_smem = pt.ncols <= a.xs_cols;
+            x_in_smem = gr.ncols <= a.xs_cols;
             if (x_in_smem) {
                 // stage the columns' q8_1 rows: warp w copies columns w, w+CW, ...
-                // (every warp is past the previous group's products: the group
-                // barrier below; the epilogue does not read xs)
-                for (int c = warp; c < pt.ncols; c += CW) {
+                // (every warp is past the previous part's barrier)
+                for (int c = warp; c < gr.ncols; c += CW) {
                     const int t = __shfl_sync(0xffffffffu, my_t, c);
                     const uint32_t *src = a.xq + (size_t)t * xstride;
                     uint32_t *dst = xs + (size_t)c * xstride;
                     for (int w = lane; w < xstride; w += 32)
                         dst[w] = __ldg(src + w);
                 }
-                named_barrier(1, cthreads);
+                __syncthreads();
             }
         }
-        float *hb = hbuf + par * 32 * HB_STRIDE;
-        for (int p = 0; p < a.CL; p++, q++) {
-            const uint32_t slot = q % a.NS, use = q / a.NS;
+        float *hb = hlead + par * 32 * HB_STRIDE; // possibly in the other CTA
+        for (int p = 0; p < PPG; p++, q++) {
+            const uint32_t slot = (uint32_t)(q % a.NS), use = (uint32_t)(q / a.NS);
             if (!dead && *(volatile int *)&s_abort)
                 dead = true;
             if (!dead) {
@@ -271,16 +255,18 @@ __global__ void __launch_bounds__(THREADS, 1) k_glu_pair(const GluArgs a)
                         *(volatile int *)&s_abort = 1;
                     }
                     dead = true;
+                } else if (tid == 0) {
+                    waited = q + 1;
                 }
             }
             if (!dead) {
                 const uint8_t *st = ring + (size_t)slot * stage_bytes;
                 for (int i = warp; i < a.RU; i += CW) {
-                    const int prow = p * a.RU + i; // row within the 32-row group
+                    const int prow = crank * RPC + p * a.RU + i; // row within the group
                     const uint8_t *grow = st + (size_t)i * a.rowbytes;
                     const uint8_t *urow = st + half_bytes + (size_t)i * a.rowbytes;
-                    for (int c0 = 0; c0 < pt.ncols; c0 += NC) {
-                        const int nc = min(NC, pt.ncols - c0);
+                    for (int c0 = 0; c0 < gr.ncols; c0 += NC) {
+                        const int nc = min(NC, gr.ncols - c0);
                         const uint32_t *xc[NC]; // activation row of each column (shared or global)
 #pragma unroll
                         for (int c = 0; c < NC; c++) {
@@ -320,39 +306,76 @@ __global__ void __launch_bounds__(THREADS, 1) k_glu_pair(const GluArgs a)
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0 && !dead)
-                mbar_arrive(&empty[slot]);
-        }
-        // the group is complete: h and its q8_1 block per column
-        named_barrier(1, cthreads);
-        if (!dead && !*(volatile int *)&s_abort) {
-            for (int c = warp; c < pt.ncols; c += CW) {
-                const int r = __shfl_sync(0xffffffffu, my_r, c);
-                const float v = hb[lane * HB_STRIDE + c];
-                a.h[(size_t)r * a.I + (size_t)pt.grp * 32 + lane] = v;
-                quantize_q8_1_warp(v, a.hq + ((size_t)r * G + pt.grp) * Q8_1_WORDS, lane);
+            __syncthreads(); // every warp is done with this stage
+            if (tid == 0 && !*(volatile int *)&s_abort && issued < NP) {
+                issue(issued); // into the stage just released
+                issued++;
             }
+        }
+        // all 32 rows of the group are in the leader's buffer
+        cluster.sync();
+        if (crank == 0 && !dead && !*(volatile int *)&s_abort) {
+            for (int c = warp; c < gr.ncols; c += CW) {
+                const int r = __shfl_sync(0xffffffffu, my_r, c);
+                const float v = hbuf[par * 32 * HB_STRIDE + lane * HB_STRIDE + c];
+                a.h[(size_t)r * a.I + (size_t)gr.grp * 32 + lane] = v;
+                quantize_q8_1_warp(v, a.hq + ((size_t)r * G + gr.grp) * Q8_1_WORDS, lane);
+            }
+        }
+    }
+    // no bulk copy may still be writing shared memory when the CTA exits (only
+    // after a timeout can a requested part be left unwaited; each stage holds
+    // at most one of them, since nothing is requested after the abort)
+    if (tid == 0) {
+        for (long long r = waited; r < issued; r++) {
+            if (!mbar_wait_bounded(&full[r % a.NS], (uint32_t)(r / a.NS) & 1u))
+                atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
         }
     }
 }
 
-// Per template instance and device: the dynamic shared memory the kernel may
-// use (cached, so that steady-state calls make no attribute calls).
+// Per template instance, device and cluster size: the dynamic shared memory
+// set on the kernel and the clusters that fit at once (cached, so that
+// steady-state calls make no attribute or occupancy query).
+struct LaunchCache {
+    size_t smem = 0;
+    int clusters[3] = {0, 0, 0};
+};
+
 template <int NC>
-luce_status launch_glu(const GluArgs &a, cudaStream_t stream, size_t smem)
+luce_status launch_glu(const GluArgs &a, cudaStream_t stream, size_t smem, int csize)
 {
-    static size_t smem_set[64] = {0};
+    static LaunchCache cache[64];
     auto kern = k_glu_pair<NC>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return LUCE_ERR_CUDA;
-    if (smem_set[dev] < smem) {
+    LaunchCache &c = cache[dev];
+    if (c.smem != smem) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return LUCE_ERR_CUDA;
-        smem_set[dev] = smem;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess)
+            (void)cudaGetLastError();
+        c.smem = smem;
+        c.clusters[1] = c.clusters[2] = 0;
     }
-    return luce_host::launch(kern, dim3(luce_host::sm_count()), dim3(THREADS), smem, stream, a);
+    const int nsm = luce_host::sm_count();
+    if (c.clusters[csize] == 0) {
+        int n = nsm / csize;
+        if (csize > 1) {
+            cudaLaunchConfig_t cfg;
+            cudaLaunchAttribute attr[2];
+            luce_host::make_config(cfg, attr, dim3(nsm / csize * csize), dim3(THREADS), smem, stream, csize);
+            int m = 0;
+            if (cudaOccupancyMaxActiveClusters(&m, kern, &cfg) != cudaSuccess || m < 1) {
+                (void)cudaGetLastError();
+                return LUCE_ERR_CUDA;
+            }
+            n = std::min(n, m);
+        }
+        c.clusters[csize] = n;
+    }
+    return luce_host::launch_ex(kern, dim3(c.clusters[csize] * csize), dim3(THREADS), smem, stream, csize, a);
 }
 
 } // namespace
@@ -397,13 +420,18 @@ extern "C" luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const lu
     a.clamp = clamp;
     a.nb = H / 32;
     a.rowbytes = a.nb * Q8_0_BYTES;
+    // clusters of two CTAs when the groups are few (decode), to spread them
+    // evenly over the SMs; one CTA per cluster otherwise
+    const long long Tk = (long long)T * k;
+    const long long nv_up = std::min<long long>(E, Tk) + Tk / NCU + (ws_gate ? (T + NCU - 1) / NCU : 0);
+    const int csize = (nv_up * (I / 32) < 4LL * sm_count()) ? 2 : 1;
+    const int RPC = 32 / csize;
     // a part (RU gate rows + RU up rows) of about 35 KB, but at least one row
-    // per consumer warp while a part stays under 72 KB
-    int RU = 32;
+    // per warp while a part stays under 72 KB
+    int RU = RPC;
     while (RU > 1 && 2 * RU * a.rowbytes > 36 * 1024 && !(RU <= CW && 2 * RU * a.rowbytes <= 72 * 1024))
         RU /= 2;
     a.RU = RU;
-    a.CL = 32 / RU;
     // activation rows in shared memory when up to 32 columns fit in 40 KB
     const int maxcols = std::min(T, NCU);
     const size_t xrow = (size_t)a.nb * Q8_1_BYTES;
@@ -412,16 +440,16 @@ extern "C" luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const lu
     const size_t fixed = (size_t)a.xs_cols * xrow + (size_t)(E + 1) * sizeof(int) +
                          (size_t)2 * 32 * HB_STRIDE * sizeof(float) + 64;
     const size_t budget = 216 * 1024;
-    int NS = (int)std::min<size_t>(16, (budget - fixed) / (stage + 16));
+    int NS = (int)std::min<size_t>(16, (budget - fixed) / (stage + 8));
     NS = std::max(NS, 2);
     a.NS = NS;
-    const size_t smem = (size_t)NS * stage + (size_t)2 * NS * sizeof(uint64_t) + fixed;
+    const size_t smem = (size_t)NS * stage + (size_t)NS * sizeof(uint64_t) + fixed;
     cudaStream_t st = as_stream(stream);
     if (maxcols <= 1)
-        return launch_glu<1>(a, st, smem);
+        return launch_glu<1>(a, st, smem, csize);
     if (maxcols <= 2)
-        return launch_glu<2>(a, st, smem);
+        return launch_glu<2>(a, st, smem, csize);
     if (maxcols <= 4)
-        return launch_glu<4>(a, st, smem);
-    return launch_glu<8>(a, st, smem);
+        return launch_glu<4>(a, st, smem, csize);
+    return launch_glu<8>(a, st, smem, csize);
 }
