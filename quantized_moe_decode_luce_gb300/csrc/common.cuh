@@ -234,6 +234,13 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy()
     return pol;
 }
 
+__device__ __forceinline__ uint64_t l2_evict_normal_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
 // global to shared memory, completing `bytes` of transaction on `bar`.
 __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
@@ -286,6 +293,22 @@ inline luce_status launch_status()
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+
+// Launch-shape parameters of the streaming kernels.  The values here are the
+// library's choices; they are plain data so that a tuning build can sweep
+// them, and every setting computes the same result.
+struct Tuning {
+    int glu_csize = 0;        // CTAs per cluster for the gate/up kernel (0: automatic)
+    int glu_part_kb = 36;     // target bytes of one part (RU gate + RU up rows)
+    int glu_budget_kb = 216;  // shared-memory ring budget per CTA
+    int glu_cps = 1;          // gate/up CTAs per SM
+    int glu_xs = 1;           // stage activation rows in shared memory
+    int glu_prefetch = 1;     // warm L2 with the shared expert before waiting
+    int down_budget_kb = 100; // down/combine ring budget per CTA
+    int down_stage = 1;       // stage the tile's activation rows in shared memory
+    int evict_first = 1;      // stream weights with the L2 evict-first policy
+};
+extern Tuning g_tuning;
 
 // Whether kernels are launched with the programmatic-dependent-launch
 // attribute (luce_set_pdl; process-wide, default off).

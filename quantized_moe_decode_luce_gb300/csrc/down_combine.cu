@@ -51,6 +51,7 @@ struct DownArgs {
     int TT; // tokens per tile
     int NS; // ring stages
     int hs_rows; // activation rows staged in shared memory (0: read through L1)
+    int evict_first;
 };
 
 struct VUnit {
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__((CW + 1) * 32) k_down_combine(const DownArgs a
         // ---------------- producer: weights only, no wait on the gate/up kernel ----------------
         if (lane != 0)
             return;
-        const uint64_t pol = l2_evict_first_policy();
+        const uint64_t pol = a.evict_first ? l2_evict_first_policy() : l2_evict_normal_policy();
         uint32_t q = 0;
         for (int v = 0; v < NV; v++, q++) {
             const VUnit un = decode(v);
@@ -231,7 +232,7 @@ __global__ void __launch_bounds__((CW + 1) * 32) k_down_combine(const DownArgs a
                     row = a.T * a.k + t0 + (ys - ntok * a.k);
                 }
                 bulk_copy_g2s(hs + (size_t)ys * xstride, a.hq + (size_t)row * xstride, xrow, hs_bar,
-                              l2_evict_first_policy());
+                              l2_evict_normal_policy());
             }
         }
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(hs_bar, 0))) {
@@ -401,12 +402,13 @@ extern "C" luce_status luce_moe_down_combine(const luce_block_q8_0 *w_down, cons
     const long long Tk = (long long)a.TT * k;
     const long long nv_up = std::min<long long>(E, Tk) + Tk / NCU + (ws_down ? (a.TT + NCU - 1) / NCU : 0);
     const int stage = RN * a.rowbytes;
-    a.NS = (int)std::max<long long>(2, std::min<long long>(nv_up, (100 * 1024) / stage));
+    a.NS = (int)std::max<long long>(2, std::min<long long>(nv_up, ((long long)g_tuning.down_budget_kb * 1024) / stage));
+    a.evict_first = g_tuning.evict_first;
     // activation rows of a tile in shared memory when they fit in 24 KB (a row
     // is a multiple of 16 bytes since I % 256 == 0)
     const size_t xrow = (size_t)a.nbI * Q8_1_BYTES;
     const int slots = a.TT * k + (ws_down ? a.TT : 0);
-    a.hs_rows = ((size_t)slots * xrow <= 24 * 1024) ? slots : 0;
+    a.hs_rows = (g_tuning.down_stage && (size_t)slots * xrow <= 24 * 1024) ? slots : 0;
     const size_t smem = (size_t)a.NS * stage + (size_t)(2 * a.NS + 2) * sizeof(uint64_t) + (size_t)a.hs_rows * xrow +
                         (size_t)(a.TT * k + a.TT) * RN * sizeof(float) + (size_t)(3 * E + 1) * sizeof(int);
     const int tiles = (T + a.TT - 1) / a.TT;

@@ -69,6 +69,8 @@ struct GluArgs {
     int RU;      // rows per part (divides 32 / cluster size)
     int NS;      // stages (one part each) in the ring
     int xs_cols; // activation columns staged in shared memory (0: read through L1)
+    int prefetch; // warm L2 with the shared expert before waiting
+    int evict_first;
 };
 
 struct Group {
@@ -111,7 +113,7 @@ __device__ __forceinline__ Group decode_group(const GluArgs &a, const int *vpre,
 }
 
 template <int NC>
-__global__ void __launch_bounds__(THREADS, 1) k_glu_pair(const GluArgs a)
+__global__ void __launch_bounds__(THREADS) k_glu_pair(const GluArgs a)
 {
     namespace cg = cooperative_groups;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -136,7 +138,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_glu_pair(const GluArgs a)
         s_abort = 0;
         // before the grouping has finished: warm L2 with this CTA's slice of
         // the shared expert (needed whatever the routing)
-        if (a.wsg) {
+        if (a.wsg && a.prefetch) {
             const size_t total = (size_t)a.I * a.rowbytes; // multiple of 16
             const size_t chunk = ((total / gridDim.x) + 15) & ~size_t(15);
             const size_t off = chunk * blockIdx.x;
@@ -184,7 +186,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_glu_pair(const GluArgs a)
     const int RPC = 32 / csize;   // rows of each group this CTA streams
     const int PPG = RPC / a.RU;   // parts per group
     const long long NP = (g1 - g0) * PPG;
-    const uint64_t pol = l2_evict_first_policy();
+    const uint64_t pol = a.evict_first ? l2_evict_first_policy() : l2_evict_normal_policy();
 
     // thread 0 requests part q (of this CTA's NP) into stage q % NS
     auto issue = [&](long long q) {
@@ -339,6 +341,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_glu_pair(const GluArgs a)
 // steady-state calls make no attribute or occupancy query).
 struct LaunchCache {
     size_t smem = 0;
+    int cps = 0;
     int clusters[3] = {0, 0, 0};
 };
 
@@ -359,7 +362,12 @@ luce_status launch_glu(const GluArgs &a, cudaStream_t stream, size_t smem, int c
         c.smem = smem;
         c.clusters[1] = c.clusters[2] = 0;
     }
-    const int nsm = luce_host::sm_count();
+    const int cps = std::max(1, luce_host::g_tuning.glu_cps);
+    if (c.cps != cps) {
+        c.cps = cps;
+        c.clusters[1] = c.clusters[2] = 0;
+    }
+    const int nsm = luce_host::sm_count() * cps;
     if (c.clusters[csize] == 0) {
         int n = nsm / csize;
         if (csize > 1) {
@@ -424,22 +432,26 @@ extern "C" luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const lu
     // evenly over the SMs; one CTA per cluster otherwise
     const long long Tk = (long long)T * k;
     const long long nv_up = std::min<long long>(E, Tk) + Tk / NCU + (ws_gate ? (T + NCU - 1) / NCU : 0);
-    const int csize = (nv_up * (I / 32) < 4LL * sm_count()) ? 2 : 1;
+    const Tuning &tu = g_tuning;
+    const int csize = tu.glu_csize ? tu.glu_csize : ((nv_up * (I / 32) < 4LL * sm_count()) ? 2 : 1);
     const int RPC = 32 / csize;
     // a part (RU gate rows + RU up rows) of about 35 KB, but at least one row
     // per warp while a part stays under 72 KB
     int RU = RPC;
-    while (RU > 1 && 2 * RU * a.rowbytes > 36 * 1024 && !(RU <= CW && 2 * RU * a.rowbytes <= 72 * 1024))
+    while (RU > 1 && 2 * RU * a.rowbytes > tu.glu_part_kb * 1024 &&
+           !(RU <= CW && 2 * RU * a.rowbytes <= 2 * tu.glu_part_kb * 1024))
         RU /= 2;
     a.RU = RU;
     // activation rows in shared memory when up to 32 columns fit in 40 KB
     const int maxcols = std::min(T, NCU);
     const size_t xrow = (size_t)a.nb * Q8_1_BYTES;
-    a.xs_cols = (maxcols * xrow <= 40 * 1024) ? maxcols : 0;
+    a.xs_cols = (tu.glu_xs && maxcols * xrow <= 40 * 1024) ? maxcols : 0;
+    a.prefetch = tu.glu_prefetch;
+    a.evict_first = tu.evict_first;
     const size_t stage = (size_t)2 * RU * a.rowbytes;
     const size_t fixed = (size_t)a.xs_cols * xrow + (size_t)(E + 1) * sizeof(int) +
                          (size_t)2 * 32 * HB_STRIDE * sizeof(float) + 64;
-    const size_t budget = 216 * 1024;
+    const size_t budget = (size_t)tu.glu_budget_kb * 1024;
     int NS = (int)std::min<size_t>(16, (budget - fixed) / (stage + 8));
     NS = std::max(NS, 2);
     a.NS = NS;

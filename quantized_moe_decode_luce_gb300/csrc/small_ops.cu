@@ -437,6 +437,7 @@ extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault
 extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault_down(unsigned int *bits);
 
 namespace luce_host {
+Tuning g_tuning;
 static int g_pdl = 0;
 bool pdl_enabled() { return __atomic_load_n(&g_pdl, __ATOMIC_RELAXED) != 0; }
 
