@@ -297,11 +297,14 @@ int sm_count();
 // Launch-shape parameters of the streaming kernels.  The values here are the
 // library's choices; they are plain data so that a tuning build can sweep
 // them, and every setting computes the same result.
+// Defaults measured on GB300 with the 43-layer decode stack (graph + PDL):
+// two gate/up CTAs per SM with ~108 KB rings leave room for the down kernel's
+// CTAs to start early and stream their weights while the gate/up kernel runs.
 struct Tuning {
-    int glu_csize = 0;        // CTAs per cluster for the gate/up kernel (0: automatic)
+    int glu_csize = 1;        // CTAs per cluster for the gate/up kernel (0: automatic)
     int glu_part_kb = 36;     // target bytes of one part (RU gate + RU up rows)
-    int glu_budget_kb = 216;  // shared-memory ring budget per CTA
-    int glu_cps = 1;          // gate/up CTAs per SM
+    int glu_budget_kb = 108;  // shared-memory ring budget per CTA
+    int glu_cps = 2;          // gate/up CTAs per SM
     int glu_xs = 1;           // stage activation rows in shared memory
     int glu_prefetch = 1;     // warm L2 with the shared expert before waiting
     int down_budget_kb = 100; // down/combine ring budget per CTA
