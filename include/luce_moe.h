@@ -211,6 +211,30 @@ LUCE_API luce_status luce_argmax(const float *logits, int R, int64_t V, int32_t 
 LUCE_API size_t luce_argmax_workspace_bytes(int R, int64_t V);
 
 /* ------------------------------------------------------------------------
+ * luce_argmax_noalloc -- the same argmax as luce_argmax, for callers that
+ * cannot allocate device memory: a host application that owns every device
+ * allocation and hands this library none, or a loop that must never call
+ * into the CUDA allocator.  Such callers cannot supply the workspace of
+ * luce_argmax, so this call uses scratch that the library itself holds: a
+ * fixed 16 KB array of device memory that exists on every GPU that loads the
+ * library, from load to exit.  (The pages have no counterpart of this call;
+ * it exists only for such callers.)
+ *
+ *   logits [R][V] fp32   idx [R] int32 out   val [R] fp32 out or NULL
+ * Results are identical to luce_argmax.  Allocates nothing: no cudaMalloc,
+ * no cudaFree, no allocating library routine.  R above 1024 rows, or a
+ * (R, V) whose scratch need (luce_argmax_workspace_bytes) exceeds 16 KB,
+ * returns LUCE_ERR_UNSUPPORTED: use luce_argmax with a workspace instead.
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture begins.
+ * Every call clears the part of the array that must start at zero.  All
+ * calls share the one array, so calls that overlap on the GPU (on different
+ * streams, or from different host threads) race: order them on one stream.
+ */
+LUCE_API luce_status luce_argmax_noalloc(const float *logits, int R, int64_t V, int32_t *idx, float *val,
+                                         void *stream);
+
+/* ------------------------------------------------------------------------
  * luce_moe_prep -- luce_route_topk, luce_quantize_q8_1 (K = H) and
  * luce_moe_group in ONE launch (one CTA) when T <= 32 and E <= 256, else the
  * three launches in that order.  Same arguments, outputs and results as the

@@ -48,6 +48,7 @@ def lib() -> ctypes.CDLL:
             "luce_moe_prep": [P, P, P, i32, i32, i32, i32, P, P, P, P, P, P, P],
             "luce_moe_down_combine": [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, P, i32, P],
             "luce_argmax": [P, i32, i64, P, P, P, sz, P],
+            "luce_argmax_noalloc": [P, i32, i64, P, P, P],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -159,6 +160,13 @@ def luce_argmax(logits, idx, val, workspace, stream=None) -> None:
         _ptr(workspace, u8, "workspace"), workspace.numel() if workspace is not None else 0, _stream(stream)))
 
 
+def luce_argmax_noalloc(logits, idx, val, stream=None) -> None:
+    """The argmax with the library's own fixed scratch (no allocation)."""
+    R, V = logits.shape
+    _check("luce_argmax_noalloc", lib().luce_argmax_noalloc(
+        _ptr(logits, f32, "logits"), R, V, _ptr(idx, i32, "idx"), _ptr(val, f32, "val"), _stream(stream)))
+
+
 def luce_get_fault() -> int:
     bits = ctypes.c_uint(0)
     _check("luce_get_fault", lib().luce_get_fault(ctypes.byref(bits)))
@@ -171,6 +179,6 @@ def luce_version() -> int:
 
 __all__ = ["LuceError", "lib", "status_string", "luce_route_topk", "luce_quantize_q8_1", "luce_moe_group",
            "luce_moe_glu_pair", "luce_moe_prep", "luce_set_pdl",
-           "luce_moe_down_combine", "luce_argmax", "luce_argmax_workspace_bytes",
+           "luce_moe_down_combine", "luce_argmax", "luce_argmax_workspace_bytes", "luce_argmax_noalloc",
            "luce_get_fault", "luce_version", "LUCE_OK", "LUCE_ERR_INVALID_ARG", "LUCE_ERR_UNSUPPORTED",
            "LUCE_ERR_CUDA", "LUCE_FAULT_BAD_ID", "LUCE_FAULT_TIMEOUT"]

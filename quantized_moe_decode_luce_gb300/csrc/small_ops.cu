@@ -611,3 +611,63 @@ extern "C" luce_status luce_moe_prep(const float *logits, const float *bias, con
         return launch(k_moe_prep<4>, dim3(1), dim3(GROUP_THREADS), smem, st, a);
     return launch(k_moe_prep<8>, dim3(1), dim3(GROUP_THREADS), smem, st, a);
 }
+
+// ===========================================================================
+// luce_argmax_noalloc: the argmax pair/pick with library-owned scratch.
+//
+// Some callers cannot allocate device memory at all: a host application that
+// owns every device allocation and gives this library none, or a loop that
+// must never call into the CUDA allocator.  They cannot provide the
+// workspace luce_argmax needs, so this entry point keeps its scratch (the
+// per-chunk pairs and the per-row counters) in a fixed array of device memory
+// that the library holds from load to exit on every GPU that loads it.
+// ===========================================================================
+namespace {
+constexpr size_t kNoallocScratchBytes = 16384; // the fixed maximum
+constexpr int kNoallocMaxRows = 1024;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+// Device address of g_noalloc_scratch per device, set once by the first call
+// made with that device current (in host code the array's name is only a
+// stand-in, not a device address).
+static void *g_noalloc_scratch_addr[64];
+} // namespace
+
+extern "C" luce_status luce_argmax_noalloc(const float *logits, int R, int64_t V, int32_t *idx, float *val,
+                                           void *stream)
+{
+    if (R < 0 || V < 1 || V >= ((int64_t)1 << 31))
+        return LUCE_ERR_INVALID_ARG;
+    if (R == 0)
+        return LUCE_OK;
+    if (!logits || !idx || !aligned(logits, 4) || !aligned(idx, 4) || (val && !aligned(val, 4)))
+        return LUCE_ERR_INVALID_ARG;
+    const size_t need = luce_argmax_workspace_bytes(R, V);
+    if (R > kNoallocMaxRows || need > kNoallocScratchBytes)
+        return LUCE_ERR_UNSUPPORTED; // beyond the fixed scratch: use luce_argmax with a workspace
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return LUCE_ERR_CUDA;
+    void *base = g_noalloc_scratch_addr[dev];
+    if (base == nullptr) {
+        if (cudaGetSymbolAddress(&base, g_noalloc_scratch) != cudaSuccess || base == nullptr) {
+            (void)cudaGetLastError();
+            return LUCE_ERR_CUDA;
+        }
+        g_noalloc_scratch_addr[dev] = base;
+    }
+    int64_t L;
+    int C;
+    argmax_chunks(R, V, L, C);
+    ArgPair *pairs = reinterpret_cast<ArgPair *>(base);
+    unsigned int *counters =
+        reinterpret_cast<unsigned int *>(reinterpret_cast<uint8_t *>(base) + argmax_pairs_bytes(R, C));
+    // the row counters must start at zero whatever an earlier call left
+    if (cudaMemsetAsync(counters, 0, (size_t)R * sizeof(unsigned int), as_stream(stream)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return LUCE_ERR_CUDA;
+    }
+    const bool vec4 = (V % 4 == 0) && aligned(logits, 16);
+    dim3 grid((unsigned)C, (unsigned)R);
+    return launch(k_argmax, grid, dim3(ARGMAX_THREADS), 0, as_stream(stream), logits, V, L, C, vec4, pairs, counters,
+                  idx, val);
+}
