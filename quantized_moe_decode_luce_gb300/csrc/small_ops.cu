@@ -311,6 +311,85 @@ __global__ void __launch_bounds__(GROUP_THREADS) k_moe_prep(const PrepArgs a)
     group_body(ids_s, a.T * a.k, a.E, 32, hist, excl, a.counts, a.offsets, a.routes);
 }
 
+// Small prep: T <= 8 tokens, T*k <= 64 routes, E <= 256 experts (decode and
+// verify).  256 threads: warp t routes token t while every warp quantizes
+// its share of the input blocks; after one CTA barrier, warp 0 alone groups
+// the routes with shuffles (no further CTA barrier): lane l counts experts
+// l, l+32, ..., a warp scan gives the offsets, and route r's slot is its
+// expert's offset plus the number of earlier routes of that expert.
+constexpr int PREP_SMALL_THREADS = 256;
+constexpr int PREP_SMALL_MAX_T = 8;
+constexpr int PREP_SMALL_MAX_R = 64;
+
+template <int EPL>
+__global__ void __launch_bounds__(PREP_SMALL_THREADS) k_moe_prep_small(const PrepArgs a)
+{
+    __shared__ int ids_s[PREP_SMALL_MAX_R];
+    __shared__ int s_off[256];
+    pdl_wait();
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = PREP_SMALL_THREADS / 32;
+    if (warp < a.T) {
+        const size_t o = (size_t)warp * a.k;
+        route_token_regs<EPL>(a.logits + (size_t)warp * a.E, a.bias, a.E, a.k, ids_s + o, a.ids + o,
+                              a.weights + o, lane);
+    }
+    const int nbl = a.T * (a.H / QK);
+    for (int b = warp; b < nbl; b += nwarps)
+        quantize_q8_1_warp(a.x[(size_t)b * QK + lane], a.xq + (size_t)b * Q8_1_WORDS, lane);
+    __syncthreads();
+    if (warp != 0)
+        return;
+    const int R = a.T * a.k;
+    // counts of experts lane + 32 i, then an exclusive scan in expert order
+    int cnt[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; i++)
+        cnt[i] = 0;
+    for (int r = 0; r < R; r++) {
+        const int e = ids_s[r];
+#pragma unroll
+        for (int i = 0; i < EPL; i++)
+            cnt[i] += (e == lane + 32 * i) ? 1 : 0;
+    }
+    int carry = 0;
+    int off[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; i++) {
+        int inc = cnt[i];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o)
+                inc += v;
+        }
+        off[i] = carry + inc - cnt[i];
+        carry += __shfl_sync(0xffffffffu, inc, 31);
+        const int e = lane + 32 * i;
+        if (e < a.E) {
+            a.counts[e] = cnt[i];
+            a.offsets[e] = off[i];
+            s_off[e] = off[i];
+        }
+    }
+    if (lane == 0)
+        a.offsets[a.E] = carry;
+    __syncwarp();
+    // route r goes to its expert's offset plus the earlier routes of that expert
+    for (int r = lane; r < R; r += 32) {
+        const int e = ids_s[r];
+        if (e < 0 || e >= a.E)
+            continue;
+        int before = 0;
+        for (int q = 0; q < r; q++)
+            before += (ids_s[q] == e) ? 1 : 0;
+        a.routes[s_off[e] + before] = r;
+    }
+    for (int r = carry + lane; r < R; r += 32)
+        a.routes[r] = -1;
+}
+
 // ---------------------------------------------------------------------------
 // Argmax pair/pick ([PR826], commit "fused DS4.1 decode kernels").  CTA
 // (c, r) reduces chunk c of row r to a (value, index) pair; the CTA that
@@ -603,6 +682,16 @@ extern "C" luce_status luce_moe_prep(const float *logits, const float *bias, con
     const size_t smem = ((size_t)T * k + 32 * (size_t)E + E + 1) * sizeof(int);
     const int epl = (E + 31) / 32;
     cudaStream_t st = as_stream(stream);
+    if (T <= PREP_SMALL_MAX_T && T * k <= PREP_SMALL_MAX_R) {
+        const dim3 g1(1), b1(PREP_SMALL_THREADS);
+        if (epl <= 1)
+            return launch(k_moe_prep_small<1>, g1, b1, 0, st, a);
+        if (epl <= 2)
+            return launch(k_moe_prep_small<2>, g1, b1, 0, st, a);
+        if (epl <= 4)
+            return launch(k_moe_prep_small<4>, g1, b1, 0, st, a);
+        return launch(k_moe_prep_small<8>, g1, b1, 0, st, a);
+    }
     if (epl <= 1)
         return launch(k_moe_prep<1>, dim3(1), dim3(GROUP_THREADS), smem, st, a);
     if (epl <= 2)
