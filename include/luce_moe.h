@@ -155,6 +155,11 @@ LUCE_API luce_status luce_moe_group(const int32_t *ids, int T, int k, int E, int
  *                  Every call leaves it zero-filled again, so one buffer
  *                  serves any number of calls on one stream; calls that
  *                  overlap on the GPU must not share it.
+ *   w_down, ws_down  optional (NULL to skip): the down weights of the
+ *                  luce_moe_down_combine call that follows.  The CTAs then
+ *                  also ask L2 for the rows of every expert with routes (and
+ *                  of the shared expert), so that the down product reads
+ *                  them from L2.  Results do not depend on them.
  *   variant        0 = automatic (only one kernel exists in this build)
  * Requires H % 256 == 0, I % 256 == 0, H/32 <= 1024; w_*, xq, hq 16-byte
  * aligned; ws_gate and ws_up both given or both NULL.
@@ -163,7 +168,8 @@ LUCE_API luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const luce
                               const luce_block_q8_0 *ws_gate, const luce_block_q8_0 *ws_up,
                               const luce_block_q8_1 *xq, const int32_t *offsets, const int32_t *routes, int T, int k,
                               int E, int H, int I, float clamp, float *h, luce_block_q8_1 *hq, void *workspace,
-                              size_t workspace_bytes, int variant, void *stream);
+                              size_t workspace_bytes, const luce_block_q8_0 *w_down,
+                              const luce_block_q8_0 *ws_down, int variant, void *stream);
 LUCE_API size_t luce_moe_glu_workspace_bytes(int T, int k, int E, int I);
 
 /* ------------------------------------------------------------------------

@@ -44,7 +44,7 @@ def lib() -> ctypes.CDLL:
             "luce_route_topk": [P, P, i32, i32, i32, P, P, P],
             "luce_quantize_q8_1": [P, i32, i32, P, P],
             "luce_moe_group": [P, i32, i32, i32, P, P, P, P],
-            "luce_moe_glu_pair": [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, P, sz, i32, P],
+            "luce_moe_glu_pair": [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, P, sz, P, P, i32, P],
             "luce_moe_prep": [P, P, P, i32, i32, i32, i32, P, P, P, P, P, P, P],
             "luce_moe_down_combine": [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, P, i32, P],
             "luce_argmax": [P, i32, i64, P, P, P, sz, P],
@@ -127,12 +127,14 @@ def luce_moe_glu_workspace_bytes(T: int, k: int, E: int, I: int) -> int:
 
 
 def luce_moe_glu_pair(w_gate, w_up, ws_gate, ws_up, xq, offsets, routes, T: int, k: int, E: int, H: int, I: int,
-                      clamp: float, h, hq, workspace, variant: int = 0, stream=None) -> None:
+                      clamp: float, h, hq, workspace, w_down=None, ws_down=None, variant: int = 0,
+                      stream=None) -> None:
     _check("luce_moe_glu_pair", lib().luce_moe_glu_pair(
         _ptr(w_gate, u8, "w_gate"), _ptr(w_up, u8, "w_up"), _ptr(ws_gate, u8, "ws_gate"), _ptr(ws_up, u8, "ws_up"),
         _ptr(xq, u8, "xq"), _ptr(offsets, i32, "offsets"), _ptr(routes, i32, "routes"), T, k, E, H, I,
         float(clamp), _ptr(h, f32, "h"), _ptr(hq, u8, "hq"), _ptr(workspace, u8, "workspace"),
-        workspace.numel() if workspace is not None else 0, variant, _stream(stream)))
+        workspace.numel() if workspace is not None else 0, _ptr(w_down, u8, "w_down"),
+        _ptr(ws_down, u8, "ws_down"), variant, _stream(stream)))
 
 
 def luce_moe_prep(logits, bias, x, k: int, ids, weights, xq, counts, offsets, routes, stream=None) -> None:

@@ -268,6 +268,13 @@ __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Per-thread prefetch of one 128-byte line into L2 (load/store path, not the
+// bulk-copy engine).
+__device__ __forceinline__ void prefetch_line_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Named barrier among `nthreads` threads (id 0 is __syncthreads).
 __device__ __forceinline__ void named_barrier(int id, int nthreads)
 {
@@ -309,6 +316,8 @@ struct Tuning {
     int glu_prefetch = 1;     // warm L2 with the shared expert before waiting
     int down_budget_kb = 100; // down/combine ring budget per CTA
     int down_stage = 1;       // stage the tile's activation rows in shared memory
+    int glu_l2pf = 1;         // gate/up CTAs prefetch their own parts into L2 per thread
+    int glu_down_pf = 1;      // gate/up CTAs prefetch the active experts' down rows into L2
     int evict_first = 1;      // stream weights with the L2 evict-first policy
 };
 extern Tuning g_tuning;

@@ -62,6 +62,7 @@ struct GluArgs {
     float *h;                 // [T*k+T][I]
     uint32_t *hq;             // [T*k+T][I/32] q8_1 blocks
     unsigned int *group_cnt;  // [nv_max * I/32] zero-filled counters, left zero-filled
+    const uint8_t *wd, *wsd;  // down weights to prefetch into L2, or null
     int T, k, E, H, I;
     float clamp;
     int nb, rowbytes;
@@ -70,6 +71,7 @@ struct GluArgs {
     int xs_cols; // activation columns staged in shared memory (0: read through L1)
     int prefetch; // warm L2 with the shared expert before waiting
     int evict_first;
+    int l2pf;     // prefetch this CTA's own parts into L2 (per thread)
 };
 
 struct Group {
@@ -196,6 +198,39 @@ __global__ void __launch_bounds__(THREADS) k_glu_pair(const GluArgs a)
     if (tid == 0) {
         for (; issued < NP && issued < a.NS; issued++)
             issue(issued);
+    }
+    // Parts beyond the first ring-full: ask L2 for them now, through the
+    // load/store path (one 128-byte line per thread and instruction), so that
+    // their bulk copies later hit L2.  The bulk-copy engine of an SM moves far
+    // less than its share of HBM bandwidth, and these requests use the rest.
+    if (a.l2pf) {
+        for (long long q = a.NS + warp; q < NP; q += CW) {
+            const long long u = u0 + q;
+            const Group gr = decode_group(a, vpre, NVr, u / CL);
+            const size_t row0 = (size_t)gr.grp * 32 + (size_t)(u % CL) * a.RU;
+            for (int off = lane * 128; off < half_bytes; off += 32 * 128) {
+                prefetch_line_l2(gr.g + row0 * a.rowbytes + off);
+                prefetch_line_l2(gr.u + row0 * a.rowbytes + off);
+            }
+        }
+    }
+    // The following down product's rows of the active experts (and of the
+    // shared expert): this CTA's slice of them, into L2.
+    if (a.wd) {
+        const size_t dbytes = (size_t)a.H * (a.I / 32) * Q8_0_BYTES; // one expert's down matrix
+        const int nact = NVr > 0 ? a.E : 0;
+        const size_t per = ((dbytes / gridDim.x) + 127) & ~size_t(127);
+        const size_t lo = per * blockIdx.x, hi = min(dbytes, lo + per);
+        for (int e = 0; e < nact; e++) {
+            if (vpre[e + 1] == vpre[e])
+                continue; // no routes for this expert
+            const uint8_t *base = a.wd + (size_t)e * dbytes;
+            for (size_t off = lo + (size_t)tid * 128; off < hi; off += (size_t)THREADS * 128)
+                prefetch_line_l2(base + off);
+        }
+        if (a.wsd)
+            for (size_t off = lo + (size_t)tid * 128; off < hi; off += (size_t)THREADS * 128)
+                prefetch_line_l2(a.wsd + off);
     }
 
     const int xstride = a.nb * Q8_1_WORDS; // words per activation row
@@ -409,7 +444,8 @@ extern "C" luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const lu
                                          const luce_block_q8_0 *ws_gate, const luce_block_q8_0 *ws_up,
                                          const luce_block_q8_1 *xq, const int32_t *offsets, const int32_t *routes,
                                          int T, int k, int E, int H, int I, float clamp, float *h,
-                                         luce_block_q8_1 *hq, void *workspace, size_t workspace_bytes, int variant,
+                                         luce_block_q8_1 *hq, void *workspace, size_t workspace_bytes,
+                                         const luce_block_q8_0 *w_down, const luce_block_q8_0 *ws_down, int variant,
                                          void *stream)
 {
     if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 64 || (int64_t)T * k > (1 << 20))
@@ -462,6 +498,9 @@ extern "C" luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const lu
     a.xs_cols = (tu.glu_xs && maxcols * xrow <= 40 * 1024) ? maxcols : 0;
     a.prefetch = tu.glu_prefetch;
     a.evict_first = tu.evict_first;
+    a.l2pf = tu.glu_l2pf;
+    a.wd = tu.glu_down_pf ? reinterpret_cast<const uint8_t *>(w_down) : nullptr;
+    a.wsd = (tu.glu_down_pf && w_down) ? reinterpret_cast<const uint8_t *>(ws_down) : nullptr;
     const size_t stage = (size_t)2 * RU * a.rowbytes;
     const size_t fixed = (size_t)a.xs_cols * xrow + (size_t)(E + 1) * sizeof(int) +
                          (size_t)2 * 32 * HB_STRIDE * sizeof(float) + 64;

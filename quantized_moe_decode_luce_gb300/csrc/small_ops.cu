@@ -312,12 +312,12 @@ __global__ void __launch_bounds__(GROUP_THREADS) k_moe_prep(const PrepArgs a)
 }
 
 // Small prep: T <= 8 tokens, T*k <= 64 routes, E <= 256 experts (decode and
-// verify).  256 threads: warp t routes token t while every warp quantizes
-// its share of the input blocks; after one CTA barrier, warp 0 alone groups
+// verify).  512 threads: warp t routes token t while the other warps share
+// the quantization of the input blocks; after one CTA barrier, warp 0 alone groups
 // the routes with shuffles (no further CTA barrier): lane l counts experts
 // l, l+32, ..., a warp scan gives the offsets, and route r's slot is its
 // expert's offset plus the number of earlier routes of that expert.
-constexpr int PREP_SMALL_THREADS = 256;
+constexpr int PREP_SMALL_THREADS = 512;
 constexpr int PREP_SMALL_MAX_T = 8;
 constexpr int PREP_SMALL_MAX_R = 64;
 
@@ -335,9 +335,11 @@ __global__ void __launch_bounds__(PREP_SMALL_THREADS) k_moe_prep_small(const Pre
         route_token_regs<EPL>(a.logits + (size_t)warp * a.E, a.bias, a.E, a.k, ids_s + o, a.ids + o,
                               a.weights + o, lane);
     }
+    // the routing warps do not quantize: the other warps share the blocks
     const int nbl = a.T * (a.H / QK);
-    for (int b = warp; b < nbl; b += nwarps)
-        quantize_q8_1_warp(a.x[(size_t)b * QK + lane], a.xq + (size_t)b * Q8_1_WORDS, lane);
+    if (warp >= a.T)
+        for (int b = warp - a.T; b < nbl; b += nwarps - a.T)
+            quantize_q8_1_warp(a.x[(size_t)b * QK + lane], a.xq + (size_t)b * Q8_1_WORDS, lane);
     __syncthreads();
     if (warp != 0)
         return;

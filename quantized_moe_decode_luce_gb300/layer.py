@@ -49,7 +49,7 @@ class MoEStep:
         wsu = layer.wsu if self.shared else None
         wsd = layer.wsd if self.shared else None
         B.luce_moe_glu_pair(layer.wg, layer.wu, wsg, wsu, self.xq, self.offsets, self.routes, T, k, E, H, I,
-                            self.clamp, self.h, self.hq, self.glu_ws, 0, stream)
+                            self.clamp, self.h, self.hq, self.glu_ws, layer.wd, wsd, 0, stream)
         B.luce_moe_down_combine(layer.wd, wsd, self.hq, self.ids, self.weights, self.offsets, self.routes,
                                 T, k, E, H, I, out, 0, stream)
         return out

@@ -93,7 +93,7 @@ def test_group_validation(lib):
 def test_glu_and_down_validation(lib):
     g = lib.luce_moe_glu_pair
     g.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int] * 5 + [ctypes.c_float] + [ctypes.c_void_p] * 3 + \
-        [ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
+        [ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
     wsb = lib.luce_moe_glu_workspace_bytes
     wsb.argtypes = [ctypes.c_int] * 4
     wsb.restype = ctypes.c_size_t
@@ -102,14 +102,14 @@ def test_glu_and_down_validation(lib):
     assert wsb(512, 8, 128, 1536) == (128 + 128 + 16) * 48 * 4
     P = [_p(GOOD)] * 7
     W3 = (_p(GOOD), _p(GOOD), _p(GOOD))
-    assert g(*P, 1, 2, 8, 480, 256, 0.0, *W3, n, 0, None) == 1       # H % 256
-    assert g(*P, 1, 2, 8, 512, 96, 0.0, *W3, n, 0, None) == 1        # I % 256
-    assert g(*P, 1, 2, 8, 512, 256, 0.0, *W3, n, 7, None) == 1       # variant
-    assert g(_p(GOOD + 8), *P[1:], 1, 2, 8, 512, 256, 0.0, *W3, n, 0, None) == 1  # 16-B alignment
-    assert g(P[0], P[1], P[2], None, *P[4:], 1, 2, 8, 512, 256, 0.0, *W3, n, 0, None) == 1
-    assert g(*P, 1, 2, 8, 512, 256, 0.0, _p(GOOD), _p(GOOD), None, n, 0, None) == 1   # no workspace
-    assert g(*P, 1, 2, 8, 512, 256, 0.0, *W3, n - 4, 0, None) == 1                     # workspace too small
-    assert g(*P, 0, 2, 8, 512, 256, 0.0, *W3, n, 0, None) == 0       # T = 0
+    assert g(*P, 1, 2, 8, 480, 256, 0.0, *W3, n, None, None, 0, None) == 1       # H % 256
+    assert g(*P, 1, 2, 8, 512, 96, 0.0, *W3, n, None, None, 0, None) == 1        # I % 256
+    assert g(*P, 1, 2, 8, 512, 256, 0.0, *W3, n, None, None, 7, None) == 1       # variant
+    assert g(_p(GOOD + 8), *P[1:], 1, 2, 8, 512, 256, 0.0, *W3, n, None, None, 0, None) == 1  # 16-B alignment
+    assert g(P[0], P[1], P[2], None, *P[4:], 1, 2, 8, 512, 256, 0.0, *W3, n, None, None, 0, None) == 1
+    assert g(*P, 1, 2, 8, 512, 256, 0.0, _p(GOOD), _p(GOOD), None, n, None, None, 0, None) == 1   # no workspace
+    assert g(*P, 1, 2, 8, 512, 256, 0.0, *W3, n - 4, None, None, 0, None) == 1                     # workspace too small
+    assert g(*P, 0, 2, 8, 512, 256, 0.0, *W3, n, None, None, 0, None) == 0       # T = 0
     d = lib.luce_moe_down_combine
     d.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int] * 5 + [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
     assert d(*P, 1, 2, 8, 512, 100, _p(GOOD), 0, None) == 1
