@@ -321,7 +321,7 @@ def run_ours(args, wl, layers):
                 e0, e1, e2 = record[l]
                 e0.record()
             Bd.luce_moe_glu_pair(lay.wg, lay.wu, lay.wsg, lay.wsu, bufs.xq, bufs.offsets, bufs.routes, wl.T,
-                                 wl.k, wl.E, wl.H, wl.I, wl.clamp, bufs.h, bufs.hq, bufs.glu_ws, lay.wd, lay.wsd)
+                                 wl.k, wl.E, wl.H, wl.I, wl.clamp, bufs.h, bufs.hq)
             if record is not None:
                 e1.record()
             Bd.luce_moe_down_combine(lay.wd, lay.wsd, bufs.hq, bufs.ids, bufs.weights, bufs.offsets, bufs.routes,

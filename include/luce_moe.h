@@ -148,18 +148,6 @@ LUCE_API luce_status luce_moe_group(const int32_t *ids, int T, int k, int E, int
  *   w_gate, w_up   [E][I][H/32] Q8_0        ws_gate, ws_up [I][H/32] or NULL
  *   xq             [T][H/32] q8_1           offsets [E+1], routes [T*k]
  *   h              [T*k + T][I] fp32 out    hq [T*k + T][I/32] q8_1 out
- *   workspace      device scratch of at least luce_moe_glu_workspace_bytes
- *                  (T, k, E, I) bytes, 4-byte aligned, ZERO-FILLED before its
- *                  first use: one counter per (expert, 32-row group) lets the
- *                  CTA that completes a group shared by two CTAs quantize it.
- *                  Every call leaves it zero-filled again, so one buffer
- *                  serves any number of calls on one stream; calls that
- *                  overlap on the GPU must not share it.
- *   w_down, ws_down  optional (NULL to skip): the down weights of the
- *                  luce_moe_down_combine call that follows.  The CTAs then
- *                  also ask L2 for the rows of every expert with routes (and
- *                  of the shared expert), so that the down product reads
- *                  them from L2.  Results do not depend on them.
  *   variant        0 = automatic (only one kernel exists in this build)
  * Requires H % 256 == 0, I % 256 == 0, H/32 <= 1024; w_*, xq, hq 16-byte
  * aligned; ws_gate and ws_up both given or both NULL.
@@ -167,10 +155,8 @@ LUCE_API luce_status luce_moe_group(const int32_t *ids, int T, int k, int E, int
 LUCE_API luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const luce_block_q8_0 *w_up,
                               const luce_block_q8_0 *ws_gate, const luce_block_q8_0 *ws_up,
                               const luce_block_q8_1 *xq, const int32_t *offsets, const int32_t *routes, int T, int k,
-                              int E, int H, int I, float clamp, float *h, luce_block_q8_1 *hq, void *workspace,
-                              size_t workspace_bytes, const luce_block_q8_0 *w_down,
-                              const luce_block_q8_0 *ws_down, int variant, void *stream);
-LUCE_API size_t luce_moe_glu_workspace_bytes(int T, int k, int E, int I);
+                              int E, int H, int I, float clamp, float *h, luce_block_q8_1 *hq, int variant,
+                              void *stream);
 
 /* ------------------------------------------------------------------------
  * luce_moe_down_combine -- the Q8_0 down product of every route and of the

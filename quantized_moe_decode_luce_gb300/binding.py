@@ -44,7 +44,7 @@ def lib() -> ctypes.CDLL:
             "luce_route_topk": [P, P, i32, i32, i32, P, P, P],
             "luce_quantize_q8_1": [P, i32, i32, P, P],
             "luce_moe_group": [P, i32, i32, i32, P, P, P, P],
-            "luce_moe_glu_pair": [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, P, sz, P, P, i32, P],
+            "luce_moe_glu_pair": [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, i32, P],
             "luce_moe_prep": [P, P, P, i32, i32, i32, i32, P, P, P, P, P, P, P],
             "luce_moe_down_combine": [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, P, i32, P],
             "luce_argmax": [P, i32, i64, P, P, P, sz, P],
@@ -54,8 +54,6 @@ def lib() -> ctypes.CDLL:
             fn = getattr(L, name)
             fn.argtypes = args
             fn.restype = ctypes.c_int
-        L.luce_moe_glu_workspace_bytes.argtypes = [i32, i32, i32, i32]
-        L.luce_moe_glu_workspace_bytes.restype = sz
         L.luce_set_pdl.argtypes = [i32]
         L.luce_set_pdl.restype = ctypes.c_int
         L.luce_argmax_workspace_bytes.argtypes = [i32, i64]
@@ -122,19 +120,12 @@ def luce_moe_group(ids, E: int, counts, offsets, routes, stream=None) -> None:
         _ptr(routes, i32, "routes"), _stream(stream)))
 
 
-def luce_moe_glu_workspace_bytes(T: int, k: int, E: int, I: int) -> int:
-    return int(lib().luce_moe_glu_workspace_bytes(T, k, E, I))
-
-
 def luce_moe_glu_pair(w_gate, w_up, ws_gate, ws_up, xq, offsets, routes, T: int, k: int, E: int, H: int, I: int,
-                      clamp: float, h, hq, workspace, w_down=None, ws_down=None, variant: int = 0,
-                      stream=None) -> None:
+                      clamp: float, h, hq, variant: int = 0, stream=None) -> None:
     _check("luce_moe_glu_pair", lib().luce_moe_glu_pair(
         _ptr(w_gate, u8, "w_gate"), _ptr(w_up, u8, "w_up"), _ptr(ws_gate, u8, "ws_gate"), _ptr(ws_up, u8, "ws_up"),
         _ptr(xq, u8, "xq"), _ptr(offsets, i32, "offsets"), _ptr(routes, i32, "routes"), T, k, E, H, I,
-        float(clamp), _ptr(h, f32, "h"), _ptr(hq, u8, "hq"), _ptr(workspace, u8, "workspace"),
-        workspace.numel() if workspace is not None else 0, _ptr(w_down, u8, "w_down"),
-        _ptr(ws_down, u8, "ws_down"), variant, _stream(stream)))
+        float(clamp), _ptr(h, f32, "h"), _ptr(hq, u8, "hq"), variant, _stream(stream)))
 
 
 def luce_moe_prep(logits, bias, x, k: int, ids, weights, xq, counts, offsets, routes, stream=None) -> None:
@@ -187,7 +178,7 @@ def luce_version() -> int:
 
 
 __all__ = ["LuceError", "lib", "status_string", "luce_route_topk", "luce_quantize_q8_1", "luce_moe_group",
-           "luce_moe_glu_pair", "luce_moe_glu_workspace_bytes", "luce_moe_prep", "luce_set_pdl",
+           "luce_moe_glu_pair", "luce_moe_prep", "luce_set_pdl",
            "luce_moe_down_combine", "luce_argmax", "luce_argmax_workspace_bytes", "luce_argmax_noalloc",
            "luce_get_fault", "luce_version", "LUCE_OK", "LUCE_ERR_INVALID_ARG", "LUCE_ERR_UNSUPPORTED",
            "LUCE_ERR_CUDA", "LUCE_FAULT_BAD_ID", "LUCE_FAULT_TIMEOUT"]

@@ -268,13 +268,6 @@ __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
-// Per-thread prefetch of one 128-byte line into L2 (load/store path, not the
-// bulk-copy engine).
-__device__ __forceinline__ void prefetch_line_l2(const void *p)
-{
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 // Named barrier among `nthreads` threads (id 0 is __syncthreads).
 __device__ __forceinline__ void named_barrier(int id, int nthreads)
 {
@@ -308,7 +301,6 @@ int sm_count();
 // two gate/up CTAs per SM with ~108 KB rings leave room for the down kernel's
 // CTAs to start early and stream their weights while the gate/up kernel runs.
 struct Tuning {
-    int glu_csize = 1;        // CTAs per cluster for the gate/up kernel (0: automatic)
     int glu_part_kb = 36;     // target bytes of one part (RU gate + RU up rows)
     int glu_budget_kb = 108;  // shared-memory ring budget per CTA
     int glu_cps = 2;          // gate/up CTAs per SM
@@ -316,8 +308,6 @@ struct Tuning {
     int glu_prefetch = 1;     // warm L2 with the shared expert before waiting
     int down_budget_kb = 100; // down/combine ring budget per CTA
     int down_stage = 1;       // stage the tile's activation rows in shared memory
-    int glu_l2pf = 1;         // gate/up CTAs prefetch their own parts into L2 per thread
-    int glu_down_pf = 1;      // gate/up CTAs prefetch the active experts' down rows into L2
     int evict_first = 1;      // stream weights with the L2 evict-first policy
 };
 extern Tuning g_tuning;
@@ -326,10 +316,10 @@ extern Tuning g_tuning;
 // attribute (luce_set_pdl; process-wide, default off).
 bool pdl_enabled();
 
-// Launch configuration: the PDL attribute when enabled and, if cluster > 1, a
-// 1-D thread-block cluster of that size.  `attr` must hold two entries.
+// Launch configuration with the PDL attribute when enabled.  `attr` must
+// hold one entry.
 inline void make_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, dim3 grid, dim3 block, size_t smem,
-                        cudaStream_t stream, int cluster)
+                        cudaStream_t stream)
 {
     cfg = cudaLaunchConfig_t{};
     cfg.gridDim = grid;
@@ -342,32 +332,8 @@ inline void make_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, dim3
         attr[n].val.programmaticStreamSerializationAllowed = 1;
         n++;
     }
-    if (cluster > 1) {
-        attr[n].id = cudaLaunchAttributeClusterDimension;
-        attr[n].val.clusterDim.x = (unsigned)cluster;
-        attr[n].val.clusterDim.y = 1;
-        attr[n].val.clusterDim.z = 1;
-        n++;
-    }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-}
-
-// Launch `kern` with cudaLaunchKernelEx (PDL attribute when enabled, optional
-// cluster size).
-template <typename... KArgs, typename... Args>
-luce_status launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, int cluster,
-                      Args... args)
-{
-    cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[2];
-    make_config(cfg, attr, grid, block, smem, stream, cluster);
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
-    if (e != cudaSuccess) {
-        (void)cudaGetLastError();
-        return LUCE_ERR_CUDA;
-    }
-    return LUCE_OK;
 }
 
 // Launch `kern` with cudaLaunchKernelEx, with the PDL attribute when enabled.
@@ -375,8 +341,8 @@ template <typename... KArgs, typename... Args>
 luce_status launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args)
 {
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[2];
-    make_config(cfg, attr, grid, block, smem, stream, 1);
+    cudaLaunchAttribute attr[1];
+    make_config(cfg, attr, grid, block, smem, stream);
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();

@@ -30,7 +30,6 @@ class MoEStep:
         self.h = torch.empty((max(1, rows), I), dtype=torch.float32, device=dev)
         self.hq = torch.empty((max(1, rows), I // QK, Q8_1_BYTES), dtype=torch.uint8, device=dev)
         self.out = torch.empty((T, H), dtype=torch.float32, device=dev)
-        self.glu_ws = torch.zeros(max(16, B.luce_moe_glu_workspace_bytes(T, k, E, I)), dtype=torch.uint8, device=dev)
         self.fused_prep = True
 
     def run(self, layer, x, logits, bias=None, stream=None, out=None) -> torch.Tensor:
@@ -49,7 +48,7 @@ class MoEStep:
         wsu = layer.wsu if self.shared else None
         wsd = layer.wsd if self.shared else None
         B.luce_moe_glu_pair(layer.wg, layer.wu, wsg, wsu, self.xq, self.offsets, self.routes, T, k, E, H, I,
-                            self.clamp, self.h, self.hq, self.glu_ws, layer.wd, wsd, 0, stream)
+                            self.clamp, self.h, self.hq, 0, stream)
         B.luce_moe_down_combine(layer.wd, wsd, self.hq, self.ids, self.weights, self.offsets, self.routes,
                                 T, k, E, H, I, out, 0, stream)
         return out

@@ -28,7 +28,7 @@ def declared_symbols():
 def test_header_declares_the_six_ops_and_helpers():
     names = declared_symbols()
     for want in ["luce_route_topk", "luce_quantize_q8_1", "luce_moe_group", "luce_moe_glu_pair",
-                 "luce_moe_glu_workspace_bytes", "luce_moe_prep", "luce_set_pdl",
+                 "luce_moe_prep", "luce_set_pdl",
                  "luce_moe_down_combine", "luce_argmax", "luce_argmax_workspace_bytes", "luce_status_string",
                  "luce_get_fault", "luce_version"]:
         assert want in names
@@ -92,24 +92,16 @@ def test_group_validation(lib):
 
 def test_glu_and_down_validation(lib):
     g = lib.luce_moe_glu_pair
-    g.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int] * 5 + [ctypes.c_float] + [ctypes.c_void_p] * 3 + \
-        [ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
-    wsb = lib.luce_moe_glu_workspace_bytes
-    wsb.argtypes = [ctypes.c_int] * 4
-    wsb.restype = ctypes.c_size_t
-    n = wsb(1, 2, 8, 256)
-    assert n == (2 + 0 + 1) * (256 // 32) * 4          # (routed + shared) virtual experts x row groups
-    assert wsb(512, 8, 128, 1536) == (128 + 128 + 16) * 48 * 4
+    g.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int] * 5 + [ctypes.c_float] + [ctypes.c_void_p] * 2 + \
+        [ctypes.c_int, ctypes.c_void_p]
     P = [_p(GOOD)] * 7
-    W3 = (_p(GOOD), _p(GOOD), _p(GOOD))
-    assert g(*P, 1, 2, 8, 480, 256, 0.0, *W3, n, None, None, 0, None) == 1       # H % 256
-    assert g(*P, 1, 2, 8, 512, 96, 0.0, *W3, n, None, None, 0, None) == 1        # I % 256
-    assert g(*P, 1, 2, 8, 512, 256, 0.0, *W3, n, None, None, 7, None) == 1       # variant
-    assert g(_p(GOOD + 8), *P[1:], 1, 2, 8, 512, 256, 0.0, *W3, n, None, None, 0, None) == 1  # 16-B alignment
-    assert g(P[0], P[1], P[2], None, *P[4:], 1, 2, 8, 512, 256, 0.0, *W3, n, None, None, 0, None) == 1
-    assert g(*P, 1, 2, 8, 512, 256, 0.0, _p(GOOD), _p(GOOD), None, n, None, None, 0, None) == 1   # no workspace
-    assert g(*P, 1, 2, 8, 512, 256, 0.0, *W3, n - 4, None, None, 0, None) == 1                     # workspace too small
-    assert g(*P, 0, 2, 8, 512, 256, 0.0, *W3, n, None, None, 0, None) == 0       # T = 0
+    assert g(*P, 1, 2, 8, 480, 256, 0.0, _p(GOOD), _p(GOOD), 0, None) == 1       # H % 256
+    assert g(*P, 1, 2, 8, 512, 96, 0.0, _p(GOOD), _p(GOOD), 0, None) == 1        # I % 256
+    assert g(*P, 1, 2, 8, 512, 256, 0.0, _p(GOOD), _p(GOOD), 7, None) == 1       # variant
+    assert g(_p(GOOD + 8), *P[1:], 1, 2, 8, 512, 256, 0.0, _p(GOOD), _p(GOOD), 0, None) == 1  # 16-B alignment
+    assert g(P[0], P[1], P[2], None, *P[4:], 1, 2, 8, 512, 256, 0.0, _p(GOOD), _p(GOOD), 0, None) == 1
+    assert g(*P, 1, 2, 8, 512, 256, 0.0, _p(GOOD), None, 0, None) == 1           # hq missing
+    assert g(*P, 0, 2, 8, 512, 256, 0.0, _p(GOOD), _p(GOOD), 0, None) == 0       # T = 0
     d = lib.luce_moe_down_combine
     d.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int] * 5 + [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
     assert d(*P, 1, 2, 8, 512, 100, _p(GOOD), 0, None) == 1
