@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying CUDA graphs")
     p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--path", choices=["layer", "split"], default="split",
+                   help="layer: each MoE layer is one launch (luce_moe_layer); split: prep, gate/up, down launches")
     p.add_argument("--layers", type=int, default=None, help="(debug) fewer layers; invalid as a bench number")
     p.add_argument("--input-steps", type=int, default=None,
                    help="pre-drawn input steps to cycle (default 64; fewer keeps profiling runs short)")
@@ -251,15 +253,17 @@ def source_hash(files):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_files):
-    """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
+def profiled_traffic(kernel_files, kernel):
+    """dram bytes per launch of `kernel` from the committed ncu summaries, if
+    they were taken on the current kernel source (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        if d.get("source_hash") == source_hash(kernel_files):
-            return d.get("dram_bytes_per_launch")
+        entries = d if isinstance(d, list) else [d]
+        for ent in entries:
+            if ent.get("kernel") == kernel and ent.get("source_hash") == source_hash(kernel_files):
+                return ent.get("dram_bytes_per_launch")
     except Exception:
         pass
     return None
@@ -311,10 +315,22 @@ def run_ours(args, wl, layers):
         except TypeError:
             return torch.cuda.Event(enable_timing=True)
 
+    one_launch = args.path == "layer"
+    sync = torch.zeros(4, dtype=torch.int32, device=dev)  # device barrier state of the one-launch layer
+
     def run_step(s, x_src, lg_src, v_src, out_dst, record):
         bufs = step_bufs
         for l in range(layers):
             lay = dls[l]
+            if one_launch:
+                if record is not None:
+                    record[l][0].record()
+                Bd.luce_moe_layer(lg_src[s, l], b_d[l], x_src[s, l], wl.k, wl.I, lay.wg, lay.wu, lay.wd, lay.wsg,
+                                  lay.wsu, lay.wsd, wl.clamp, bufs.ids, bufs.weights, bufs.xq, bufs.counts,
+                                  bufs.offsets, bufs.routes, bufs.h, bufs.hq, out_dst[l], sync)
+                if record is not None:
+                    record[l][1].record()
+                continue
             Bd.luce_moe_prep(lg_src[s, l], b_d[l], x_src[s, l], wl.k, bufs.ids, bufs.weights, bufs.xq, bufs.counts,
                              bufs.offsets, bufs.routes)
             if record is not None:
@@ -330,7 +346,8 @@ def run_ours(args, wl, layers):
                 e2.record()
         am.run(v_src[s])
 
-    launches_per_step = layers * 3 + 1  # prep, gate/up, down per layer; argmax
+    # per layer: one launch, or prep + gate/up + down; then the argmax
+    launches_per_step = layers * (1 if one_launch else 3) + 1
     S = wl.steps
     stream = torch.cuda.Stream(device=dev)
     # per-kernel timing: only the graph of input slot 0 carries event records
@@ -384,7 +401,8 @@ def run_ours(args, wl, layers):
         for (e0, e1, e2) in (rec or []):
             try:
                 glu_ms.append(e0.elapsed_time(e1))
-                down_ms.append(e1.elapsed_time(e2))
+                if not one_launch:
+                    down_ms.append(e1.elapsed_time(e2))
             except Exception:
                 pass
     tmax = torch.tensor([ms], dtype=torch.float64, device=dev)
@@ -399,20 +417,32 @@ def run_ours(args, wl, layers):
     peak, peak_kind = measured_peaks()
     glu_avg = float(np.mean(glu_ms)) if glu_ms else None
     down_avg = float(np.mean(down_ms)) if down_ms else None
-    gb = glu_bytes(wl, n_active)
-    kernel_files = ["quantized_moe_decode_luce_gb300/csrc/glu_pair.cu", "quantized_moe_decode_luce_gb300/csrc/common.cuh"]
-    roofline = None
-    if glu_avg:
-        ach = gb / (glu_avg * 1e-3) / 1e9
-        roofline = {"kernel": "k_glu_pair", "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
-                    "frac": ach / peak, "peak_kind": f"{peak_kind} (STREAM-style copy)",
-                    "frac_of_8TBps_spec": ach / SPEC_HBM_GBS, "bytes_per_launch": gb,
-                    "avg_launch_us": glu_avg * 1e3, "traffic": profiled_traffic(kernel_files)}
     kernels = {}
-    if down_avg:
-        db = down_bytes(wl, n_active)
-        kernels["k_down_combine"] = {"avg_launch_us": down_avg * 1e3, "bytes_per_launch": db,
-                                     "GBps": db / (down_avg * 1e-3) / 1e9}
+    roofline = None
+    if one_launch:
+        # the dominant (and only) layer kernel: all of the layer's algorithmic bytes
+        kernel_files = ["quantized_moe_decode_luce_gb300/csrc/moe_layer.cu",
+                        "quantized_moe_decode_luce_gb300/csrc/common.cuh"]
+        if glu_avg:
+            ach = lb / (glu_avg * 1e-3) / 1e9
+            roofline = {"kernel": "k_moe_layer", "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                        "frac": ach / peak, "peak_kind": f"{peak_kind} (STREAM-style copy)",
+                        "frac_of_8TBps_spec": ach / SPEC_HBM_GBS, "bytes_per_launch": lb,
+                        "avg_launch_us": glu_avg * 1e3, "traffic": profiled_traffic(kernel_files, "k_moe_layer")}
+    else:
+        gb = glu_bytes(wl, n_active)
+        kernel_files = ["quantized_moe_decode_luce_gb300/csrc/glu_pair.cu",
+                        "quantized_moe_decode_luce_gb300/csrc/common.cuh"]
+        if glu_avg:
+            ach = gb / (glu_avg * 1e-3) / 1e9
+            roofline = {"kernel": "k_glu_pair", "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                        "frac": ach / peak, "peak_kind": f"{peak_kind} (STREAM-style copy)",
+                        "frac_of_8TBps_spec": ach / SPEC_HBM_GBS, "bytes_per_launch": gb,
+                        "avg_launch_us": glu_avg * 1e3, "traffic": profiled_traffic(kernel_files, "k_glu_pair")}
+        if down_avg:
+            db = down_bytes(wl, n_active)
+            kernels["k_down_combine"] = {"avg_launch_us": down_avg * 1e3, "bytes_per_launch": db,
+                                         "GBps": db / (down_avg * 1e-3) / 1e9}
 
     # e2e: host inputs -> device, the same step, result back to the host
     e2e = None
@@ -487,7 +517,8 @@ def run_ours(args, wl, layers):
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "i8 codes (dp4a int32 block sums), f32 scales/accumulation",
                 "data": "synthetic (seeded Q8_0 weights, N(0,1) activations, Zipf-skewed router logits)",
-                "config": {**config_dict(wl, layers, graph), "pdl": not args.no_pdl},
+                "config": {**config_dict(wl, layers, graph), "pdl": not args.no_pdl,
+                           "path": "one launch per layer" if one_launch else "prep + gate/up + down launches"},
                 "layer_us": ms_per_step * 1e3 / layers,
                 "stack_weight_GBps": step_bytes / (ms_per_step * 1e-3) / 1e9,
                 "stack_frac_of_measured_hbm": step_bytes / (ms_per_step * 1e-3) / 1e9 / peak,

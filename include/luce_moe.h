@@ -248,6 +248,42 @@ LUCE_API luce_status luce_moe_prep(const float *logits, const float *bias, const
                                    int32_t *offsets, int32_t *routes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * luce_moe_layer -- one whole MoE FFN layer in ONE launch: the results of
+ * luce_moe_prep, then luce_moe_glu_pair, then luce_moe_down_combine on the
+ * same arguments, bit for bit (ids, weights, xq, counts, offsets, routes, h,
+ * hq and out are all written).  [PR826], commits "fused DS4.1 decode
+ * kernels" (select and weights, grouping, q8_1 memo), "RDNA4 Q8_0 gate/up
+ * pair" and "fused routed combine and q8_1 inputs for the hybrid owners";
+ * the single launch is this library's own.
+ *
+ *   logits [T][E] f32, bias [E] f32 or NULL, x [T][H] f32 (16-byte aligned);
+ *   w_gate, w_up [E][I][H/32] and w_down [E][H][I/32] Q8_0 blocks;
+ *   ws_gate, ws_up [I][H/32] and ws_down [H][I/32]: all three or none;
+ *   clamp as in luce_moe_glu_pair; outputs as in the three calls.  h
+ *   [T*k+T][I] f32 (16-byte aligned) is required: the launch keeps h there
+ *   between its gate/up and down parts.
+ *   sync: 8 bytes of device memory owned by the caller, zero before the
+ *   first call and left consistent by every call that returns LUCE_OK and
+ *   raises no fault.  Launches that may run at the same time (other streams)
+ *   need distinct sync words.  After a LUCE_FAULT_TIMEOUT, zero it again.
+ *
+ * The grid is launched cooperatively (all CTAs resident at once; its CTAs
+ * meet at a device-wide barrier between the gate/up and the down parts, and
+ * at a second one after the q8_1 of h when hq exceeds 24 KB).
+ * Supported: 1 <= T <= 8, T*k <= 64, E <= 256 (else LUCE_ERR_UNSUPPORTED,
+ * and the three calls serve); H, I multiples of 256 up to 32768.  Argument
+ * errors as in the three calls.  Not allowed inside a kernel that the caller
+ * runs concurrently with another cooperative grid on the same device.
+ */
+LUCE_API luce_status luce_moe_layer(const float *logits, const float *bias, const float *x,
+                                    const luce_block_q8_0 *w_gate, const luce_block_q8_0 *w_up,
+                                    const luce_block_q8_0 *w_down, const luce_block_q8_0 *ws_gate,
+                                    const luce_block_q8_0 *ws_up, const luce_block_q8_0 *ws_down, int T, int E, int k,
+                                    int H, int I, float clamp, int32_t *ids, float *weights, luce_block_q8_1 *xq,
+                                    int32_t *counts, int32_t *offsets, int32_t *routes, float *h,
+                                    luce_block_q8_1 *hq, float *out, uint32_t *sync, void *stream);
+
+/* ------------------------------------------------------------------------
  * luce_set_pdl -- process-wide switch (default 0 = off) for programmatic
  * dependent launch: each library kernel may then start before the previous
  * kernel on the stream has finished, run its prologue, and wait on the GPU

@@ -46,6 +46,8 @@ def lib() -> ctypes.CDLL:
             "luce_moe_group": [P, i32, i32, i32, P, P, P, P],
             "luce_moe_glu_pair": [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, i32, P],
             "luce_moe_prep": [P, P, P, i32, i32, i32, i32, P, P, P, P, P, P, P],
+            "luce_moe_layer": [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, P, P, P, P, P, P, P,
+                               P, P],
             "luce_moe_down_combine": [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, P, i32, P],
             "luce_argmax": [P, i32, i64, P, P, P, sz, P],
             "luce_argmax_noalloc": [P, i32, i64, P, P, P],
@@ -137,6 +139,23 @@ def luce_moe_prep(logits, bias, x, k: int, ids, weights, xq, counts, offsets, ro
         _ptr(offsets, i32, "offsets"), _ptr(routes, i32, "routes"), _stream(stream)))
 
 
+def luce_moe_layer(logits, bias, x, k: int, I: int, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, clamp: float,
+                   ids, weights, xq, counts, offsets, routes, h, hq, out, sync, stream=None) -> None:
+    """The whole layer in one launch; `sync` is an int32 CUDA tensor of >= 2
+    elements, zero before the first call (the library keeps it consistent)."""
+    T, E = logits.shape
+    H = x.shape[1]
+    if sync is None or sync.numel() < 2:
+        raise ValueError("sync must hold at least 2 int32 elements")
+    _check("luce_moe_layer", lib().luce_moe_layer(
+        _ptr(logits, f32, "logits"), _ptr(bias, f32, "bias"), _ptr(x, f32, "x"), _ptr(w_gate, u8, "w_gate"),
+        _ptr(w_up, u8, "w_up"), _ptr(w_down, u8, "w_down"), _ptr(ws_gate, u8, "ws_gate"), _ptr(ws_up, u8, "ws_up"),
+        _ptr(ws_down, u8, "ws_down"), T, E, k, H, I, float(clamp), _ptr(ids, i32, "ids"),
+        _ptr(weights, f32, "weights"), _ptr(xq, u8, "xq"), _ptr(counts, i32, "counts"),
+        _ptr(offsets, i32, "offsets"), _ptr(routes, i32, "routes"), _ptr(h, f32, "h"), _ptr(hq, u8, "hq"),
+        _ptr(out, f32, "out"), _ptr(sync, i32, "sync"), _stream(stream)))
+
+
 def luce_set_pdl(enable: bool) -> None:
     _check("luce_set_pdl", lib().luce_set_pdl(1 if enable else 0))
 
@@ -178,7 +197,7 @@ def luce_version() -> int:
 
 
 __all__ = ["LuceError", "lib", "status_string", "luce_route_topk", "luce_quantize_q8_1", "luce_moe_group",
-           "luce_moe_glu_pair", "luce_moe_prep", "luce_set_pdl",
+           "luce_moe_glu_pair", "luce_moe_prep", "luce_moe_layer", "luce_set_pdl",
            "luce_moe_down_combine", "luce_argmax", "luce_argmax_workspace_bytes", "luce_argmax_noalloc",
            "luce_get_fault", "luce_version", "LUCE_OK", "LUCE_ERR_INVALID_ARG", "LUCE_ERR_UNSUPPORTED",
            "LUCE_ERR_CUDA", "LUCE_FAULT_BAD_ID", "LUCE_FAULT_TIMEOUT"]

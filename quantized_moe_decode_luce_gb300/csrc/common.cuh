@@ -6,6 +6,8 @@
 // checks live here too.
 #pragma once
 
+#include <math.h>
+
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -87,7 +89,8 @@ __device__ __forceinline__ void quantize_q8_1_warp(float x, uint32_t *__restrict
 {
     const float amax = warp_max(fabsf(x));
     const float d = __fdiv_rn(amax, 127.0f);
-    const int q = (amax == 0.0f) ? 0 : (int)roundf(__fdiv_rn(x, d));
+    // an all-zero block divides its zeros by 1 (codes 0) instead of by 0
+    const int q = (int)roundf(__fdiv_rn(x, amax == 0.0f ? 1.0f : d));
     const int sum = warp_sum_i(q);
     uint32_t byte = (uint32_t)(q & 0xff);
     uint32_t w = byte;
@@ -150,13 +153,20 @@ __device__ __forceinline__ void load_q8_1_any(const uint32_t *words, Q81Block &b
         blk.q[i] = (int)words[1 + i];
 }
 
+// Exact int32 block sum of 32 int8 products; four independent partial sums
+// keep the dp4a dependency chains short (integer addition is exact, so the
+// result does not depend on the grouping).
 __device__ __forceinline__ int dot_q8_block(const uint32_t (&w)[8], const int (&x)[8])
 {
-    int s = 0;
-#pragma unroll
-    for (int i = 0; i < 8; i++)
-        s = __dp4a((int)w[i], x[i], s);
-    return s;
+    int s0 = __dp4a((int)w[0], x[0], 0);
+    int s1 = __dp4a((int)w[1], x[1], 0);
+    int s2 = __dp4a((int)w[2], x[2], 0);
+    int s3 = __dp4a((int)w[3], x[3], 0);
+    s0 = __dp4a((int)w[4], x[4], s0);
+    s1 = __dp4a((int)w[5], x[5], s1);
+    s2 = __dp4a((int)w[6], x[6], s2);
+    s3 = __dp4a((int)w[7], x[7], s3);
+    return (s0 + s1) + (s2 + s3);
 }
 
 // SwiGLU of the pages: silu(g) * u, optionally silu(min(g, L)) * clamp(u, -L, L).
@@ -168,6 +178,26 @@ __device__ __forceinline__ float swiglu(float g, float u, float clamp)
     }
     const float s = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
     return __fmul_rn(s, u);
+}
+
+// Router weights of one token, held by a warp: lane j < k holds sel0 = the
+// unbiased logit of slot j, lane j + 32 < k holds sel1 = that of slot j + 32.
+// w[j] = exp(l_j - m) / sum_i exp(l_i - m), m the largest selected logit; the
+// sum is a butterfly over the lanes, so every lane sees the same value.
+__device__ __forceinline__ void route_softmax_warp(float sel0, float sel1, int k, float *w_out, int lane)
+{
+    const bool has0 = lane < k, has1 = lane + 32 < k;
+    float m = has0 ? sel0 : -INFINITY;
+    if (has1)
+        m = fmaxf(m, sel1);
+    m = warp_max(m);
+    const float e0 = has0 ? expf(__fsub_rn(sel0, m)) : 0.0f;
+    const float e1 = has1 ? expf(__fsub_rn(sel1, m)) : 0.0f;
+    const float den = warp_sum(__fadd_rn(e0, e1));
+    if (has0)
+        w_out[lane] = __fdiv_rn(e0, den);
+    if (has1)
+        w_out[lane + 32] = __fdiv_rn(e1, den);
 }
 
 // ---------------------------------------------------------------------------
@@ -309,6 +339,11 @@ struct Tuning {
     int down_budget_kb = 100; // down/combine ring budget per CTA
     int down_stage = 1;       // stage the tile's activation rows in shared memory
     int evict_first = 1;      // stream weights with the L2 evict-first policy
+    int layer_part_kb = 36;   // whole-layer kernel: bytes of one gate/up part
+    int layer_budget_kb = 222; // whole-layer kernel: shared memory per CTA
+    int layer_cps = 1;        // whole-layer kernel: CTAs per SM
+    int layer_prefetch = 1;   // whole-layer kernel: warm L2 with the shared expert
+    int layer_hs_own = 1;     // whole-layer kernel: each CTA quantizes all of a small hq itself
 };
 extern Tuning g_tuning;
 

@@ -13,8 +13,8 @@
 // cp.async.bulk stage per expert, through a shared-memory ring; each weight
 // row crosses HBM once per token tile (once per step for decode and verify,
 // where one tile holds every token).  Each consumer warp takes whole stages
-// (all RN rows of one expert), so the experts' activation loads proceed in
-// parallel across warps.  Each route's product y stays in shared memory, so
+// (all RN rows of one expert) when the ring allows it, else every warp takes
+// part in every stage.  Each route's product y stays in shared memory, so
 // the combine needs no second pass and no atomics: one thread sums out[t][n]
 // over the k slots in slot order with separately rounded products and sums
 // (__fmul_rn / __fadd_rn), then adds the shared expert.  Deterministic; no
@@ -37,6 +37,7 @@ using namespace luce;
 constexpr int NCU = 32; // columns per virtual expert
 constexpr int CW = 4;   // consumer warps
 constexpr int RN = 8;   // output rows per CTA
+constexpr int RPW = RN / CW; // rows of a stage per consumer warp
 
 struct DownArgs {
     const uint8_t *wd;    // [E][H][rowbytes]
@@ -52,6 +53,7 @@ struct DownArgs {
     int NS; // ring stages
     int hs_rows; // activation rows staged in shared memory (0: read through L1)
     int evict_first;
+    int coop;    // all consumer warps on every stage (rings of fewer than CW stages)
 };
 
 struct VUnit {
@@ -61,8 +63,51 @@ struct VUnit {
     int col0, ncols;
 };
 
-template <int NC>
-__global__ void __launch_bounds__((CW + 1) * 32) k_down_combine(const DownArgs a)
+// y of the NR rows row0, row0 + rstep, ... of one stage for the nc columns
+// whose activation rows are xc[] and whose y slots are ys[]: per lane the
+// blocks b = lane, lane + 32, ... accumulated in that order, then a warp sum.
+template <int NR, int NC>
+__device__ __forceinline__ void stage_dots(const uint8_t *st, int rowbytes, int row0, int rstep,
+                                           const uint32_t *const (&xc)[NC], const int (&ys)[NC], int nc, int nbI,
+                                           int lane, float *ybuf)
+{
+    float acc[NR][NC];
+#pragma unroll
+    for (int i = 0; i < NR; i++)
+#pragma unroll
+        for (int c = 0; c < NC; c++)
+            acc[i][c] = 0.0f;
+    for (int b = lane; b < nbI; b += 32) {
+        Q81Block xb[NC];
+#pragma unroll
+        for (int c = 0; c < NC; c++)
+            if (c < nc)
+                load_q8_1_any(xc[c] + (size_t)b * Q8_1_WORDS, xb[c]);
+#pragma unroll
+        for (int i = 0; i < NR; i++) {
+            Q80Block wb;
+            load_q8_0_smem(st + (size_t)(row0 + i * rstep) * rowbytes, b, wb);
+#pragma unroll
+            for (int c = 0; c < NC; c++)
+                if (c < nc)
+                    acc[i][c] = fmaf(wb.d * xb[c].d, (float)dot_q8_block(wb.q, xb[c].q), acc[i][c]);
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < NC; c++) {
+        if (c < nc) {
+#pragma unroll
+            for (int i = 0; i < NR; i++) {
+                const float y = warp_sum(acc[i][c]);
+                if (lane == 0)
+                    ybuf[ys[c] * RN + row0 + i * rstep] = y;
+            }
+        }
+    }
+}
+
+template <int NC, bool COOP>
+__global__ void __launch_bounds__((CW + 1) * 32, 2) k_down_combine(const DownArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const int stage_bytes = RN * a.rowbytes;
@@ -243,7 +288,14 @@ __global__ void __launch_bounds__((CW + 1) * 32) k_down_combine(const DownArgs a
             dead = true;
         }
     }
-    for (int v = warp; v < NV; v += CW) {
+    // Two ways to consume the ring, both safe for its parity waits (a warp
+    // must never wait on a slot's use u while use u - 1 may be pending):
+    //  * one warp per stage (all RN rows): warp v % CW takes stage v.  The host
+    //    picks this when the ring holds every stage or NS is a multiple of CW,
+    //    so that every use of a slot falls to the same warp, in order.
+    //  * coop: every consumer warp takes part in every stage, in order, RN / CW
+    //    rows each (rings of fewer than CW stages).
+    for (int v = COOP ? 0 : warp; v < NV; v += COOP ? 1 : CW) {
         const VUnit un = decode(v);
         int my_r = 0, my_slot = 0; // column `lane`: its hq row and its y slot
         if (lane < un.ncols) {
@@ -257,7 +309,8 @@ __global__ void __launch_bounds__((CW + 1) * 32) k_down_combine(const DownArgs a
             }
         }
         const uint32_t slot = (uint32_t)v % a.NS, use = (uint32_t)v / a.NS;
-        if (!dead && *(volatile int *)&s_abort)
+        // warp-uniform: every lane takes the same branch to the __all_sync
+        if (__any_sync(0xffffffffu, *(volatile int *)&s_abort != 0))
             dead = true;
         if (!dead) {
             const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], use & 1u));
@@ -271,56 +324,35 @@ __global__ void __launch_bounds__((CW + 1) * 32) k_down_combine(const DownArgs a
         }
         if (!dead) {
             const uint8_t *st = ring + (size_t)slot * stage_bytes;
-            for (int c0 = 0; c0 < un.ncols; c0 += NC) {
-                const int nc = min(NC, un.ncols - c0);
-                float acc[RN][NC];
-#pragma unroll
-                for (int m = 0; m < RN; m++)
-#pragma unroll
-                    for (int c = 0; c < NC; c++)
-                        acc[m][c] = 0.0f;
+            // columns per pass: all RN rows of a stage take at most 4 (registers)
+            constexpr int NCC = COOP ? NC : (NC > 4 ? 4 : NC);
+            for (int c0 = 0; c0 < un.ncols; c0 += NCC) {
+                const int nc = min(NCC, un.ncols - c0);
                 // warp-collective shuffles stay outside the lane-dependent block loop
-                const uint32_t *xc[NC]; // activation row of each column (shared or global)
+                const uint32_t *xc[NCC]; // activation row of each column (shared or global)
+                int ys[NCC];
 #pragma unroll
-                for (int c = 0; c < NC; c++) {
+                for (int c = 0; c < NCC; c++) {
                     const int cc = c0 + (c < nc ? c : 0);
                     const int r = __shfl_sync(0xffffffffu, my_r, cc);
-                    const int ys = __shfl_sync(0xffffffffu, my_slot, cc);
-                    xc[c] = hs_on ? hs + (size_t)ys * xstride : a.hq + (size_t)r * xstride;
+                    ys[c] = __shfl_sync(0xffffffffu, my_slot, cc);
+                    xc[c] = hs_on ? hs + (size_t)ys[c] * xstride : a.hq + (size_t)r * xstride;
                 }
-                for (int b = lane; b < a.nbI; b += 32) {
-                    Q81Block xb[NC];
-#pragma unroll
-                    for (int c = 0; c < NC; c++)
-                        if (c < nc)
-                            load_q8_1_any(xc[c] + (size_t)b * Q8_1_WORDS, xb[c]);
-#pragma unroll
-                    for (int m = 0; m < RN; m++) {
-                        Q80Block wb;
-                        load_q8_0_smem(st + (size_t)m * a.rowbytes, b, wb);
-#pragma unroll
-                        for (int c = 0; c < NC; c++)
-                            if (c < nc)
-                                acc[m][c] = fmaf(wb.d * xb[c].d, (float)dot_q8_block(wb.q, xb[c].q), acc[m][c]);
-                    }
-                }
-#pragma unroll
-                for (int c = 0; c < NC; c++) {
-                    if (c < nc) {
-                        const int ys = __shfl_sync(0xffffffffu, my_slot, c0 + c);
-#pragma unroll
-                        for (int m = 0; m < RN; m++) {
-                            const float y = warp_sum(acc[m][c]);
-                            if (lane == m)
-                                ybuf[ys * RN + m] = y;
-                        }
-                    }
-                }
+                if (COOP)
+                    stage_dots<RPW, NCC>(st, a.rowbytes, warp, CW, xc, ys, nc, a.nbI, lane, ybuf);
+                else
+                    stage_dots<RN, NCC>(st, a.rowbytes, 0, 1, xc, ys, nc, a.nbI, lane, ybuf);
             }
         }
-        __syncwarp();
-        if (lane == 0 && !dead)
-            mbar_arrive(&empty[slot]);
+        if (COOP) {
+            named_barrier(1, CW * 32); // every consumer warp is done with the stage
+            if (tid == 0 && !dead)
+                mbar_arrive(&empty[slot]);
+        } else {
+            __syncwarp();
+            if (lane == 0 && !dead)
+                mbar_arrive(&empty[slot]);
+        }
     }
     named_barrier(1, CW * 32);
     if (dead || *(volatile int *)&s_abort)
@@ -341,11 +373,11 @@ __global__ void __launch_bounds__((CW + 1) * 32) k_down_combine(const DownArgs a
     }
 }
 
-template <int NC>
+template <int NC, bool COOP>
 luce_status launch_down(const DownArgs &a, dim3 grid, size_t smem, cudaStream_t stream)
 {
     static size_t smem_set[64] = {0}; // per device: the attribute value in force
-    auto kern = k_down_combine<NC>;
+    auto kern = k_down_combine<NC, COOP>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return LUCE_ERR_CUDA;
@@ -355,6 +387,12 @@ luce_status launch_down(const DownArgs &a, dim3 grid, size_t smem, cudaStream_t 
         smem_set[dev] = smem;
     }
     return luce_host::launch(kern, grid, dim3((CW + 1) * 32), smem, stream, a);
+}
+
+template <int NC>
+luce_status launch_down_mode(const DownArgs &a, dim3 grid, size_t smem, cudaStream_t stream)
+{
+    return a.coop ? launch_down<NC, true>(a, grid, smem, stream) : launch_down<NC, false>(a, grid, smem, stream);
 }
 
 } // namespace
@@ -403,6 +441,15 @@ extern "C" luce_status luce_moe_down_combine(const luce_block_q8_0 *w_down, cons
     const long long nv_up = std::min<long long>(E, Tk) + Tk / NCU + (ws_down ? (a.TT + NCU - 1) / NCU : 0);
     const int stage = RN * a.rowbytes;
     a.NS = (int)std::max<long long>(2, std::min<long long>(nv_up, ((long long)g_tuning.down_budget_kb * 1024) / stage));
+    // a ring that is reused is consumed one warp per stage only when NS is a
+    // multiple of CW (each slot then always falls to the same warp)
+    a.coop = 0;
+    if (a.NS < nv_up) {
+        if (a.NS >= CW)
+            a.NS -= a.NS % CW;
+        else
+            a.coop = 1;
+    }
     a.evict_first = g_tuning.evict_first;
     // activation rows of a tile in shared memory when they fit in 24 KB (a row
     // is a multiple of 16 bytes since I % 256 == 0)
@@ -416,10 +463,10 @@ extern "C" luce_status luce_moe_down_combine(const luce_block_q8_0 *w_down, cons
     const int maxcols = std::min(a.TT, NCU);
     cudaStream_t st = as_stream(stream);
     if (maxcols <= 1)
-        return launch_down<1>(a, grid, smem, st);
+        return launch_down_mode<1>(a, grid, smem, st);
     if (maxcols <= 2)
-        return launch_down<2>(a, grid, smem, st);
+        return launch_down_mode<2>(a, grid, smem, st);
     if (maxcols <= 4)
-        return launch_down<4>(a, grid, smem, st);
-    return launch_down<8>(a, grid, smem, st);
+        return launch_down_mode<4>(a, grid, smem, st);
+    return launch_down_mode<8>(a, grid, smem, st);
 }

@@ -236,7 +236,8 @@ __global__ void __launch_bounds__(THREADS) k_glu_pair(const GluArgs a)
         float *hb = hbuf + par * 32 * HB_STRIDE;
         for (int p = 0; p < PPG; p++, q++) {
             const uint32_t slot = (uint32_t)(q % a.NS), use = (uint32_t)(q / a.NS);
-            if (!dead && *(volatile int *)&s_abort)
+            // warp-uniform: every lane takes the same branch to the __all_sync
+            if (__any_sync(0xffffffffu, *(volatile int *)&s_abort != 0))
                 dead = true;
             if (!dead) {
                 const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], use & 1u));

@@ -75,18 +75,7 @@ __global__ void __launch_bounds__(ROUTE_WARPS * 32)
         else if (j == lane + 32)
             sel1 = l[bi];
     }
-    const bool has0 = lane < k, has1 = lane + 32 < k;
-    float m = has0 ? sel0 : -INFINITY;
-    if (has1)
-        m = fmaxf(m, sel1);
-    m = warp_max(m);
-    const float e0 = has0 ? expf(__fsub_rn(sel0, m)) : 0.0f;
-    const float e1 = has1 ? expf(__fsub_rn(sel1, m)) : 0.0f;
-    const float den = warp_sum(__fadd_rn(e0, e1));
-    if (has0)
-        weights[(size_t)t * k + lane] = __fdiv_rn(e0, den);
-    if (has1)
-        weights[(size_t)t * k + lane + 32] = __fdiv_rn(e1, den);
+    route_softmax_warp(sel0, sel1, k, weights + (size_t)t * k, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -275,18 +264,7 @@ __device__ __forceinline__ void route_token_regs(const float *__restrict__ l, co
         else if (j == lane + 32)
             sel1 = l[bi];
     }
-    const bool has0 = lane < k, has1 = lane + 32 < k;
-    float m = has0 ? sel0 : -INFINITY;
-    if (has1)
-        m = fmaxf(m, sel1);
-    m = warp_max(m);
-    const float e0 = has0 ? expf(__fsub_rn(sel0, m)) : 0.0f;
-    const float e1 = has1 ? expf(__fsub_rn(sel1, m)) : 0.0f;
-    const float den = warp_sum(__fadd_rn(e0, e1));
-    if (has0)
-        w_g[lane] = __fdiv_rn(e0, den);
-    if (has1)
-        w_g[lane + 32] = __fdiv_rn(e1, den);
+    route_softmax_warp(sel0, sel1, k, w_g, lane);
 }
 
 template <int EPL>
@@ -516,6 +494,7 @@ size_t argmax_pairs_bytes(int R, int C) { return ((size_t)R * C * sizeof(ArgPair
 // ===========================================================================
 extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault_glu(unsigned int *bits);
 extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault_down(unsigned int *bits);
+extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault_layer(unsigned int *bits);
 
 namespace luce_host {
 Tuning g_tuning;
@@ -573,7 +552,9 @@ extern "C" luce_status luce_get_fault(unsigned int *bits)
     cudaError_t e1 = luce_internal_fault_small_ops(bits);
     cudaError_t e2 = luce_internal_fault_glu(bits);
     cudaError_t e3 = luce_internal_fault_down(bits);
-    return (e1 == cudaSuccess && e2 == cudaSuccess && e3 == cudaSuccess) ? LUCE_OK : LUCE_ERR_CUDA;
+    cudaError_t e4 = luce_internal_fault_layer(bits);
+    return (e1 == cudaSuccess && e2 == cudaSuccess && e3 == cudaSuccess && e4 == cudaSuccess) ? LUCE_OK
+                                                                                           : LUCE_ERR_CUDA;
 }
 
 extern "C" luce_status luce_route_topk(const float *logits, const float *bias, int T, int E, int k, int32_t *ids,

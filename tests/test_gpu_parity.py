@@ -194,6 +194,9 @@ DOWN_CASES = [
     ("wide_tiles", 130, 3, 6, 256, 256, True, 0.1),
     ("all_masked", 3, 2, 4, 256, 256, True, 1.0),
     ("no_shared_masked", 4, 4, 8, 512, 256, False, 0.4),
+    # large I: 69.6 KB stages, a ring of two, seven stages through it
+    ("large_i_two_stage_ring", 1, 6, 8, 256, 8192, True, 0.0),
+    ("large_i_tokens", 9, 4, 8, 256, 4096, True, 0.1),
 ]
 
 
@@ -221,13 +224,15 @@ def test_down_combine(case):
 
 
 # ----------------------------------------------------------------------------- whole step
-def _run_chain(wl, L, layer=None):
+def _run_chain(wl, L, layer=None, path="layer"):
     step = MoEStep(wl.T, wl.H, wl.I, wl.E, wl.k, wl.shared, wl.clamp)
+    step.path = path
     if layer is None:
         layer = W.DeviceLayer(dev(L.wg), dev(L.wu), dev(L.wd), dev(L.wsg) if wl.shared else None,
                               dev(L.wsu) if wl.shared else None, dev(L.wsd) if wl.shared else None)
     out = step.run(layer, dev(L.x), dev(L.logits), dev(L.bias) if L.bias is not None else None)
     torch.cuda.synchronize()
+    assert step.path == path  # the one-launch path did not decline the shape
     return step, out
 
 
@@ -245,26 +250,29 @@ def _check_chain(wl, L, step):
     return flips
 
 
+@pytest.mark.parametrize("path", ["layer", "split"])
 @pytest.mark.parametrize("name", ["tiny", "decode_layer"])
-def test_layer_chain_workloads(name):
+def test_layer_chain_workloads(name, path):
     wl = W.WORKLOADS[name]
     L = W.host_layer(wl)
-    step, _ = _run_chain(wl, L)
+    step, _ = _run_chain(wl, L, path=path)
     _check_chain(wl, L, step)
 
 
-def test_layer_chain_verify_like_small():
+@pytest.mark.parametrize("path", ["layer", "split"])
+def test_layer_chain_verify_like_small(path):
     wl = W.Workload("verify_small", T=5, H=1024, I=512, E=32, k=8, shared=True, clamp=10.0, seed=21,
                     logits="shared_col")
     L = W.host_layer(wl)
-    step, _ = _run_chain(wl, L)
+    step, _ = _run_chain(wl, L, path=path)
     _check_chain(wl, L, step)
 
 
-def test_layer_is_deterministic():
+@pytest.mark.parametrize("path", ["layer", "split"])
+def test_layer_is_deterministic(path):
     wl = W.WORKLOADS["decode_layer"]
     L = W.host_layer(wl)
-    step, out1 = _run_chain(wl, L)
+    step, out1 = _run_chain(wl, L, path=path)
     a = (out1.clone(), step.h.clone(), step.hq.clone())
     layer = W.DeviceLayer(dev(L.wg), dev(L.wu), dev(L.wd), dev(L.wsg), dev(L.wsu), dev(L.wsd))
     for _ in range(3):
@@ -280,15 +288,18 @@ def _compact(wl, dl, used):
             host(dl.wd.index_select(0, idx)))
 
 
-def test_verify_layer_full_size():
+@pytest.mark.parametrize("path", ["layer", "split"])
+def test_verify_layer_full_size(path):
     wl = W.WORKLOADS["verify_layer"]
     dl = W.device_layer(wl, wl.seed, "cuda")
     gx = W.rng(wl.seed, 2)
     x = W.activations(gx, wl.T, wl.H)
     logits, bias = W.router_logits(W.rng(wl.seed, 3), wl)
     step = MoEStep(wl.T, wl.H, wl.I, wl.E, wl.k, wl.shared, wl.clamp)
+    step.path = path
     step.run(dl, dev(x), dev(logits), None)
     torch.cuda.synchronize()
+    assert step.path == path
     ids_ref, w_ref = oracle.route_topk(logits, bias, wl.k)
     assert np.array_equal(host(step.ids), ids_ref)
     c_ref, o_ref, r_ref = oracle.moe_group(ids_ref, wl.E)
@@ -411,13 +422,14 @@ def test_moe_prep_matches_the_three_calls(T, E, k, H, bias):
     assert np.array_equal(host(routes), r_ref)
 
 
+@pytest.mark.parametrize("path", ["layer", "split"])
 @pytest.mark.parametrize("name", ["decode_layer", "tiny"])
-def test_layer_chain_with_programmatic_launch(name):
+def test_layer_chain_with_programmatic_launch(name, path):
     wl = W.WORKLOADS[name]
     L = W.host_layer(wl)
     B.luce_set_pdl(True)
     try:
-        step, _ = _run_chain(wl, L)
+        step, _ = _run_chain(wl, L, path=path)
         _check_chain(wl, L, step)
         # back-to-back steps on one stream: each one's early start must not
         # read the previous step's buffers before they are complete
@@ -436,6 +448,7 @@ def test_layer_chain_unfused_prep_path():
     wl = W.WORKLOADS["decode_layer"]
     L = W.host_layer(wl)
     step = MoEStep(wl.T, wl.H, wl.I, wl.E, wl.k, wl.shared, wl.clamp)
+    step.path = "split"
     step.fused_prep = False
     layer = W.DeviceLayer(dev(L.wg), dev(L.wu), dev(L.wd), dev(L.wsg), dev(L.wsu), dev(L.wsd))
     step.run(layer, dev(L.x), dev(L.logits), dev(L.bias))
