@@ -130,6 +130,42 @@ __device__ __forceinline__ void load_q8_0_smem(const uint8_t *row, int b, Q80Blo
         blk.q[i] = __funnelshift_rc(w[i], w[i + 1], sh);
 }
 
+// Which blocks of a Q8_0 row (nb blocks of 34 B, row start 16-byte aligned)
+// a lane takes, and in which order it accumulates them.  34-byte blocks b and
+// b + 32 start 272 words, i.e. 16 banks, apart, and so do two consecutive rows
+// of 32 blocks; the mappings below make each 32-bit load instruction of a warp
+// touch 32 distinct shared-memory banks.
+//   ROWMAP_PAIRS (nb % 64 == 0): 32 lanes per row; block j of lane L is
+//     64 (j >> 1) + 16 (j & 1) + (L & 15) + 32 (L >> 4).
+//   ROWMAP_TWO_ROWS (nb == 32, where used): 16 lanes per row, lanes 16..31 on
+//     the next row; block j of lane L is (L & 15) + 16 j.
+//   ROWMAP_PLAIN (otherwise): 32 lanes per row; block j of lane L is L + 32 j.
+// Every kernel that reduces the same row uses the same mapping, so partial
+// sums are formed and added in the same order everywhere.
+enum RowMap { ROWMAP_PLAIN = 0, ROWMAP_TWO_ROWS = 1, ROWMAP_PAIRS = 2 };
+
+__device__ __forceinline__ int rowmap_blocks(int map, int nb, int lane)
+{
+    return map == ROWMAP_PAIRS ? (nb >> 5) : map == ROWMAP_TWO_ROWS ? 2 : ((nb - lane + 31) >> 5);
+}
+
+__device__ __forceinline__ int rowmap_block(int map, int lane, int j)
+{
+    return map == ROWMAP_PAIRS ? ((j >> 1) << 6) + ((j & 1) << 4) + (lane & 15) + ((lane >> 4) << 5)
+         : map == ROWMAP_TWO_ROWS ? (lane & 15) + (j << 4)
+                                  : lane + (j << 5);
+}
+
+// Sum over each half-warp (lanes 0..15 and 16..31 separately): the tree of
+// warp_sum without its first level.
+__device__ __forceinline__ float half_warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
 // q8_1 block from global memory (read-only path, L1-cached): scale + codes.
 struct Q81Block {
     float d;

@@ -64,20 +64,67 @@ struct VUnit {
 };
 
 // y of the NR rows row0, row0 + rstep, ... of one stage for the nc columns
-// whose activation rows are xc[] and whose y slots are ys[]: per lane the
-// blocks b = lane, lane + 32, ... accumulated in that order, then a warp sum.
+// whose activation rows are xc[] and whose y slots are ys[].  Rows of 32
+// blocks go two at a time (ROWMAP_TWO_ROWS: lanes 0..15 on row 2q, lanes
+// 16..31 on row 2q + 1, each lane on blocks l and l + 16, then a half-warp
+// sum); other rows take all 32 lanes (ROWMAP_PAIRS or ROWMAP_PLAIN, then a
+// warp sum).
 template <int NR, int NC>
 __device__ __forceinline__ void stage_dots(const uint8_t *st, int rowbytes, int row0, int rstep,
                                            const uint32_t *const (&xc)[NC], const int (&ys)[NC], int nc, int nbI,
                                            int lane, float *ybuf)
 {
+    if (nbI == 32) {
+        constexpr int NP = NR / 2;
+        static_assert(NR % 2 == 0, "rows go in pairs");
+        const int h = lane >> 4;
+        float acc[NP][NC];
+#pragma unroll
+        for (int i = 0; i < NP; i++)
+#pragma unroll
+            for (int c = 0; c < NC; c++)
+                acc[i][c] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const int b = rowmap_block(ROWMAP_TWO_ROWS, lane, j);
+            Q81Block xb[NC];
+#pragma unroll
+            for (int c = 0; c < NC; c++)
+                if (c < nc)
+                    load_q8_1_any(xc[c] + (size_t)b * Q8_1_WORDS, xb[c]);
+#pragma unroll
+            for (int i = 0; i < NP; i++) {
+                Q80Block wb;
+                load_q8_0_smem(st + (size_t)(row0 + (2 * i + h) * rstep) * rowbytes, b, wb);
+#pragma unroll
+                for (int c = 0; c < NC; c++)
+                    if (c < nc)
+                        acc[i][c] = fmaf(wb.d * xb[c].d, (float)dot_q8_block(wb.q, xb[c].q), acc[i][c]);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < NC; c++) {
+            if (c < nc) {
+#pragma unroll
+                for (int i = 0; i < NP; i++) {
+                    const float y = half_warp_sum(acc[i][c]);
+                    if ((lane & 15) == 0)
+                        ybuf[ys[c] * RN + row0 + (2 * i + h) * rstep] = y;
+                }
+            }
+        }
+        return;
+    }
+    const int map = (nbI % 64 == 0) ? ROWMAP_PAIRS : ROWMAP_PLAIN;
     float acc[NR][NC];
 #pragma unroll
     for (int i = 0; i < NR; i++)
 #pragma unroll
         for (int c = 0; c < NC; c++)
             acc[i][c] = 0.0f;
-    for (int b = lane; b < nbI; b += 32) {
+    const int nbl = rowmap_blocks(map, nbI, lane);
+    for (int j = 0; j < nbl; j++) {
+        const int b = rowmap_block(map, lane, j);
         Q81Block xb[NC];
 #pragma unroll
         for (int c = 0; c < NC; c++)
@@ -324,8 +371,8 @@ __global__ void __launch_bounds__((CW + 1) * 32, 2) k_down_combine(const DownArg
         }
         if (!dead) {
             const uint8_t *st = ring + (size_t)slot * stage_bytes;
-            // columns per pass: all RN rows of a stage take at most 4 (registers)
-            constexpr int NCC = COOP ? NC : (NC > 4 ? 4 : NC);
+            // columns per pass: at most 4 (registers)
+            constexpr int NCC = NC > 4 ? 4 : NC;
             for (int c0 = 0; c0 < un.ncols; c0 += NCC) {
                 const int nc = min(NCC, un.ncols - c0);
                 // warp-collective shuffles stay outside the lane-dependent block loop

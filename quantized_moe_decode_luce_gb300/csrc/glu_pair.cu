@@ -119,8 +119,14 @@ __global__ void __launch_bounds__(THREADS) k_glu_pair(const GluArgs a)
     const int stage_bytes = 2 * half_bytes;
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.NS * stage_bytes);
-    uint32_t *xs = reinterpret_cast<uint32_t *>(full + a.NS); // [xs_cols][nb][9]
-    int *vpre = reinterpret_cast<int *>(xs + (size_t)a.xs_cols * a.nb * Q8_1_WORDS); // [E + 1]
+    // lane -> block mapping of the weight rows (conflict-free for nb % 64 == 0)
+    const int map = (a.nb % 64 == 0) ? ROWMAP_PAIRS : ROWMAP_PLAIN;
+    // staged activation rows: block b at word 9 b + xpad (b / 32), so that
+    // blocks b and b + 32 (read by one load instruction) sit 16 banks apart
+    const int xpad = map == ROWMAP_PAIRS ? 16 : 0;
+    const int xs_stride = a.nb * Q8_1_WORDS + xpad * (a.nb >> 5);
+    uint32_t *xs = reinterpret_cast<uint32_t *>(full + a.NS); // [xs_cols][xs_stride]
+    int *vpre = reinterpret_cast<int *>(xs + (size_t)a.xs_cols * xs_stride); // [E + 1]
     float *hbuf = reinterpret_cast<float *>(vpre + a.E + 1); // [2][32][HB_STRIDE]
     __shared__ int s_abort;
 
@@ -226,9 +232,9 @@ __global__ void __launch_bounds__(THREADS) k_glu_pair(const GluArgs a)
                 for (int c = warp; c < gr.ncols; c += CW) {
                     const int t = __shfl_sync(0xffffffffu, my_t, c);
                     const uint32_t *src = a.xq + (size_t)t * xstride;
-                    uint32_t *dst = xs + (size_t)c * xstride;
+                    uint32_t *dst = xs + (size_t)c * xs_stride;
                     for (int w = lane; w < xstride; w += 32)
-                        dst[w] = __ldg(src + w);
+                        dst[w + xpad * ((w / Q8_1_WORDS) >> 5)] = __ldg(src + w);
                 }
                 __syncthreads();
             }
@@ -264,13 +270,16 @@ __global__ void __launch_bounds__(THREADS) k_glu_pair(const GluArgs a)
                         for (int c = 0; c < NC; c++) {
                             const int cc = c0 + (c < nc ? c : 0);
                             const int t = __shfl_sync(0xffffffffu, my_t, cc);
-                            xc[c] = x_in_smem ? xs + (size_t)cc * xstride : a.xq + (size_t)t * xstride;
+                            xc[c] = x_in_smem ? xs + (size_t)cc * xs_stride : a.xq + (size_t)t * xstride;
                         }
                         float ag[NC], au[NC];
 #pragma unroll
                         for (int c = 0; c < NC; c++)
                             ag[c] = au[c] = 0.0f;
-                        for (int b = lane; b < a.nb; b += 32) {
+                        const int xp = x_in_smem ? xpad : 0;
+                        const int nbl = rowmap_blocks(map, a.nb, lane);
+                        for (int j = 0; j < nbl; j++) {
+                            const int b = rowmap_block(map, lane, j);
                             Q80Block gb, ub;
                             load_q8_0_smem(grow, b, gb);
                             load_q8_0_smem(urow, b, ub);
@@ -278,7 +287,7 @@ __global__ void __launch_bounds__(THREADS) k_glu_pair(const GluArgs a)
                             for (int c = 0; c < NC; c++) {
                                 if (c < nc) {
                                     Q81Block xb;
-                                    load_q8_1_any(xc[c] + (size_t)b * Q8_1_WORDS, xb);
+                                    load_q8_1_any(xc[c] + (size_t)b * Q8_1_WORDS + xp * (b >> 5), xb);
                                     const int sg = dot_q8_block(gb.q, xb.q);
                                     const int su = dot_q8_block(ub.q, xb.q);
                                     ag[c] = fmaf(gb.d * xb.d, (float)sg, ag[c]);
@@ -396,11 +405,12 @@ extern "C" luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const lu
     // activation rows in shared memory when up to 32 columns fit in 40 KB
     const int maxcols = std::min(T, NCU);
     const size_t xrow = (size_t)a.nb * Q8_1_BYTES;
-    a.xs_cols = (tu.glu_xs && maxcols * xrow <= 40 * 1024) ? maxcols : 0;
+    const size_t xrow_pad = xrow + (a.nb % 64 == 0 ? (size_t)64 * (a.nb / 32) : 0); // staged row with bank padding
+    a.xs_cols = (tu.glu_xs && maxcols * xrow_pad <= 40 * 1024) ? maxcols : 0;
     a.prefetch = tu.glu_prefetch;
     a.evict_first = tu.evict_first;
     const size_t stage = (size_t)2 * RU * a.rowbytes;
-    const size_t fixed = (size_t)a.xs_cols * xrow + (size_t)(E + 1) * sizeof(int) +
+    const size_t fixed = (size_t)a.xs_cols * xrow_pad + (size_t)(E + 1) * sizeof(int) +
                          (size_t)2 * 32 * HB_STRIDE * sizeof(float) + 64;
     const size_t budget = (size_t)tu.glu_budget_kb * 1024;
     int NS = (int)std::min<size_t>(16, (budget - fixed) / (stage + 8));

@@ -214,7 +214,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     uint32_t *xs = reinterpret_cast<uint32_t *>(empty + a.NS); // [T][nbH][9], 16-byte aligned
     const int R = a.T * a.k;
     const int nslots = R + a.T;
-    uint32_t *hs = xs + (size_t)a.T * a.nbH * Q8_1_WORDS; // [nslots][nbI][9]
+    // x rows: block g of token t at word t * xstride + 9 g + xpad (g / 32): blocks g
+    // and g + 32, read by one load instruction, sit 16 banks apart
+    const int gmap = (a.nbH % 64 == 0) ? ROWMAP_PAIRS : ROWMAP_PLAIN; // gate/up row mapping
+    const int xpad = gmap == ROWMAP_PAIRS ? 16 : 0;
+    const int xstride = a.nbH * Q8_1_WORDS + xpad * (a.nbH >> 5);
+    uint32_t *hs = xs + (size_t)a.T * xstride; // [nslots][nbI][9]
     float *ybuf = reinterpret_cast<float *>(hs + (a.hs_on ? (size_t)nslots * a.nbI * Q8_1_WORDS : 0)); // [nslots][RB]
     float *scores = ybuf + (size_t)nslots * RB_MAX; // [T][E] logit + bias
     float *lsm = scores + (size_t)a.T * a.E;        // [T][E] logits
@@ -277,7 +282,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                 for (int i = 0; i < 8; i++)
                     v[i] = 0.0f;
             }
-            uint32_t *dst = xs + (size_t)(valid ? b : 0) * Q8_1_WORDS;
+            const int bt = valid ? b / a.nbH : 0, bg = valid ? b - bt * a.nbH : 0;
+            uint32_t *dst = xs + (size_t)bt * xstride + (size_t)bg * Q8_1_WORDS + xpad * (bg >> 5);
             quantize_q8_1_quad(v, valid, dst, qj);
             if (cta0 && valid) {
                 uint32_t *g = a.xq + (size_t)b * Q8_1_WORDS;
@@ -502,7 +508,6 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     // ---------------- consumers (warps 0 .. CW-1) ----------------
     const int grp = warp / GW, wl = warp - grp * GW; // group, warp within it
     const int gtid = tid - grp * GTHREADS;
-    const int xstride = a.nbH * Q8_1_WORDS;
     bool dead = false;
     int q = 0;
     // waits for stage q; false if this CTA gave up (now or earlier)
@@ -539,6 +544,23 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     };
 
     // ---------------- 5. gate/up rows -> h ----------------
+    // one token (NC == 1): this lane's x blocks stay in registers for every row
+    constexpr int XR = 4;
+    const int nblg = rowmap_blocks(gmap, a.nbH, lane);
+    const bool x_regs = NC == 1 && a.T == 1 && nblg <= XR;
+    Q81Block xreg[XR];
+#pragma unroll
+    for (int j = 0; j < XR; j++) {
+        if (x_regs && j < nblg) {
+            const int b = rowmap_block(gmap, lane, j);
+            load_q8_1_any(xs + (size_t)b * Q8_1_WORDS + xpad * (b >> 5), xreg[j]);
+        } else {
+            xreg[j].d = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                xreg[j].q[i] = 0;
+        }
+    }
     {
         int gr = r0;
         for (; q < NPg; q++) {
@@ -568,19 +590,37 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
 #pragma unroll
                         for (int c = 0; c < NC; c++)
                             ag[c] = au[c] = 0.0f;
-                        for (int b = lane; b < a.nbH; b += 32) {
-                            Q80Block gbk, ubk;
-                            load_q8_0_smem(grow, b, gbk);
-                            load_q8_0_smem(urow, b, ubk);
+                        if (x_regs) {
+                            // one token: its x blocks are in registers
 #pragma unroll
-                            for (int c = 0; c < NC; c++) {
-                                if (c < nc) {
-                                    Q81Block xb;
-                                    load_q8_1_any(xc[c] + (size_t)b * Q8_1_WORDS, xb);
-                                    const int sg = dot_q8_block(gbk.q, xb.q);
-                                    const int su = dot_q8_block(ubk.q, xb.q);
-                                    ag[c] = fmaf(gbk.d * xb.d, (float)sg, ag[c]);
-                                    au[c] = fmaf(ubk.d * xb.d, (float)su, au[c]);
+                            for (int j = 0; j < XR; j++) {
+                                if (j < nblg) {
+                                    const int b = rowmap_block(gmap, lane, j);
+                                    Q80Block gbk, ubk;
+                                    load_q8_0_smem(grow, b, gbk);
+                                    load_q8_0_smem(urow, b, ubk);
+                                    const int sg = dot_q8_block(gbk.q, xreg[j].q);
+                                    const int su = dot_q8_block(ubk.q, xreg[j].q);
+                                    ag[0] = fmaf(gbk.d * xreg[j].d, (float)sg, ag[0]);
+                                    au[0] = fmaf(ubk.d * xreg[j].d, (float)su, au[0]);
+                                }
+                            }
+                        } else {
+                            for (int j = 0; j < nblg; j++) {
+                                const int b = rowmap_block(gmap, lane, j);
+                                Q80Block gbk, ubk;
+                                load_q8_0_smem(grow, b, gbk);
+                                load_q8_0_smem(urow, b, ubk);
+#pragma unroll
+                                for (int c = 0; c < NC; c++) {
+                                    if (c < nc) {
+                                        Q81Block xb;
+                                        load_q8_1_any(xc[c] + (size_t)b * Q8_1_WORDS + xpad * (b >> 5), xb);
+                                        const int sg = dot_q8_block(gbk.q, xb.q);
+                                        const int su = dot_q8_block(ubk.q, xb.q);
+                                        ag[c] = fmaf(gbk.d * xb.d, (float)sg, ag[c]);
+                                        au[c] = fmaf(ubk.d * xb.d, (float)su, au[c]);
+                                    }
                                 }
                             }
                         }
@@ -651,6 +691,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                     for (int i = 0; i < 8; i++)
                         vj[i] = j == 0 ? v[0][i] : j == 1 ? v[1][i] : j == 2 ? v[2][i] : v[3][i];
                     const bool ok = j == 0 ? val[0] : j == 1 ? val[1] : j == 2 ? val[2] : val[3];
+                    if (!__any_sync(FULL, ok))
+                        continue; // a warp with no block in this pass does no work
                     const int u = ok ? (j == 0 ? uu[0] : j == 1 ? uu[1] : j == 2 ? uu[2] : uu[3]) : 0;
                     uint32_t *dst = (own ? hs : a.hq) + (size_t)u * Q8_1_WORDS;
                     quantize_q8_1_quad(vj, ok, dst, qj);
@@ -695,60 +737,137 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         const bool mine = (q & 1) == grp;
         if (mine && wait_stage(q)) {
             const uint8_t *st = ring + (size_t)(q % a.NS) * a.stage_bytes;
-            // units (item, column), items wl, wl + GW, ...; four per pass
-            int it = wl, col = 0;
-            while (it < i1 - i0) {
-                const uint8_t *wr[4];
-                const uint32_t *xr[4];
-                int yo[4];
-                int nu = 0;
+            const uint32_t *xbase = a.hs_on ? hs : a.hq;
+            const int ni = i1 - i0;
+            if (a.nbI == 32) {
+                // two rows per warp (ROWMAP_TWO_ROWS): half h of the warp walks the
+                // items 2 p + h, p = wl, wl + GW, ..., and their columns, two units
+                // per pass; a half-warp reduce-scatter leaves the sums at lanes
+                // 0, 8 (half 0) and 16, 24 (half 1)
+                const int h = lane >> 4;
+                int p = wl, col = 0;
+                const uint32_t *xlast = nullptr;
+                Q81Block xb[2];
+                while (__any_sync(FULL, 2 * p + h < ni)) { // warp-uniform trip count
+                    const uint8_t *wr[2];
+                    const uint32_t *xr[2];
+                    int yo[2];
+                    bool live[2];
 #pragma unroll
-                for (int z = 0; z < 4; z++) {
-                    wr[z] = st;
-                    xr[z] = a.hs_on ? hs : a.hq;
-                    yo[z] = 0;
-                    if (it < i1 - i0) {
-                        const int i = i0 + it;
-                        const int v = i / rows, m = i - v * rows;
-                        const int ys = v_e[v] < E ? routes_s[v_first[v] + col] : R + col; // hq row = y slot
-                        wr[z] = st + (size_t)it * a.rbd;
-                        xr[z] = (a.hs_on ? hs : a.hq) + (size_t)ys * ibytes_w;
-                        yo[z] = ys * RB_MAX + m;
-                        nu++;
-                        if (++col == v_ncols[v]) {
-                            col = 0;
-                            it += GW;
+                    for (int z = 0; z < 2; z++) {
+                        const int it = 2 * p + h;
+                        live[z] = it < ni;
+                        wr[z] = st;
+                        xr[z] = xbase;
+                        yo[z] = 0;
+                        if (live[z]) {
+                            const int i = i0 + it;
+                            const int v = i / rows, m = i - v * rows;
+                            const int ys = v_e[v] < E ? routes_s[v_first[v] + col] : R + col; // hq row = y slot
+                            wr[z] = st + (size_t)it * a.rbd;
+                            xr[z] = xbase + (size_t)ys * ibytes_w;
+                            yo[z] = ys * RB_MAX + m;
+                            if (++col == v_ncols[v]) {
+                                col = 0;
+                                p += GW;
+                            }
                         }
                     }
-                }
-                float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                for (int b = lane; b < a.nbI; b += 32) {
-                    Q81Block xb; // the activation block, kept while the units share their hq row
+                    float acc[2] = {0.0f, 0.0f};
 #pragma unroll
-                    for (int z = 0; z < 4; z++) {
-                        if (z < nu) {
-                            Q80Block wb;
-                            load_q8_0_smem(wr[z], b, wb);
-                            if (z == 0 || xr[z] != xr[z - 1]) {
-                                const uint32_t *xw = xr[z] + (size_t)b * Q8_1_WORDS;
-                                if (a.hs_on) {
-                                    load_q8_1_any(xw, xb);
-                                } else {
-                                    xb.d = half_bits_to_float(__ldcg(xw));
+                    for (int z = 0; z < 2; z++) {
+                        if (live[z]) {
+                            if (xr[z] != xlast) { // this half's activation blocks, reloaded on a new hq row
+                                xlast = xr[z];
 #pragma unroll
-                                    for (int w = 0; w < 8; w++)
-                                        xb.q[w] = (int)__ldcg(xw + 1 + w);
+                                for (int j = 0; j < 2; j++) {
+                                    const uint32_t *xw = xr[z] + (size_t)rowmap_block(ROWMAP_TWO_ROWS, lane, j) * Q8_1_WORDS;
+                                    if (a.hs_on) {
+                                        load_q8_1_any(xw, xb[j]);
+                                    } else {
+                                        xb[j].d = half_bits_to_float(__ldcg(xw));
+#pragma unroll
+                                        for (int w = 0; w < 8; w++)
+                                            xb[j].q[w] = (int)__ldcg(xw + 1 + w);
+                                    }
                                 }
                             }
-                            acc[z] = fmaf(wb.d * xb.d, (float)dot_q8_block(wb.q, xb.q), acc[z]);
+#pragma unroll
+                            for (int j = 0; j < 2; j++) {
+                                Q80Block wb;
+                                load_q8_0_smem(wr[z], rowmap_block(ROWMAP_TWO_ROWS, lane, j), wb);
+                                acc[z] = fmaf(wb.d * xb[j].d, (float)dot_q8_block(wb.q, xb[j].q), acc[z]);
+                            }
                         }
                     }
+                    const bool h8 = lane & 8;
+                    float y = (h8 ? acc[1] : acc[0]) + __shfl_xor_sync(FULL, h8 ? acc[0] : acc[1], 8);
+                    y += __shfl_xor_sync(FULL, y, 4);
+                    y += __shfl_xor_sync(FULL, y, 2);
+                    y += __shfl_xor_sync(FULL, y, 1);
+                    const int z = (lane >> 3) & 1;
+                    if ((lane & 7) == 0 && (z ? live[1] : live[0]))
+                        ybuf[z ? yo[1] : yo[0]] = y;
                 }
-                const float y = reduce4(acc[0], acc[1], acc[2], acc[3], lane);
-                const int z = lane >> 3;
-                const int yz = z == 0 ? yo[0] : z == 1 ? yo[1] : z == 2 ? yo[2] : yo[3];
-                if ((lane & 7) == 0 && z < nu)
-                    ybuf[yz] = y;
+            } else {
+                // 32 lanes per unit (item, column), four units per pass
+                const int dmap = (a.nbI % 64 == 0) ? ROWMAP_PAIRS : ROWMAP_PLAIN;
+                const int nbl = rowmap_blocks(dmap, a.nbI, lane);
+                int it = wl, col = 0;
+                while (it < ni) {
+                    const uint8_t *wr[4];
+                    const uint32_t *xr[4];
+                    int yo[4];
+                    int nu = 0;
+#pragma unroll
+                    for (int z = 0; z < 4; z++) {
+                        wr[z] = st;
+                        xr[z] = xbase;
+                        yo[z] = 0;
+                        if (it < ni) {
+                            const int i = i0 + it;
+                            const int v = i / rows, m = i - v * rows;
+                            const int ys = v_e[v] < E ? routes_s[v_first[v] + col] : R + col; // hq row = y slot
+                            wr[z] = st + (size_t)it * a.rbd;
+                            xr[z] = xbase + (size_t)ys * ibytes_w;
+                            yo[z] = ys * RB_MAX + m;
+                            nu++;
+                            if (++col == v_ncols[v]) {
+                                col = 0;
+                                it += GW;
+                            }
+                        }
+                    }
+                    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    for (int j = 0; j < nbl; j++) {
+                        const int b = rowmap_block(dmap, lane, j);
+                        Q81Block xb; // the activation block, kept while the units share their hq row
+#pragma unroll
+                        for (int z = 0; z < 4; z++) {
+                            if (z < nu) {
+                                Q80Block wb;
+                                load_q8_0_smem(wr[z], b, wb);
+                                if (z == 0 || xr[z] != xr[z - 1]) {
+                                    const uint32_t *xw = xr[z] + (size_t)b * Q8_1_WORDS;
+                                    if (a.hs_on) {
+                                        load_q8_1_any(xw, xb);
+                                    } else {
+                                        xb.d = half_bits_to_float(__ldcg(xw));
+#pragma unroll
+                                        for (int w = 0; w < 8; w++)
+                                            xb.q[w] = (int)__ldcg(xw + 1 + w);
+                                    }
+                                }
+                                acc[z] = fmaf(wb.d * xb.d, (float)dot_q8_block(wb.q, xb.q), acc[z]);
+                            }
+                        }
+                    }
+                    const float y = reduce4(acc[0], acc[1], acc[2], acc[3], lane);
+                    const int z = lane >> 3;
+                    const int yz = z == 0 ? yo[0] : z == 1 ? yo[1] : z == 2 ? yo[2] : yo[3];
+                    if ((lane & 7) == 0 && z < nu)
+                        ybuf[yz] = y;
+                }
             }
         }
         if (mine)
@@ -893,7 +1012,8 @@ extern "C" luce_status luce_moe_layer(const float *logits, const float *bias, co
     const size_t hs_bytes = (size_t)nslots * a.nbI * Q8_1_BYTES;
     a.hs_on = hs_bytes <= 24 * 1024 ? 1 : 0;
     a.hs_own = tu.layer_hs_own;
-    const size_t fixed = (size_t)T * a.nbH * Q8_1_BYTES + (a.hs_on ? hs_bytes : 0) +
+    const size_t xrow = (size_t)a.nbH * Q8_1_BYTES + (a.nbH % 64 == 0 ? (size_t)64 * (a.nbH / 32) : 0);
+    const size_t fixed = (size_t)T * xrow + (a.hs_on ? hs_bytes : 0) +
                          (size_t)nslots * RB_MAX * sizeof(float) + (size_t)2 * T * E * sizeof(float);
     const size_t budget = (size_t)tu.layer_budget_kb * 1024;
     if (budget < fixed + 2 * ((size_t)a.stage_bytes + 16))
