@@ -49,7 +49,7 @@ def parse():
     p.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying CUDA graphs")
     p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--path", choices=["layer", "split"], default="split",
+    p.add_argument("--path", choices=["layer", "split"], default="layer",
                    help="layer: each MoE layer is one launch (luce_moe_layer); split: prep, gate/up, down launches")
     p.add_argument("--layers", type=int, default=None, help="(debug) fewer layers; invalid as a bench number")
     p.add_argument("--input-steps", type=int, default=None,

@@ -262,10 +262,12 @@ LUCE_API luce_status luce_moe_prep(const float *logits, const float *bias, const
  *   clamp as in luce_moe_glu_pair; outputs as in the three calls.  h
  *   [T*k+T][I] f32 (16-byte aligned) is required: the launch keeps h there
  *   between its gate/up and down parts.
- *   sync: 8 bytes of device memory owned by the caller, zero before the
- *   first call and left consistent by every call that returns LUCE_OK and
- *   raises no fault.  Launches that may run at the same time (other streams)
- *   need distinct sync words.  After a LUCE_FAULT_TIMEOUT, zero it again.
+ *   sync: 8 bytes of device memory (8-byte aligned) owned by the caller,
+ *   zero before the first call: a 64-bit count of barrier arrivals that
+ *   only grows and needs no reset.  Calls that share it must run on the
+ *   same device with the same shapes (the same grid), one at a time (one
+ *   stream or ordered streams); calls that may run at the same time need
+ *   distinct words.  After a LUCE_FAULT_TIMEOUT, zero it again.
  *
  * The grid is launched cooperatively (all CTAs resident at once; its CTAs
  * meet at a device-wide barrier between the gate/up and the down parts, and

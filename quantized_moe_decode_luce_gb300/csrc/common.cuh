@@ -380,6 +380,7 @@ struct Tuning {
     int layer_cps = 1;        // whole-layer kernel: CTAs per SM
     int layer_prefetch = 1;   // whole-layer kernel: warm L2 with the shared expert
     int layer_hs_own = 1;     // whole-layer kernel: each CTA quantizes all of a small hq itself
+    int layer_hq_bulk = 1;    // whole-layer kernel: stage a shared hq with one bulk copy
 };
 extern Tuning g_tuning;
 

@@ -29,10 +29,9 @@
 //  * The gate/up part stores h in fp32.  The down product needs all of h:
 //    each CTA arrives at a device-wide barrier.  The grid is launched
 //    cooperatively, so all of its CTAs are resident at once and the barrier
-//    cannot wait for a CTA that has not started.  Its state (an arrival count
-//    and a generation) lives in caller memory and is reset on the device by
-//    the last CTA to arrive, so graph replays need no host update.  Its wait
-//    is bounded (LUCE_FAULT_TIMEOUT).
+//    cannot wait for a CTA that has not started.  Its state (a monotonic
+//    arrival count) lives in caller memory and needs no reset, so graph
+//    replays need no host update.  Its wait is bounded (LUCE_FAULT_TIMEOUT).
 //  * Then h -> q8_1 (the q8_1 rule of the separate kernels): when all of hq
 //    fits in 24 KB every CTA quantizes all of it into its own shared memory
 //    (CTA 0 also stores it); otherwise each CTA quantizes and stores its
@@ -83,7 +82,7 @@ struct LayerArgs {
     float *h;     // [T*k+T][I]
     uint32_t *hq; // [T*k+T][nbI] q8_1 blocks
     float *out;   // [T][H]
-    unsigned *sync; // [0] arrivals, [1] generation
+    unsigned long long *sync; // arrivals of every barrier (monotonic)
     int nbH, nbI, rbg, rbd;
     int RU;          // gate/up rows per part
     int stage_bytes; // one ring stage
@@ -91,6 +90,7 @@ struct LayerArgs {
     int SR;          // down rows per stage
     int hs_on;       // every CTA holds all of hq in shared memory
     int hs_own;      // ... quantized by itself from h (else staged from hq after a second barrier)
+    int hq_bulk;     // stage hq with one bulk copy (else 16-byte loads)
     int prefetch;
     int evict_first;
 };
@@ -104,25 +104,27 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
 
 // Device-wide barrier of the n CTAs of a cooperative grid, called by one
 // thread per CTA after a CTA barrier that follows the CTA's stores (the
-// release of the arrival covers them).  The generation is read before
-// arriving: it cannot advance before this CTA has arrived.  The last CTA
-// resets the count and then advances the generation, so the same words serve
-// the next barrier.  Returns false if the wait ran out (never in a correct
-// run).
-__device__ bool grid_barrier(unsigned *sync, unsigned n)
+// release of the arrival covers them).  `count` (64-bit, never wraps) only
+// grows: every barrier of every launch adds n, and all launches that share it
+// have the same n.  A CTA reads c before arriving; the CTAs already counted
+// in this barrier do not change floor(c / n), so the barrier ends when the
+// count reaches (floor(c / n) + 1) n.  Arrival is a reduction (no reply to
+// wait for).  Returns false if the wait ran out (never in a correct run).
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long *p)
 {
-    unsigned *count = sync, *gen = sync + 1;
-    const unsigned g = ld_acquire_gpu(gen);
-    unsigned old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(count) : "memory");
-    if (old == n - 1) {
-        asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(count) : "memory");
-        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(gen) : "memory");
-        return true;
-    }
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ bool grid_barrier(unsigned long long *count, unsigned n)
+{
+    const unsigned long long c0 = ld_acquire_gpu_u64(count);
+    const unsigned long long target = (c0 / n + 1ull) * n;
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(count) : "memory");
     const unsigned long long t0 = global_timer_ns();
     for (uint32_t i = 1;; i++) {
-        if (ld_acquire_gpu(gen) != g)
+        if (ld_acquire_gpu_u64(count) >= target)
             return true;
         if ((i & 15u) == 0u && global_timer_ns() - t0 > WAIT_LIMIT_NS)
             return false;
@@ -230,6 +232,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     __shared__ int v_e[MAX_V], v_first[MAX_V], v_ncols[MAX_V];
     __shared__ int wcnt[CW + 1];
     __shared__ int s_abort;
+    __shared__ __align__(8) uint64_t hq_bar; // the bulk copy of hq
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = a.T, E = a.E, k = a.k;
@@ -239,6 +242,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
+        mbar_init(&hq_bar, 1);
         fence_mbar_init();
         s_abort = 0;
     }
@@ -711,16 +715,34 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         } else {
             cta_barrier(); // every CTA's share of hq is stored
             if (a.hs_on && !*(volatile int *)&s_abort) {
-                // all of hq into shared memory: 16-byte loads at L2, each CTA
-                // starting at another offset (rows are multiples of 16 bytes)
-                const int n4 = nlive * ibytes_w / 4;
-                const int r4 = (int)(((long long)bx * 37) % n4);
-                const uint4 *src4 = reinterpret_cast<const uint4 *>(a.hq);
-                uint4 *dst4 = reinterpret_cast<uint4 *>(hs);
+                if (a.hq_bulk) {
+                    // all of hq into shared memory with one bulk copy (the rows
+                    // are multiples of 16 bytes); the proxy fence orders the
+                    // other CTAs' stores, seen through the barrier, before it
+                    const uint32_t bytes = (uint32_t)(nlive * ibytes_w * 4);
+                    if (tid == 0) {
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        mbar_arrive_expect_tx(&hq_bar, bytes);
+                        bulk_copy_g2s(hs, a.hq, bytes, &hq_bar, l2_evict_normal_policy());
+                    }
+                    if (!__all_sync(FULL, mbar_wait_bounded(&hq_bar, 0))) {
+                        if (lane == 0) {
+                            atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
+                            *(volatile int *)&s_abort = 1;
+                        }
+                    }
+                } else {
+                    // all of hq into shared memory: 16-byte loads at L2, each CTA
+                    // starting at another offset (rows are multiples of 16 bytes)
+                    const int n4 = nlive * ibytes_w / 4;
+                    const int r4 = (int)(((long long)bx * 37) % n4);
+                    const uint4 *src4 = reinterpret_cast<const uint4 *>(a.hq);
+                    uint4 *dst4 = reinterpret_cast<uint4 *>(hs);
 #pragma unroll 4
-                for (int i = tid; i < n4; i += CTHREADS) {
-                    const int j = i + r4 < n4 ? i + r4 : i + r4 - n4;
-                    dst4[j] = __ldcg(src4 + j);
+                    for (int i = tid; i < n4; i += CTHREADS) {
+                        const int j = i + r4 < n4 ? i + r4 : i + r4 - n4;
+                        dst4[j] = __ldcg(src4 + j);
+                    }
                 }
                 named_barrier(BAR_ALL, CTHREADS);
             }
@@ -991,7 +1013,7 @@ extern "C" luce_status luce_moe_layer(const float *logits, const float *bias, co
     a.h = h;
     a.hq = reinterpret_cast<uint32_t *>(hq);
     a.out = out;
-    a.sync = sync;
+    a.sync = reinterpret_cast<unsigned long long *>(sync);
     a.nbH = H / 32;
     a.nbI = I / 32;
     a.rbg = a.nbH * Q8_0_BYTES;
@@ -1012,6 +1034,7 @@ extern "C" luce_status luce_moe_layer(const float *logits, const float *bias, co
     const size_t hs_bytes = (size_t)nslots * a.nbI * Q8_1_BYTES;
     a.hs_on = hs_bytes <= 24 * 1024 ? 1 : 0;
     a.hs_own = tu.layer_hs_own;
+    a.hq_bulk = tu.layer_hq_bulk;
     const size_t xrow = (size_t)a.nbH * Q8_1_BYTES + (a.nbH % 64 == 0 ? (size_t)64 * (a.nbH / 32) : 0);
     const size_t fixed = (size_t)T * xrow + (a.hs_on ? hs_bytes : 0) +
                          (size_t)nslots * RB_MAX * sizeof(float) + (size_t)2 * T * E * sizeof(float);

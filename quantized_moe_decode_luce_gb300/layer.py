@@ -32,10 +32,10 @@ class MoEStep:
         self.out = torch.empty((T, H), dtype=torch.float32, device=dev)
         self.sync = torch.zeros(4, dtype=torch.int32, device=dev)  # device barrier state of luce_moe_layer
         self.fused_prep = True
-        # "split" (three launches) is the measured faster path on GB300 today;
-        # "layer" runs the whole layer in one cooperative launch (T <= 8,
-        # T*k <= 64, E <= 256) with bitwise the same results
-        self.path = "split"
+        # "layer": the whole layer in one cooperative launch (T <= 8, T*k <= 64,
+        # E <= 256), measured faster on GB300; "split": three launches, any
+        # shape.  Both give bitwise the same results.
+        self.path = "layer" if (T <= 8 and T * k <= 64 and E <= 256) else "split"
 
     def run(self, layer, x, logits, bias=None, stream=None, out=None) -> torch.Tensor:
         """layer: object with wg, wu, wd (+ wsg, wsu, wsd) uint8 CUDA tensors.
