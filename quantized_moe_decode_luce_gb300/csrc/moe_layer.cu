@@ -62,6 +62,8 @@ constexpr int GTHREADS = GW * 32;
 constexpr int CTHREADS = CW * 32;
 constexpr int THREADS = CTHREADS + 32;
 constexpr int BAR_ALL = 3;
+constexpr int BAR_ROUTE = 4;                 // the routing warps GW .. CW
+constexpr int RTHREADS = THREADS - GTHREADS; // routing threads (E <= this)
 constexpr int MAX_T = 8;
 constexpr int MAX_R = 64;  // T * k
 constexpr int MAX_E = 256; // one thread per expert in the grouping
@@ -94,13 +96,6 @@ struct LayerArgs {
     int prefetch;
     int evict_first;
 };
-
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
-{
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
 
 // Device-wide barrier of the n CTAs of a cooperative grid, called by one
 // thread per CTA after a CTA barrier that follows the CTA's stores (the
@@ -230,14 +225,37 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     __shared__ float w_s[MAX_R];
     __shared__ int cnt_s[MAX_E], off_s[MAX_E + 1];
     __shared__ int v_e[MAX_V], v_first[MAX_V], v_ncols[MAX_V];
-    __shared__ int wcnt[CW + 1];
+    __shared__ int wcnt[RTHREADS / 32];
     __shared__ int s_abort;
+    __shared__ int s_xnext; // next x block to quantize
+    __shared__ int s_nvr;   // routed virtual experts
     __shared__ __align__(8) uint64_t hq_bar; // the bulk copy of hq
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = a.T, E = a.E, k = a.k;
     const bool cta0 = blockIdx.x == 0;
-    if (tid == 0) {
+    const int nb = gridDim.x, bx = blockIdx.x;
+    const int half_bytes = a.RU * a.rbg;
+    // This CTA's slice of the shared expert's gate/up rows, [s0, s1): it does
+    // not depend on the routing, so its parts are requested at once and (for
+    // a single pass of x) computed while the other warps route.
+    const int s0 = a.wsg ? (int)((unsigned)(a.I * bx) / (unsigned)nb) : 0;
+    const int s1 = a.wsg ? (int)((unsigned)(a.I * (bx + 1)) / (unsigned)nb) : 0;
+    const int NPs = (s1 - s0 + a.RU - 1) / a.RU; // shared parts: RU rows each, the last shorter
+    const int NPe = min(NPs, a.NS);              // of them requested before the routing
+    const int nbx = T * a.nbH;                   // x blocks
+    const bool early = NPe > 0 && nbx <= GTHREADS / 4; // group 0 quantizes x in one pass, then takes them
+    const uint64_t pol = a.evict_first ? l2_evict_first_policy() : l2_evict_normal_policy();
+    auto issue_shared = [&](int qq) {
+        const uint32_t slot = (uint32_t)(qq % a.NS);
+        uint8_t *dst = ring + (size_t)slot * a.stage_bytes;
+        const int row = s0 + qq * a.RU, len = min(a.RU, s1 - row);
+        const uint32_t bytes = (uint32_t)(len * a.rbg);
+        mbar_arrive_expect_tx(&full[slot], 2 * bytes);
+        bulk_copy_g2s(dst, a.wsg + (size_t)row * a.rbg, bytes, &full[slot], pol);
+        bulk_copy_g2s(dst + half_bytes, a.wsu + (size_t)row * a.rbg, bytes, &full[slot], pol);
+    };
+    if (tid == CTHREADS) {
         for (int s = 0; s < a.NS; s++) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
@@ -245,276 +263,30 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         mbar_init(&hq_bar, 1);
         fence_mbar_init();
         s_abort = 0;
+        s_xnext = 0;
     }
-    if (tid == CTHREADS && a.wsg && a.prefetch) {
-        // before the previous kernel has finished: warm L2 with this CTA's
-        // slice of the shared expert (needed whatever the routing)
-        const size_t tot_gu = (size_t)a.I * a.rbg, tot_d = (size_t)a.H * a.rbd; // multiples of 16
-        const size_t cg = ((tot_gu / gridDim.x) + 15) & ~size_t(15);
-        const size_t cd = ((tot_d / gridDim.x) + 15) & ~size_t(15);
-        const size_t og = cg * blockIdx.x, od = cd * blockIdx.x;
-        if (og < tot_gu) {
-            const uint32_t n = (uint32_t)min(cg, tot_gu - og);
-            prefetch_l2(a.wsg + og, n);
-            prefetch_l2(a.wsu + og, n);
+    __syncthreads(); // barriers initialized
+    if (tid == CTHREADS) {
+        // weights do not depend on the previous kernel: request them before waiting for it
+        for (int qq = 0; qq < NPe; qq++)
+            issue_shared(qq);
+        if (a.wsd && a.prefetch) {
+            // and warm L2 with this CTA's slice of the shared expert's down rows
+            const size_t tot_d = (size_t)a.H * a.rbd; // a multiple of 16
+            const size_t cd = ((tot_d / nb) + 15) & ~size_t(15);
+            const size_t od = cd * bx;
+            if (od < tot_d)
+                prefetch_l2(a.wsd + od, (uint32_t)min(cd, tot_d - od));
         }
-        if (od < tot_d)
-            prefetch_l2(a.wsd + od, (uint32_t)min(cd, tot_d - od));
     }
     pdl_wait();
     pdl_trigger();
 
-    // ---------------- 1. scores, and x -> q8_1 in shared memory ----------------
-    for (int i = tid; i < T * E; i += THREADS) {
-        const float l = a.logits[i];
-        lsm[i] = l;
-        scores[i] = a.bias ? __fadd_rn(l, a.bias[i % E]) : l;
-    }
-    for (int i = tid; i < R; i += THREADS)
-        ids_s[i] = -1;
-    {
-        const int nbx = T * a.nbH;
-        const int qj = lane & 3;
-        for (int base = 0; base < nbx; base += THREADS / 4) { // warp-uniform trip count
-            const int b = base + (tid >> 2);
-            const bool valid = b < nbx;
-            float v[8];
-            if (valid) {
-                load8(a.x + (size_t)b * QK + qj * 8, v, false);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; i++)
-                    v[i] = 0.0f;
-            }
-            const int bt = valid ? b / a.nbH : 0, bg = valid ? b - bt * a.nbH : 0;
-            uint32_t *dst = xs + (size_t)bt * xstride + (size_t)bg * Q8_1_WORDS + xpad * (bg >> 5);
-            quantize_q8_1_quad(v, valid, dst, qj);
-            if (cta0 && valid) {
-                uint32_t *g = a.xq + (size_t)b * Q8_1_WORDS;
-                g[1 + 2 * qj] = dst[1 + 2 * qj]; // this lane's own words
-                g[2 + 2 * qj] = dst[2 + 2 * qj];
-                if (qj == 0)
-                    g[0] = dst[0];
-            }
-        }
-    }
-    __syncthreads();
-
-    // ---------------- 2. selection by rank (4 threads per (token, expert)) ----------------
-    {
-        const int npair = T * E;
-        const int qj = lane & 3;
-        const int qE = (E + 3) >> 2;
-        for (int base = 0; base < npair; base += THREADS / 4) { // warp-uniform trip count
-            const int p = base + (tid >> 2);
-            int rank = 0;
-            int t = 0, e = 0;
-            if (p < npair) {
-                t = p / E;
-                e = p - t * E;
-                const float *s = scores + (size_t)t * E;
-                const float v = s[e];
-                const int e_end = min(E, (qj + 1) * qE);
-                for (int e2 = qj * qE; e2 < e_end; e2++) {
-                    const float o = s[e2];
-                    rank += (o > v || (o == v && e2 < e)) ? 1 : 0;
-                }
-            }
-            rank += __shfl_xor_sync(FULL, rank, 1);
-            rank += __shfl_xor_sync(FULL, rank, 2);
-            if (p < npair && qj == 0 && rank < k)
-                ids_s[t * k + rank] = e;
-        }
-    }
-    __syncthreads();
-
-    // ---------------- 3. weights (warp t) and grouping ----------------
-    if (warp < T) {
-        const int t = warp;
-        float sel0 = 0.0f, sel1 = 0.0f;
-        if (lane < k) {
-            const int e = ids_s[t * k + lane];
-            sel0 = e >= 0 ? lsm[t * E + e] : 0.0f;
-        }
-        if (lane + 32 < k) {
-            const int e = ids_s[t * k + lane + 32];
-            sel1 = e >= 0 ? lsm[t * E + e] : 0.0f;
-        }
-        route_softmax_warp(sel0, sel1, k, w_s + t * k, lane);
-    }
-    if (tid < R) {
-        // slot of route r in the (expert, route) order; masked routes have none
-        const int e = ids_s[tid];
-        int pos = -1;
-        if (e >= 0) {
-            pos = 0;
-            for (int r2 = 0; r2 < R; r2++) {
-                const int e2 = ids_s[r2];
-                pos += (e2 >= 0 && (e2 < e || (e2 == e && r2 < tid))) ? 1 : 0;
-            }
-        }
-        pos_s[tid] = pos;
-    }
-    {
-        const int e = tid; // E <= THREADS
-        int c = 0, o = 0;
-        if (e < E) {
-            for (int r2 = 0; r2 < R; r2++) {
-                const int e2 = ids_s[r2];
-                c += e2 == e ? 1 : 0;
-                o += (e2 >= 0 && e2 < e) ? 1 : 0;
-            }
-            cnt_s[e] = c;
-            off_s[e] = o;
-        }
-        if (e == 0) {
-            int nvalid = 0;
-            for (int r2 = 0; r2 < R; r2++)
-                nvalid += ids_s[r2] >= 0 ? 1 : 0;
-            off_s[E] = nvalid;
-        }
-        const unsigned bal = __ballot_sync(FULL, e < E && c > 0);
-        if (lane == 0)
-            wcnt[warp] = __popc(bal);
-    }
-    __syncthreads();
-    if (tid < R) {
-        if (pos_s[tid] >= 0)
-            routes_s[pos_s[tid]] = tid;
-        if (tid >= off_s[E])
-            routes_s[tid] = -1;
-    }
-    {
-        const int e = tid;
-        const bool act = e < E && cnt_s[e] > 0;
-        const unsigned bal = __ballot_sync(FULL, act);
-        int before = __popc(bal & ((1u << lane) - 1u));
-        for (int w = 0; w < warp; w++)
-            before += wcnt[w];
-        if (act) {
-            v_e[before] = e;
-            v_first[before] = off_s[e];
-            v_ncols[before] = cnt_s[e];
-        }
-    }
-    int NVr = 0;
-    for (int w = 0; w <= CW; w++)
-        NVr += wcnt[w];
-    const int NV = NVr + (a.wsg ? 1 : 0);
-    if (tid == 0 && a.wsg) {
-        v_e[NVr] = E;
-        v_first[NVr] = 0;
-        v_ncols[NVr] = T;
-    }
-    __syncthreads();
-    if (cta0) {
-        for (int i = tid; i < R; i += THREADS) {
-            a.ids[i] = ids_s[i];
-            a.weights[i] = w_s[i];
-            a.routes[i] = routes_s[i];
-        }
-        for (int e = tid; e < E; e += THREADS) {
-            a.counts[e] = cnt_s[e];
-            a.offsets[e] = off_s[e];
-        }
-        if (tid == 0)
-            a.offsets[E] = off_s[E];
-    }
-
-    // ---------------- 4. this CTA's work ----------------
-    // gate/up rows [r0, r1) of all NV * I rows (virtual expert major); down
-    // output rows [dn0, dn1)
-    // (unsigned 32-bit: NV * I <= 65 * 32768 rows, times at most 1024 CTAs < 2^32)
-    const int nb = gridDim.x, bx = blockIdx.x;
-    const int NR = NV * a.I;
-    const int r0 = (int)((unsigned)(NR * bx) / (unsigned)nb), r1 = (int)((unsigned)(NR * (bx + 1)) / (unsigned)nb);
-    const int dn0 = a.H * bx / nb, dn1 = a.H * (bx + 1) / nb;
-    int NPg = 0;
-    for (int gr = r0; gr < r1; NPg++)
-        gr += part_at(gr, r1, a.I, a.RU).len;
-    // down rows in nrb row blocks of rpb rows (the last may be shorter); a row
-    // block's NV * rows items (expert major) are cut into stages of SR rows
-    const int SR = a.SR;
-    const int nrows = dn1 - dn0;
-    const int nrb = (nrows + RB_MAX - 1) / RB_MAX;
-    const int rpb = nrb ? (nrows + nrb - 1) / nrb : 0;
-    const int rlast = nrows - (nrb - 1) * rpb;
-    const int spr = nrb ? (NV * rpb + SR - 1) / SR : 0;     // stages of a full row block
-    const int slast = nrb ? (NV * rlast + SR - 1) / SR : 0; // stages of the last one
-    const int NPd = nrb ? (nrb - 1) * spr + slast : 0;
-    const int NP = NPg + NPd;
-    auto down_stage = [&](int d, int &rb, int &sp) {
-        rb = d / max(spr, 1);
-        if (rb >= nrb - 1) {
-            rb = nrb - 1;
-            sp = d - (nrb - 1) * spr;
-        } else {
-            sp = d - rb * spr;
-        }
-    };
-    const int half_bytes = a.RU * a.rbg;
-
-    if (warp == CW) {
-        // ---------------- the producer: every stage of this CTA, in order ----------------
-        if (lane != 0)
-            return;
-        const uint64_t pol = a.evict_first ? l2_evict_first_policy() : l2_evict_normal_policy();
-        int gr = r0;
-        int issued = 0;
-        for (; issued < NP; issued++) {
-            const uint32_t slot = (uint32_t)(issued % a.NS), use = (uint32_t)(issued / a.NS);
-            if (use > 0 && !mbar_wait_bounded(&empty[slot], (use - 1) & 1u)) {
-                atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
-                *(volatile int *)&s_abort = 1;
-                break;
-            }
-            if (*(volatile int *)&s_abort)
-                break;
-            uint8_t *dst = ring + (size_t)slot * a.stage_bytes;
-            if (issued < NPg) {
-                const Part pt = part_at(gr, r1, a.I, a.RU);
-                gr += pt.len;
-                const int e = v_e[pt.v];
-                const uint8_t *gsrc = (e < E ? a.wg + (size_t)e * a.I * a.rbg : a.wsg) + (size_t)pt.row * a.rbg;
-                const uint8_t *usrc = (e < E ? a.wu + (size_t)e * a.I * a.rbg : a.wsu) + (size_t)pt.row * a.rbg;
-                const uint32_t bytes = (uint32_t)(pt.len * a.rbg);
-                mbar_arrive_expect_tx(&full[slot], 2 * bytes);
-                bulk_copy_g2s(dst, gsrc, bytes, &full[slot], pol);
-                bulk_copy_g2s(dst + half_bytes, usrc, bytes, &full[slot], pol);
-            } else {
-                int rb, sp;
-                down_stage(issued - NPg, rb, sp);
-                const int nr0 = dn0 + rb * rpb;
-                const int rows = rb == nrb - 1 ? rlast : rpb;
-                const int i0 = sp * SR, i1 = min(NV * rows, i0 + SR);
-                mbar_arrive_expect_tx(&full[slot], (uint32_t)((i1 - i0) * a.rbd));
-                for (int i = i0; i < i1;) {
-                    const int v = i / rows, m = i - v * rows;
-                    const int cnt = min(i1 - i, rows - m);
-                    const int e = v_e[v];
-                    const uint8_t *src = e < E ? a.wd + ((size_t)e * a.H + nr0 + m) * a.rbd
-                                               : a.wsd + (size_t)(nr0 + m) * a.rbd;
-                    bulk_copy_g2s(dst + (size_t)(i - i0) * a.rbd, src, (uint32_t)(cnt * a.rbd), &full[slot], pol);
-                    i += cnt;
-                }
-            }
-        }
-        // no bulk copy may still be writing shared memory when the CTA exits
-        const int n_slots = issued < a.NS ? issued : a.NS;
-        for (int sl = 0; sl < n_slots; sl++) {
-            const int last_use = (issued - 1 - sl) / a.NS;
-            if (!mbar_wait_bounded(&full[sl], (uint32_t)last_use & 1u))
-                atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
-        }
-        return;
-    }
-
-    // ---------------- consumers (warps 0 .. CW-1) ----------------
-    const int grp = warp / GW, wl = warp - grp * GW; // group, warp within it
+    // ---------------- consumer helpers ----------------
+    const int grp = warp / GW, wl = warp - grp * GW; // consumer group, warp within it
     const int gtid = tid - grp * GTHREADS;
     bool dead = false;
-    int q = 0;
-    // waits for stage q; false if this CTA gave up (now or earlier)
+    // waits for stage qq; false if this CTA gave up (now or earlier)
     auto wait_stage = [&](int qq) -> bool {
         // warp-uniform: every lane takes the same branch to the __all_sync
         if (__any_sync(FULL, *(volatile int *)&s_abort != 0))
@@ -547,108 +319,401 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         named_barrier(BAR_ALL, CTHREADS);
     };
 
-    // ---------------- 5. gate/up rows -> h ----------------
+    // x -> q8_1 into shared memory (CTA 0 also stores xq): a warp claims 8
+    // blocks at a time, 4 lanes per block
+    auto quantize_x = [&]() {
+        const int qj = lane & 3;
+        for (;;) { // warp-uniform trip count
+            int base = 0;
+            if (lane == 0)
+                base = atomicAdd(&s_xnext, 8);
+            base = __shfl_sync(FULL, base, 0);
+            if (base >= nbx)
+                break;
+            const int b = base + (lane >> 2);
+            const bool valid = b < nbx;
+            float v[8];
+            if (valid) {
+                load8(a.x + (size_t)b * QK + qj * 8, v, false);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; i++)
+                    v[i] = 0.0f;
+            }
+            const int bt = valid ? b / a.nbH : 0, bg = valid ? b - bt * a.nbH : 0;
+            uint32_t *dst = xs + (size_t)bt * xstride + (size_t)bg * Q8_1_WORDS + xpad * (bg >> 5);
+            quantize_q8_1_quad(v, valid, dst, qj);
+            if (cta0 && valid) {
+                uint32_t *g = a.xq + (size_t)b * Q8_1_WORDS;
+                g[1 + 2 * qj] = dst[1 + 2 * qj]; // this lane's own words
+                g[2 + 2 * qj] = dst[2 + 2 * qj];
+                if (qj == 0)
+                    g[0] = dst[0];
+            }
+        }
+    };
+
     // one token (NC == 1): this lane's x blocks stay in registers for every row
     constexpr int XR = 4;
     const int nblg = rowmap_blocks(gmap, a.nbH, lane);
     const bool x_regs = NC == 1 && a.T == 1 && nblg <= XR;
     Q81Block xreg[XR];
+    auto load_xregs = [&]() {
 #pragma unroll
-    for (int j = 0; j < XR; j++) {
-        if (x_regs && j < nblg) {
-            const int b = rowmap_block(gmap, lane, j);
-            load_q8_1_any(xs + (size_t)b * Q8_1_WORDS + xpad * (b >> 5), xreg[j]);
-        } else {
-            xreg[j].d = 0.0f;
+        for (int j = 0; j < XR; j++) {
+            if (x_regs && j < nblg) {
+                const int b = rowmap_block(gmap, lane, j);
+                load_q8_1_any(xs + (size_t)b * Q8_1_WORDS + xpad * (b >> 5), xreg[j]);
+            } else {
+                xreg[j].d = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 8; i++)
-                xreg[j].q[i] = 0;
+                for (int i = 0; i < 8; i++)
+                    xreg[j].q[i] = 0;
+            }
         }
-    }
-    {
-        int gr = r0;
-        for (; q < NPg; q++) {
-            const Part pt = part_at(gr, r1, a.I, a.RU);
-            gr += pt.len;
-            if ((q & 1) != grp)
-                continue; // the other group's stage
-            const int e = v_e[pt.v], first = v_first[pt.v], ncols = v_ncols[pt.v];
-            const bool routed = e < E;
-            if (wait_stage(q)) {
-                const uint8_t *st = ring + (size_t)(q % a.NS) * a.stage_bytes;
-                for (int i = wl; i < pt.len; i += GW) {
-                    const int row = pt.row + i;
-                    const uint8_t *grow = st + (size_t)i * a.rbg;
-                    const uint8_t *urow = st + half_bytes + (size_t)i * a.rbg;
-                    for (int c0 = 0; c0 < ncols; c0 += NC) {
-                        const int nc = min(NC, ncols - c0);
-                        const uint32_t *xc[NC];
-                        int rr[NC];
+    };
+
+    // gate/up rows [row, row + len) of one part in stage qq -> h; columns of
+    // a routed expert (first, ncols) or, routed == false, the T shared tokens
+    auto glu_part = [&](int qq, int row0, int len, bool routed, int first, int ncols) {
+        if (wait_stage(qq)) {
+            const uint8_t *st = ring + (size_t)(qq % a.NS) * a.stage_bytes;
+            for (int i = wl; i < len; i += GW) {
+                const int row = row0 + i;
+                const uint8_t *grow = st + (size_t)i * a.rbg;
+                const uint8_t *urow = st + half_bytes + (size_t)i * a.rbg;
+                for (int c0 = 0; c0 < ncols; c0 += NC) {
+                    const int nc = min(NC, ncols - c0);
+                    const uint32_t *xc[NC];
+                    int rr[NC];
 #pragma unroll
-                        for (int c = 0; c < NC; c++) {
-                            const int cc = c0 + (c < nc ? c : 0);
-                            rr[c] = routed ? routes_s[first + cc] : R + cc; // h row
-                            xc[c] = xs + (size_t)(routed ? rr[c] / k : cc) * xstride;
-                        }
-                        float ag[NC], au[NC];
+                    for (int c = 0; c < NC; c++) {
+                        const int cc = c0 + (c < nc ? c : 0);
+                        rr[c] = routed ? routes_s[first + cc] : R + cc; // h row
+                        xc[c] = xs + (size_t)(routed ? rr[c] / k : cc) * xstride;
+                    }
+                    float ag[NC], au[NC];
 #pragma unroll
-                        for (int c = 0; c < NC; c++)
-                            ag[c] = au[c] = 0.0f;
-                        if (x_regs) {
-                            // one token: its x blocks are in registers
+                    for (int c = 0; c < NC; c++)
+                        ag[c] = au[c] = 0.0f;
+                    if (x_regs) {
+                        // one token: its x blocks are in registers
 #pragma unroll
-                            for (int j = 0; j < XR; j++) {
-                                if (j < nblg) {
-                                    const int b = rowmap_block(gmap, lane, j);
-                                    Q80Block gbk, ubk;
-                                    load_q8_0_smem(grow, b, gbk);
-                                    load_q8_0_smem(urow, b, ubk);
-                                    const int sg = dot_q8_block(gbk.q, xreg[j].q);
-                                    const int su = dot_q8_block(ubk.q, xreg[j].q);
-                                    ag[0] = fmaf(gbk.d * xreg[j].d, (float)sg, ag[0]);
-                                    au[0] = fmaf(ubk.d * xreg[j].d, (float)su, au[0]);
-                                }
-                            }
-                        } else {
-                            for (int j = 0; j < nblg; j++) {
+                        for (int j = 0; j < XR; j++) {
+                            if (j < nblg) {
                                 const int b = rowmap_block(gmap, lane, j);
                                 Q80Block gbk, ubk;
                                 load_q8_0_smem(grow, b, gbk);
                                 load_q8_0_smem(urow, b, ubk);
+                                const int sg = dot_q8_block(gbk.q, xreg[j].q);
+                                const int su = dot_q8_block(ubk.q, xreg[j].q);
+                                ag[0] = fmaf(gbk.d * xreg[j].d, (float)sg, ag[0]);
+                                au[0] = fmaf(ubk.d * xreg[j].d, (float)su, au[0]);
+                            }
+                        }
+                    } else {
+                        for (int j = 0; j < nblg; j++) {
+                            const int b = rowmap_block(gmap, lane, j);
+                            Q80Block gbk, ubk;
+                            load_q8_0_smem(grow, b, gbk);
+                            load_q8_0_smem(urow, b, ubk);
 #pragma unroll
-                                for (int c = 0; c < NC; c++) {
-                                    if (c < nc) {
-                                        Q81Block xb;
-                                        load_q8_1_any(xc[c] + (size_t)b * Q8_1_WORDS + xpad * (b >> 5), xb);
-                                        const int sg = dot_q8_block(gbk.q, xb.q);
-                                        const int su = dot_q8_block(ubk.q, xb.q);
-                                        ag[c] = fmaf(gbk.d * xb.d, (float)sg, ag[c]);
-                                        au[c] = fmaf(ubk.d * xb.d, (float)su, au[c]);
-                                    }
+                            for (int c = 0; c < NC; c++) {
+                                if (c < nc) {
+                                    Q81Block xb;
+                                    load_q8_1_any(xc[c] + (size_t)b * Q8_1_WORDS + xpad * (b >> 5), xb);
+                                    const int sg = dot_q8_block(gbk.q, xb.q);
+                                    const int su = dot_q8_block(ubk.q, xb.q);
+                                    ag[c] = fmaf(gbk.d * xb.d, (float)sg, ag[c]);
+                                    au[c] = fmaf(ubk.d * xb.d, (float)su, au[c]);
                                 }
                             }
                         }
-                        // two columns per pass: g0, u0, g1, u1 at lanes 0, 8, 16, 24
+                    }
+                    // two columns per pass: g0, u0, g1, u1 at lanes 0, 8, 16, 24
 #pragma unroll
-                        for (int c = 0; c < NC; c += 2) {
-                            if (c < nc) {
-                                const bool two = c + 1 < nc;
-                                const float g1 = two ? ag[(c + 1) % NC] : 0.0f;
-                                const float u1 = two ? au[(c + 1) % NC] : 0.0f;
-                                const float s = reduce4(ag[c], au[c], g1, u1, lane);
-                                const float u = __shfl_down_sync(FULL, s, 8); // lane 0: u0, lane 16: u1
-                                if (lane == 0)
-                                    a.h[(size_t)rr[c] * a.I + row] = swiglu(s, u, a.clamp);
-                                if (two && lane == 16)
-                                    a.h[(size_t)rr[(c + 1) % NC] * a.I + row] = swiglu(s, u, a.clamp);
-                            }
+                    for (int c = 0; c < NC; c += 2) {
+                        if (c < nc) {
+                            const bool two = c + 1 < nc;
+                            const float g1 = two ? ag[(c + 1) % NC] : 0.0f;
+                            const float u1 = two ? au[(c + 1) % NC] : 0.0f;
+                            const float sm = reduce4(ag[c], au[c], g1, u1, lane);
+                            const float u = __shfl_down_sync(FULL, sm, 8); // lane 0: u0, lane 16: u1
+                            if (lane == 0)
+                                a.h[(size_t)rr[c] * a.I + row] = swiglu(sm, u, a.clamp);
+                            if (two && lane == 16)
+                                a.h[(size_t)rr[(c + 1) % NC] * a.I + row] = swiglu(sm, u, a.clamp);
                         }
                     }
                 }
             }
-            release_stage(q);
+        }
+        release_stage(qq);
+    };
+
+    // ---------------- 1-3. x -> q8_1 (warps 0 .. GW-1) while warps GW .. CW route ----------------
+    if (warp < GW) {
+        quantize_x();
+        if (early) {
+            named_barrier(1, GTHREADS); // all of x is quantized (one pass, by this group)
+            load_xregs();
+            for (int qq = 0; qq < NPe; qq += 2) { // group 0's stages: the even ones
+                const int row = s0 + qq * a.RU;
+                glu_part(qq, row, min(a.RU, s1 - row), false, 0, T);
+            }
+        }
+    } else {
+        const int rt = tid - GTHREADS;      // routing threads 0 .. RTHREADS-1
+        const int rw = warp - GW;           // routing warp
+        for (int i = rt; i < T * E; i += RTHREADS) {
+            const float l = a.logits[i];
+            lsm[i] = l;
+            scores[i] = a.bias ? __fadd_rn(l, a.bias[i % E]) : l;
+        }
+        for (int i = rt; i < R; i += RTHREADS)
+            ids_s[i] = -1;
+        named_barrier(BAR_ROUTE, RTHREADS);
+        // selection by rank, 4 threads per (token, expert)
+        {
+            const int npair = T * E;
+            const int qj = lane & 3;
+            const int qE = (E + 3) >> 2;
+            for (int base = 0; base < npair; base += RTHREADS / 4) { // warp-uniform trip count
+                const int p = base + (rt >> 2);
+                int rank = 0;
+                int t = 0, e = 0;
+                if (p < npair) {
+                    t = p / E;
+                    e = p - t * E;
+                    const float *sc = scores + (size_t)t * E;
+                    const float v = sc[e];
+                    const int e_end = min(E, (qj + 1) * qE);
+                    for (int e2 = qj * qE; e2 < e_end; e2++) {
+                        const float o = sc[e2];
+                        rank += (o > v || (o == v && e2 < e)) ? 1 : 0;
+                    }
+                }
+                rank += __shfl_xor_sync(FULL, rank, 1);
+                rank += __shfl_xor_sync(FULL, rank, 2);
+                if (p < npair && qj == 0 && rank < k)
+                    ids_s[t * k + rank] = e;
+            }
+        }
+        named_barrier(BAR_ROUTE, RTHREADS);
+        // weights (routing warp t) and grouping
+        if (rw < T) {
+            const int t = rw;
+            float sel0 = 0.0f, sel1 = 0.0f;
+            if (lane < k) {
+                const int e = ids_s[t * k + lane];
+                sel0 = e >= 0 ? lsm[t * E + e] : 0.0f;
+            }
+            if (lane + 32 < k) {
+                const int e = ids_s[t * k + lane + 32];
+                sel1 = e >= 0 ? lsm[t * E + e] : 0.0f;
+            }
+            route_softmax_warp(sel0, sel1, k, w_s + t * k, lane);
+        }
+        if (rt < R) {
+            // slot of route r in the (expert, route) order; masked routes have none
+            const int e = ids_s[rt];
+            int pos = -1;
+            if (e >= 0) {
+                pos = 0;
+                for (int r2 = 0; r2 < R; r2++) {
+                    const int e2 = ids_s[r2];
+                    pos += (e2 >= 0 && (e2 < e || (e2 == e && r2 < rt))) ? 1 : 0;
+                }
+            }
+            pos_s[rt] = pos;
+        }
+        {
+            const int e = rt; // E <= RTHREADS
+            int c = 0, o = 0;
+            if (e < E) {
+                for (int r2 = 0; r2 < R; r2++) {
+                    const int e2 = ids_s[r2];
+                    c += e2 == e ? 1 : 0;
+                    o += (e2 >= 0 && e2 < e) ? 1 : 0;
+                }
+                cnt_s[e] = c;
+                off_s[e] = o;
+            }
+            if (e == 0) {
+                int nvalid = 0;
+                for (int r2 = 0; r2 < R; r2++)
+                    nvalid += ids_s[r2] >= 0 ? 1 : 0;
+                off_s[E] = nvalid;
+            }
+            const unsigned bal = __ballot_sync(FULL, e < E && c > 0);
+            if (lane == 0)
+                wcnt[rw] = __popc(bal);
+        }
+        named_barrier(BAR_ROUTE, RTHREADS);
+        if (rt < R) {
+            if (pos_s[rt] >= 0)
+                routes_s[pos_s[rt]] = rt;
+            if (rt >= off_s[E])
+                routes_s[rt] = -1;
+        }
+        {
+            const int e = rt;
+            const bool act = e < E && cnt_s[e] > 0;
+            const unsigned bal = __ballot_sync(FULL, act);
+            int before = __popc(bal & ((1u << lane) - 1u));
+            for (int w = 0; w < rw; w++)
+                before += wcnt[w];
+            if (act) {
+                v_e[before] = e;
+                v_first[before] = off_s[e];
+                v_ncols[before] = cnt_s[e];
+            }
+            if (rt == 0) {
+                int nvr = 0;
+                for (int w = 0; w < RTHREADS / 32; w++)
+                    nvr += wcnt[w];
+                s_nvr = nvr;
+                if (a.wsg) {
+                    v_e[nvr] = E;
+                    v_first[nvr] = 0;
+                    v_ncols[nvr] = T;
+                }
+            }
+        }
+        named_barrier(BAR_ROUTE, RTHREADS);
+        if (cta0) {
+            for (int i = rt; i < R; i += RTHREADS) {
+                a.ids[i] = ids_s[i];
+                a.weights[i] = w_s[i];
+                a.routes[i] = routes_s[i];
+            }
+            for (int e = rt; e < E; e += RTHREADS) {
+                a.counts[e] = cnt_s[e];
+                a.offsets[e] = off_s[e];
+            }
+            if (rt == 0)
+                a.offsets[E] = off_s[E];
+        }
+        if (!early)
+            quantize_x(); // what is left of x (with the early stage, group 0 alone quantizes all of it)
+    }
+    __syncthreads(); // routing tables and all of x are in shared memory
+
+    // ---------------- 4. this CTA's work ----------------
+    // gate/up: the shared slice [s0, s1), then the routed rows [r0, r1) of all
+    // NVr * I routed rows (expert major); down output rows [dn0, dn1)
+    // (unsigned 32-bit: NVr * I <= 64 * 32768 rows, times at most 1024 CTAs < 2^32)
+    const int NVr = s_nvr;
+    const int NV = NVr + (a.wsg ? 1 : 0);
+    const int NRr = NVr * a.I;
+    const int r0 = (int)((unsigned)(NRr * bx) / (unsigned)nb), r1 = (int)((unsigned)(NRr * (bx + 1)) / (unsigned)nb);
+    const int dn0 = a.H * bx / nb, dn1 = a.H * (bx + 1) / nb;
+    // down rows in nrb row blocks of rpb rows (the last may be shorter); a row
+    // block's NV * rows items (expert major) are cut into stages of SR rows
+    const int SR = a.SR;
+    int nrb, rpb, rlast, spr, slast, NPd;
+    auto plan_down = [&]() {
+        const int nrows = dn1 - dn0;
+        nrb = (nrows + RB_MAX - 1) / RB_MAX;
+        rpb = nrb ? (nrows + nrb - 1) / nrb : 0;
+        rlast = nrows - (nrb - 1) * rpb;
+        spr = nrb ? (NV * rpb + SR - 1) / SR : 0;     // stages of a full row block
+        slast = nrb ? (NV * rlast + SR - 1) / SR : 0; // stages of the last one
+        NPd = nrb ? (nrb - 1) * spr + slast : 0;
+    };
+    auto down_stage = [&](int d, int &rb, int &sp) {
+        rb = d / max(spr, 1);
+        if (rb >= nrb - 1) {
+            rb = nrb - 1;
+            sp = d - (nrb - 1) * spr;
+        } else {
+            sp = d - rb * spr;
+        }
+    };
+
+    if (warp == CW) {
+        // ---------------- the producer: every stage of this CTA, in order ----------------
+        if (lane != 0)
+            return;
+        int NPg = NPs;
+        for (int gr = r0; gr < r1; NPg++)
+            gr += part_at(gr, r1, a.I, a.RU).len;
+        plan_down();
+        const int NP = NPg + NPd;
+        int gr = r0;
+        int issued = NPe; // the first shared parts went out before the routing
+        for (; issued < NP; issued++) {
+            const uint32_t slot = (uint32_t)(issued % a.NS), use = (uint32_t)(issued / a.NS);
+            if (use > 0 && !mbar_wait_bounded(&empty[slot], (use - 1) & 1u)) {
+                atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
+                *(volatile int *)&s_abort = 1;
+                break;
+            }
+            if (*(volatile int *)&s_abort)
+                break;
+            uint8_t *dst = ring + (size_t)slot * a.stage_bytes;
+            if (issued < NPs) {
+                issue_shared(issued);
+            } else if (issued < NPg) {
+                const Part pt = part_at(gr, r1, a.I, a.RU);
+                gr += pt.len;
+                const int e = v_e[pt.v];
+                const uint8_t *gsrc = a.wg + ((size_t)e * a.I + pt.row) * a.rbg;
+                const uint8_t *usrc = a.wu + ((size_t)e * a.I + pt.row) * a.rbg;
+                const uint32_t bytes = (uint32_t)(pt.len * a.rbg);
+                mbar_arrive_expect_tx(&full[slot], 2 * bytes);
+                bulk_copy_g2s(dst, gsrc, bytes, &full[slot], pol);
+                bulk_copy_g2s(dst + half_bytes, usrc, bytes, &full[slot], pol);
+            } else {
+                int rb, sp;
+                down_stage(issued - NPg, rb, sp);
+                const int nr0 = dn0 + rb * rpb;
+                const int rows = rb == nrb - 1 ? rlast : rpb;
+                const int i0 = sp * SR, i1 = min(NV * rows, i0 + SR);
+                mbar_arrive_expect_tx(&full[slot], (uint32_t)((i1 - i0) * a.rbd));
+                for (int i = i0; i < i1;) {
+                    const int v = i / rows, m = i - v * rows;
+                    const int cnt = min(i1 - i, rows - m);
+                    const int e = v_e[v];
+                    const uint8_t *src = e < E ? a.wd + ((size_t)e * a.H + nr0 + m) * a.rbd
+                                               : a.wsd + (size_t)(nr0 + m) * a.rbd;
+                    bulk_copy_g2s(dst + (size_t)(i - i0) * a.rbd, src, (uint32_t)(cnt * a.rbd), &full[slot], pol);
+                    i += cnt;
+                }
+            }
+        }
+        // no bulk copy may still be writing shared memory when the CTA exits
+        const int n_slots = issued < a.NS ? issued : a.NS;
+        for (int sl = 0; sl < n_slots; sl++) {
+            const int last_use = (issued - 1 - sl) / a.NS;
+            if (!mbar_wait_bounded(&full[sl], (uint32_t)last_use & 1u))
+                atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
+        }
+        return;
+    }
+
+    // ---------------- 5. gate/up rows -> h (consumer warps) ----------------
+    if (!(early && grp == 0))
+        load_xregs();
+    int q = 0;
+    {
+        int gr = r0;
+        for (; q < NPs || gr < r1; q++) {
+            if (q < NPs) {
+                if ((q & 1) != grp || (early && grp == 0 && q < NPe))
+                    continue; // the other group's stage, or one group 0 took before the routing
+                const int row = s0 + q * a.RU;
+                glu_part(q, row, min(a.RU, s1 - row), false, 0, T);
+                continue;
+            }
+            const Part pt = part_at(gr, r1, a.I, a.RU);
+            gr += pt.len;
+            if ((q & 1) != grp)
+                continue; // the other group's stage
+            glu_part(q, pt.row, pt.len, true, v_first[pt.v], v_ncols[pt.v]);
         }
     }
+    plan_down(); // q is now the first down stage
 
     // ---------------- 6. all of h is stored: h -> q8_1 ----------------
     cta_barrier();
