@@ -277,6 +277,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// Whether the phase of `parity` has completed, without waiting.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase of `parity` to complete, for at most WAIT_LIMIT_NS.
 // Returns false (and the caller raises LUCE_FAULT_TIMEOUT) if it gave up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity)
@@ -340,6 +354,19 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Arrival at a named barrier without waiting (the threads that wait there
+// with named_barrier see the memory writes made before the arrival).
+__device__ __forceinline__ void named_barrier_arrive(int id, int nthreads)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Hint: bring the 128-byte line holding p into L2.
+__device__ __forceinline__ void prefetch_line_l2(const void *p)
+{
+    asm volatile("prefetch.L2 [%0];" ::"l"(p));
+}
+
 } // namespace luce
 
 // ---------------------------------------------------------------------------
@@ -379,7 +406,9 @@ struct Tuning {
     int layer_budget_kb = 222; // whole-layer kernel: shared memory per CTA
     int layer_cps = 1;        // whole-layer kernel: CTAs per SM
     int layer_prefetch = 1;   // whole-layer kernel: warm L2 with the shared expert
-    int layer_hs_own = 1;     // whole-layer kernel: each CTA quantizes all of a small hq itself
+    int layer_dsplit = 0;     // whole-layer kernel: down rows split by weight across CTAs
+    int layer_psleep = 0;     // whole-layer kernel: producer back-off in ns while the ring is full
+    int layer_down_early = 0; // whole-layer kernel: down stages before every gate/up part is requested
     int layer_hq_bulk = 1;    // whole-layer kernel: stage a shared hq with one bulk copy
 };
 extern Tuning g_tuning;

@@ -63,12 +63,15 @@ constexpr int CTHREADS = CW * 32;
 constexpr int THREADS = CTHREADS + 32;
 constexpr int BAR_ALL = 3;
 constexpr int BAR_ROUTE = 4;                 // the routing warps GW .. CW
+constexpr int BAR_TABLES = 5;                // consumers wait, the producer arrives: routing done
 constexpr int RTHREADS = THREADS - GTHREADS; // routing threads (E <= this)
 constexpr int MAX_T = 8;
 constexpr int MAX_R = 64;  // T * k
 constexpr int MAX_E = 256; // one thread per expert in the grouping
 constexpr int MAX_V = MAX_R + 1;
 constexpr int RB_MAX = 64; // down rows per row block (y buffer rows)
+constexpr int HB_STRIDE = MAX_T + 1; // h of a 32-row group: [32][HB_STRIDE]
+constexpr int MAX_UNITS = 4 * 32 * HB_STRIDE / 2; // down work units listed in the h buffers (8 B each)
 constexpr unsigned FULL = 0xffffffffu;
 
 struct LayerArgs {
@@ -90,21 +93,25 @@ struct LayerArgs {
     int stage_bytes; // one ring stage
     int NS;          // ring stages
     int SR;          // down rows per stage
-    int hs_on;       // every CTA holds all of hq in shared memory
-    int hs_own;      // ... quantized by itself from h (else staged from hq after a second barrier)
+    int hs_on;       // every CTA stages all of hq in shared memory
     int hq_bulk;     // stage hq with one bulk copy (else 16-byte loads)
     int prefetch;
     int evict_first;
+    int dsplit; // down rows by weight (else an even split)
+    int psleep; // producer back-off (ns) while no slot is free
+    int down_early; // down stages as soon as a slot is free (else after every gate/up part)
 };
 
 // Device-wide barrier of the n CTAs of a cooperative grid, called by one
 // thread per CTA after a CTA barrier that follows the CTA's stores (the
 // release of the arrival covers them).  `count` (64-bit, never wraps) only
 // grows: every barrier of every launch adds n, and all launches that share it
-// have the same n.  A CTA reads c before arriving; the CTAs already counted
-// in this barrier do not change floor(c / n), so the barrier ends when the
-// count reaches (floor(c / n) + 1) n.  Arrival is a reduction (no reply to
-// wait for).  Returns false if the wait ran out (never in a correct run).
+// have the same n.  A CTA reads c0 at any time after the previous barrier on
+// `count` has ended and before its own arrival (the kernel does it at its
+// start); the CTAs already counted in this barrier do not change
+// floor(c0 / n), so the barrier ends when the count reaches
+// (floor(c0 / n) + 1) n.  Arrival is a reduction (no reply to wait for).
+// Returns false if the wait ran out (never in a correct run).
 __device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long *p)
 {
     unsigned long long v;
@@ -112,9 +119,8 @@ __device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned 
     return v;
 }
 
-__device__ bool grid_barrier(unsigned long long *count, unsigned n)
+__device__ bool grid_barrier(unsigned long long *count, unsigned n, unsigned long long c0)
 {
-    const unsigned long long c0 = ld_acquire_gpu_u64(count);
     const unsigned long long target = (c0 / n + 1ull) * n;
     asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(count) : "memory");
     const unsigned long long t0 = global_timer_ns();
@@ -186,19 +192,42 @@ __device__ __forceinline__ void load8(const float *p, float (&v)[8], bool cg)
     v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
 }
 
-// A gate/up part: rows [row, row + len) of virtual expert v (len <= RU, not
-// crossing an expert).  Parts follow each other over the CTA's row range.
-struct Part {
-    int v, row, len;
+// This CTA's work (see make_plan in the kernel).
+struct LayerPlan {
+    int NVr, NV;            // routed virtual experts; all of them
+    int g0, g1, nsh, ngr;   // gate/up groups [g0, g1), nsh shared ones, ngr in all
+    int dn0, nrows;         // down rows [dn0, dn0 + nrows)
+    int nrb, rpb, rlast;    // row blocks, their rows, the last one's rows
+    int spr, slast, NPd;    // stages of a full row block, of the last one, in all
+    int nglu0, nglu1, dlt;  // gate/up parts of ring half 0 and 1, their difference
+    int nd0, nd1;           // down stages of half 0 and 1
 };
 
-__device__ __forceinline__ Part part_at(int gr, int r1, int I, int RU)
+// Row block and stage within it of down stage d.
+__device__ __forceinline__ void down_stage(const LayerPlan &P, int d, int &rb, int &sp)
 {
-    Part p;
-    p.v = gr / I;
-    p.row = gr - p.v * I;
-    p.len = min(min(RU, I - p.row), r1 - gr);
-    return p;
+    rb = d / max(P.spr, 1);
+    if (rb >= P.nrb - 1) {
+        rb = P.nrb - 1;
+        sp = d - (P.nrb - 1) * P.spr;
+    } else {
+        sp = d - rb * P.spr;
+    }
+}
+
+// Ring half and sequence number within it of down stage d.
+__device__ __forceinline__ void down_slot_of(const LayerPlan &P, int d, int &hh, int &n)
+{
+    int pos;
+    if (d < P.dlt) {
+        hh = 1;
+        pos = d;
+    } else {
+        const int e = d - P.dlt;
+        hh = e & 1;
+        pos = (e & 1) ? P.dlt + (e >> 1) : (e >> 1);
+    }
+    n = (hh ? P.nglu1 : P.nglu0) + pos;
 }
 
 template <int NC>
@@ -208,7 +237,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.NS * a.stage_bytes);
     uint64_t *empty = full + a.NS;
-    uint32_t *xs = reinterpret_cast<uint32_t *>(empty + a.NS); // [T][nbH][9], 16-byte aligned
+    uint32_t *xs = reinterpret_cast<uint32_t *>(empty + a.NS); // [T][xstride], 16-byte aligned
     const int R = a.T * a.k;
     const int nslots = R + a.T;
     // x rows: block g of token t at word t * xstride + 9 g + xpad (g / 32): blocks g
@@ -220,40 +249,57 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     float *ybuf = reinterpret_cast<float *>(hs + (a.hs_on ? (size_t)nslots * a.nbI * Q8_1_WORDS : 0)); // [nslots][RB]
     float *scores = ybuf + (size_t)nslots * RB_MAX; // [T][E] logit + bias
     float *lsm = scores + (size_t)a.T * a.E;        // [T][E] logits
+    float *hbuf = lsm + (size_t)a.T * a.E;          // [2 groups][2 buffers][32][HB_STRIDE]
 
-    __shared__ int ids_s[MAX_R], pos_s[MAX_R], routes_s[MAX_R];
+    __shared__ int ids_s[MAX_R], routes_s[MAX_R];
     __shared__ float w_s[MAX_R];
     __shared__ int cnt_s[MAX_E], off_s[MAX_E + 1];
     __shared__ int v_e[MAX_V], v_first[MAX_V], v_ncols[MAX_V];
-    __shared__ int wcnt[RTHREADS / 32];
+    __shared__ uint32_t sel_bits[MAX_T][MAX_E / 32]; // expert e selected by token t
     __shared__ int s_abort;
     __shared__ int s_xnext; // next x block to quantize
     __shared__ int s_nvr;   // routed virtual experts
     __shared__ __align__(8) uint64_t hq_bar; // the bulk copy of hq
+    __shared__ unsigned long long s_c0;       // barrier count at the start
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = a.T, E = a.E, k = a.k;
     const bool cta0 = blockIdx.x == 0;
     const int nb = gridDim.x, bx = blockIdx.x;
     const int half_bytes = a.RU * a.rbg;
-    // This CTA's slice of the shared expert's gate/up rows, [s0, s1): it does
-    // not depend on the routing, so its parts are requested at once and (for
-    // a single pass of x) computed while the other warps route.
-    const int s0 = a.wsg ? (int)((unsigned)(a.I * bx) / (unsigned)nb) : 0;
-    const int s1 = a.wsg ? (int)((unsigned)(a.I * (bx + 1)) / (unsigned)nb) : 0;
-    const int NPs = (s1 - s0 + a.RU - 1) / a.RU; // shared parts: RU rows each, the last shorter
-    const int NPe = min(NPs, a.NS);              // of them requested before the routing
-    const int nbx = T * a.nbH;                   // x blocks
-    const bool early = NPe > 0 && nbx <= GTHREADS / 4; // group 0 quantizes x in one pass, then takes them
+    const int G32 = a.I / 32;  // 32-row groups per expert
+    const int PPG = 32 / a.RU; // parts per group
+    const int HALF = a.NS / 2; // ring slots of each consumer group
     const uint64_t pol = a.evict_first ? l2_evict_first_policy() : l2_evict_normal_policy();
-    auto issue_shared = [&](int qq) {
-        const uint32_t slot = (uint32_t)(qq % a.NS);
+
+    // This CTA's gate/up groups: [g0, g1) of all NV * G32 groups (virtual expert
+    // major, the shared expert last), taken shared ones first; the j-th group
+    // it takes goes to consumer group j % 2, each with its own half of the
+    // ring.  With one token the routing always yields k experts, so NV = k + 1
+    // and the ranges are known before the routing: the first shared group's
+    // parts are then requested at once and (one pass of x) computed while the
+    // other warps route.
+    const bool predict = a.wsg && T == 1;
+    const int NVp = k + 1;
+    int pg0 = 0, pg1 = 0, psh = 0; // predicted range and its shared groups
+    if (predict) {
+        const int NGp = NVp * G32;
+        pg0 = (int)((unsigned)(NGp * bx) / (unsigned)nb);
+        pg1 = (int)((unsigned)(NGp * (bx + 1)) / (unsigned)nb);
+        psh = max(0, pg1 - max(pg0, k * G32));
+    }
+    const int nbx = T * a.nbH; // x blocks
+    const int NPe = psh > 0 ? min(PPG, HALF) : 0; // parts of the first (shared) group requested at once
+    const bool early = NPe > 0 && nbx <= GTHREADS / 4;
+    // part p of a group: RU gate rows then RU up rows into half c, sequence n
+    auto issue_part = [&](int c, int n, int gi, int p, const uint8_t *wg_e, const uint8_t *wu_e) {
+        const uint32_t slot = (uint32_t)(c * HALF + n % HALF);
         uint8_t *dst = ring + (size_t)slot * a.stage_bytes;
-        const int row = s0 + qq * a.RU, len = min(a.RU, s1 - row);
-        const uint32_t bytes = (uint32_t)(len * a.rbg);
+        const size_t row = (size_t)(gi % G32) * 32 + (size_t)p * a.RU;
+        const uint32_t bytes = (uint32_t)(a.RU * a.rbg);
         mbar_arrive_expect_tx(&full[slot], 2 * bytes);
-        bulk_copy_g2s(dst, a.wsg + (size_t)row * a.rbg, bytes, &full[slot], pol);
-        bulk_copy_g2s(dst + half_bytes, a.wsu + (size_t)row * a.rbg, bytes, &full[slot], pol);
+        bulk_copy_g2s(dst, wg_e + row * a.rbg, bytes, &full[slot], pol);
+        bulk_copy_g2s(dst + half_bytes, wu_e + row * a.rbg, bytes, &full[slot], pol);
     };
     if (tid == CTHREADS) {
         for (int s = 0; s < a.NS; s++) {
@@ -268,8 +314,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     __syncthreads(); // barriers initialized
     if (tid == CTHREADS) {
         // weights do not depend on the previous kernel: request them before waiting for it
-        for (int qq = 0; qq < NPe; qq++)
-            issue_shared(qq);
+        for (int p = 0; p < NPe; p++)
+            issue_part(0, p, pg1 - psh, p, a.wsg, a.wsu);
         if (a.wsd && a.prefetch) {
             // and warm L2 with this CTA's slice of the shared expert's down rows
             const size_t tot_d = (size_t)a.H * a.rbd; // a multiple of 16
@@ -279,22 +325,35 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                 prefetch_l2(a.wsd + od, (uint32_t)min(cd, tot_d - od));
         }
     }
+    if (warp == GW + 1) {
+        // the inputs of the routing and of the quantization into L2 (a hint:
+        // whatever the previous kernel still writes reaches L2 as well)
+        for (int i = lane; i < (T * E + 31) / 32; i += 32)
+            prefetch_line_l2(a.logits + 32 * i);
+        for (int i = lane; a.bias && i < (E + 31) / 32; i += 32)
+            prefetch_line_l2(a.bias + 32 * i);
+        for (int i = lane; i < T * a.H / 32; i += 32)
+            prefetch_line_l2(a.x + 32 * i);
+    }
     pdl_wait();
     pdl_trigger();
+    // the barrier count before this launch's barrier (every earlier one has ended)
+    if (tid == 0)
+        s_c0 = ld_acquire_gpu_u64(a.sync);
 
+    // ---------------- helpers ----------------
     // ---------------- consumer helpers ----------------
     const int grp = warp / GW, wl = warp - grp * GW; // consumer group, warp within it
     const int gtid = tid - grp * GTHREADS;
     bool dead = false;
-    // waits for stage qq; false if this CTA gave up (now or earlier)
-    auto wait_stage = [&](int qq) -> bool {
+    // waits for the stage in `slot`, use `use`; false if this CTA gave up
+    auto wait_slot = [&](int slot, int use) -> bool {
         // warp-uniform: every lane takes the same branch to the __all_sync
         if (__any_sync(FULL, *(volatile int *)&s_abort != 0))
             dead = true;
         if (dead)
             return false;
-        const uint32_t slot = (uint32_t)(qq % a.NS), use = (uint32_t)(qq / a.NS);
-        const bool got = __all_sync(FULL, mbar_wait_bounded(&full[slot], use & 1u));
+        const bool got = __all_sync(FULL, mbar_wait_bounded(&full[slot], (uint32_t)use & 1u));
         if (!got) {
             if (lane == 0) {
                 atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
@@ -305,19 +364,73 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         }
         return true;
     };
-    auto release_stage = [&](int qq) {
-        named_barrier(1 + grp, GTHREADS); // every warp of the group is done with the stage
-        if (gtid == 0 && !dead)
-            mbar_arrive(&empty[qq % a.NS]);
-    };
-    auto cta_barrier = [&]() {
-        named_barrier(BAR_ALL, CTHREADS);
-        if (tid == 0 && !grid_barrier(a.sync, gridDim.x)) {
-            atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
-            *(volatile int *)&s_abort = 1;
+
+    // Down rows [m0, m1) of this CTA (warp-collective).  By weight (dsplit):
+    // each CTA should stream about the same bytes, gate/up groups plus down
+    // rows, so D(b), the down rows of the CTAs before b, is the cost not yet
+    // covered by their groups at the even share b / nb, in rows of all nv
+    // experts, made non-decreasing by a suffix minimum (D(nb) = H).  Every
+    // CTA evaluates the same expressions, so neighbours agree on their
+    // boundary.  Otherwise an even split.
+    auto down_rows = [&](int nv, int &m0, int &m1) {
+        if (a.dsplit && nv > 0) {
+            m0 = a.H;
+            m1 = a.H;
+            const unsigned ng = (unsigned)(nv * G32);
+            const float Cg = 64.0f * (float)a.nbH, Cd = (float)nv * (float)a.nbI; // bytes / 34
+            const float W = (float)ng * Cg + (float)a.H * Cd;
+            for (int b = bx + lane; b < nb; b += 32) {
+                const float gb = (float)((ng * (unsigned)b) / (unsigned)nb) * Cg;
+                const float r = floorf((W * (float)b / (float)nb - gb) / Cd);
+                const int d = r <= 0.0f ? 0 : r >= (float)a.H ? a.H : (int)r;
+                m0 = min(m0, d);
+                if (b > bx)
+                    m1 = min(m1, d);
+            }
+            m0 = __reduce_min_sync(FULL, m0);
+            m1 = __reduce_min_sync(FULL, m1);
+        } else {
+            m0 = a.H * bx / nb;
+            m1 = a.H * (bx + 1) / nb;
         }
-        named_barrier(BAR_ALL, CTHREADS);
     };
+    // This CTA's work once nvr, the routed virtual experts, is known
+    // (warp-collective).  Gate/up: groups [g0, g1) of all NV * G32 (virtual
+    // expert major, the shared expert last), shared ones taken first.  Down:
+    // rows [dn0, dn0 + nrows) in nrb row blocks of rpb rows (the last one
+    // rlast); a row block's NV * rows items (expert major) are cut into
+    // stages of SR rows.  Each half of the ring takes the gate/up parts of its
+    // consumer group's groups, then down stages: the first dlt of them to
+    // half 1 (which has dlt gate/up parts fewer), then alternately half 0 and
+    // half 1.  (Unsigned 32-bit: NV * G32 <= 65 * 1024, times at most 1024
+    // CTAs, stays below 2^32.)
+    auto make_plan = [&](int nvr) {
+        LayerPlan q;
+        q.NVr = nvr;
+        q.NV = nvr + (a.wsg ? 1 : 0);
+        const unsigned NG = (unsigned)(q.NV * G32);
+        q.g0 = (int)(NG * (unsigned)bx / (unsigned)nb);
+        q.g1 = (int)(NG * (unsigned)(bx + 1) / (unsigned)nb);
+        q.nsh = a.wsg ? max(0, q.g1 - max(q.g0, nvr * G32)) : 0;
+        q.ngr = q.g1 - q.g0;
+        int m0, m1;
+        down_rows(q.NV, m0, m1);
+        q.dn0 = m0;
+        q.nrows = m1 - m0;
+        q.nrb = (q.nrows + RB_MAX - 1) / RB_MAX;
+        q.rpb = q.nrb ? (q.nrows + q.nrb - 1) / q.nrb : 0;
+        q.rlast = q.nrows - (q.nrb - 1) * q.rpb;
+        q.spr = q.nrb ? (q.NV * q.rpb + a.SR - 1) / a.SR : 0;
+        q.slast = q.nrb ? (q.NV * q.rlast + a.SR - 1) / a.SR : 0;
+        q.NPd = q.nrb ? (q.nrb - 1) * q.spr + q.slast : 0;
+        q.nglu0 = ((q.ngr + 1) / 2) * PPG;
+        q.nglu1 = (q.ngr / 2) * PPG;
+        q.dlt = q.nglu0 - q.nglu1;
+        q.nd0 = q.NPd > q.dlt ? (q.NPd - q.dlt + 1) / 2 : 0;
+        q.nd1 = min(q.dlt, q.NPd) + (q.NPd > q.dlt ? (q.NPd - q.dlt) / 2 : 0);
+        return q;
+    };
+    const int SR = a.SR;
 
     // x -> q8_1 into shared memory (CTA 0 also stores xq): a warp claims 8
     // blocks at a time, 4 lanes per block
@@ -354,7 +467,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     };
 
     // one token (NC == 1): this lane's x blocks stay in registers for every row
-    constexpr int XR = 4;
+    constexpr int XR = 2;
     const int nblg = rowmap_blocks(gmap, a.nbH, lane);
     const bool x_regs = NC == 1 && a.T == 1 && nblg <= XR;
     Q81Block xreg[XR];
@@ -373,25 +486,19 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         }
     };
 
-    // gate/up rows [row, row + len) of one part in stage qq -> h; columns of
-    // a routed expert (first, ncols) or, routed == false, the T shared tokens
-    auto glu_part = [&](int qq, int row0, int len, bool routed, int first, int ncols) {
-        if (wait_stage(qq)) {
-            const uint8_t *st = ring + (size_t)(qq % a.NS) * a.stage_bytes;
-            for (int i = wl; i < len; i += GW) {
-                const int row = row0 + i;
+
+    // rows [p RU, (p + 1) RU) of a 32-row group from the stage in `slot` -> hb
+    // (h of the group's rows, 32 x HB_STRIDE); columns of a routed expert
+    // (first, ncols) or, routed == false, the T shared tokens
+    auto glu_part = [&](int slot, int use, int p, bool routed, int first, int ncols, float *hb) {
+        if (wait_slot(slot, use)) {
+            const uint8_t *st = ring + (size_t)slot * a.stage_bytes;
+            for (int i = wl; i < a.RU; i += GW) {
+                const int prow = p * a.RU + i; // row within the group
                 const uint8_t *grow = st + (size_t)i * a.rbg;
                 const uint8_t *urow = st + half_bytes + (size_t)i * a.rbg;
                 for (int c0 = 0; c0 < ncols; c0 += NC) {
                     const int nc = min(NC, ncols - c0);
-                    const uint32_t *xc[NC];
-                    int rr[NC];
-#pragma unroll
-                    for (int c = 0; c < NC; c++) {
-                        const int cc = c0 + (c < nc ? c : 0);
-                        rr[c] = routed ? routes_s[first + cc] : R + cc; // h row
-                        xc[c] = xs + (size_t)(routed ? rr[c] / k : cc) * xstride;
-                    }
                     float ag[NC], au[NC];
 #pragma unroll
                     for (int c = 0; c < NC; c++)
@@ -412,6 +519,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                             }
                         }
                     } else {
+                        const uint32_t *xc[NC]; // x row of each column's token
+#pragma unroll
+                        for (int c = 0; c < NC; c++) {
+                            const int cc = c0 + (c < nc ? c : 0);
+                            xc[c] = xs + (size_t)(routed ? routes_s[first + cc] / k : cc) * xstride;
+                        }
                         for (int j = 0; j < nblg; j++) {
                             const int b = rowmap_block(gmap, lane, j);
                             Q80Block gbk, ubk;
@@ -440,346 +553,358 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                             const float sm = reduce4(ag[c], au[c], g1, u1, lane);
                             const float u = __shfl_down_sync(FULL, sm, 8); // lane 0: u0, lane 16: u1
                             if (lane == 0)
-                                a.h[(size_t)rr[c] * a.I + row] = swiglu(sm, u, a.clamp);
+                                hb[prow * HB_STRIDE + c0 + c] = swiglu(sm, u, a.clamp);
                             if (two && lane == 16)
-                                a.h[(size_t)rr[(c + 1) % NC] * a.I + row] = swiglu(sm, u, a.clamp);
+                                hb[prow * HB_STRIDE + c0 + c + 1] = swiglu(sm, u, a.clamp);
                         }
                     }
                 }
             }
         }
-        release_stage(qq);
+        named_barrier(1 + grp, GTHREADS); // every warp of the group is done with the stage
+        if (gtid == 0 && !dead)
+            mbar_arrive(&empty[slot]);
+    };
+    // a finished 32-row group in hb -> h and its q8_1 blocks (warp per column)
+    auto glu_epilogue = [&](int gi, bool routed, int first, int ncols, const float *hb) {
+        if (dead || *(volatile int *)&s_abort)
+            return;
+        const int grow0 = (gi % G32) * 32;
+        for (int c = wl; c < ncols; c += GW) {
+            const int r = routed ? routes_s[first + c] : R + c;
+            const float hv = hb[lane * HB_STRIDE + c];
+            a.h[(size_t)r * a.I + grow0 + lane] = hv;
+            quantize_q8_1_warp(hv, a.hq + ((size_t)r * a.nbI + grow0 / 32) * Q8_1_WORDS, lane);
+        }
     };
 
-    // ---------------- 1-3. x -> q8_1 (warps 0 .. GW-1) while warps GW .. CW route ----------------
+    // ---------------- 1-3. routing, x -> q8_1 ----------------
+    // Scores and ranks by the routing warps GW .. CW (the producer among
+    // them); a NaN score ranks below every number and ties go to the lower
+    // index, a total order, so each token selects exactly k distinct experts.
+    auto route_rank = [&]() {
+        const int rt = tid - GTHREADS; // routing threads 0 .. RTHREADS-1
+        for (int i = rt; i < T * E; i += RTHREADS) {
+            const float l = a.logits[i];
+            lsm[i] = l;
+            const float sc = a.bias ? __fadd_rn(l, a.bias[i % E]) : l;
+            scores[i] = sc == sc ? sc : -INFINITY;
+        }
+        for (int i = rt; i < MAX_T * (MAX_E / 32); i += RTHREADS)
+            (&sel_bits[0][0])[i] = 0u;
+        named_barrier(BAR_ROUTE, RTHREADS);
+        // rank of every (token, expert) pair, four threads per pair
+        const int npair = T * E;
+        const int qj = lane & 3;
+        const int qE = (E + 3) >> 2;
+        for (int base = 0; base < npair; base += RTHREADS / 4) { // warp-uniform trip count
+            const int p = base + (rt >> 2);
+            int rank = 0;
+            int t = 0, e = 0;
+            if (p < npair) {
+                t = p / E;
+                e = p - t * E;
+                const float *sc = scores + (size_t)t * E;
+                const float v = sc[e];
+                const int e_end = min(E, (qj + 1) * qE);
+#pragma unroll 4
+                for (int e2 = qj * qE; e2 < e_end; e2++) {
+                    const float o = sc[e2];
+                    rank += (o > v || (o == v && e2 < e)) ? 1 : 0;
+                }
+            }
+            rank += __shfl_xor_sync(FULL, rank, 1);
+            rank += __shfl_xor_sync(FULL, rank, 2);
+            if (p < npair && qj == 0 && rank < k) {
+                ids_s[t * k + rank] = e;
+                atomicOr(&sel_bits[t][e >> 5], 1u << (e & 31));
+            }
+        }
+        named_barrier(BAR_ROUTE, RTHREADS);
+    };
+    // The expert tables (one warp): virtual expert v is the v-th selected
+    // expert in index order; its columns are the routes that chose it, in
+    // route order, at [first, first + ncols) of the route list.
+    auto build_tables = [&]() {
+        int nact = 0, offp = 0;
+        for (int c = 0; c < E; c += 32) { // warp-uniform trip count
+            const int e = c + lane;
+            int cnt = 0;
+            if (e < E)
+                for (int t = 0; t < T; t++)
+                    cnt += (sel_bits[t][e >> 5] >> (e & 31)) & 1u;
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(FULL, incl, o);
+                if (lane >= o)
+                    incl += y;
+            }
+            const unsigned bal = __ballot_sync(FULL, cnt > 0);
+            const int v = nact + __popc(bal & ((1u << lane) - 1u));
+            const int off = offp + incl - cnt;
+            if (e < E) {
+                cnt_s[e] = cnt;
+                off_s[e] = off;
+            }
+            if (cnt > 0) {
+                v_e[v] = e;
+                v_first[v] = off;
+                v_ncols[v] = cnt;
+            }
+            nact += __popc(bal);
+            offp += __shfl_sync(FULL, incl, 31);
+        }
+        if (lane == 0) {
+            off_s[E] = offp;
+            s_nvr = nact;
+            if (a.wsg) {
+                v_e[nact] = E;
+                v_first[nact] = 0;
+                v_ncols[nact] = T;
+            }
+        }
+    };
+    // route weights (routing warp w0 + t for token t) and the route list:
+    // route r = t k + j goes to position pos(r), the routes ahead of it in
+    // (expert, route) order; threads [r0, r0 + rn) of the routing warps
+    auto weights_routes = [&](int w0, int r0, int rn) {
+        const int rt = tid - GTHREADS, t = warp - GW - w0;
+        if (t >= 0 && t < T) {
+            const float sel0 = lane < k ? lsm[t * E + ids_s[t * k + lane]] : 0.0f;
+            const float sel1 = lane + 32 < k ? lsm[t * E + ids_s[t * k + lane + 32]] : 0.0f;
+            route_softmax_warp(sel0, sel1, k, w_s + t * k, lane);
+        }
+        for (int r = rt - r0; r >= 0 && r < R; r += rn) {
+            const int e = ids_s[r];
+            int pos = 0;
+            for (int r2 = 0; r2 < R; r2++) {
+                const int e2 = ids_s[r2];
+                pos += (e2 < e || (e2 == e && r2 < r)) ? 1 : 0;
+            }
+            routes_s[pos] = r;
+        }
+    };
+
+    LayerPlan P;
+    int eg_parts = 0; // parts of the first shared group that group 0 took before the routing
+    if (warp == CW) {
+        // ---------------- the producer: every stage of this CTA ----------------
+        // With one token the plan is known at once (k experts); the producer
+        // then needs only the selection itself, the v-th selected expert.
+        if (T == 1)
+            P = make_plan(k);
+        route_rank();
+        if (T != 1) {
+            build_tables();
+            __syncwarp();
+            named_barrier_arrive(BAR_TABLES, THREADS);
+            P = make_plan(s_nvr);
+        }
+        if (lane != 0)
+            return;
+        // expert of routed virtual expert v
+        auto vexp = [&](int v) -> int {
+            if (T != 1)
+                return v_e[v];
+            for (int w = 0; w < (E + 31) / 32; w++) {
+                const uint32_t m = sel_bits[0][w];
+                const int c = __popc(m);
+                if (v < c)
+                    return 32 * w + (int)__fns(m, 0u, v + 1);
+                v -= c;
+            }
+            return E; // not reached: a token selects k experts
+        };
+        auto group_of = [&](int j) { return j < P.nsh ? P.g1 - P.nsh + j : P.g0 + (j - P.nsh); };
+        int n[2] = {NPe, 0};  // stages requested per half
+        int dq[2] = {0, 0};   // down stages requested per half
+        const int nglu[2] = {P.nglu0, P.nglu1};
+        unsigned long long t_idle = 0;
+        for (uint32_t it = 0;;) {
+            bool left = false, moved = false;
+            for (int h = 0; h < 2; h++) {
+                int d = -1; // the next stage of half h: a gate/up part, or down stage d
+                if (n[h] >= nglu[h]) {
+                    if (!a.down_early && (n[0] < nglu[0] || n[1] < nglu[1])) {
+                        left = true; // down stages wait until every gate/up part is requested
+                        continue;
+                    }
+                    const int i = dq[h];
+                    d = h == 0 ? P.dlt + 2 * i : (i < P.dlt ? i : P.dlt + 2 * (i - P.dlt) + 1);
+                    if (d >= P.NPd)
+                        continue;
+                }
+                left = true;
+                const int slot = h * HALF + n[h] % HALF, use = n[h] / HALF;
+                if (use > 0 && !mbar_test_wait(&empty[slot], (uint32_t)(use - 1) & 1u))
+                    continue;
+                if (d < 0) {
+                    const int j = h + 2 * (n[h] / PPG), p = n[h] % PPG;
+                    const int gi = group_of(j);
+                    const int v = gi / G32;
+                    const bool routed = v < P.NVr;
+                    const int e = routed ? vexp(v) : E;
+                    issue_part(h, n[h], gi, p, routed ? a.wg + (size_t)e * a.I * a.rbg : a.wsg,
+                               routed ? a.wu + (size_t)e * a.I * a.rbg : a.wsu);
+                } else {
+                    uint8_t *dst = ring + (size_t)slot * a.stage_bytes;
+                    int rb, sp;
+                    down_stage(P, d, rb, sp);
+                    const int nr0 = P.dn0 + rb * P.rpb;
+                    const int rows = rb == P.nrb - 1 ? P.rlast : P.rpb;
+                    const int i0 = sp * SR, i1 = min(P.NV * rows, i0 + SR);
+                    mbar_arrive_expect_tx(&full[slot], (uint32_t)((i1 - i0) * a.rbd));
+                    for (int i = i0; i < i1;) {
+                        const int v = i / rows, m = i - v * rows;
+                        const int cnt = min(i1 - i, rows - m);
+                        const int e = v < P.NVr ? vexp(v) : E;
+                        const uint8_t *src = e < E ? a.wd + ((size_t)e * a.H + nr0 + m) * a.rbd
+                                                   : a.wsd + (size_t)(nr0 + m) * a.rbd;
+                        bulk_copy_g2s(dst + (size_t)(i - i0) * a.rbd, src, (uint32_t)(cnt * a.rbd), &full[slot],
+                                      pol);
+                        i += cnt;
+                    }
+                    dq[h]++;
+                }
+                n[h]++;
+                moved = true;
+            }
+            if (!left || *(volatile int *)&s_abort)
+                break;
+            if (moved) {
+                t_idle = 0;
+                continue;
+            }
+            if (a.psleep)
+                __nanosleep((unsigned)a.psleep); // leave the issue slots to the consumer warps
+            if ((++it & 31u) == 0u) {
+                const unsigned long long now = global_timer_ns();
+                if (t_idle == 0) {
+                    t_idle = now;
+                } else if (now - t_idle > WAIT_LIMIT_NS) {
+                    atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
+                    *(volatile int *)&s_abort = 1;
+                    break;
+                }
+            }
+        }
+        // no bulk copy may still be writing shared memory when the CTA exits
+        for (int h = 0; h < 2; h++) {
+            for (int u = 0; u < HALF && u < n[h]; u++) {
+                const int last = n[h] - 1 - u; // the last use of slot h * HALF + last % HALF
+                if (!mbar_wait_bounded(&full[h * HALF + last % HALF], (uint32_t)(last / HALF) & 1u))
+                    atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
+            }
+        }
+        return;
+    }
     if (warp < GW) {
         quantize_x();
         if (early) {
             named_barrier(1, GTHREADS); // all of x is quantized (one pass, by this group)
             load_xregs();
-            for (int qq = 0; qq < NPe; qq += 2) { // group 0's stages: the even ones
-                const int row = s0 + qq * a.RU;
-                glu_part(qq, row, min(a.RU, s1 - row), false, 0, T);
-            }
+            float *hb = hbuf; // group 0, buffer 0
+            for (int p = 0; p < NPe; p++)
+                glu_part(p % HALF, p / HALF, p, false, 0, T, hb);
+            eg_parts = NPe;
         }
     } else {
-        const int rt = tid - GTHREADS;      // routing threads 0 .. RTHREADS-1
-        const int rw = warp - GW;           // routing warp
-        for (int i = rt; i < T * E; i += RTHREADS) {
-            const float l = a.logits[i];
-            lsm[i] = l;
-            scores[i] = a.bias ? __fadd_rn(l, a.bias[i % E]) : l;
-        }
-        for (int i = rt; i < R; i += RTHREADS)
-            ids_s[i] = -1;
-        named_barrier(BAR_ROUTE, RTHREADS);
-        // selection by rank, 4 threads per (token, expert)
-        {
-            const int npair = T * E;
-            const int qj = lane & 3;
-            const int qE = (E + 3) >> 2;
-            for (int base = 0; base < npair; base += RTHREADS / 4) { // warp-uniform trip count
-                const int p = base + (rt >> 2);
-                int rank = 0;
-                int t = 0, e = 0;
-                if (p < npair) {
-                    t = p / E;
-                    e = p - t * E;
-                    const float *sc = scores + (size_t)t * E;
-                    const float v = sc[e];
-                    const int e_end = min(E, (qj + 1) * qE);
-                    for (int e2 = qj * qE; e2 < e_end; e2++) {
-                        const float o = sc[e2];
-                        rank += (o > v || (o == v && e2 < e)) ? 1 : 0;
-                    }
-                }
-                rank += __shfl_xor_sync(FULL, rank, 1);
-                rank += __shfl_xor_sync(FULL, rank, 2);
-                if (p < npair && qj == 0 && rank < k)
-                    ids_s[t * k + rank] = e;
-            }
-        }
-        named_barrier(BAR_ROUTE, RTHREADS);
-        // weights (routing warp t) and grouping
-        if (rw < T) {
-            const int t = rw;
-            float sel0 = 0.0f, sel1 = 0.0f;
-            if (lane < k) {
-                const int e = ids_s[t * k + lane];
-                sel0 = e >= 0 ? lsm[t * E + e] : 0.0f;
-            }
-            if (lane + 32 < k) {
-                const int e = ids_s[t * k + lane + 32];
-                sel1 = e >= 0 ? lsm[t * E + e] : 0.0f;
-            }
-            route_softmax_warp(sel0, sel1, k, w_s + t * k, lane);
-        }
-        if (rt < R) {
-            // slot of route r in the (expert, route) order; masked routes have none
-            const int e = ids_s[rt];
-            int pos = -1;
-            if (e >= 0) {
-                pos = 0;
-                for (int r2 = 0; r2 < R; r2++) {
-                    const int e2 = ids_s[r2];
-                    pos += (e2 >= 0 && (e2 < e || (e2 == e && r2 < rt))) ? 1 : 0;
-                }
-            }
-            pos_s[rt] = pos;
-        }
-        {
-            const int e = rt; // E <= RTHREADS
-            int c = 0, o = 0;
-            if (e < E) {
-                for (int r2 = 0; r2 < R; r2++) {
-                    const int e2 = ids_s[r2];
-                    c += e2 == e ? 1 : 0;
-                    o += (e2 >= 0 && e2 < e) ? 1 : 0;
-                }
-                cnt_s[e] = c;
-                off_s[e] = o;
-            }
-            if (e == 0) {
-                int nvalid = 0;
-                for (int r2 = 0; r2 < R; r2++)
-                    nvalid += ids_s[r2] >= 0 ? 1 : 0;
-                off_s[E] = nvalid;
-            }
-            const unsigned bal = __ballot_sync(FULL, e < E && c > 0);
-            if (lane == 0)
-                wcnt[rw] = __popc(bal);
-        }
-        named_barrier(BAR_ROUTE, RTHREADS);
-        if (rt < R) {
-            if (pos_s[rt] >= 0)
-                routes_s[pos_s[rt]] = rt;
-            if (rt >= off_s[E])
-                routes_s[rt] = -1;
-        }
-        {
-            const int e = rt;
-            const bool act = e < E && cnt_s[e] > 0;
-            const unsigned bal = __ballot_sync(FULL, act);
-            int before = __popc(bal & ((1u << lane) - 1u));
-            for (int w = 0; w < rw; w++)
-                before += wcnt[w];
-            if (act) {
-                v_e[before] = e;
-                v_first[before] = off_s[e];
-                v_ncols[before] = cnt_s[e];
-            }
-            if (rt == 0) {
-                int nvr = 0;
-                for (int w = 0; w < RTHREADS / 32; w++)
-                    nvr += wcnt[w];
-                s_nvr = nvr;
-                if (a.wsg) {
-                    v_e[nvr] = E;
-                    v_first[nvr] = 0;
-                    v_ncols[nvr] = T;
-                }
-            }
-        }
-        named_barrier(BAR_ROUTE, RTHREADS);
-        if (cta0) {
-            for (int i = rt; i < R; i += RTHREADS) {
-                a.ids[i] = ids_s[i];
-                a.weights[i] = w_s[i];
-                a.routes[i] = routes_s[i];
-            }
-            for (int e = rt; e < E; e += RTHREADS) {
-                a.counts[e] = cnt_s[e];
-                a.offsets[e] = off_s[e];
-            }
-            if (rt == 0)
-                a.offsets[E] = off_s[E];
+        route_rank();
+        if (T == 1) {
+            // the producer does without the tables: warp GW builds them for
+            // the consumers while the others weigh and order the routes
+            if (warp == GW)
+                build_tables();
+            else
+                weights_routes(1, 32, RTHREADS - 64);
+        } else {
+            weights_routes(0, 0, RTHREADS - 32);
         }
         if (!early)
             quantize_x(); // what is left of x (with the early stage, group 0 alone quantizes all of it)
     }
-    __syncthreads(); // routing tables and all of x are in shared memory
-
-    // ---------------- 4. this CTA's work ----------------
-    // gate/up: the shared slice [s0, s1), then the routed rows [r0, r1) of all
-    // NVr * I routed rows (expert major); down output rows [dn0, dn1)
-    // (unsigned 32-bit: NVr * I <= 64 * 32768 rows, times at most 1024 CTAs < 2^32)
-    const int NVr = s_nvr;
-    const int NV = NVr + (a.wsg ? 1 : 0);
-    const int NRr = NVr * a.I;
-    const int r0 = (int)((unsigned)(NRr * bx) / (unsigned)nb), r1 = (int)((unsigned)(NRr * (bx + 1)) / (unsigned)nb);
-    const int dn0 = a.H * bx / nb, dn1 = a.H * (bx + 1) / nb;
-    // down rows in nrb row blocks of rpb rows (the last may be shorter); a row
-    // block's NV * rows items (expert major) are cut into stages of SR rows
-    const int SR = a.SR;
-    int nrb, rpb, rlast, spr, slast, NPd;
-    auto plan_down = [&]() {
-        const int nrows = dn1 - dn0;
-        nrb = (nrows + RB_MAX - 1) / RB_MAX;
-        rpb = nrb ? (nrows + nrb - 1) / nrb : 0;
-        rlast = nrows - (nrb - 1) * rpb;
-        spr = nrb ? (NV * rpb + SR - 1) / SR : 0;     // stages of a full row block
-        slast = nrb ? (NV * rlast + SR - 1) / SR : 0; // stages of the last one
-        NPd = nrb ? (nrb - 1) * spr + slast : 0;
-    };
-    auto down_stage = [&](int d, int &rb, int &sp) {
-        rb = d / max(spr, 1);
-        if (rb >= nrb - 1) {
-            rb = nrb - 1;
-            sp = d - (nrb - 1) * spr;
-        } else {
-            sp = d - rb * spr;
+    // tables, weights, route list and x are in shared memory
+    named_barrier(BAR_TABLES, T == 1 ? CTHREADS : THREADS);
+    if (cta0 && warp >= GW) {
+        const int rt = tid - GTHREADS;
+        for (int i = rt; i < R; i += RTHREADS - 32) {
+            a.ids[i] = ids_s[i];
+            a.weights[i] = w_s[i];
+            a.routes[i] = routes_s[i];
         }
-    };
-
-    if (warp == CW) {
-        // ---------------- the producer: every stage of this CTA, in order ----------------
-        if (lane != 0)
-            return;
-        int NPg = NPs;
-        for (int gr = r0; gr < r1; NPg++)
-            gr += part_at(gr, r1, a.I, a.RU).len;
-        plan_down();
-        const int NP = NPg + NPd;
-        int gr = r0;
-        int issued = NPe; // the first shared parts went out before the routing
-        for (; issued < NP; issued++) {
-            const uint32_t slot = (uint32_t)(issued % a.NS), use = (uint32_t)(issued / a.NS);
-            if (use > 0 && !mbar_wait_bounded(&empty[slot], (use - 1) & 1u)) {
-                atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
-                *(volatile int *)&s_abort = 1;
-                break;
-            }
-            if (*(volatile int *)&s_abort)
-                break;
-            uint8_t *dst = ring + (size_t)slot * a.stage_bytes;
-            if (issued < NPs) {
-                issue_shared(issued);
-            } else if (issued < NPg) {
-                const Part pt = part_at(gr, r1, a.I, a.RU);
-                gr += pt.len;
-                const int e = v_e[pt.v];
-                const uint8_t *gsrc = a.wg + ((size_t)e * a.I + pt.row) * a.rbg;
-                const uint8_t *usrc = a.wu + ((size_t)e * a.I + pt.row) * a.rbg;
-                const uint32_t bytes = (uint32_t)(pt.len * a.rbg);
-                mbar_arrive_expect_tx(&full[slot], 2 * bytes);
-                bulk_copy_g2s(dst, gsrc, bytes, &full[slot], pol);
-                bulk_copy_g2s(dst + half_bytes, usrc, bytes, &full[slot], pol);
-            } else {
-                int rb, sp;
-                down_stage(issued - NPg, rb, sp);
-                const int nr0 = dn0 + rb * rpb;
-                const int rows = rb == nrb - 1 ? rlast : rpb;
-                const int i0 = sp * SR, i1 = min(NV * rows, i0 + SR);
-                mbar_arrive_expect_tx(&full[slot], (uint32_t)((i1 - i0) * a.rbd));
-                for (int i = i0; i < i1;) {
-                    const int v = i / rows, m = i - v * rows;
-                    const int cnt = min(i1 - i, rows - m);
-                    const int e = v_e[v];
-                    const uint8_t *src = e < E ? a.wd + ((size_t)e * a.H + nr0 + m) * a.rbd
-                                               : a.wsd + (size_t)(nr0 + m) * a.rbd;
-                    bulk_copy_g2s(dst + (size_t)(i - i0) * a.rbd, src, (uint32_t)(cnt * a.rbd), &full[slot], pol);
-                    i += cnt;
-                }
-            }
+        for (int e = rt; e < E; e += RTHREADS - 32) {
+            a.counts[e] = cnt_s[e];
+            a.offsets[e] = off_s[e];
         }
-        // no bulk copy may still be writing shared memory when the CTA exits
-        const int n_slots = issued < a.NS ? issued : a.NS;
-        for (int sl = 0; sl < n_slots; sl++) {
-            const int last_use = (issued - 1 - sl) / a.NS;
-            if (!mbar_wait_bounded(&full[sl], (uint32_t)last_use & 1u))
-                atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
-        }
-        return;
+        if (rt == 0)
+            a.offsets[E] = off_s[E];
     }
+    P = make_plan(T == 1 ? k : s_nvr);
+    auto group_of = [&](int j) { return j < P.nsh ? P.g1 - P.nsh + j : P.g0 + (j - P.nsh); };
+    auto down_slot = [&](int d, int &hh, int &n) { down_slot_of(P, d, hh, n); };
 
-    // ---------------- 5. gate/up rows -> h (consumer warps) ----------------
+    // ---------------- 4. gate/up groups -> h, hq (consumer group grp takes j = grp, grp + 2, ...) ----------------
     if (!(early && grp == 0))
         load_xregs();
-    int q = 0;
     {
-        int gr = r0;
-        for (; q < NPs || gr < r1; q++) {
-            if (q < NPs) {
-                if ((q & 1) != grp || (early && grp == 0 && q < NPe))
-                    continue; // the other group's stage, or one group 0 took before the routing
-                const int row = s0 + q * a.RU;
-                glu_part(q, row, min(a.RU, s1 - row), false, 0, T);
-                continue;
+        int n = 0;  // stages of this group's half
+        int lb = 0; // h buffer
+        for (int j = grp; j < P.ngr; j += 2, lb ^= 1) {
+            const int gi = group_of(j);
+            const int v = gi / G32;
+            const bool routed = v < P.NVr;
+            const int first = routed ? v_first[v] : 0, ncols = routed ? v_ncols[v] : T;
+            float *hb = hbuf + (size_t)(grp * 2 + lb) * 32 * HB_STRIDE;
+            for (int p = 0; p < PPG; p++, n++) {
+                if (j == 0 && p < eg_parts)
+                    continue; // taken before the routing
+                glu_part(grp * HALF + n % HALF, n / HALF, p, routed, first, ncols, hb);
             }
-            const Part pt = part_at(gr, r1, a.I, a.RU);
-            gr += pt.len;
-            if ((q & 1) != grp)
-                continue; // the other group's stage
-            glu_part(q, pt.row, pt.len, true, v_first[pt.v], v_ncols[pt.v]);
+            named_barrier(1 + grp, GTHREADS); // all 32 rows of the group are in hb
+            glu_epilogue(gi, routed, first, ncols, hb);
         }
     }
-    plan_down(); // q is now the first down stage
 
-    // ---------------- 6. all of h is stored: h -> q8_1 ----------------
-    cta_barrier();
-    const int ibytes_w = a.nbI * Q8_1_WORDS; // words per hq row
-    {
-        // blocks u = (slot, g) of the live slots: the routes, then the shared
-        // tokens.  All of them (every CTA, rotated so that the CTAs do not
-        // all start on the same lines) or this CTA's share; the loads of four
-        // passes are issued before any block is quantized.
-        const int nlive = R + (a.wsd ? T : 0);
-        const int U = nlive * a.nbI;
-        const bool own = a.hs_on && a.hs_own;
-        const int u0 = own ? 0 : (int)((long long)U * bx / nb);
-        const int u1 = own ? U : (int)((long long)U * (bx + 1) / nb);
-        const int rot = own ? (int)(((long long)bx * 67) % U) : 0;
-        const int qj = lane & 3;
-        constexpr int NQ = CTHREADS / 4; // quads of all consumer warps
-        if (!*(volatile int *)&s_abort) {
-            for (int base = u0; base < u1; base += 4 * NQ) { // warp-uniform trip count
-                float v[4][8];
-                int uu[4];
-                bool val[4];
-#pragma unroll
-                for (int j = 0; j < 4; j++) {
-                    const int w = base + j * NQ + (tid >> 2);
-                    int u = w - u0 + rot;
-                    u = (u >= u1 - u0 ? u - (u1 - u0) : u) + u0;
-                    const int slot = u / a.nbI, g = u - slot * a.nbI;
-                    uu[j] = u;
-                    val[j] = w < u1 && (slot >= R || ids_s[slot] >= 0);
-                    if (val[j]) {
-                        load8(a.h + (size_t)slot * a.I + (size_t)g * QK + qj * 8, v[j], true); // other CTAs' h
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 8; i++)
-                            v[j][i] = 0.0f;
-                    }
-                }
-#pragma unroll 1
-                for (int j = 0; j < 4; j++) {
-                    // pass j's values by selects (one copy of the quantizer, no local memory)
-                    float vj[8];
-#pragma unroll
-                    for (int i = 0; i < 8; i++)
-                        vj[i] = j == 0 ? v[0][i] : j == 1 ? v[1][i] : j == 2 ? v[2][i] : v[3][i];
-                    const bool ok = j == 0 ? val[0] : j == 1 ? val[1] : j == 2 ? val[2] : val[3];
-                    if (!__any_sync(FULL, ok))
-                        continue; // a warp with no block in this pass does no work
-                    const int u = ok ? (j == 0 ? uu[0] : j == 1 ? uu[1] : j == 2 ? uu[2] : uu[3]) : 0;
-                    uint32_t *dst = (own ? hs : a.hq) + (size_t)u * Q8_1_WORDS;
-                    quantize_q8_1_quad(vj, ok, dst, qj);
-                    if (own && cta0 && ok) {
-                        uint32_t *gq = a.hq + (size_t)u * Q8_1_WORDS;
-                        gq[1 + 2 * qj] = dst[1 + 2 * qj]; // this lane's own words
-                        gq[2 + 2 * qj] = dst[2 + 2 * qj];
-                        if (qj == 0)
-                            gq[0] = dst[0];
-                    }
-                }
+    // ---------------- 5. every CTA's hq is stored ----------------
+    // One row block whose down stages all fit the ring at once (no slot is
+    // used twice by down stages): the work units (item, column) are listed
+    // while thread 0 waits at the device-wide barrier, in the h buffers
+    // (free by then), and each warp then walks its units in one go.
+    const int nunits = P.nrows * (off_s[E] + (a.wsd ? T : 0));
+    const bool by_units = P.nrb == 1 && P.nd0 <= HALF && P.nd1 <= HALF && nunits <= MAX_UNITS;
+    uint2 *units = reinterpret_cast<uint2 *>(hbuf);
+    named_barrier(BAR_ALL, CTHREADS); // this CTA's h and hq are stored
+    if (warp == 0) {
+        if (lane == 0 && !grid_barrier(a.sync, gridDim.x, s_c0)) {
+            atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
+            *(volatile int *)&s_abort = 1;
+        }
+        __syncwarp();
+    } else if (by_units) {
+        // unit (item i = v rows + m, column c) is number rows F(v) + m ncols(v) + c,
+        // F(v) the columns of the virtual experts before v: item order
+        const int fsh = off_s[E];
+        for (int i = tid - 32; i < P.NV * P.nrows; i += CTHREADS - 32) {
+            const int v = i / P.nrows, m = i - v * P.nrows;
+            const bool routed = v < P.NVr;
+            const int nc = routed ? v_ncols[v] : T;
+            const int F = routed ? v_first[v] : fsh;
+            const int d = i / SR;
+            int hh, nq;
+            down_slot(d, hh, nq);
+            const uint32_t woff = (uint32_t)((hh * HALF + nq % HALF) * a.stage_bytes + (i - d * SR) * a.rbd);
+            for (int c = 0; c < nc; c++) {
+                const int ys = routed ? routes_s[F + c] : R + c; // hq row = y slot
+                units[P.nrows * F + m * nc + c] = make_uint2(woff, (uint32_t)ys | ((uint32_t)m << 8) | ((uint32_t)d << 16));
             }
         }
-        if (own) {
-            named_barrier(BAR_ALL, CTHREADS);
-        } else {
-            cta_barrier(); // every CTA's share of hq is stored
-            if (a.hs_on && !*(volatile int *)&s_abort) {
+    }
+    named_barrier(BAR_ALL, CTHREADS); // every CTA's hq is stored
+    const int ibytes_w = a.nbI * Q8_1_WORDS; // words per hq row
+    {
+        const int nlive = R + (a.wsd ? T : 0);
+        if (a.hs_on && !*(volatile int *)&s_abort) {
                 if (a.hq_bulk) {
                     // all of hq into shared memory with one bulk copy (the rows
                     // are multiples of 16 bytes); the proxy fence orders the
@@ -810,172 +935,301 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                     }
                 }
                 named_barrier(BAR_ALL, CTHREADS);
-            }
         }
     }
 
-    // ---------------- 7. down rows, combine ----------------
-    for (int d = 0; d < NPd; d++, q++) {
-        int rb, sp;
-        down_stage(d, rb, sp);
-        const int nr0 = dn0 + rb * rpb;
-        const int rows = rb == nrb - 1 ? rlast : rpb;
-        const int i0 = sp * SR, i1 = min(NV * rows, i0 + SR);
-        const bool mine = (q & 1) == grp;
-        if (mine && wait_stage(q)) {
-            const uint8_t *st = ring + (size_t)(q % a.NS) * a.stage_bytes;
-            const uint32_t *xbase = a.hs_on ? hs : a.hq;
-            const int ni = i1 - i0;
-            if (a.nbI == 32) {
-                // two rows per warp (ROWMAP_TWO_ROWS): half h of the warp walks the
-                // items 2 p + h, p = wl, wl + GW, ..., and their columns, two units
-                // per pass; a half-warp reduce-scatter leaves the sums at lanes
-                // 0, 8 (half 0) and 16, 24 (half 1)
-                const int h = lane >> 4;
-                int p = wl, col = 0;
-                const uint32_t *xlast = nullptr;
-                Q81Block xb[2];
-                while (__any_sync(FULL, 2 * p + h < ni)) { // warp-uniform trip count
-                    const uint8_t *wr[2];
-                    const uint32_t *xr[2];
-                    int yo[2];
-                    bool live[2];
+    // ---------------- 6. down rows (all consumer warps), combine ----------------
+    const uint32_t *xbase = a.hs_on ? hs : a.hq;
+    // Units of work: item i0 + it of a row block (virtual expert v = i / rows,
+    // row m = i - v rows), it in [0, ni), times each of its columns.  rowp(it)
+    // is the item's weight row in shared memory; ensure(it) makes sure the
+    // stages up to that of item it have landed (warp-collective, uniform it).
+    // The y values go to ybuf.
+    auto down_units = [&](int ni, int i0, int rows, auto rowp, auto ensure) {
+        if (a.nbI == 32) {
+            // two rows per warp (ROWMAP_TWO_ROWS): half h of the warp walks the
+            // items 2 p + h, p = warp, warp + CW, ..., and their columns, two units
+            // per pass; a half-warp reduce-scatter leaves the sums at lanes
+            // 0, 8 (half 0) and 16, 24 (half 1)
+            const int h = lane >> 4;
+            int p = warp, col = 0;
+            const uint32_t *xlast = nullptr;
+            Q81Block xb[2];
+            while (__any_sync(FULL, 2 * p + h < ni)) { // warp-uniform trip count
+                // the stages of the items this pass may reach
+                ensure(__reduce_max_sync(FULL, min(ni - 1, 2 * (p + CW) + h)));
+                const uint8_t *wr[2];
+                const uint32_t *xr[2];
+                int yo[2];
+                bool live[2];
 #pragma unroll
-                    for (int z = 0; z < 2; z++) {
-                        const int it = 2 * p + h;
-                        live[z] = it < ni;
-                        wr[z] = st;
-                        xr[z] = xbase;
-                        yo[z] = 0;
-                        if (live[z]) {
-                            const int i = i0 + it;
-                            const int v = i / rows, m = i - v * rows;
-                            const int ys = v_e[v] < E ? routes_s[v_first[v] + col] : R + col; // hq row = y slot
-                            wr[z] = st + (size_t)it * a.rbd;
-                            xr[z] = xbase + (size_t)ys * ibytes_w;
-                            yo[z] = ys * RB_MAX + m;
-                            if (++col == v_ncols[v]) {
-                                col = 0;
-                                p += GW;
-                            }
+                for (int z = 0; z < 2; z++) {
+                    const int it = 2 * p + h;
+                    live[z] = it < ni;
+                    wr[z] = ring;
+                    xr[z] = xbase;
+                    yo[z] = 0;
+                    if (live[z]) {
+                        const int i = i0 + it;
+                        const int v = i / rows, m = i - v * rows;
+                        const int ys = v_e[v] < E ? routes_s[v_first[v] + col] : R + col; // hq row = y slot
+                        wr[z] = rowp(it);
+                        xr[z] = xbase + (size_t)ys * ibytes_w;
+                        yo[z] = ys * RB_MAX + m;
+                        if (++col == v_ncols[v]) {
+                            col = 0;
+                            p += CW;
                         }
                     }
-                    float acc[2] = {0.0f, 0.0f};
+                }
+                float acc[2] = {0.0f, 0.0f};
 #pragma unroll
-                    for (int z = 0; z < 2; z++) {
-                        if (live[z]) {
-                            if (xr[z] != xlast) { // this half's activation blocks, reloaded on a new hq row
-                                xlast = xr[z];
-#pragma unroll
-                                for (int j = 0; j < 2; j++) {
-                                    const uint32_t *xw = xr[z] + (size_t)rowmap_block(ROWMAP_TWO_ROWS, lane, j) * Q8_1_WORDS;
-                                    if (a.hs_on) {
-                                        load_q8_1_any(xw, xb[j]);
-                                    } else {
-                                        xb[j].d = half_bits_to_float(__ldcg(xw));
-#pragma unroll
-                                        for (int w = 0; w < 8; w++)
-                                            xb[j].q[w] = (int)__ldcg(xw + 1 + w);
-                                    }
-                                }
-                            }
+                for (int z = 0; z < 2; z++) {
+                    if (live[z]) {
+                        if (xr[z] != xlast) { // this half's activation blocks, reloaded on a new hq row
+                            xlast = xr[z];
 #pragma unroll
                             for (int j = 0; j < 2; j++) {
-                                Q80Block wb;
-                                load_q8_0_smem(wr[z], rowmap_block(ROWMAP_TWO_ROWS, lane, j), wb);
-                                acc[z] = fmaf(wb.d * xb[j].d, (float)dot_q8_block(wb.q, xb[j].q), acc[z]);
+                                const uint32_t *xw = xr[z] + (size_t)rowmap_block(ROWMAP_TWO_ROWS, lane, j) * Q8_1_WORDS;
+                                if (a.hs_on) {
+                                    load_q8_1_any(xw, xb[j]);
+                                } else {
+                                    xb[j].d = half_bits_to_float(__ldcg(xw));
+#pragma unroll
+                                    for (int w = 0; w < 8; w++)
+                                        xb[j].q[w] = (int)__ldcg(xw + 1 + w);
+                                }
                             }
                         }
+#pragma unroll
+                        for (int j = 0; j < 2; j++) {
+                            Q80Block wb;
+                            load_q8_0_smem(wr[z], rowmap_block(ROWMAP_TWO_ROWS, lane, j), wb);
+                            acc[z] = fmaf(wb.d * xb[j].d, (float)dot_q8_block(wb.q, xb[j].q), acc[z]);
+                        }
                     }
-                    const bool h8 = lane & 8;
-                    float y = (h8 ? acc[1] : acc[0]) + __shfl_xor_sync(FULL, h8 ? acc[0] : acc[1], 8);
-                    y += __shfl_xor_sync(FULL, y, 4);
-                    y += __shfl_xor_sync(FULL, y, 2);
-                    y += __shfl_xor_sync(FULL, y, 1);
-                    const int z = (lane >> 3) & 1;
-                    if ((lane & 7) == 0 && (z ? live[1] : live[0]))
-                        ybuf[z ? yo[1] : yo[0]] = y;
                 }
-            } else {
-                // 32 lanes per unit (item, column), four units per pass
-                const int dmap = (a.nbI % 64 == 0) ? ROWMAP_PAIRS : ROWMAP_PLAIN;
-                const int nbl = rowmap_blocks(dmap, a.nbI, lane);
-                int it = wl, col = 0;
-                while (it < ni) {
-                    const uint8_t *wr[4];
-                    const uint32_t *xr[4];
-                    int yo[4];
-                    int nu = 0;
+                const bool h8 = lane & 8;
+                float y = (h8 ? acc[1] : acc[0]) + __shfl_xor_sync(FULL, h8 ? acc[0] : acc[1], 8);
+                y += __shfl_xor_sync(FULL, y, 4);
+                y += __shfl_xor_sync(FULL, y, 2);
+                y += __shfl_xor_sync(FULL, y, 1);
+                const int z = (lane >> 3) & 1;
+                if ((lane & 7) == 0 && (z ? live[1] : live[0]))
+                    ybuf[z ? yo[1] : yo[0]] = y;
+            }
+        } else {
+            // 32 lanes per unit (item, column), four units per pass
+            const int dmap = (a.nbI % 64 == 0) ? ROWMAP_PAIRS : ROWMAP_PLAIN;
+            const int nbl = rowmap_blocks(dmap, a.nbI, lane);
+            int it = warp, col = 0;
+            while (it < ni) {
+                ensure(min(ni - 1, it + 3 * CW)); // the stages of the items this pass may reach
+                const uint8_t *wr[4];
+                const uint32_t *xr[4];
+                int yo[4];
+                int nu = 0;
+#pragma unroll
+                for (int z = 0; z < 4; z++) {
+                    wr[z] = ring;
+                    xr[z] = xbase;
+                    yo[z] = 0;
+                    if (it < ni) {
+                        const int i = i0 + it;
+                        const int v = i / rows, m = i - v * rows;
+                        const int ys = v_e[v] < E ? routes_s[v_first[v] + col] : R + col; // hq row = y slot
+                        wr[z] = rowp(it);
+                        xr[z] = xbase + (size_t)ys * ibytes_w;
+                        yo[z] = ys * RB_MAX + m;
+                        nu++;
+                        if (++col == v_ncols[v]) {
+                            col = 0;
+                            it += CW;
+                        }
+                    }
+                }
+                float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                for (int j = 0; j < nbl; j++) {
+                    const int b = rowmap_block(dmap, lane, j);
+                    Q81Block xb; // the activation block, kept while the units share their hq row
 #pragma unroll
                     for (int z = 0; z < 4; z++) {
-                        wr[z] = st;
-                        xr[z] = xbase;
-                        yo[z] = 0;
-                        if (it < ni) {
-                            const int i = i0 + it;
-                            const int v = i / rows, m = i - v * rows;
-                            const int ys = v_e[v] < E ? routes_s[v_first[v] + col] : R + col; // hq row = y slot
-                            wr[z] = st + (size_t)it * a.rbd;
-                            xr[z] = xbase + (size_t)ys * ibytes_w;
-                            yo[z] = ys * RB_MAX + m;
-                            nu++;
-                            if (++col == v_ncols[v]) {
-                                col = 0;
-                                it += GW;
-                            }
-                        }
-                    }
-                    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                    for (int j = 0; j < nbl; j++) {
-                        const int b = rowmap_block(dmap, lane, j);
-                        Q81Block xb; // the activation block, kept while the units share their hq row
+                        if (z < nu) {
+                            Q80Block wb;
+                            load_q8_0_smem(wr[z], b, wb);
+                            if (z == 0 || xr[z] != xr[z - 1]) {
+                                const uint32_t *xw = xr[z] + (size_t)b * Q8_1_WORDS;
+                                if (a.hs_on) {
+                                    load_q8_1_any(xw, xb);
+                                } else {
+                                    xb.d = half_bits_to_float(__ldcg(xw));
 #pragma unroll
-                        for (int z = 0; z < 4; z++) {
-                            if (z < nu) {
-                                Q80Block wb;
-                                load_q8_0_smem(wr[z], b, wb);
-                                if (z == 0 || xr[z] != xr[z - 1]) {
-                                    const uint32_t *xw = xr[z] + (size_t)b * Q8_1_WORDS;
-                                    if (a.hs_on) {
-                                        load_q8_1_any(xw, xb);
-                                    } else {
-                                        xb.d = half_bits_to_float(__ldcg(xw));
-#pragma unroll
-                                        for (int w = 0; w < 8; w++)
-                                            xb.q[w] = (int)__ldcg(xw + 1 + w);
-                                    }
+                                    for (int w = 0; w < 8; w++)
+                                        xb.q[w] = (int)__ldcg(xw + 1 + w);
                                 }
-                                acc[z] = fmaf(wb.d * xb.d, (float)dot_q8_block(wb.q, xb.q), acc[z]);
                             }
+                            acc[z] = fmaf(wb.d * xb.d, (float)dot_q8_block(wb.q, xb.q), acc[z]);
                         }
                     }
-                    const float y = reduce4(acc[0], acc[1], acc[2], acc[3], lane);
-                    const int z = lane >> 3;
-                    const int yz = z == 0 ? yo[0] : z == 1 ? yo[1] : z == 2 ? yo[2] : yo[3];
-                    if ((lane & 7) == 0 && z < nu)
-                        ybuf[yz] = y;
                 }
+                const float y = reduce4(acc[0], acc[1], acc[2], acc[3], lane);
+                const int z = lane >> 3;
+                const int yz = z == 0 ? yo[0] : z == 1 ? yo[1] : z == 2 ? yo[2] : yo[3];
+                if ((lane & 7) == 0 && z < nu)
+                    ybuf[yz] = y;
             }
         }
-        if (mine)
-            release_stage(q);
-        if (sp == (rb == nrb - 1 ? slast : spr) - 1) {
-            named_barrier(BAR_ALL, CTHREADS); // both groups' y of the row block are in ybuf
-            // out[t][n] = sum_j fl(w * y) in slot order, then + shared
-            if (!dead && !*(volatile int *)&s_abort) {
-                for (int idx = tid; idx < T * rows; idx += CTHREADS) {
-                    const int t = idx / rows, m = idx - t * rows;
-                    float acc = 0.0f;
-                    for (int j = 0; j < k; j++) {
-                        const int e = ids_s[t * k + j];
-                        if (e >= 0)
-                            acc = __fadd_rn(acc, __fmul_rn(w_s[t * k + j], ybuf[(t * k + j) * RB_MAX + m]));
+    };
+    // out rows [nr0, nr0 + rows) from ybuf
+    auto combine = [&](int nr0, int rows) {
+        // out[t][n] = sum_j fl(w * y) in slot order, then + shared
+        if (!dead && !*(volatile int *)&s_abort) {
+            for (int idx = tid; idx < T * rows; idx += CTHREADS) {
+                const int t = idx / rows, m = idx - t * rows;
+                float acc = 0.0f;
+                for (int j = 0; j < k; j++) {
+                    const int e = ids_s[t * k + j];
+                    if (e >= 0)
+                        acc = __fadd_rn(acc, __fmul_rn(w_s[t * k + j], ybuf[(t * k + j) * RB_MAX + m]));
+                }
+                if (a.wsd)
+                    acc = __fadd_rn(acc, ybuf[(R + t) * RB_MAX + m]);
+                a.out[(size_t)t * a.H + nr0 + m] = acc;
+            }
+        }
+    };
+    if (by_units) {
+        int dw = -1; // the last stage this warp waited for
+        auto ensure = [&](int dn) { // warp-uniform dn
+            while (dw < dn) {
+                int hh, nq;
+                down_slot(++dw, hh, nq);
+                wait_slot(hh * HALF + nq % HALF, nq / HALF);
+            }
+        };
+        if (a.nbI == 32) {
+            // half-warps (16 lanes, ROWMAP_TWO_ROWS) take units hw, hw + 32, ...,
+            // UZ at a time; sums by the half-warp butterfly
+            constexpr int UZ = 3;
+            const int hw = 2 * warp + (lane >> 4);
+            for (int base = 0; base < nunits; base += 32 * UZ) { // uniform trip count
+                uint2 ud[UZ];
+                int dmax = -1;
+#pragma unroll
+                for (int z = 0; z < UZ; z++) {
+                    const int u = base + hw + 32 * z;
+                    ud[z] = u < nunits ? units[u] : make_uint2(0u, 0u);
+                    if (u < nunits)
+                        dmax = max(dmax, (int)(ud[z].y >> 16));
+                }
+                ensure(__reduce_max_sync(FULL, dmax));
+                float acc[UZ];
+#pragma unroll
+                for (int z = 0; z < UZ; z++) {
+                    acc[z] = 0.0f;
+                    const int u = base + hw + 32 * z;
+                    if (u < nunits) {
+                        const uint8_t *wr = ring + ud[z].x;
+                        const uint32_t *xr = xbase + (size_t)(ud[z].y & 0xffu) * ibytes_w;
+#pragma unroll
+                        for (int j = 0; j < 2; j++) {
+                            const int b = rowmap_block(ROWMAP_TWO_ROWS, lane, j);
+                            Q81Block xb;
+                            const uint32_t *xw = xr + (size_t)b * Q8_1_WORDS;
+                            if (a.hs_on) {
+                                load_q8_1_any(xw, xb);
+                            } else {
+                                xb.d = half_bits_to_float(__ldcg(xw));
+#pragma unroll
+                                for (int w = 0; w < 8; w++)
+                                    xb.q[w] = (int)__ldcg(xw + 1 + w);
+                            }
+                            Q80Block wb;
+                            load_q8_0_smem(wr, b, wb);
+                            acc[z] = fmaf(wb.d * xb.d, (float)dot_q8_block(wb.q, xb.q), acc[z]);
+                        }
                     }
-                    if (a.wsd)
-                        acc = __fadd_rn(acc, ybuf[(R + t) * RB_MAX + m]);
-                    a.out[(size_t)t * a.H + nr0 + m] = acc;
+                }
+#pragma unroll
+                for (int z = 0; z < UZ; z++) {
+                    const float y = half_warp_sum(acc[z]);
+                    const int u = base + hw + 32 * z;
+                    if ((lane & 15) == 0 && u < nunits)
+                        ybuf[(ud[z].y & 0xffu) * RB_MAX + ((ud[z].y >> 8) & 0xffu)] = y;
                 }
             }
+        } else {
+            // warps (32 lanes) take units warp, warp + CW, ..., four at a time
+            const int dmap = (a.nbI % 64 == 0) ? ROWMAP_PAIRS : ROWMAP_PLAIN;
+            const int nbl = rowmap_blocks(dmap, a.nbI, lane);
+            for (int base = warp; base < nunits; base += 4 * CW) {
+                uint2 ud[4];
+                int dmax = -1;
+#pragma unroll
+                for (int z = 0; z < 4; z++) {
+                    const int u = base + CW * z;
+                    ud[z] = u < nunits ? units[u] : make_uint2(0u, 0u);
+                    if (u < nunits)
+                        dmax = max(dmax, (int)(ud[z].y >> 16));
+                }
+                ensure(dmax);
+                float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                for (int j = 0; j < nbl; j++) {
+                    const int b = rowmap_block(dmap, lane, j);
+#pragma unroll
+                    for (int z = 0; z < 4; z++) {
+                        if (base + CW * z < nunits) {
+                            Q80Block wb;
+                            load_q8_0_smem(ring + ud[z].x, b, wb);
+                            Q81Block xb;
+                            const uint32_t *xw = xbase + (size_t)(ud[z].y & 0xffu) * ibytes_w + (size_t)b * Q8_1_WORDS;
+                            if (a.hs_on) {
+                                load_q8_1_any(xw, xb);
+                            } else {
+                                xb.d = half_bits_to_float(__ldcg(xw));
+#pragma unroll
+                                for (int w = 0; w < 8; w++)
+                                    xb.q[w] = (int)__ldcg(xw + 1 + w);
+                            }
+                            acc[z] = fmaf(wb.d * xb.d, (float)dot_q8_block(wb.q, xb.q), acc[z]);
+                        }
+                    }
+                }
+                const float y = reduce4(acc[0], acc[1], acc[2], acc[3], lane);
+                const int z = lane >> 3;
+                const uint32_t yd = z == 0 ? ud[0].y : z == 1 ? ud[1].y : z == 2 ? ud[2].y : ud[3].y;
+                if ((lane & 7) == 0 && base + CW * z < nunits)
+                    ybuf[(yd & 0xffu) * RB_MAX + ((yd >> 8) & 0xffu)] = y;
+            }
+        }
+        named_barrier(BAR_ALL, CTHREADS); // every y value is in ybuf
+        combine(P.dn0, P.nrows);
+        return;
+    }
+    for (int d = 0; d < P.NPd; d++) {
+        int rb, sp;
+        down_stage(P, d, rb, sp);
+        const int nr0 = P.dn0 + rb * P.rpb;
+        const int rows = rb == P.nrb - 1 ? P.rlast : P.rpb;
+        const int i0 = sp * SR, i1 = min(P.NV * rows, i0 + SR);
+        int hh, nq;
+        down_slot(d, hh, nq);
+        const int slot = hh * HALF + nq % HALF, use = nq / HALF;
+        if (wait_slot(slot, use)) {
+            const uint8_t *st = ring + (size_t)slot * a.stage_bytes;
+            down_units(i1 - i0, i0, rows, [&](int it) -> const uint8_t * { return st + (size_t)it * a.rbd; },
+                       [](int) {});
+        }
+        const bool rb_end = sp == (rb == P.nrb - 1 ? P.slast : P.spr) - 1;
+        if (nq + HALF < (hh ? P.nglu1 + P.nd1 : P.nglu0 + P.nd0)) {
+            // the producer reuses the slot: every consumer warp must be done with it
+            named_barrier(BAR_ALL, CTHREADS);
+            if (tid == 0 && !dead)
+                mbar_arrive(&empty[slot]);
+        }
+        if (rb_end) {
+            named_barrier(BAR_ALL, CTHREADS); // the row block's y values are in ybuf
+            combine(nr0, rows);
             named_barrier(BAR_ALL, CTHREADS); // ybuf is free for the next row block
         }
     }
@@ -1088,21 +1342,24 @@ extern "C" luce_status luce_moe_layer(const float *logits, const float *bias, co
     // least one row per warp while a part stays under twice that
     int RU = 32;
     while (RU > 1 && 2 * RU * a.rbg > tu.layer_part_kb * 1024 &&
-           !(RU <= CW && 2 * RU * a.rbg <= 2 * tu.layer_part_kb * 1024))
+           !(RU <= GW && 2 * RU * a.rbg <= 2 * tu.layer_part_kb * 1024))
         RU /= 2;
     a.RU = RU;
     a.stage_bytes = std::max(2 * RU * a.rbg, a.rbd);
     a.SR = a.stage_bytes / a.rbd;
     a.prefetch = tu.layer_prefetch;
+    a.dsplit = tu.layer_dsplit;
+    a.psleep = tu.layer_psleep;
+    a.down_early = tu.layer_down_early;
     a.evict_first = tu.evict_first;
     const int nslots = T * k + T;
     const size_t hs_bytes = (size_t)nslots * a.nbI * Q8_1_BYTES;
     a.hs_on = hs_bytes <= 24 * 1024 ? 1 : 0;
-    a.hs_own = tu.layer_hs_own;
     a.hq_bulk = tu.layer_hq_bulk;
     const size_t xrow = (size_t)a.nbH * Q8_1_BYTES + (a.nbH % 64 == 0 ? (size_t)64 * (a.nbH / 32) : 0);
     const size_t fixed = (size_t)T * xrow + (a.hs_on ? hs_bytes : 0) +
-                         (size_t)nslots * RB_MAX * sizeof(float) + (size_t)2 * T * E * sizeof(float);
+                         (size_t)nslots * RB_MAX * sizeof(float) + (size_t)2 * T * E * sizeof(float) +
+                         (size_t)4 * 32 * HB_STRIDE * sizeof(float);
     const size_t budget = (size_t)tu.layer_budget_kb * 1024;
     if (budget < fixed + 2 * ((size_t)a.stage_bytes + 16))
         return LUCE_ERR_UNSUPPORTED;
