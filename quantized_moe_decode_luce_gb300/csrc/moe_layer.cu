@@ -17,28 +17,34 @@
 //    tables and xq.  Selection is by rank: expert e of token t takes slot
 //    #{e' : (s_e', e') before (s_e, e)} when that is below k, which is the
 //    (score descending, index ascending) order of the sequential selection.
-//  * Work per CTA: an equal share of all gate/up ROWS of the active experts
-//    (the shared expert last) and an equal share of the down output rows n,
-//    so every CTA streams the same bytes.  One producer warp streams the
-//    CTA's gate/up parts and then its down stages through a ring of
-//    shared-memory stages with cp.async.bulk; the down rows do not depend on
-//    h, so they arrive while the gate/up rows are computed.  Sixteen
-//    consumer warps compute, in two groups that take alternate stages (the
-//    ring has an even number of stages, so every use of a slot falls to the
-//    same group, in order); they never issue copies.
-//  * The gate/up part stores h in fp32.  The down product needs all of h:
-//    each CTA arrives at a device-wide barrier.  The grid is launched
-//    cooperatively, so all of its CTAs are resident at once and the barrier
-//    cannot wait for a CTA that has not started.  Its state (a monotonic
-//    arrival count) lives in caller memory and needs no reset, so graph
-//    replays need no host update.  Its wait is bounded (LUCE_FAULT_TIMEOUT).
-//  * Then h -> q8_1 (the q8_1 rule of the separate kernels): when all of hq
-//    fits in 24 KB every CTA quantizes all of it into its own shared memory
-//    (CTA 0 also stores it); otherwise each CTA quantizes and stores its
-//    share and a second barrier follows.
-//  * Each CTA computes its down rows from shared memory, keeps every y in
-//    shared memory and combines out[t][n] in slot order with separately
-//    rounded products and sums, then adds the shared expert.
+//    A NaN score ranks below every number, so the order is total and every
+//    token selects exactly k distinct experts.
+//  * Gate/up work per CTA: an equal share of all 32-row groups of the active
+//    experts (the shared expert last; a CTA takes its shared groups first).
+//    A group is the span of one q8_1 block of h, so the CTA that computes a
+//    group's h also quantizes it, in the group's epilogue, and stores h and
+//    hq.  Down work per CTA: an equal share of the output rows n.
+//  * One producer warp streams the CTA's stages through a ring of shared
+//    memory with cp.async.bulk: two halves, one per consumer group of eight
+//    warps (group c takes the CTA's groups j = c, c + 2, ...), each half a
+//    queue of its own; after the gate/up parts come the down stages,
+//    alternating between the halves.  The down rows do not depend on h, so
+//    they arrive while h is computed.  The consumer warps never issue copies;
+//    each warp releases a stage by its own arrival.
+//  * With one token the routing yields k experts, so the plan is known
+//    before the routing: the producer requests the first shared group at
+//    once and starts on the routed experts as soon as the ranks exist.
+//  * The down product needs all of hq: each CTA arrives at a device-wide
+//    barrier.  The grid is launched cooperatively, so all of its CTAs are
+//    resident at once and the barrier cannot wait for a CTA that has not
+//    started.  Its state (a monotonic arrival count) lives in caller memory
+//    and needs no reset, so graph replays need no host update.  Its wait is
+//    bounded (LUCE_FAULT_TIMEOUT).  While thread 0 waits, the other warps
+//    list the CTA's down work units (item, column).
+//  * After the barrier each CTA copies all of hq into shared memory (one bulk
+//    copy when it fits in 24 KB), computes its down rows from shared memory,
+//    keeps every y in shared memory and combines out[t][n] in slot order with
+//    separately rounded products and sums, then adds the shared expert.
 //  * Warp sums use a reduce-scatter butterfly (several sums per pass) whose
 //    additions pair the lanes exactly as a full butterfly does, so every sum
 //    is bitwise the one of the separate kernels.
@@ -54,7 +60,7 @@ namespace {
 
 using namespace luce;
 
-// Consumer warps in two groups of GW that take alternate ring stages; warp CW
+// Consumer warps in two groups of GW, each with its half of the ring; warp CW
 // streams the weights.  Named barriers: 1 + group (a group), 3 (all consumers).
 constexpr int GW = 8;
 constexpr int CW = 2 * GW;
@@ -63,11 +69,11 @@ constexpr int CTHREADS = CW * 32;
 constexpr int THREADS = CTHREADS + 32;
 constexpr int BAR_ALL = 3;
 constexpr int BAR_ROUTE = 4;                 // the routing warps GW .. CW
-constexpr int BAR_TABLES = 5;                // consumers wait, the producer arrives: routing done
+constexpr int BAR_TABLES = 5;                // routing done: the consumers wait (the producer arrives when T > 1)
 constexpr int RTHREADS = THREADS - GTHREADS; // routing threads (E <= this)
 constexpr int MAX_T = 8;
 constexpr int MAX_R = 64;  // T * k
-constexpr int MAX_E = 256; // one thread per expert in the grouping
+constexpr int MAX_E = 256; // experts (selection bit masks of MAX_E / 32 words)
 constexpr int MAX_V = MAX_R + 1;
 constexpr int RB_MAX = 64; // down rows per row block (y buffer rows)
 constexpr int HB_STRIDE = MAX_T + 1; // h of a 32-row group: [32][HB_STRIDE]
@@ -147,6 +153,26 @@ __device__ __forceinline__ float reduce4(float v0, float v1, float v2, float v3,
     return k;
 }
 
+// Warp sums of eight values per lane: lane L ends with the sum of
+// v[(L >> 2) & 7].  As in reduce4, each addition pairs the same lanes, in the
+// same order, as the butterfly of warp_sum, so each sum is bitwise warp_sum's.
+__device__ __forceinline__ float reduce8(const float (&v)[8], int lane)
+{
+    const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
+    float k[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        k[i] = (h16 ? v[4 + i] : v[i]) + __shfl_xor_sync(FULL, h16 ? v[i] : v[4 + i], 16);
+    float m[2];
+#pragma unroll
+    for (int i = 0; i < 2; i++)
+        m[i] = (h8 ? k[2 + i] : k[i]) + __shfl_xor_sync(FULL, h8 ? k[i] : k[2 + i], 8);
+    float n = (h4 ? m[1] : m[0]) + __shfl_xor_sync(FULL, h4 ? m[0] : m[1], 4);
+    n += __shfl_xor_sync(FULL, n, 2);
+    n += __shfl_xor_sync(FULL, n, 1);
+    return n;
+}
+
 // q8_1 rule for one block held by 4 lanes (lane 4i + j holds x[8j .. 8j+7] of
 // block i of the warp's 8): the same arithmetic as quantize_q8_1_warp (the
 // maximum and the integer sum do not depend on the order).
@@ -199,7 +225,7 @@ struct LayerPlan {
     int dn0, nrows;         // down rows [dn0, dn0 + nrows)
     int nrb, rpb, rlast;    // row blocks, their rows, the last one's rows
     int spr, slast, NPd;    // stages of a full row block, of the last one, in all
-    int nglu0, nglu1, dlt;  // gate/up parts of ring half 0 and 1, their difference
+    int nglu0, nglu1, s1;   // gate/up parts of ring half 0 and 1; down stages start in half s1
     int nd0, nd1;           // down stages of half 0 and 1
 };
 
@@ -215,18 +241,13 @@ __device__ __forceinline__ void down_stage(const LayerPlan &P, int d, int &rb, i
     }
 }
 
-// Ring half and sequence number within it of down stage d.
+// Ring half and sequence number within it of down stage d: the down stages
+// alternate between the halves, starting with the half that has fewer
+// gate/up parts (s = 1: half 1).
 __device__ __forceinline__ void down_slot_of(const LayerPlan &P, int d, int &hh, int &n)
 {
-    int pos;
-    if (d < P.dlt) {
-        hh = 1;
-        pos = d;
-    } else {
-        const int e = d - P.dlt;
-        hh = e & 1;
-        pos = (e & 1) ? P.dlt + (e >> 1) : (e >> 1);
-    }
+    hh = (d & 1) ^ P.s1;
+    const int pos = d >> 1;
     n = (hh ? P.nglu1 : P.nglu0) + pos;
 }
 
@@ -304,7 +325,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     if (tid == CTHREADS) {
         for (int s = 0; s < a.NS; s++) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], GW); // the warps of a consumer group
         }
         mbar_init(&hq_bar, 1);
         fence_mbar_init();
@@ -400,9 +421,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     // rows [dn0, dn0 + nrows) in nrb row blocks of rpb rows (the last one
     // rlast); a row block's NV * rows items (expert major) are cut into
     // stages of SR rows.  Each half of the ring takes the gate/up parts of its
-    // consumer group's groups, then down stages: the first dlt of them to
-    // half 1 (which has dlt gate/up parts fewer), then alternately half 0 and
-    // half 1.  (Unsigned 32-bit: NV * G32 <= 65 * 1024, times at most 1024
+    // consumer group's groups, then down stages, alternately, starting with
+    // the half that has fewer gate/up parts.  (Unsigned 32-bit: NV * G32 <= 65 * 1024, times at most 1024
     // CTAs, stays below 2^32.)
     auto make_plan = [&](int nvr) {
         LayerPlan q;
@@ -425,9 +445,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         q.NPd = q.nrb ? (q.nrb - 1) * q.spr + q.slast : 0;
         q.nglu0 = ((q.ngr + 1) / 2) * PPG;
         q.nglu1 = (q.ngr / 2) * PPG;
-        q.dlt = q.nglu0 - q.nglu1;
-        q.nd0 = q.NPd > q.dlt ? (q.NPd - q.dlt + 1) / 2 : 0;
-        q.nd1 = min(q.dlt, q.NPd) + (q.NPd > q.dlt ? (q.NPd - q.dlt) / 2 : 0);
+        q.s1 = q.nglu1 < q.nglu0 ? 1 : 0;
+        q.nd0 = q.s1 ? q.NPd / 2 : (q.NPd + 1) / 2;
+        q.nd1 = q.NPd - q.nd0;
         return q;
     };
     const int SR = a.SR;
@@ -487,6 +507,15 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     };
 
 
+    // One token with whole rows per warp (RU a multiple of GW): each warp
+    // holds the lane partial sums of its four rows of a group (gate, up) and
+    // reduces them once, when the group is done.
+    const bool defer = x_regs && a.RU % GW == 0;
+    const int rpw = a.RU / GW; // rows of a part per warp
+    float dacc[8];
+#pragma unroll
+    for (int q = 0; q < 8; q++)
+        dacc[q] = 0.0f;
     // rows [p RU, (p + 1) RU) of a 32-row group from the stage in `slot` -> hb
     // (h of the group's rows, 32 x HB_STRIDE); columns of a routed expert
     // (first, ncols) or, routed == false, the T shared tokens
@@ -543,6 +572,19 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                             }
                         }
                     }
+                    if (defer) {
+                        // one token: the row's partial sums wait for one
+                        // reduction of the warp's four rows of the group
+                        const int r = p * rpw + (i - wl) / GW;
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            if (q == r) {
+                                dacc[2 * q] = ag[0];
+                                dacc[2 * q + 1] = au[0];
+                            }
+                        }
+                        continue;
+                    }
                     // two columns per pass: g0, u0, g1, u1 at lanes 0, 8, 16, 24
 #pragma unroll
                     for (int c = 0; c < NC; c += 2) {
@@ -561,9 +603,20 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                 }
             }
         }
-        named_barrier(1 + grp, GTHREADS); // every warp of the group is done with the stage
-        if (gtid == 0 && !dead)
-            mbar_arrive(&empty[slot]);
+        __syncwarp();
+        if (lane == 0 && !dead)
+            mbar_arrive(&empty[slot]); // this warp is done with the stage
+    };
+    // one token: h of this warp's four rows of a finished group -> hb (the
+    // sums of row r at lanes 8 r (gate) and 8 r + 4 (up))
+    auto glu_finish = [&](float *hb) {
+        const float n = reduce8(dacc, lane);
+        const float u = __shfl_down_sync(FULL, n, 4);
+        if ((lane & 7) == 0) {
+            const int r = lane >> 3;
+            const int prow = (r / rpw) * a.RU + wl + GW * (r % rpw);
+            hb[prow * HB_STRIDE] = swiglu(n, u, a.clamp);
+        }
     };
     // a finished 32-row group in hb -> h and its q8_1 blocks (warp per column)
     auto glu_epilogue = [&](int gi, bool routed, int first, int ncols, const float *hb) {
@@ -731,7 +784,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                         continue;
                     }
                     const int i = dq[h];
-                    d = h == 0 ? P.dlt + 2 * i : (i < P.dlt ? i : P.dlt + 2 * (i - P.dlt) + 1);
+                    d = 2 * i + (h ^ P.s1);
                     if (d >= P.NPd)
                         continue;
                 }
@@ -861,6 +914,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                     continue; // taken before the routing
                 glu_part(grp * HALF + n % HALF, n / HALF, p, routed, first, ncols, hb);
             }
+            if (defer)
+                glu_finish(hb);
             named_barrier(1 + grp, GTHREADS); // all 32 rows of the group are in hb
             glu_epilogue(gi, routed, first, ncols, hb);
         }
@@ -1225,7 +1280,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
             // the producer reuses the slot: every consumer warp must be done with it
             named_barrier(BAR_ALL, CTHREADS);
             if (tid == 0 && !dead)
-                mbar_arrive(&empty[slot]);
+                mbar_arrive_count(&empty[slot], GW);
         }
         if (rb_end) {
             named_barrier(BAR_ALL, CTHREADS); // the row block's y values are in ybuf
