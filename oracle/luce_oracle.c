@@ -245,7 +245,9 @@ static double swiglu_terms(double g, double u, double tg, double tu, double clam
  * Per token: score_e = logit_e + bias_e in fp32; the k largest scores are
  * selected, best first, ties to the lower expert index; the weights are the
  * softmax of the selected *unbiased* logits.  Readings: bias affects
- * selection only; softmax over the k selected logits, no extra scaling.   */
+ * selection only; softmax over the k selected logits, no extra scaling; a
+ * NaN score is taken as -infinity (below every number), so the order is
+ * total and a token always selects k distinct experts.                    */
 void lo_route_topk(const float *logits, const float *bias, int T, int E, int k, int32_t *ids, double *weights)
 {
     for (int t = 0; t < T; t++) {
@@ -262,6 +264,8 @@ void lo_route_topk(const float *logits, const float *bias, int T, int E, int k, 
                 if (taken)
                     continue;
                 float s = bias ? l[e] + bias[e] : l[e];
+                if (s != s)
+                    s = -INFINITY; /* a NaN score ranks below every number */
                 if (best < 0 || s > bs) { /* strict: ties keep the lower index */
                     best = e;
                     bs = s;

@@ -37,8 +37,10 @@ __global__ void __launch_bounds__(ROUTE_WARPS * 32)
         return;
     float *s = s_scores + warp * E;
     const float *l = logits + (size_t)t * E;
-    for (int e = lane; e < E; e += 32)
-        s[e] = bias ? __fadd_rn(l[e], bias[e]) : l[e];
+    for (int e = lane; e < E; e += 32) {
+        const float v = bias ? __fadd_rn(l[e], bias[e]) : l[e];
+        s[e] = v == v ? v : -INFINITY; // a NaN score ranks below every number
+    }
     __syncwarp();
 
     const int n_i = (E + 31) >> 5;
@@ -226,9 +228,10 @@ __device__ __forceinline__ void route_token_regs(const float *__restrict__ l, co
 #pragma unroll
     for (int i = 0; i < EPL; i++) {
         const int e = lane + 32 * i;
-        if (e < E)
-            sc[i] = bias ? __fadd_rn(l[e], bias[e]) : l[e];
-        else {
+        if (e < E) {
+            const float v = bias ? __fadd_rn(l[e], bias[e]) : l[e];
+            sc[i] = v == v ? v : -INFINITY; // a NaN score ranks below every number
+        } else {
             sc[i] = 0.0f;
             taken |= 1u << i;
         }

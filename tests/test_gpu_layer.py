@@ -200,3 +200,25 @@ def test_shapes_beyond_the_limits_are_declined_without_a_launch():
     st.run(layer, x, f, None)
     torch.cuda.synchronize()
     assert st.path == "split"
+
+
+@pytest.mark.parametrize("T", [1, 3])
+def test_nan_scores_select_like_the_oracle_on_every_path(T):
+    # NaN logits (and a NaN bias entry): both paths and the separate router
+    # rank them below every number, as the oracle does; no fault is raised
+    wl = W.Workload("nan_scores", T=T, H=256, I=256, E=40, k=6, shared=True, clamp=0.0, seed=77 + T,
+                    logits="normal", bias_std=0.1)
+    L = W.host_layer(wl)
+    L.logits[:, ::3] = np.float32("nan")
+    L.bias[5] = np.float32("nan")
+    a, b = _both(wl, L)
+    ids_ref, _ = oracle.route_topk(L.logits, L.bias, wl.k)
+    assert np.array_equal(host(a.ids), ids_ref)
+    assert np.array_equal(host(b.ids), ids_ref)
+    ids = torch.empty((T, wl.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, wl.k), dtype=torch.float32, device="cuda")
+    B.luce_route_topk(dev(L.logits), dev(L.bias), wl.k, ids, w)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(ids), ids_ref)
+    for name in ("counts", "offsets", "routes"):
+        assert torch.equal(getattr(a, name), getattr(b, name))

@@ -243,6 +243,20 @@ def test_router_k1_weight_is_exactly_one():
     assert np.array_equal(ids[:, 0], np.argmax(logits, axis=1))
 
 
+def test_router_nan_scores_rank_below_every_number():
+    # a NaN score counts as -infinity: never ahead of a number, ties to the
+    # lower index among NaN and -infinity scores, and k distinct experts always
+    nan, inf = float("nan"), float("inf")
+    logits = np.array([[nan, 1.0, nan, 0.5],
+                       [-inf, nan, 2.0, nan]], np.float32)
+    ids, _ = oracle.route_topk(logits, None, 3)
+    assert ids[0].tolist() == [1, 3, 0]
+    assert ids[1].tolist() == [2, 0, 1]
+    # a NaN bias on a finite logit gives a NaN score too
+    ids, _ = oracle.route_topk(np.array([[3.0, 1.0, 2.0]], np.float32), np.array([nan, 0.0, 0.0], np.float32), 2)
+    assert ids[0].tolist() == [2, 1]
+
+
 def test_router_bias_changes_selection_not_weights():
     logits = np.array([[1.0, 0.9, 0.0, -1.0]], np.float32)
     bias = np.array([0.0, 0.0, 2.0, 0.0], np.float32)
