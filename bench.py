@@ -33,6 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from quantized_moe_decode_luce_gb300 import workloads as W  # noqa: E402
+from quantized_moe_decode_luce_gb300.replicas import job_throughput, rank_seed  # noqa: E402
 
 METRIC = "MoE-FFN layer µs, tokens/s and expert-weight HBM GB/s vs GB300 peak"
 UNIT = "tokens/s"
@@ -77,7 +78,7 @@ def config_dict(wl, layers, graph):
 # ----------------------------------------------------------------------------- inputs
 def draw_inputs(wl, layers, rank):
     """Per layer bias, per (step, layer) x and logits, per step vocab logits."""
-    seed = wl.seed * 1000 + rank
+    seed = rank_seed(wl.seed, rank)
     xs = np.empty((wl.steps, layers, wl.T, wl.H), np.float32)
     lg = np.empty((wl.steps, layers, wl.T, wl.E), np.float32)
     biases = []
@@ -405,13 +406,8 @@ def run_ours(args, wl, layers):
                     down_ms.append(e1.elapsed_time(e2))
             except Exception:
                 pass
-    tmax = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-    ms = float(tmax.item())
+    value, ms = job_throughput(ms, args.steps * wl.T, world, dev)
     ms_per_step = ms / args.steps
-    tokens = args.steps * wl.T * world
-    value = tokens / (ms / 1e3)
     lb = layer_bytes(wl, n_active)
     step_bytes = layers * lb + VOCAB * 4
     peak, peak_kind = measured_peaks()
@@ -490,11 +486,8 @@ def run_ours(args, wl, layers):
                 e2e_step(i)
             s1.record(stream)
             barrier()
-        e_ms = s0.elapsed_time(s1)
-        et = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(et, op=dist.ReduceOp.MAX)
-        e2e = {"value": K2 * wl.T * world / (float(et.item()) / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+        e_value, _ = job_throughput(s0.elapsed_time(s1), K2 * wl.T, world, dev)
+        e2e = {"value": e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": K2,
                "path": "pinned host x/logits/vocab -> device copies -> C-ABI step -> outputs + token to pinned host"}
 
