@@ -73,6 +73,8 @@ def _lib():
         lib.lo_glu_pair.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, d, P, P]
         lib.lo_down_combine.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, P, P]
         lib.lo_argmax.argtypes = [P, i32, i64, P, P]
+        lib.lo_argmax_pick.argtypes = [P, P, i32, i32, P, P]
+        lib.lo_rmsnorm_router.argtypes = [P, P, d, P, i32, i32, i32, P, P, P]
         _LIB = lib
     return _LIB
 
@@ -234,6 +236,71 @@ def argmax(logits):
     val = np.empty(R, np.float32)
     _lib().lo_argmax(_p(logits), R, V, _p(idx), _p(val))
     return idx, val
+
+
+def argmax_pick(vals, idxs):
+    """Pairs of S vocabulary shards, vals f32 [S, R] and global idxs int32 [S, R]
+    -> idx int32 [R], val f32 [R] (largest value, ties to the lower index)."""
+    vals = _c(vals, np.float32)
+    idxs = _c(idxs, np.int32)
+    S, R = vals.shape
+    idx = np.empty(R, np.int32)
+    val = np.empty(R, np.float32)
+    _lib().lo_argmax_pick(_p(vals), _p(idxs), S, R, _p(idx), _p(val))
+    return idx, val
+
+
+def rmsnorm_router(x, gamma, eps: float, w_router):
+    """x [T, H] f32, gamma [H] f32, w_router [E, H] f32 -> (xn f64 [T, H],
+    logits f64 [T, E], logit error scale f64 [T, E])."""
+    x = _c(x, np.float32)
+    gamma = _c(gamma, np.float32)
+    w_router = _c(w_router, np.float32)
+    T, H = x.shape
+    E = w_router.shape[0]
+    xn = np.empty((T, H), np.float64)
+    logits = np.empty((T, E), np.float64)
+    terms = np.empty((T, E), np.float64)
+    _lib().lo_rmsnorm_router(_p(x), _p(gamma), float(eps), _p(w_router), T, E, H, _p(xn), _p(logits), _p(terms))
+    return xn, logits, terms
+
+
+def ep_layer(wg, wu, wd, wsg, wsu, wsd, x, logits, bias, k: int, clamp: float, bounds):
+    """The step split over len(bounds) - 1 expert-parallel ranks ([PR826]:
+    each rank holds a share of the routed experts, routes it does not own
+    reach it masked to id -1, and the ranks sum their partial outputs every
+    layer).  Rank s owns the routed experts [bounds[s], bounds[s + 1]); rank
+    0 also runs the shared expert.  Each rank's partial is moe_layer's
+    arithmetic with the other ranks' routes masked; out is the sum of the
+    partials in rank order, each addition rounded to fp32.
+
+    Returns a dict with ids (unmasked), weights, partials, out, out_terms and
+    the q8_1 flip allowance of h (every route's h is computed by one rank).
+    """
+    x = _c(x, np.float32)
+    T, H = x.shape
+    E = wg.shape[0]
+    I = wg.shape[1]
+    ids, w = route_topk(logits, bias, k)
+    xq = quantize_q8_1(x)
+    parts, terms, allow = [], np.zeros((T, H)), None
+    for s in range(len(bounds) - 1):
+        ids_s = np.where((ids >= bounds[s]) & (ids < bounds[s + 1]), ids, -1).astype(np.int32)
+        sg, su, sd = (wsg, wsu, wsd) if s == 0 else (None, None, None)
+        h, ht = glu_pair(wg, wu, sg, su, xq, ids_s, E, H, I, clamp)
+        h32 = np.nan_to_num(h, nan=0.0).astype(np.float32)
+        a = hq_flip_allowance(h32, tol(np.nan_to_num(ht, nan=0.0)))
+        a[:T * k][ids_s.reshape(-1) < 0] = 0.0  # rows of routes this rank does not own
+        if allow is None:
+            allow = np.zeros((T * k + (T if wsg is not None else 0), I))
+        allow[:a.shape[0]] += a
+        out_s, ot = down_combine(wd, sd, quantize_q8_1(h32), ids_s, w.astype(np.float32), E, H, I)
+        parts.append(out_s)
+        terms += ot
+    out = parts[0].copy()
+    for p in parts[1:]:
+        out = (out + p).astype(np.float32)
+    return dict(ids=ids, weights=w, partials=parts, out=out, out_terms=terms, h_allow=allow)
 
 
 # ----------------------------------------------------------------------------- tolerance

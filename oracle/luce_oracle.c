@@ -419,6 +419,66 @@ void lo_argmax(const float *logits, int R, int64_t V, int32_t *idx, float *val)
 }
 
 /* ------------------------------------------------------------------------ */
+/* Argmax of a vocabulary split across ranks ([PR826], commit "fused DS4.1
+ * decode kernels": the argmax pair/pick of a vocabulary split across ranks,
+ * exact; the cluster runtime commit: the greedy verify head with its
+ * vocabulary split across the ranks).  Shard s reports the pair
+ * (vals[s][r], idxs[s][r]): its first maximum and that column's index in
+ * the whole vocabulary.  The pick keeps the largest value and, among equal
+ * values, the lower index, which is the first maximum of the whole row.    */
+void lo_argmax_pick(const float *vals, const int32_t *idxs, int S, int R, int32_t *idx, float *val)
+{
+    for (int r = 0; r < R; r++) {
+        float bv = vals[r];
+        int32_t bi = idxs[r];
+        for (int s = 1; s < S; s++) {
+            const float v = vals[(int64_t)s * R + r];
+            const int32_t i = idxs[(int64_t)s * R + r];
+            if (v > bv || (v == bv && i < bi)) {
+                bv = v;
+                bi = i;
+            }
+        }
+        idx[r] = bi;
+        if (val)
+            val[r] = bv;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* The step before the router ([PR826], commit "fused DS4.1 decode kernels":
+ * RMS norm among the fused launches; the HC pre-mix commit: an RMS norm
+ * whose sum of squares and products run in F32).  Readings: the standard
+ * RMS norm, xn_i = x_i * gamma_i / sqrt(mean_i x_i^2 + eps) with eps a
+ * parameter, and the router logits are the product of the normed row with
+ * the router matrix W_r [E][H] held in F32.  Computed in double: xn [T][H],
+ * logits [T][E] and, per logit, the error scale sum_i |W_r[e][i] xn_i|.   */
+void lo_rmsnorm_router(const float *x, const float *gamma, double eps, const float *w_router, int T, int E, int H,
+                       double *xn, double *logits, double *terms)
+{
+    for (int t = 0; t < T; t++) {
+        const float *xt = x + (int64_t)t * H;
+        double ss = 0.0;
+        for (int i = 0; i < H; i++)
+            ss += (double)xt[i] * (double)xt[i];
+        const double r = 1.0 / sqrt(ss / (double)H + eps);
+        double *xnt = xn + (int64_t)t * H;
+        for (int i = 0; i < H; i++)
+            xnt[i] = (double)xt[i] * r * (double)gamma[i];
+        for (int e = 0; e < E; e++) {
+            const float *w = w_router + (int64_t)e * H;
+            double acc = 0.0, mag = 0.0;
+            for (int i = 0; i < H; i++) {
+                acc += (double)w[i] * xnt[i];
+                mag += fabs((double)w[i] * xnt[i]);
+            }
+            logits[(int64_t)t * E + e] = acc;
+            terms[(int64_t)t * E + e] = mag;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Array forms of the fp16 conversions, for the Python wrapper.            */
 void lo_fp16_encode_n(const float *x, int64_t n, uint16_t *out)
 {

@@ -416,3 +416,82 @@ def test_argmax_exhaustive_against_numpy():
     assert np.array_equal(idx, np.argmax(x, axis=1))
     assert np.array_equal(val, x[np.arange(50), idx])
     assert idx[1] == 0 and idx[2] == 0 and idx[3] == 776 and idx[4] == 10 and idx[5] == 0
+
+
+def test_argmax_pick_over_shards_equals_the_whole_row():
+    # any split of the vocabulary into shards, each reporting its first
+    # maximum with its global index, picks the whole row's first maximum
+    g = np.random.default_rng(16)
+    x = g.standard_normal((9, 1000)).astype(np.float32)
+    x[1, 499] = x[1, 500] = 9.0    # a tie across the 2-way boundary -> 499
+    x[2, 0] = x[2, 999] = 9.0      # first and last column tie -> 0
+    x[3, :] = 1.0                  # all equal -> 0
+    x[4, 250] = x[4, 750] = 9.0    # tie across non-adjacent shards -> 250
+    full, fval = oracle.argmax(x)
+    for cuts in ([0, 500, 1000], [0, 1, 999, 1000], [0, 250, 251, 750, 1000], [0, 1000]):
+        vals, idxs = [], []
+        for a, b in zip(cuts[:-1], cuts[1:]):
+            i, v = oracle.argmax(x[:, a:b])
+            vals.append(v)
+            idxs.append(i + a)
+        idx, val = oracle.argmax_pick(np.stack(vals), np.stack(idxs))
+        assert np.array_equal(idx, full) and np.array_equal(val, fval)
+    assert full[1] == 499 and full[2] == 0 and full[3] == 0 and full[4] == 250
+
+
+# ----------------------------------------------------------------------------- the steps either side
+def test_rmsnorm_closed_forms():
+    one = np.ones(2, np.float32)
+    # (3, 4): mean square 12.5, so xn = (3, 4) / sqrt(12.5)
+    xn, _, _ = oracle.rmsnorm_router(np.array([[3.0, 4.0]], np.float32), one, 0.0, np.eye(2, dtype=np.float32))
+    assert np.allclose(xn[0], np.array([3.0, 4.0]) / math.sqrt(12.5), rtol=1e-15)
+    # a constant row c: xn = c / sqrt(c^2 + eps); gamma scales each element
+    H, c, eps = 64, 0.5, 1e-3
+    gamma = np.linspace(0.5, 2.0, H).astype(np.float32)
+    xn, _, _ = oracle.rmsnorm_router(np.full((1, H), c, np.float32), gamma, eps, np.zeros((1, H), np.float32))
+    assert np.allclose(xn[0], c / math.sqrt(c * c + eps) * gamma.astype(np.float64), rtol=1e-14)
+    # zero input stays zero; scaling x by 2 (eps = 0) leaves xn unchanged exactly
+    xn, lg, _ = oracle.rmsnorm_router(np.zeros((1, H), np.float32), gamma, 1e-6, np.ones((3, H), np.float32))
+    assert np.all(xn == 0.0) and np.all(lg == 0.0)
+    g = np.random.default_rng(17)
+    x = g.standard_normal((3, H)).astype(np.float32)
+    a, _, _ = oracle.rmsnorm_router(x, gamma, 0.0, np.zeros((1, H), np.float32))
+    b, _, _ = oracle.rmsnorm_router(2.0 * x, gamma, 0.0, np.zeros((1, H), np.float32))
+    assert np.array_equal(a, b)
+    # with gamma = 1 and eps = 0 the normed row has mean square 1
+    a, _, _ = oracle.rmsnorm_router(x, np.ones(H, np.float32), 0.0, np.zeros((1, H), np.float32))
+    assert np.allclose((a ** 2).mean(axis=1), 1.0, rtol=1e-14)
+
+
+def test_router_logits_against_numpy_and_one_hot_rows():
+    g = np.random.default_rng(18)
+    T, E, H = 3, 12, 256
+    x = g.standard_normal((T, H)).astype(np.float32)
+    gamma = g.uniform(0.5, 1.5, H).astype(np.float32)
+    w = (g.standard_normal((E, H)) * 0.05).astype(np.float32)
+    w[0] = 0.0
+    w[0, 7] = 1.0                  # one-hot row: logit = xn[7]
+    xn, lg, terms = oracle.rmsnorm_router(x, gamma, 1e-6, w)
+    ref = xn @ w.astype(np.float64).T
+    assert np.allclose(lg, ref, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(lg[:, 0], xn[:, 7])
+    assert np.allclose(terms, np.abs(xn) @ np.abs(w.astype(np.float64)).T, rtol=1e-12)
+
+
+def test_ep_split_sums_to_the_single_device_step():
+    # two expert-parallel ranks (routed experts [0, E/2) with the shared
+    # expert, and [E/2, E)): each route is computed by one rank, so the sum of
+    # the partials is the single-device output up to the order of the sums
+    wl = W.Workload("ep_pin", T=3, H=256, I=256, E=8, k=3, shared=True, clamp=0.0, seed=41, bias_std=0.1)
+    L = W.host_layer(wl)
+    full = oracle.moe_layer(L.wg, L.wu, L.wd, L.wsg, L.wsu, L.wsd, L.x, L.logits, L.bias, wl.k, wl.clamp)
+    ep = oracle.ep_layer(L.wg, L.wu, L.wd, L.wsg, L.wsu, L.wsd, L.x, L.logits, L.bias, wl.k, wl.clamp, [0, 4, 8])
+    assert np.array_equal(ep["ids"], full["ids"])
+    assert np.all(np.abs(ep["out"] - full["out"]) <= oracle.tol(full["out_terms"]))
+    assert np.allclose(ep["out_terms"], full["out_terms"], rtol=1e-12)
+    # one rank owning everything is the single-device step, bit for bit
+    one = oracle.ep_layer(L.wg, L.wu, L.wd, L.wsg, L.wsu, L.wsd, L.x, L.logits, L.bias, wl.k, wl.clamp, [0, 8])
+    assert np.array_equal(one["out"], full["out"])
+    # a rank that owns none of the selected experts contributes zero (rank 1 here has no shared expert)
+    none = oracle.ep_layer(L.wg, L.wu, L.wd, L.wsg, L.wsu, L.wsd, L.x, L.logits, L.bias, wl.k, wl.clamp, [0, 8, 8])
+    assert np.all(none["partials"][1] == 0.0) and np.array_equal(none["out"], full["out"])
