@@ -33,7 +33,7 @@
  *                    (review of the commit "whole-row-lane slice").
  *   luce_block_q8_1  fp16 d, fp16 s = d*sum(q), 32 int8 codes; 36 bytes.
  *                    The q8_1 activation rows of [PR826], commit "fused
- *                    DS4.1 decode kernels" ("a q8_1 activation memo").
+ *                    DS4.1 decode kernels" (the q8_1 activation memo).
  *   A Q8_0 matrix [rows][K] is rows*K/32 blocks, row after row.
  *   Expert weights: w_gate, w_up [E][I][H/32] blocks; w_down [E][H][I/32].
  *   The shared expert's weights have the same shapes without the E axis.
@@ -78,8 +78,8 @@ typedef struct {
 
 /* ------------------------------------------------------------------------
  * luce_route_topk -- router select + weights in one launch.
- * [PR826], commit "fused DS4.1 decode kernels": "one launch ... for the
- * router's select and weights over the same logits".
+ * [PR826], commit "fused DS4.1 decode kernels": the router's selection and
+ * its weights, both read from one set of logits, run as a single launch.
  *
  * Per token t: score_e = logits[t][e] + bias[e] (fp32 add).  The k largest
  * scores are selected, best first; equal scores go to the lower index.
@@ -95,10 +95,10 @@ LUCE_API luce_status luce_route_topk(const float *logits, const float *bias, int
 
 /* ------------------------------------------------------------------------
  * luce_quantize_q8_1 -- quantize fp32 rows to q8_1 blocks, once per layer.
- * [PR826], commit "fused DS4.1 decode kernels" ("a q8_1 activation memo
- * shared across reshapes") and commit "fused routed combine and q8_1 inputs
- * for the hybrid owners" (the FFN input "as the q8_1 rows its MMVQ reads,
- * quantized once").
+ * [PR826], commit "fused DS4.1 decode kernels" (the q8_1 activation memo,
+ * reused by every reshape) and commit "fused routed combine and q8_1 inputs
+ * for the hybrid owners" (the FFN input is quantized once, to the q8_1 rows
+ * the matrix-vector kernels read).
  *
  * Per 32-value block: amax = max|x|, d = amax / 127 (fp32 IEEE division),
  * q = roundf(x / d) (half away from zero; 0 when amax == 0), stored
@@ -112,7 +112,7 @@ LUCE_API luce_status luce_quantize_q8_1(const float *x, int T, int K, luce_block
 /* ------------------------------------------------------------------------
  * luce_moe_group -- group the T*k routes by expert (one counting sort per
  * layer, shared by gate, up and down).  [PR826], commit "fused DS4.1 decode
- * kernels": "one expert grouping per MoE layer for gate, up and down".
+ * kernels": a single grouping per MoE layer serves gate, up and down.
  *
  * Route r = t*k + j has expert ids[r].  Outputs:
  *   counts  [E]    number of routes of expert e (masked routes excluded)
@@ -161,9 +161,9 @@ LUCE_API luce_status luce_moe_glu_pair(const luce_block_q8_0 *w_gate, const luce
 /* ------------------------------------------------------------------------
  * luce_moe_down_combine -- the Q8_0 down product of every route and of the
  * shared expert, fused with the masked, route-weighted combine.  [PR826],
- * commit "fused routed combine and q8_1 inputs for the hybrid owners": "the
- * owner route mask, the route weighting and the route sum run in one
- * launch; the masked combine rounds its products and its sums separately".
+ * commit "fused routed combine and q8_1 inputs for the hybrid owners": masking
+ * the routes, weighting them and summing them is one launch, and the masked
+ * combine rounds every product and every sum on its own.
  *
  *   y[r][n]  = W_down[ids[r]][n] . hq[r]        (fp32, as in luce_moe_glu_pair)
  *   yS[t][n] = Ws_down[n] . hq[T*k + t]         (if ws_down is given)
@@ -189,8 +189,7 @@ LUCE_API luce_status luce_moe_down_combine(const luce_block_q8_0 *w_down, const 
  * luce_argmax -- exact greedy argmax per row, as a "pair/pick": each CTA
  * reduces a chunk of a row to a (value, index) pair; the last CTA of the
  * row picks among the pairs.  [PR826], commit "fused DS4.1 decode kernels":
- * "an argmax pair/pick that finds the greedy token of a vocabulary ...
- * exactly".
+ * the greedy token comes from an exact argmax done as pairs and a pick.
  *
  * idx[r] = the lowest index of the maximum of logits[r][0..V) (float
  * comparison: -0 == +0 is a tie; inputs must hold no NaN); val[r] = that
@@ -235,13 +234,75 @@ LUCE_API luce_status luce_argmax_noalloc(const float *logits, int R, int64_t V, 
                                          void *stream);
 
 /* ------------------------------------------------------------------------
+ * luce_argmax_shard / luce_argmax_pick -- the greedy token of a vocabulary
+ * split into S shards (one per rank).  [PR826], commit "fused DS4.1 decode
+ * kernels" (the argmax pair/pick over a vocabulary split across ranks, exact)
+ * and the cluster runtime commit (the greedy verify head with its vocabulary
+ * split across the ranks).
+ *
+ * luce_argmax_shard: the argmax of one shard, logits [R][Vs] fp32 whose
+ *   column 0 is column v0 of the whole vocabulary: idx[r] = v0 + the lowest
+ *   index of the shard row's maximum, val[r] = that maximum.  Same kernel,
+ *   workspace (luce_argmax_workspace_bytes(R, Vs), zero-filled, left zero)
+ *   and rules as luce_argmax.  Requires v0 >= 0 and v0 + Vs < 2^31.
+ * luce_argmax_pick: vals [S][R] fp32 and idxs [S][R] int32 are the shards'
+ *   results (shard-major, as gathered from the ranks); idx[r] / val[r] (val
+ *   may be NULL) = the pair with the largest value, among equal values the
+ *   lower index.  With shards covering disjoint column ranges this is
+ *   exactly luce_argmax of the whole rows.  S >= 1, R >= 0; 4-byte aligned.
+ */
+LUCE_API luce_status luce_argmax_shard(const float *logits, int R, int64_t Vs, int64_t v0, int32_t *idx, float *val,
+                                       void *workspace, size_t workspace_bytes, void *stream);
+LUCE_API luce_status luce_argmax_pick(const float *vals, const int32_t *idxs, int S, int R, int32_t *idx, float *val,
+                                      void *stream);
+
+/* ------------------------------------------------------------------------
+ * luce_rmsnorm_router -- the step before the router: the RMS norm of the
+ * hidden rows and the router logits of the normed rows.  [PR826], commit
+ * "fused DS4.1 decode kernels" (the RMS norm among the fused launches) and
+ * the HC pre-mix commit (an RMS norm with its sum of squares and products in
+ * F32).  The pages do not spell out either formula; this is the standard RMS
+ * norm and a plain product with an F32 router matrix:
+ *   xn[t][i]     = x[t][i] * r_t * gamma[i],  r_t = 1 / sqrt(mean_i x[t][i]^2 + eps)
+ *   logits[t][e] = sum_i w_router[e][i] * xn[t][i]
+ * in fp32 (IEEE square root and divisions; the sums in the kernel's order,
+ * graded by tolerance against a double-precision oracle).
+ *
+ *   x [T][H] fp32 (16-byte aligned)    gamma [H] fp32    eps >= 0, finite
+ *   w_router [E][H] fp32 (16-byte aligned)
+ *   xn [T][H] fp32 out or NULL (not stored); must not overlap x
+ *   logits [T][E] fp32 out (the input of luce_route_topk / luce_moe_layer)
+ * Requires H % 4 == 0, 4 <= H <= 12288, E >= 1, T >= 0.
+ */
+LUCE_API luce_status luce_rmsnorm_router(const float *x, const float *gamma, float eps, const float *w_router, int T,
+                                         int E, int H, float *xn, float *logits, void *stream);
+
+/* ------------------------------------------------------------------------
+ * luce_ep_mask / luce_add_f32 -- the two pieces of an expert-parallel split
+ * of the step.  [PR826], the cluster runtime commit (each rank holds a share
+ * of the routed experts, and the ranks sum their outputs every MoE layer) and
+ * the review "moe_combine_masked_kernel indexes valid with an unchecked
+ * (possibly -1) route id" (routes a rank does not own reach it as id -1).
+ * A rank owning routed experts [e0, e1) masks the router's ids, runs
+ * luce_moe_group, luce_moe_glu_pair and luce_moe_down_combine with the
+ * masked ids (one rank also passes the shared expert), and the partial
+ * outputs are summed.
+ *
+ * luce_ep_mask: ids_out[i] = ids[i] if e0 <= ids[i] < e1, else -1, for
+ *   n int32 entries (ids_out may equal ids).  0 <= e0 <= e1.
+ * luce_add_f32: out[i] = a[i] + b[i] (fp32, one rounding), n entries; out
+ *   may equal a or b.
+ */
+LUCE_API luce_status luce_ep_mask(const int32_t *ids, int64_t n, int e0, int e1, int32_t *ids_out, void *stream);
+LUCE_API luce_status luce_add_f32(const float *a, const float *b, float *out, int64_t n, void *stream);
+
+/* ------------------------------------------------------------------------
  * luce_moe_prep -- luce_route_topk, luce_quantize_q8_1 (K = H) and
  * luce_moe_group in ONE launch (one CTA) when T <= 32 and E <= 256, else the
  * three launches in that order.  Same arguments, outputs and results as the
  * three calls.  [PR826], commit "fused DS4.1 decode kernels": the verify
- * step "runs many short kernels per layer", cut by one launch for the
- * router's select and weights, one expert grouping per layer and a q8_1
- * activation memo.
+ * step's many short per-layer kernels are merged, among them the router's
+ * selection and weights, the expert grouping and the q8_1 activation memo.
  */
 LUCE_API luce_status luce_moe_prep(const float *logits, const float *bias, const float *x, int T, int E, int k,
                                    int H, int32_t *ids, float *weights, luce_block_q8_1 *xq, int32_t *counts,

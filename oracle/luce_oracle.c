@@ -241,7 +241,8 @@ static double swiglu_terms(double g, double u, double tg, double tu, double clam
 
 /* ------------------------------------------------------------------------ */
 /* Router select + weights ([PR826, commit "fused DS4.1 decode kernels"]:
- * one launch for "the router's select and weights over the same logits").
+ * the selection and the weights are read from the same logits, in one
+ * launch).
  * Per token: score_e = logit_e + bias_e in fp32; the k largest scores are
  * selected, best first, ties to the lower expert index; the weights are the
  * softmax of the selected *unbiased* logits.  Readings: bias affects
@@ -286,8 +287,8 @@ void lo_route_topk(const float *logits, const float *bias, int T, int E, int k, 
 }
 
 /* ------------------------------------------------------------------------ */
-/* Expert grouping ([PR826, commit "fused DS4.1 decode kernels"]: "one expert
- * grouping per MoE layer for gate, up and down").  The T*k routes
+/* Expert grouping ([PR826, commit "fused DS4.1 decode kernels"]: a single
+ * grouping per MoE layer, used by gate, up and down).  The T*k routes
  * r = t*k + j are sorted by expert id, stable in r.  Masked routes (id < 0,
  * [PR826, review of moe_combine_masked_kernel]) are left out.  counts[e],
  * offsets[e] = sum of counts below e (offsets[E] = number of kept routes),
@@ -356,9 +357,8 @@ void lo_glu_pair(const uint8_t *wg, const uint8_t *wu, const uint8_t *wsg, const
 
 /* ------------------------------------------------------------------------ */
 /* Down product and masked, route-weighted combine ([PR826, commit "fused
- * routed combine ..."]: route mask, route weighting and route sum in one
- * launch; "the masked combine rounds its products and its sums
- * separately").  For every token t and output row n:
+ * routed combine ..."]: masking, weighting and summing the routes is one
+ * launch whose combine rounds each product and each sum on its own).  For every token t and output row n:
  *   y[r][n]  = Wd[ids[r]][n] . hq[r]      (r = t*k + j, ids[r] >= 0)
  *   yS[t][n] = Ws_d[n] . hq[T*k + t]      (when the shared expert is given)
  *   out[t][n] = 0; for j = 0..k-1 with ids >= 0: out = fl(out + fl(w * y));
@@ -401,8 +401,8 @@ void lo_down_combine(const uint8_t *wd, const uint8_t *wsd, const uint8_t *hq, c
 }
 
 /* ------------------------------------------------------------------------ */
-/* Greedy argmax ([PR826, commit "fused DS4.1 decode kernels"]: "an argmax
- * pair/pick that finds the greedy token ... exactly").  Per row: the first
+/* Greedy argmax ([PR826, commit "fused DS4.1 decode kernels"]: the greedy
+ * token is found exactly by an argmax done as pairs and a pick).  Per row: the first
  * index of the maximum value (ties to the lower index; -0 equals +0).     */
 void lo_argmax(const float *logits, int R, int64_t V, int32_t *idx, float *val)
 {

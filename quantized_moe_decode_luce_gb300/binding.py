@@ -51,6 +51,11 @@ def lib() -> ctypes.CDLL:
             "luce_moe_down_combine": [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, P, i32, P],
             "luce_argmax": [P, i32, i64, P, P, P, sz, P],
             "luce_argmax_noalloc": [P, i32, i64, P, P, P],
+            "luce_argmax_shard": [P, i32, i64, i64, P, P, P, sz, P],
+            "luce_argmax_pick": [P, P, i32, i32, P, P, P],
+            "luce_rmsnorm_router": [P, P, f32, P, i32, i32, i32, P, P, P],
+            "luce_ep_mask": [P, i64, i32, i32, P, P],
+            "luce_add_f32": [P, P, P, i64, P],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -186,6 +191,43 @@ def luce_argmax_noalloc(logits, idx, val, stream=None) -> None:
         _ptr(logits, f32, "logits"), R, V, _ptr(idx, i32, "idx"), _ptr(val, f32, "val"), _stream(stream)))
 
 
+def luce_argmax_shard(logits, v0: int, idx, val, workspace, stream=None) -> None:
+    """Argmax of a vocabulary shard whose column 0 is column v0 of the whole vocabulary."""
+    R, Vs = logits.shape
+    _check("luce_argmax_shard", lib().luce_argmax_shard(
+        _ptr(logits, f32, "logits"), R, Vs, int(v0), _ptr(idx, i32, "idx"), _ptr(val, f32, "val"),
+        _ptr(workspace, u8, "workspace"), workspace.numel() if workspace is not None else 0, _stream(stream)))
+
+
+def luce_argmax_pick(vals, idxs, idx, val, stream=None) -> None:
+    """vals [S, R] fp32, idxs [S, R] int32 (the shards' results) -> idx [R], val [R]."""
+    S, R = vals.shape
+    _check("luce_argmax_pick", lib().luce_argmax_pick(
+        _ptr(vals, f32, "vals"), _ptr(idxs, i32, "idxs"), S, R, _ptr(idx, i32, "idx"), _ptr(val, f32, "val"),
+        _stream(stream)))
+
+
+def luce_rmsnorm_router(x, gamma, eps: float, w_router, xn, logits, stream=None) -> None:
+    """x [T, H], gamma [H], w_router [E, H] (fp32) -> xn [T, H] (or None), logits [T, E]."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    _check("luce_rmsnorm_router", lib().luce_rmsnorm_router(
+        _ptr(x, f32, "x"), _ptr(gamma, f32, "gamma"), float(eps), _ptr(w_router, f32, "w_router"), T, E, H,
+        _ptr(xn, f32, "xn"), _ptr(logits, f32, "logits"), _stream(stream)))
+
+
+def luce_ep_mask(ids, e0: int, e1: int, ids_out, stream=None) -> None:
+    _check("luce_ep_mask", lib().luce_ep_mask(
+        _ptr(ids, i32, "ids"), ids.numel(), int(e0), int(e1), _ptr(ids_out, i32, "ids_out"), _stream(stream)))
+
+
+def luce_add_f32(a, b, out, stream=None) -> None:
+    if a.numel() != b.numel() or a.numel() != out.numel():
+        raise ValueError("a, b and out must have the same number of elements")
+    _check("luce_add_f32", lib().luce_add_f32(
+        _ptr(a, f32, "a"), _ptr(b, f32, "b"), _ptr(out, f32, "out"), a.numel(), _stream(stream)))
+
+
 def luce_get_fault() -> int:
     bits = ctypes.c_uint(0)
     _check("luce_get_fault", lib().luce_get_fault(ctypes.byref(bits)))
@@ -199,5 +241,6 @@ def luce_version() -> int:
 __all__ = ["LuceError", "lib", "status_string", "luce_route_topk", "luce_quantize_q8_1", "luce_moe_group",
            "luce_moe_glu_pair", "luce_moe_prep", "luce_moe_layer", "luce_set_pdl",
            "luce_moe_down_combine", "luce_argmax", "luce_argmax_workspace_bytes", "luce_argmax_noalloc",
+           "luce_argmax_shard", "luce_argmax_pick", "luce_rmsnorm_router", "luce_ep_mask", "luce_add_f32",
            "luce_get_fault", "luce_version", "LUCE_OK", "LUCE_ERR_INVALID_ARG", "LUCE_ERR_UNSUPPORTED",
            "LUCE_ERR_CUDA", "LUCE_FAULT_BAD_ID", "LUCE_FAULT_TIMEOUT"]

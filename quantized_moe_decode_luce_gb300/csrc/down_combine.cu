@@ -4,9 +4,9 @@
 //
 // Pages cited by title: [PR826] = Lucebox PR #826 "feat(ds41): two-box
 // expert-parallel serving", commit "fused routed combine and q8_1 inputs for
-// the hybrid owners": the route mask, the route weighting and the route sum
-// in one launch, "the masked combine rounds its products and its sums
-// separately, as the unfused ops do".
+// the hybrid owners": masking, weighting and summing the routes is one
+// launch, and its combine rounds each product and each sum on its own, the
+// way the separate operations did.
 //
 // GB300 shape (our own): a CTA owns a slab of RN output rows n for a tile of
 // tokens and streams those RN rows of EVERY active (virtual) expert, one

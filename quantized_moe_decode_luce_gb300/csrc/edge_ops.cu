@@ -1,0 +1,223 @@
+// edge_ops.cu -- the steps either side of the routed-MoE FFN: the RMS norm
+// and the router logits before it, the pick of a vocabulary split across
+// ranks after it, and the two pieces of an expert-parallel split (masking the
+// routes a rank does not own, summing the ranks' partial outputs), with their
+// C-ABI entry points.
+//
+// Pages cited by title: [PR826] = Lucebox PR #826 "feat(ds41): two-box
+// expert-parallel serving" (section named at each use).
+#include <algorithm>
+#include <climits>
+#include <cmath>
+
+#include "common.cuh"
+
+namespace {
+
+using namespace luce;
+
+
+// ---------------------------------------------------------------------------
+// RMS norm + router logits ([PR826], commit "fused DS4.1 decode kernels": the
+// RMS norm among the launches it fuses; the HC pre-mix commit: an RMS norm
+// whose sum of squares and products run in F32).  The standard RMS norm,
+// xn_i = x_i * r * gamma_i with r = 1 / sqrt(mean_i x_i^2 + eps), and the
+// router logits logits[t][e] = sum_i W_r[e][i] xn_i with W_r in F32.
+//
+// Grid (E / RW experts, T / tpc token tiles), RW warps: every CTA normalizes
+// its tile's tokens into shared memory (warp t sums token t's squares), then
+// warp w streams router row e = blockIdx.x RW + w once for all the tile's
+// tokens.  CTAs of the first expert chunk also store xn.
+constexpr int RW = 8;   // warps (router rows) per CTA
+constexpr int TPC = 8;  // most tokens per tile
+
+__global__ void __launch_bounds__(RW * 32)
+    k_rmsnorm_router(const float *__restrict__ x, const float *__restrict__ gamma, float eps,
+                     const float *__restrict__ w_router, int T, int E, int H, int tpc, float *__restrict__ xn,
+                     float *__restrict__ logits)
+{
+    extern __shared__ __align__(16) float xs[]; // [tpc][H] normed rows
+    __shared__ float rs[TPC];
+    pdl_wait();
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.y * tpc, nt = min(tpc, T - t0);
+    const int H4 = H >> 2;
+    if (warp < nt) {
+        const float4 *xr = reinterpret_cast<const float4 *>(x + (size_t)(t0 + warp) * H);
+        float ss = 0.0f;
+        for (int i = lane; i < H4; i += 32) {
+            const float4 v = xr[i];
+            ss = fmaf(v.x, v.x, ss);
+            ss = fmaf(v.y, v.y, ss);
+            ss = fmaf(v.z, v.z, ss);
+            ss = fmaf(v.w, v.w, ss);
+        }
+        ss = warp_sum(ss);
+        if (lane == 0)
+            rs[warp] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)H), eps)));
+    }
+    __syncthreads();
+    const bool store = xn != nullptr && blockIdx.x == 0;
+    for (int j = threadIdx.x; j < nt * H; j += RW * 32) {
+        const int t = j / H, i = j - t * H;
+        const float v = __fmul_rn(__fmul_rn(x[(size_t)(t0 + t) * H + i], rs[t]), gamma[i]);
+        xs[j] = v;
+        if (store)
+            xn[(size_t)(t0 + t) * H + i] = v;
+    }
+    __syncthreads();
+    const int e = blockIdx.x * RW + warp;
+    if (e >= E)
+        return;
+    const float4 *wr = reinterpret_cast<const float4 *>(w_router + (size_t)e * H);
+    float acc[TPC];
+#pragma unroll
+    for (int t = 0; t < TPC; t++)
+        acc[t] = 0.0f;
+    for (int i = lane; i < H4; i += 32) {
+        const float4 q = __ldg(wr + i);
+#pragma unroll
+        for (int t = 0; t < TPC; t++) {
+            if (t < nt) {
+                const float4 v = reinterpret_cast<const float4 *>(xs + (size_t)t * H)[i];
+                acc[t] = fmaf(q.x, v.x, acc[t]);
+                acc[t] = fmaf(q.y, v.y, acc[t]);
+                acc[t] = fmaf(q.z, v.z, acc[t]);
+                acc[t] = fmaf(q.w, v.w, acc[t]);
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < TPC; t++) {
+        if (t < nt) {
+            const float s = warp_sum(acc[t]);
+            if (lane == 0)
+                logits[(size_t)(t0 + t) * E + e] = s;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Pick across vocabulary shards ([PR826], commit "fused DS4.1 decode
+// kernels": the argmax pair/pick of a vocabulary split across ranks; the
+// cluster runtime commit: the greedy verify head with its vocabulary split
+// across the ranks).  Shard s gave (vals[s][r], idxs[s][r]), its first
+// maximum and that column's index in the whole vocabulary; the pick keeps the
+// largest value, ties to the lower index.  One thread per row.
+__global__ void __launch_bounds__(256)
+    k_argmax_pick(const float *__restrict__ vals, const int32_t *__restrict__ idxs, int S, int R,
+                  int32_t *__restrict__ idx, float *__restrict__ val)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int r = blockIdx.x * 256 + threadIdx.x;
+    if (r >= R)
+        return;
+    float bv = vals[r];
+    int32_t bi = idxs[r];
+    for (int s = 1; s < S; s++) {
+        const float v = vals[(size_t)s * R + r];
+        const int32_t i = idxs[(size_t)s * R + r];
+        if (v > bv || (v == bv && i < bi)) {
+            bv = v;
+            bi = i;
+        }
+    }
+    idx[r] = bi;
+    if (val)
+        val[r] = bv;
+}
+
+// ---------------------------------------------------------------------------
+// Expert-parallel split ([PR826], the cluster runtime commit: each rank holds
+// a share of the routed experts and the ranks sum their outputs every layer;
+// the review of moe_combine_masked_kernel: routes a rank does not own reach
+// it masked to id -1).  The mask keeps the ids of [e0, e1) and sets the
+// others to -1; the sum adds two ranks' partial outputs, one rounding each.
+__global__ void __launch_bounds__(256)
+    k_ep_mask(const int32_t *ids, int64_t n, int e0, int e1, int32_t *out) // in place allowed
+{
+    pdl_wait();
+    pdl_trigger();
+    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
+        const int32_t e = ids[i];
+        out[i] = (e >= e0 && e < e1) ? e : -1;
+    }
+}
+
+__global__ void __launch_bounds__(256)
+    k_add_f32(const float *a, const float *b, float *out, int64_t n) // in place allowed
+{
+    pdl_wait();
+    pdl_trigger();
+    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256)
+        out[i] = __fadd_rn(a[i], b[i]);
+}
+
+unsigned grid_for(int64_t n)
+{
+    const int64_t blocks = (n + 255) / 256;
+    return (unsigned)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)luce_host::sm_count() * 8));
+}
+
+} // namespace
+
+using namespace luce_host;
+
+extern "C" luce_status luce_rmsnorm_router(const float *x, const float *gamma, float eps, const float *w_router, int T,
+                                           int E, int H, float *xn, float *logits, void *stream)
+{
+    if (T < 0 || E < 1 || H < 4 || H % 4 != 0 || H > 12288 || !(eps >= 0.0f) || !std::isfinite(eps))
+        return LUCE_ERR_INVALID_ARG;
+    if (T == 0)
+        return LUCE_OK;
+    if (!x || !gamma || !w_router || !logits || !aligned(x, 16) || !aligned(gamma, 4) || !aligned(w_router, 16) ||
+        !aligned(logits, 4) || (xn && !aligned(xn, 4)))
+        return LUCE_ERR_INVALID_ARG;
+    // a tile's normed rows stay within 48 KB of shared memory
+    const int tpc = std::max(1, std::min(TPC, 12288 / H));
+    const int64_t tiles = ((int64_t)T + tpc - 1) / tpc;
+    const int64_t chunks = ((int64_t)E + RW - 1) / RW;
+    if (tiles > 65535 || chunks > INT_MAX)
+        return LUCE_ERR_INVALID_ARG;
+    const size_t smem = (size_t)tpc * H * sizeof(float);
+    return launch(k_rmsnorm_router, dim3((unsigned)chunks, (unsigned)tiles), dim3(RW * 32), smem, as_stream(stream), x,
+                  gamma, eps, w_router, T, E, H, tpc, xn, logits);
+}
+
+extern "C" luce_status luce_argmax_pick(const float *vals, const int32_t *idxs, int S, int R, int32_t *idx, float *val,
+                                        void *stream)
+{
+    if (S < 1 || R < 0)
+        return LUCE_ERR_INVALID_ARG;
+    if (R == 0)
+        return LUCE_OK;
+    if (!vals || !idxs || !idx || !aligned(vals, 4) || !aligned(idxs, 4) || !aligned(idx, 4) ||
+        (val && !aligned(val, 4)))
+        return LUCE_ERR_INVALID_ARG;
+    return launch(k_argmax_pick, dim3((unsigned)((R + 255) / 256)), dim3(256), 0, as_stream(stream), vals, idxs, S, R,
+                  idx, val);
+}
+
+extern "C" luce_status luce_ep_mask(const int32_t *ids, int64_t n, int e0, int e1, int32_t *ids_out, void *stream)
+{
+    if (n < 0 || e0 < 0 || e1 < e0)
+        return LUCE_ERR_INVALID_ARG;
+    if (n == 0)
+        return LUCE_OK;
+    if (!ids || !ids_out || !aligned(ids, 4) || !aligned(ids_out, 4))
+        return LUCE_ERR_INVALID_ARG;
+    return launch(k_ep_mask, dim3(grid_for(n)), dim3(256), 0, as_stream(stream), ids, n, e0, e1, ids_out);
+}
+
+extern "C" luce_status luce_add_f32(const float *a, const float *b, float *out, int64_t n, void *stream)
+{
+    if (n < 0)
+        return LUCE_ERR_INVALID_ARG;
+    if (n == 0)
+        return LUCE_OK;
+    if (!a || !b || !out || !aligned(a, 4) || !aligned(b, 4) || !aligned(out, 4))
+        return LUCE_ERR_INVALID_ARG;
+    return launch(k_add_f32, dim3(grid_for(n)), dim3(256), 0, as_stream(stream), a, b, out, n);
+}

@@ -424,7 +424,7 @@ __device__ __forceinline__ void block_argmax(float &bv, int &bi)
 
 __global__ void __launch_bounds__(ARGMAX_THREADS)
     k_argmax(const float *__restrict__ logits, int64_t V, int64_t L, int C, bool vec4, ArgPair *__restrict__ pairs,
-             unsigned int *__restrict__ counters, int32_t *__restrict__ idx, float *__restrict__ val)
+             unsigned int *__restrict__ counters, int32_t *__restrict__ idx, float *__restrict__ val, int64_t v0)
 {
     pdl_wait();
     pdl_trigger();
@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(ARGMAX_THREADS)
     }
     block_argmax(bv, bi);
     if (threadIdx.x == 0) {
-        idx[r] = bi;
+        idx[r] = (int32_t)(bi + v0); // the shard's first column is column v0 of the vocabulary
         if (val)
             val[r] = bv;
         counters[r] = 0u;
@@ -537,7 +537,7 @@ extern "C" const char *luce_status_string(luce_status s)
     return "unknown status";
 }
 
-extern "C" int luce_version(void) { return 200; }
+extern "C" int luce_version(void) { return 300; }
 
 extern "C" luce_status luce_set_pdl(int enable)
 {
@@ -639,7 +639,31 @@ extern "C" luce_status luce_argmax(const float *logits, int R, int64_t V, int32_
     const bool vec4 = (V % 4 == 0) && aligned(logits, 16);
     dim3 grid((unsigned)C, (unsigned)R);
     return launch(k_argmax, grid, dim3(ARGMAX_THREADS), 0, as_stream(stream), logits, V, L, C, vec4, pairs, counters,
-                  idx, val);
+                  idx, val, (int64_t)0);
+}
+
+extern "C" luce_status luce_argmax_shard(const float *logits, int R, int64_t Vs, int64_t v0, int32_t *idx, float *val,
+                                         void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (R < 0 || Vs < 1 || v0 < 0 || v0 + Vs > ((int64_t)1 << 31) - 1 || R > 65535)
+        return LUCE_ERR_INVALID_ARG;
+    if (R == 0)
+        return LUCE_OK;
+    if (!logits || !idx || !workspace || !aligned(logits, 4) || !aligned(idx, 4) || !aligned(workspace, 8) ||
+        (val && !aligned(val, 4)))
+        return LUCE_ERR_INVALID_ARG;
+    if (workspace_bytes < luce_argmax_workspace_bytes(R, Vs))
+        return LUCE_ERR_INVALID_ARG;
+    int64_t L;
+    int C;
+    argmax_chunks(R, Vs, L, C);
+    ArgPair *pairs = reinterpret_cast<ArgPair *>(workspace);
+    unsigned int *counters =
+        reinterpret_cast<unsigned int *>(reinterpret_cast<uint8_t *>(workspace) + argmax_pairs_bytes(R, C));
+    const bool vec4 = (Vs % 4 == 0) && aligned(logits, 16);
+    dim3 grid((unsigned)C, (unsigned)R);
+    return launch(k_argmax, grid, dim3(ARGMAX_THREADS), 0, as_stream(stream), logits, Vs, L, C, vec4, pairs, counters,
+                  idx, val, v0);
 }
 
 extern "C" luce_status luce_moe_prep(const float *logits, const float *bias, const float *x, int T, int E, int k, int H,
@@ -744,5 +768,5 @@ extern "C" luce_status luce_argmax_noalloc(const float *logits, int R, int64_t V
     const bool vec4 = (V % 4 == 0) && aligned(logits, 16);
     dim3 grid((unsigned)C, (unsigned)R);
     return launch(k_argmax, grid, dim3(ARGMAX_THREADS), 0, as_stream(stream), logits, V, L, C, vec4, pairs, counters,
-                  idx, val);
+                  idx, val, (int64_t)0);
 }

@@ -136,3 +136,39 @@ def test_argmax_validation_and_workspace(lib):
     assert f(_p(GOOD), 1, 0, _p(GOOD), None, _p(GOOD), 64, None) == 1
     assert f(_p(GOOD), 1, 10, _p(GOOD), None, _p(GOOD + 4), 64, None) == 1       # workspace alignment
     assert f(_p(GOOD), 0, 10, _p(GOOD), None, _p(GOOD), 64, None) == 0
+
+
+def test_edge_ops_validation(lib):
+    f = lib.luce_rmsnorm_router
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p] + [ctypes.c_int] * 3 + \
+        [ctypes.c_void_p] * 3
+    G = _p(GOOD)
+    assert f(G, G, 1e-6, G, 1, 64, 2046, G, G, None) == 1          # H % 4
+    assert f(G, G, 1e-6, G, 1, 64, 16384, G, G, None) == 1         # H > 12288
+    assert f(G, G, -1.0, G, 1, 64, 2048, G, G, None) == 1          # eps < 0
+    assert f(G, G, float("nan"), G, 1, 64, 2048, G, G, None) == 1  # eps NaN
+    assert f(_p(GOOD + 4), G, 1e-6, G, 1, 64, 2048, G, G, None) == 1  # x not 16-byte aligned
+    assert f(G, G, 1e-6, G, 1, 0, 2048, G, G, None) == 1           # E < 1
+    assert f(G, G, 1e-6, G, 1, 64, 2048, G, None, None) == 1       # logits missing
+    assert f(G, G, 1e-6, G, 0, 64, 2048, None, G, None) == 0       # T = 0
+    s = lib.luce_argmax_shard
+    s.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    assert s(G, 2, 1000, -1, G, None, G, 1 << 20, None) == 1       # v0 < 0
+    assert s(G, 2, 1000, (1 << 31) - 10, G, None, G, 1 << 20, None) == 1  # v0 + Vs beyond int32
+    assert s(G, 2, 1000, 0, G, None, G, 0, None) == 1              # workspace too small
+    assert s(G, 0, 1000, 500, G, None, G, 0, None) == 0            # R = 0
+    p = lib.luce_argmax_pick
+    p.argtypes = [ctypes.c_void_p] * 2 + [ctypes.c_int] * 2 + [ctypes.c_void_p] * 3
+    assert p(G, G, 0, 4, G, None, None) == 1                       # S < 1
+    assert p(G, None, 2, 4, G, None, None) == 1
+    assert p(G, G, 2, 0, G, None, None) == 0
+    m = lib.luce_ep_mask
+    m.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    assert m(G, 8, 4, 2, G, None) == 1                             # e1 < e0
+    assert m(G, -1, 0, 2, G, None) == 1
+    assert m(G, 0, 0, 2, G, None) == 0
+    a = lib.luce_add_f32
+    a.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64, ctypes.c_void_p]
+    assert a(G, _p(GOOD + 2), G, 8, None) == 1                     # misaligned b
+    assert a(G, G, G, 0, None) == 0
