@@ -175,13 +175,26 @@ extern "C" luce_status luce_rmsnorm_router(const float *x, const float *gamma, f
     if (!x || !gamma || !w_router || !logits || !aligned(x, 16) || !aligned(gamma, 4) || !aligned(w_router, 16) ||
         !aligned(logits, 4) || (xn && !aligned(xn, 4)))
         return LUCE_ERR_INVALID_ARG;
-    // a tile's normed rows stay within 48 KB of shared memory
-    const int tpc = std::max(1, std::min(TPC, 12288 / H));
+    // a tile's normed rows stay within 64 KB of shared memory (the kernel's
+    // dynamic shared memory limit is raised to that once per device)
+    const int tpc = std::max(1, std::min(TPC, 16384 / H));
     const int64_t tiles = ((int64_t)T + tpc - 1) / tpc;
     const int64_t chunks = ((int64_t)E + RW - 1) / RW;
     if (tiles > 65535 || chunks > INT_MAX)
         return LUCE_ERR_INVALID_ARG;
     const size_t smem = (size_t)tpc * H * sizeof(float);
+    static bool smem_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return LUCE_ERR_CUDA;
+    if (!smem_set[dev]) {
+        if (cudaFuncSetAttribute(k_rmsnorm_router, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            return LUCE_ERR_CUDA;
+        }
+        smem_set[dev] = true;
+    }
     return launch(k_rmsnorm_router, dim3((unsigned)chunks, (unsigned)tiles), dim3(RW * 32), smem, as_stream(stream), x,
                   gamma, eps, w_router, T, E, H, tpc, xn, logits);
 }
