@@ -50,6 +50,7 @@ def parse():
     p.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying CUDA graphs")
     p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-edge-ops", action="store_true", help="skip timing the router and vocabulary-split steps")
     p.add_argument("--path", choices=["layer", "split"], default="layer",
                    help="layer: each MoE layer is one launch (luce_moe_layer); split: prep, gate/up, down launches")
     p.add_argument("--layers", type=int, default=None, help="(debug) fewer layers; invalid as a bench number")
@@ -268,6 +269,73 @@ def profiled_traffic(kernel_files, kernel):
     except Exception:
         pass
     return None
+
+
+def edge_ops_measure(dev, peak, stream):
+    """Device time of the steps either side of the layer at the decode sizes,
+    inputs rotating over more distinct buffers than L2 holds: the RMS norm +
+    router logits (T=1, E=64, H=2048, F32 router matrix) and the greedy token
+    of a 129,280-entry vocabulary split into two shards (two shard argmaxes
+    and the pick).  Returns kernels-dict entries."""
+    import torch
+    from quantized_moe_decode_luce_gb300 import binding as Bd
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(77)
+    out = {}
+    T, E, H, N = 1, 64, 2048, 320  # 320 x 0.5 MB router matrices: 168 MB > L2
+    wr = torch.randn((N, E, H), generator=g, device=dev) * 0.02
+    xs = torch.randn((N, T, H), generator=g, device=dev)
+    gamma = torch.ones(H, device=dev)
+    xn = torch.empty((T, H), device=dev)
+    lg = torch.empty((T, E), device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with torch.cuda.stream(stream):
+        for i in range(8):
+            Bd.luce_rmsnorm_router(xs[i], gamma, 1e-6, wr[i], xn, lg)
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        for i in range(N):
+            Bd.luce_rmsnorm_router(xs[i], gamma, 1e-6, wr[i], xn, lg)
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+    us = ev[0].elapsed_time(ev[1]) * 1e3 / N
+    nbytes = E * H * 4 + 2 * T * H * 4 + H * 4 + T * E * 4
+    out["k_rmsnorm_router"] = {"workload": "T=1 E=64 H=2048 fp32 router", "avg_launch_us": us,
+                               "bytes_per_launch": nbytes, "GBps": nbytes / (us * 1e-6) / 1e9,
+                               "frac": nbytes / (us * 1e-6) / 1e9 / peak, "bound": "hbm (latency-bound at this size)"}
+    del wr, xs
+    V, R, N2 = 129280, 1, 300  # 300 vocabulary rows of 517 KB: 155 MB > L2
+    half = V // 2
+    vocab = torch.randn((N2, 2, R, half), generator=g, device=dev)
+    ws = [torch.zeros(Bd.luce_argmax_workspace_bytes(R, half), dtype=torch.uint8, device=dev) for _ in range(2)]
+    vals = torch.empty((2, R), device=dev)
+    idxs = torch.empty((2, R), dtype=torch.int32, device=dev)
+    idx = torch.empty(R, dtype=torch.int32, device=dev)
+    val = torch.empty(R, device=dev)
+
+    def pick_step(i):
+        for s in range(2):
+            Bd.luce_argmax_shard(vocab[i, s], s * half, idxs[s], vals[s], ws[s])
+        Bd.luce_argmax_pick(vals, idxs, idx, val)
+
+    with torch.cuda.stream(stream):
+        for i in range(8):
+            pick_step(i)
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        for i in range(N2):
+            pick_step(i)
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+    us = ev[0].elapsed_time(ev[1]) * 1e3 / N2
+    nbytes = V * 4 * R
+    out["k_argmax_shard x2 + k_argmax_pick"] = {"workload": "1 x 129,280 fp32 logits in two shards",
+                                                "avg_step_us": us, "launches": 3, "bytes_per_step": nbytes,
+                                                "GBps": nbytes / (us * 1e-6) / 1e9,
+                                                "frac": nbytes / (us * 1e-6) / 1e9 / peak,
+                                                "bound": "hbm (latency-bound at this size)"}
+    return out
 
 
 def run_ours(args, wl, layers):
@@ -490,6 +558,12 @@ def run_ours(args, wl, layers):
         e2e = {"value": e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": K2,
                "path": "pinned host x/logits/vocab -> device copies -> C-ABI step -> outputs + token to pinned host"}
+
+    if rank == 0 and not args.no_edge_ops:
+        try:
+            kernels.update(edge_ops_measure(dev, peak, stream))
+        except Exception as exc:  # a report, never a reason to fail the bench
+            kernels["edge_ops"] = {"failed": str(exc)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
