@@ -290,16 +290,31 @@ def edge_ops_measure(dev, peak, stream):
     xn = torch.empty((T, H), device=dev)
     lg = torch.empty((T, E), device=dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    with torch.cuda.stream(stream):
-        for i in range(8):
-            Bd.luce_rmsnorm_router(xs[i], gamma, 1e-6, wr[i], xn, lg)
-        torch.cuda.synchronize()
-        ev[0].record(stream)
-        for i in range(N):
-            Bd.luce_rmsnorm_router(xs[i], gamma, 1e-6, wr[i], xn, lg)
-        ev[1].record(stream)
-        torch.cuda.synchronize()
-    us = ev[0].elapsed_time(ev[1]) * 1e3 / N
+
+    def timed_graph(body, n):
+        # the n calls captured once and replayed: device time, no host launch cost
+        with torch.cuda.stream(stream):
+            body(0, 8)
+            torch.cuda.synchronize()
+            gph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gph, stream=stream):
+                body(0, n)
+            gph.replay()
+            torch.cuda.synchronize()
+            ev[0].record(stream)
+            gph.replay()
+            ev[1].record(stream)
+            torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1]) * 1e3 / n
+
+    wr_v = [wr[i] for i in range(N)]
+    xs_v = [xs[i] for i in range(N)]
+
+    def router_calls(a, b):
+        for i in range(a, b):
+            Bd.luce_rmsnorm_router(xs_v[i], gamma, 1e-6, wr_v[i], xn, lg)
+
+    us = timed_graph(router_calls, N)
     nbytes = E * H * 4 + 2 * T * H * 4 + H * 4 + T * E * 4
     out["k_rmsnorm_router"] = {"workload": "T=1 E=64 H=2048 fp32 router", "avg_launch_us": us,
                                "bytes_per_launch": nbytes, "GBps": nbytes / (us * 1e-6) / 1e9,
@@ -314,21 +329,17 @@ def edge_ops_measure(dev, peak, stream):
     idx = torch.empty(R, dtype=torch.int32, device=dev)
     val = torch.empty(R, device=dev)
 
-    def pick_step(i):
-        for s in range(2):
-            Bd.luce_argmax_shard(vocab[i, s], s * half, idxs[s], vals[s], ws[s])
-        Bd.luce_argmax_pick(vals, idxs, idx, val)
+    shards = [[vocab[i, s] for s in range(2)] for i in range(N2)]
+    idx_v = [idxs[s] for s in range(2)]
+    val_v = [vals[s] for s in range(2)]
 
-    with torch.cuda.stream(stream):
-        for i in range(8):
-            pick_step(i)
-        torch.cuda.synchronize()
-        ev[0].record(stream)
-        for i in range(N2):
-            pick_step(i)
-        ev[1].record(stream)
-        torch.cuda.synchronize()
-    us = ev[0].elapsed_time(ev[1]) * 1e3 / N2
+    def pick_steps(a, b):
+        for i in range(a, b):
+            for s in range(2):
+                Bd.luce_argmax_shard(shards[i][s], s * half, idx_v[s], val_v[s], ws[s])
+            Bd.luce_argmax_pick(vals, idxs, idx, val)
+
+    us = timed_graph(pick_steps, N2)
     nbytes = V * 4 * R
     out["k_argmax_shard x2 + k_argmax_pick"] = {"workload": "1 x 129,280 fp32 logits in two shards",
                                                 "avg_step_us": us, "launches": 3, "bytes_per_step": nbytes,

@@ -46,6 +46,7 @@ __global__ void __launch_bounds__(RW * 32)
     if (warp < nt) {
         const float4 *xr = reinterpret_cast<const float4 *>(x + (size_t)(t0 + warp) * H);
         float ss = 0.0f;
+#pragma unroll 8
         for (int i = lane; i < H4; i += 32) {
             const float4 v = xr[i];
             ss = fmaf(v.x, v.x, ss);
@@ -75,6 +76,7 @@ __global__ void __launch_bounds__(RW * 32)
 #pragma unroll
     for (int t = 0; t < TPC; t++)
         acc[t] = 0.0f;
+#pragma unroll 8 // eight row loads in flight per lane
     for (int i = lane; i < H4; i += 32) {
         const float4 q = __ldg(wr + i);
 #pragma unroll
