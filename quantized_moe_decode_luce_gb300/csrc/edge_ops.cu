@@ -38,11 +38,22 @@ __global__ void __launch_bounds__(RW * 32)
 {
     extern __shared__ __align__(16) float xs[]; // [tpc][H] normed rows
     __shared__ float rs[TPC];
-    pdl_wait();
-    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.y * tpc, nt = min(tpc, T - t0);
     const int H4 = H >> 2;
+    const int e = blockIdx.x * RW + warp;
+    const float4 *wr = reinterpret_cast<const float4 *>(w_router + (size_t)min(e, E - 1) * H);
+    // the router row does not depend on the previous kernel: its first
+    // WP float4 per lane are requested before waiting for that kernel
+    constexpr int WP = 16;
+    float4 wpre[WP];
+#pragma unroll
+    for (int u = 0; u < WP; u++) {
+        const int i = lane + 32 * u;
+        wpre[u] = (e < E && i < H4) ? __ldg(wr + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    pdl_wait();
+    pdl_trigger();
     if (warp < nt) {
         const float4 *xr = reinterpret_cast<const float4 *>(x + (size_t)(t0 + warp) * H);
         float ss = 0.0f;
@@ -68,17 +79,13 @@ __global__ void __launch_bounds__(RW * 32)
             xn[(size_t)(t0 + t) * H + i] = v;
     }
     __syncthreads();
-    const int e = blockIdx.x * RW + warp;
     if (e >= E)
         return;
-    const float4 *wr = reinterpret_cast<const float4 *>(w_router + (size_t)e * H);
     float acc[TPC];
 #pragma unroll
     for (int t = 0; t < TPC; t++)
         acc[t] = 0.0f;
-#pragma unroll 8 // eight row loads in flight per lane
-    for (int i = lane; i < H4; i += 32) {
-        const float4 q = __ldg(wr + i);
+    auto dot4 = [&](const float4 q, int i) {
 #pragma unroll
         for (int t = 0; t < TPC; t++) {
             if (t < nt) {
@@ -89,6 +96,17 @@ __global__ void __launch_bounds__(RW * 32)
                 acc[t] = fmaf(q.w, v.w, acc[t]);
             }
         }
+    };
+#pragma unroll
+    for (int u = 0; u < WP; u++) {
+        const int i = lane + 32 * u;
+        if (i < H4)
+            dot4(wpre[u], i);
+    }
+#pragma unroll 8 // eight row loads in flight per lane
+    for (int i = lane + 32 * WP; i < H4; i += 32) {
+        const float4 q = __ldg(wr + i);
+        dot4(q, i);
     }
 #pragma unroll
     for (int t = 0; t < TPC; t++) {
