@@ -74,6 +74,11 @@ def _lib():
         lib.lo_down_combine.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, P, P]
         lib.lo_argmax.argtypes = [P, i32, i64, P, P]
         lib.lo_argmax_pick.argtypes = [P, P, i32, i32, P, P]
+        lib.lo_q4_k_scale_min.argtypes = [P, i32, P, P]
+        lib.lo_dot_q4_k_q8_1.restype = d
+        lib.lo_dot_q4_k_q8_1.argtypes = [P, P, i64, P]
+        lib.lo_glu_q4k.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, d, P, P]
+        lib.lo_down_combine_q4k.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, P, P]
         lib.lo_rmsnorm_router.argtypes = [P, P, d, P, i32, i32, i32, P, P, P]
         _LIB = lib
     return _LIB
@@ -236,6 +241,72 @@ def argmax(logits):
     val = np.empty(R, np.float32)
     _lib().lo_argmax(_p(logits), R, V, _p(idx), _p(val))
     return idx, val
+
+
+Q4_K_BYTES = 144
+QK_K = 256
+
+
+def q4_k_scale_min(scales12, j: int):
+    """(sc_j, m_j) of a Q4_K super-block's 12 packed scale bytes."""
+    s = _c(scales12, np.uint8)
+    sc = ctypes.c_int(0)
+    m = ctypes.c_int(0)
+    _lib().lo_q4_k_scale_min(_p(s), int(j), ctypes.byref(sc), ctypes.byref(m))
+    return sc.value, m.value
+
+
+def dot_q4_k_q8_1(w_row, x_row):
+    """(value, terms) of one Q4_K row [K/256, 144] times one q8_1 row [K/32, 36]."""
+    w_row = _c(w_row, np.uint8)
+    x_row = _c(x_row, np.uint8)
+    K = x_row.shape[-2] * QK
+    t = ctypes.c_double(0.0)
+    v = _lib().lo_dot_q4_k_q8_1(_p(w_row), _p(x_row), K, ctypes.byref(t))
+    return v, t.value
+
+
+def glu_q4k(wg, wu, wsg, wsu, xq, ids, E: int, H: int, I: int, clamp: float):
+    """glu_pair with Q4_K gate/up weights [E, I, H/256, 144] (shared [I, H/256, 144])."""
+    ids = _c(ids, np.int32)
+    T, k = ids.shape
+    wg, wu, xq = _c(wg, np.uint8), _c(wu, np.uint8), _c(xq, np.uint8)
+    wsg = None if wsg is None else _c(wsg, np.uint8)
+    wsu = None if wsu is None else _c(wsu, np.uint8)
+    rows = T * k + (T if wsg is not None else 0)
+    h = np.full((rows, I), np.nan, np.float64)
+    ht = np.full((rows, I), np.nan, np.float64)
+    _lib().lo_glu_q4k(_p(wg), _p(wu), _p(wsg), _p(wsu), _p(xq), _p(ids), T, k, E, H, I, float(clamp), _p(h), _p(ht))
+    return h, ht
+
+
+def down_combine_q4k(wd, wsd, hq, ids, weights, E: int, H: int, I: int):
+    """down_combine with Q4_K down weights [E, H, I/256, 144] (shared [H, I/256, 144])."""
+    ids = _c(ids, np.int32)
+    T, k = ids.shape
+    wd, hq = _c(wd, np.uint8), _c(hq, np.uint8)
+    wsd = None if wsd is None else _c(wsd, np.uint8)
+    w = _c(weights, np.float32)
+    out = np.empty((T, H), np.float32)
+    ot = np.empty((T, H), np.float64)
+    _lib().lo_down_combine_q4k(_p(wd), _p(wsd), _p(hq), _p(ids), _p(w), T, k, E, H, I, _p(out), _p(ot))
+    return out, ot
+
+
+def moe_layer_q4k(wg, wu, wd, wsg, wsu, wsd, x, logits, bias, k: int, clamp: float):
+    """moe_layer with Q4_K expert weights (the same steps and roundings)."""
+    x = _c(x, np.float32)
+    T, H = x.shape
+    E, I = wg.shape[0], wg.shape[1]
+    ids, w = route_topk(logits, bias, k)
+    xq = quantize_q8_1(x)
+    h, ht = glu_q4k(wg, wu, wsg, wsu, xq, ids, E, H, I, clamp)
+    h32 = np.nan_to_num(h, nan=0.0).astype(np.float32)
+    ht0 = np.nan_to_num(ht, nan=0.0)
+    hq = quantize_q8_1(h32)
+    out, ot = down_combine_q4k(wd, wsd, hq, ids, w.astype(np.float32), E, H, I)
+    return dict(ids=ids, weights=w, xq=xq, h=h, h_terms=ht, hq=hq, out=out, out_terms=ot,
+                h_allow=hq_flip_allowance(h32, tol(ht0)))
 
 
 def argmax_pick(vals, idxs):

@@ -40,6 +40,8 @@
 #define LO_QK 32
 #define LO_Q8_0_BYTES 34
 #define LO_Q8_1_BYTES 36
+#define LO_QK_K 256       /* values of a Q4_K super-block */
+#define LO_Q4_K_BYTES 144 /* d, dmin (fp16), 12 bytes of scales, 128 bytes of codes */
 
 /* ------------------------------------------------------------------------ */
 /* IEEE-754 binary16 conversion, written from the format definition:
@@ -358,7 +360,8 @@ void lo_glu_pair(const uint8_t *wg, const uint8_t *wu, const uint8_t *wsg, const
 /* ------------------------------------------------------------------------ */
 /* Down product and masked, route-weighted combine ([PR826, commit "fused
  * routed combine ..."]: masking, weighting and summing the routes is one
- * launch whose combine rounds each product and each sum on its own).  For every token t and output row n:
+ * launch whose combine rounds each product and each sum on its own).  For
+ * every token t and output row n:
  *   y[r][n]  = Wd[ids[r]][n] . hq[r]      (r = t*k + j, ids[r] >= 0)
  *   yS[t][n] = Ws_d[n] . hq[T*k + t]      (when the shared expert is given)
  *   out[t][n] = 0; for j = 0..k-1 with ids >= 0: out = fl(out + fl(w * y));
@@ -415,6 +418,137 @@ void lo_argmax(const float *logits, int R, int64_t V, int32_t *idx, float *val)
         idx[r] = (int32_t)best;
         if (val)
             val[r] = x[best];
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Q4_K weights ([PR826], commit "fused DS4.1 decode kernels": wide Q4_K
+ * products are among the layer's matrix products).  The pages name the
+ * format without defining it; this is the ggml K-quant layout the name
+ * refers to: a super-block of 256 values in 8 sub-blocks of 32, 144 bytes:
+ * fp16 d, fp16 dmin, 12 bytes that pack 8 six-bit scales sc_j and 8 six-bit
+ * mins m_j, then 128 bytes of 4-bit codes.  Sub-block j takes the low
+ * (j even) or high (j odd) nibbles of bytes 32 (j / 2) .. 32 (j / 2) + 31;
+ * value i of sub-block j is d sc_j q_i - dmin m_j.  Scales and mins: for
+ * j < 4, sc_j = s[j] & 63 and m_j = s[j + 4] & 63; for j >= 4 the low four
+ * bits come from s[j + 4] (sc: low nibble, m: high nibble) and the high two
+ * bits from the top bits of s[j - 4] (sc) and s[j] (m).                   */
+void lo_q4_k_scale_min(const uint8_t *s, int j, int *sc, int *m)
+{
+    if (j < 4) {
+        *sc = s[j] & 63;
+        *m = s[j + 4] & 63;
+    } else {
+        *sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+        *m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+    }
+}
+
+/* One Q4_K row times one q8_1 row over K values (K a multiple of 256; q8_1
+ * block b = 8 sb + j pairs with sub-block j of super-block sb).  Per
+ * sub-block: d sc_j d8 isum_j - dmin m_j s8, with isum_j = sum_i q_i qx_i an
+ * exact integer, d8 the block's fp16 scale and s8 its fp16 s = d8 sum(qx)
+ * as stored (the form that reads the mins against the stored sum).  Reading:
+ * the stored s (rounded to fp16) is part of the definition, so the result
+ * differs from the dequantized product by at most dmin m_j |s8 - d8 sum qx|.
+ * Accumulated in double; *terms receives sum_j (|d sc d8 isum| + |dmin m s8|). */
+double lo_dot_q4_k_q8_1(const uint8_t *w_row, const uint8_t *x_row, int64_t K, double *terms)
+{
+    int64_t nsb = K / LO_QK_K;
+    double acc = 0.0, tabs = 0.0;
+    for (int64_t sb = 0; sb < nsb; sb++) {
+        const uint8_t *w = w_row + sb * LO_Q4_K_BYTES;
+        const double d = (double)lo_fp16_decode(rd_u16(w));
+        const double dmin = (double)lo_fp16_decode(rd_u16(w + 2));
+        const uint8_t *qs = w + 16;
+        for (int j = 0; j < 8; j++) {
+            const uint8_t *xb = x_row + (sb * 8 + j) * LO_Q8_1_BYTES;
+            int sc, m;
+            lo_q4_k_scale_min(w + 4, j, &sc, &m);
+            int32_t isum = 0;
+            for (int i = 0; i < LO_QK; i++) {
+                const int q = (j & 1) ? (qs[32 * (j / 2) + i] >> 4) : (qs[32 * (j / 2) + i] & 15);
+                isum += q * (int32_t)(int8_t)xb[4 + i];
+            }
+            const double d8 = (double)lo_fp16_decode(rd_u16(xb));
+            const double s8 = (double)lo_fp16_decode(rd_u16(xb + 2));
+            const double t1 = d * (double)sc * d8 * (double)isum;
+            const double t2 = dmin * (double)m * s8;
+            acc += t1 - t2;
+            tabs += fabs(t1) + fabs(t2);
+        }
+    }
+    if (terms)
+        *terms = tabs;
+    return acc;
+}
+
+/* Gate/up pair with SwiGLU as lo_glu_pair, with Q4_K gate and up rows. */
+void lo_glu_q4k(const uint8_t *wg, const uint8_t *wu, const uint8_t *wsg, const uint8_t *wsu, const uint8_t *xq,
+                const int32_t *ids, int T, int k, int E, int H, int I, double clamp, double *h, double *h_terms)
+{
+    int64_t rowb = (int64_t)(H / LO_QK_K) * LO_Q4_K_BYTES;
+    int64_t xrow = (int64_t)(H / LO_QK) * LO_Q8_1_BYTES;
+    int64_t nrows = (int64_t)T * k + (wsg ? T : 0);
+    for (int64_t r = 0; r < nrows; r++) {
+        const uint8_t *G, *U;
+        int t;
+        if (r < (int64_t)T * k) {
+            int e = ids[r];
+            if (e < 0 || e >= E)
+                continue;
+            t = (int)(r / k);
+            G = wg + (int64_t)e * I * rowb;
+            U = wu + (int64_t)e * I * rowb;
+        } else {
+            t = (int)(r - (int64_t)T * k);
+            G = wsg;
+            U = wsu;
+        }
+        for (int i = 0; i < I; i++) {
+            double tg, tu;
+            double g = lo_dot_q4_k_q8_1(G + i * rowb, xq + t * xrow, H, &tg);
+            double u = lo_dot_q4_k_q8_1(U + i * rowb, xq + t * xrow, H, &tu);
+            h[r * I + i] = lo_swiglu(g, u, clamp);
+            if (h_terms)
+                h_terms[r * I + i] = swiglu_terms(g, u, tg, tu, clamp);
+        }
+    }
+}
+
+/* Down product and masked, route-weighted combine as lo_down_combine, with
+ * Q4_K down rows (same rounding of the combine). */
+void lo_down_combine_q4k(const uint8_t *wd, const uint8_t *wsd, const uint8_t *hq, const int32_t *ids,
+                         const float *weights, int T, int k, int E, int H, int I, float *out, double *out_terms)
+{
+    int64_t rowb = (int64_t)(I / LO_QK_K) * LO_Q4_K_BYTES;
+    int64_t hrow = (int64_t)(I / LO_QK) * LO_Q8_1_BYTES;
+    for (int t = 0; t < T; t++) {
+        for (int n = 0; n < H; n++) {
+            float acc = 0.0f;
+            double tt = 0.0;
+            for (int j = 0; j < k; j++) {
+                int64_t r = (int64_t)t * k + j;
+                int e = ids[r];
+                if (e < 0 || e >= E)
+                    continue;
+                double ty;
+                double y = lo_dot_q4_k_q8_1(wd + ((int64_t)e * H + n) * rowb, hq + r * hrow, I, &ty);
+                float w = weights[r];
+                float p = w * (float)y;
+                acc = acc + p;
+                tt += fabs((double)w) * ty;
+            }
+            if (wsd) {
+                double ty;
+                double y = lo_dot_q4_k_q8_1(wsd + (int64_t)n * rowb, hq + ((int64_t)T * k + t) * hrow, I, &ty);
+                acc = acc + (float)y;
+                tt += ty;
+            }
+            out[(int64_t)t * H + n] = acc;
+            if (out_terms)
+                out_terms[(int64_t)t * H + n] = tt;
+        }
     }
 }
 

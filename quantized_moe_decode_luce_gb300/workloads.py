@@ -102,6 +102,42 @@ def q8_0_blocks(g: np.random.Generator, rows: int, K: int) -> np.ndarray:
     return out
 
 
+Q4_K_BYTES = 144
+QK_K = 256
+
+
+def q4_k_blocks(g: np.random.Generator, rows: int, K: int) -> np.ndarray:
+    """Random Q4_K weight rows: uint8 [rows, K/256, 144] (fp16 d and dmin,
+    12 bytes of packed 6-bit scales and mins, 128 bytes of 4-bit codes; every
+    byte pattern of the scales and codes is a valid block)."""
+    assert K % QK_K == 0
+    nb = K // QK_K
+    out = np.empty((rows, nb, Q4_K_BYTES), np.uint8)
+    d = g.uniform(1e-4, 2e-3, size=(rows, nb)).astype(np.float16)
+    dmin = g.uniform(1e-4, 2e-3, size=(rows, nb)).astype(np.float16)
+    out[..., 0:2] = d.view(np.uint8).reshape(rows, nb, 2)
+    out[..., 2:4] = dmin.view(np.uint8).reshape(rows, nb, 2)
+    out[..., 4:] = g.integers(0, 256, size=(rows, nb, Q4_K_BYTES - 4), dtype=np.uint8)
+    return out
+
+
+def host_layer_q4k(wl: Workload) -> HostLayer:
+    """A whole layer with Q4_K expert weights (H and I multiples of 256)."""
+    assert wl.H % QK_K == 0 and wl.I % QK_K == 0
+    gw = rng(wl.seed, 11)
+    wg = q4_k_blocks(gw, wl.E * wl.I, wl.H).reshape(wl.E, wl.I, wl.H // QK_K, Q4_K_BYTES)
+    wu = q4_k_blocks(gw, wl.E * wl.I, wl.H).reshape(wl.E, wl.I, wl.H // QK_K, Q4_K_BYTES)
+    wd = q4_k_blocks(gw, wl.E * wl.H, wl.I).reshape(wl.E, wl.H, wl.I // QK_K, Q4_K_BYTES)
+    wsg = wsu = wsd = None
+    if wl.shared:
+        wsg = q4_k_blocks(gw, wl.I, wl.H)
+        wsu = q4_k_blocks(gw, wl.I, wl.H)
+        wsd = q4_k_blocks(gw, wl.H, wl.I)
+    x = activations(rng(wl.seed, 2), wl.T, wl.H)
+    logits, bias = router_logits(rng(wl.seed, 3), wl)
+    return HostLayer(wl, wg, wu, wd, wsg, wsu, wsd, x, logits, bias, None)
+
+
 def activations(g: np.random.Generator, T: int, H: int) -> np.ndarray:
     return g.standard_normal((T, H), dtype=np.float32)
 

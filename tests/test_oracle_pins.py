@@ -495,3 +495,91 @@ def test_ep_split_sums_to_the_single_device_step():
     # a rank that owns none of the selected experts contributes zero (rank 1 here has no shared expert)
     none = oracle.ep_layer(L.wg, L.wu, L.wd, L.wsg, L.wsu, L.wsd, L.x, L.logits, L.bias, wl.k, wl.clamp, [0, 8, 8])
     assert np.all(none["partials"][1] == 0.0) and np.array_equal(none["out"], full["out"])
+
+
+# ----------------------------------------------------------------------------- Q4_K weights
+def _pack_q4k(d, dmin, sc, m, q):
+    """One Q4_K super-block from its parts, written from the layout's
+    description in the packing direction (the oracle unpacks)."""
+    s = [0] * 12
+    for j in range(4):
+        s[j] = (sc[j] & 63) | ((sc[j + 4] >> 4) << 6)
+        s[j + 4] = (m[j] & 63) | ((m[j + 4] >> 4) << 6)
+    for j in range(4, 8):
+        s[j + 4] = (sc[j] & 15) | ((m[j] & 15) << 4)
+    qs = [0] * 128
+    for j in range(8):
+        for i in range(32):
+            qs[32 * (j // 2) + i] |= (q[j][i] & 15) << (4 * (j % 2))
+    return bytes(struct.pack("<e", d) + struct.pack("<e", dmin) + bytes(s) + bytes(qs))
+
+
+def _q8_1_block(d8, s8, codes):
+    return struct.pack("<e", d8) + struct.pack("<e", s8) + bytes((c & 255) for c in codes)
+
+
+def test_q4k_scales_and_mins_unpack_what_was_packed():
+    g = np.random.default_rng(30)
+    for _ in range(50):
+        sc = g.integers(0, 64, 8).tolist()
+        m = g.integers(0, 64, 8).tolist()
+        blk = _pack_q4k(0.5, 0.25, sc, m, [[0] * 32] * 8)
+        scales = np.frombuffer(blk[4:16], np.uint8)
+        assert [oracle.q4_k_scale_min(scales, j) for j in range(8)] == list(zip(sc, m))
+
+
+def test_q4k_dot_equals_the_exact_dequantized_dot():
+    # d, dmin, d8 powers of two and small code sums: the stored s8 = d8 sum(q8)
+    # is exact in fp16, so the dot is the exact rational dot of the values
+    g = np.random.default_rng(31)
+    for trial in range(20):
+        d, dmin = 2.0 ** -int(g.integers(6, 10)), 2.0 ** -int(g.integers(6, 10))
+        sc = g.integers(0, 64, 8).tolist()
+        m = g.integers(0, 64, 8).tolist()
+        q = g.integers(0, 16, (8, 32)).tolist()
+        w = np.frombuffer(_pack_q4k(d, dmin, sc, m, q), np.uint8).reshape(1, 144)
+        xb, exact = [], Fraction(0)
+        for j in range(8):
+            d8 = 2.0 ** -int(g.integers(5, 9))
+            codes = g.integers(-20, 21, 32).tolist()
+            s8 = d8 * sum(codes)
+            xb.append(_q8_1_block(d8, s8, codes))
+            for i in range(32):
+                val = Fraction(d) * sc[j] * q[j][i] - Fraction(dmin) * m[j]
+                exact += val * Fraction(d8) * codes[i]
+        x = np.frombuffer(b"".join(xb), np.uint8).reshape(8, 36)
+        v, terms = oracle.dot_q4_k_q8_1(w, x)
+        assert abs(Fraction(v) - exact) <= Fraction(abs(terms)) * Fraction(1, 2 ** 50)
+    # all codes zero: the value is -dmin m_j everywhere, the dot -sum_j dmin m_j s8_j
+    w = np.frombuffer(_pack_q4k(0.5, 0.125, [1] * 8, list(range(8)), [[0] * 32] * 8), np.uint8).reshape(1, 144)
+    x = np.frombuffer(b"".join(_q8_1_block(0.25, 0.25 * 3, [3] + [0] * 31) for _ in range(8)), np.uint8)
+    v, _ = oracle.dot_q4_k_q8_1(w, x.reshape(8, 36))
+    assert v == -sum(0.125 * mj * 0.75 for mj in range(8))
+
+
+def test_q4k_row_slices_add_up():
+    g = W.rng(32, 0)
+    w = W.q4_k_blocks(g, 1, 1024)[0]
+    x = oracle.quantize_q8_1(g.standard_normal(1024).astype(np.float32))
+    full, t_full = oracle.dot_q4_k_q8_1(w, x)
+    parts = [oracle.dot_q4_k_q8_1(w[s:s + 1], x[8 * s:8 * s + 8]) for s in range(4)]
+    assert abs(full - sum(p[0] for p in parts)) <= 1e-13 * t_full
+    assert abs(t_full - sum(p[1] for p in parts)) <= 1e-13 * t_full
+
+
+def test_q4k_layer_routes_and_masks_like_the_q8_0_layer():
+    wl = W.Workload("q4k_pin", T=2, H=256, I=256, E=4, k=2, shared=True, clamp=0.0, seed=33, bias_std=0.0)
+    L = W.host_layer_q4k(wl)
+    ref = oracle.moe_layer_q4k(L.wg, L.wu, L.wd, L.wsg, L.wsu, L.wsd, L.x, L.logits, L.bias, wl.k, wl.clamp)
+    ids, _ = oracle.route_topk(L.logits, L.bias, wl.k)
+    assert np.array_equal(ref["ids"], ids)
+    # one masked route: its h row stays unwritten and the combine skips it
+    m = ids.copy()
+    m[0, 1] = -1
+    xq = oracle.quantize_q8_1(L.x)
+    h, _ = oracle.glu_q4k(L.wg, L.wu, L.wsg, L.wsu, xq, m, wl.E, wl.H, wl.I, 0.0)
+    assert np.isnan(h[1]).all() and not np.isnan(h[0]).any()
+    # h is silu(g) u of the two row dots
+    g0, _ = oracle.dot_q4_k_q8_1(L.wg[m[0, 0], 5], xq[0])
+    u0, _ = oracle.dot_q4_k_q8_1(L.wu[m[0, 0], 5], xq[0])
+    assert h[0, 5] == oracle.swiglu(g0, u0)
