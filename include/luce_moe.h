@@ -72,6 +72,13 @@ typedef struct {
     int8_t qs[32]; /* codes round(x / d)          */
 } luce_block_q8_1;
 
+typedef struct {
+    uint16_t d;          /* fp16 super-block scale                       */
+    uint16_t dmin;       /* fp16 super-block scale of the mins           */
+    uint8_t scales[12];  /* eight 6-bit scales and eight 6-bit mins      */
+    uint8_t qs[128];     /* 256 4-bit codes (see luce_moe_glu_q4k)       */
+} luce_block_q4_k;
+
 /* Device fault bits (luce_get_fault). */
 #define LUCE_FAULT_BAD_ID 0x1u  /* a route id >= E was seen and skipped          */
 #define LUCE_FAULT_TIMEOUT 0x2u /* a bounded device wait gave up (never expected) */
@@ -232,6 +239,46 @@ LUCE_API size_t luce_argmax_workspace_bytes(int R, int64_t V);
  */
 LUCE_API luce_status luce_argmax_noalloc(const float *logits, int R, int64_t V, int32_t *idx, float *val,
                                          void *stream);
+
+/* ------------------------------------------------------------------------
+ * luce_moe_glu_q4k / luce_moe_down_combine_q4k -- the gate/up pair with its
+ * SwiGLU and the down product with the masked route-weighted combine, for
+ * Q4_K expert weights.  [PR826], commit "fused DS4.1 decode kernels" (wide
+ * Q4_K products among the layer's products); the arithmetic around the dot
+ * products is that of luce_moe_glu_pair and luce_moe_down_combine.
+ *
+ * Q4_K (the ggml K-quant the pages name; the pages do not define it): a
+ * super-block of 256 values, luce_block_q4_k, 144 bytes.  Sub-block j
+ * (values 32 j .. 32 j + 31) has a 6-bit scale sc_j and a 6-bit min m_j:
+ * for j < 4, sc_j = scales[j] & 63 and m_j = scales[j + 4] & 63; for j >= 4,
+ * sc_j = (scales[j + 4] & 15) | (scales[j - 4] >> 6) << 4 and
+ * m_j = (scales[j + 4] >> 4) | (scales[j] >> 6) << 4.  Its codes q are the low
+ * (j even) or high (j odd) nibbles of qs[32 (j / 2) .. 32 (j / 2) + 31], and
+ * value i is d sc_j q_i - dmin m_j.  Against a q8_1 block (d8, s8, codes)
+ * sub-block j contributes d sc_j d8 isum_j - dmin m_j s8, with the stored
+ * fp16 s8 (isum_j: exact int32 sum of code products).
+ *
+ * luce_moe_glu_q4k: w_gate, w_up [E][I][H/256] blocks (16-byte aligned);
+ *   ws_gate, ws_up [I][H/256] or both NULL; xq [T][H/32] q8_1; ids [T][k]
+ *   (id < 0: masked, its h row untouched; id >= E: skipped and
+ *   LUCE_FAULT_BAD_ID).  h [T*k (+T)][I] fp32 out: h = silu(g) u, or the
+ *   clamped form when clamp > 0 (as luce_moe_glu_pair).  hq is not written:
+ *   quantize h with luce_quantize_q8_1 (rows of masked routes: any values).
+ * luce_moe_down_combine_q4k: w_down [E][H][I/256] (16-byte aligned), ws_down
+ *   [H][I/256] or NULL, hq [T*k (+T)][I/32] q8_1, ids [T][k], weights [T][k]
+ *   fp32 -> out [T][H] fp32, the combine of luce_moe_down_combine (slot
+ *   order, each product and sum rounded, shared expert last).
+ * Requires H % 256 == 0, I % 256 == 0, 1 <= k <= min(E, 64), E <= 1024.  A
+ * first design (one warp per output value); every weight row is read once
+ * per column that needs it.
+ */
+LUCE_API luce_status luce_moe_glu_q4k(const luce_block_q4_k *w_gate, const luce_block_q4_k *w_up,
+                                      const luce_block_q4_k *ws_gate, const luce_block_q4_k *ws_up,
+                                      const luce_block_q8_1 *xq, const int32_t *ids, int T, int k, int E, int H,
+                                      int I, float clamp, float *h, void *stream);
+LUCE_API luce_status luce_moe_down_combine_q4k(const luce_block_q4_k *w_down, const luce_block_q4_k *ws_down,
+                                               const luce_block_q8_1 *hq, const int32_t *ids, const float *weights,
+                                               int T, int k, int E, int H, int I, float *out, void *stream);
 
 /* ------------------------------------------------------------------------
  * luce_argmax_shard / luce_argmax_pick -- the greedy token of a vocabulary

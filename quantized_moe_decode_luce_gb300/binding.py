@@ -56,6 +56,8 @@ def lib() -> ctypes.CDLL:
             "luce_rmsnorm_router": [P, P, f32, P, i32, i32, i32, P, P, P],
             "luce_ep_mask": [P, i64, i32, i32, P, P],
             "luce_add_f32": [P, P, P, i64, P],
+            "luce_moe_glu_q4k": [P, P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P],
+            "luce_moe_down_combine_q4k": [P, P, P, P, P, i32, i32, i32, i32, i32, P, P],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -228,6 +230,23 @@ def luce_add_f32(a, b, out, stream=None) -> None:
         _ptr(a, f32, "a"), _ptr(b, f32, "b"), _ptr(out, f32, "out"), a.numel(), _stream(stream)))
 
 
+def luce_moe_glu_q4k(w_gate, w_up, ws_gate, ws_up, xq, ids, E: int, H: int, I: int, clamp: float, h,
+                     stream=None) -> None:
+    """Q4_K gate/up pair + SwiGLU -> h (quantize h with luce_quantize_q8_1)."""
+    T, k = ids.shape
+    _check("luce_moe_glu_q4k", lib().luce_moe_glu_q4k(
+        _ptr(w_gate, u8, "w_gate"), _ptr(w_up, u8, "w_up"), _ptr(ws_gate, u8, "ws_gate"), _ptr(ws_up, u8, "ws_up"),
+        _ptr(xq, u8, "xq"), _ptr(ids, i32, "ids"), T, k, E, H, I, float(clamp), _ptr(h, f32, "h"), _stream(stream)))
+
+
+def luce_moe_down_combine_q4k(w_down, ws_down, hq, ids, weights, E: int, H: int, I: int, out, stream=None) -> None:
+    """Q4_K down product + masked route-weighted combine -> out."""
+    T, k = ids.shape
+    _check("luce_moe_down_combine_q4k", lib().luce_moe_down_combine_q4k(
+        _ptr(w_down, u8, "w_down"), _ptr(ws_down, u8, "ws_down"), _ptr(hq, u8, "hq"), _ptr(ids, i32, "ids"),
+        _ptr(weights, f32, "weights"), T, k, E, H, I, _ptr(out, f32, "out"), _stream(stream)))
+
+
 def luce_get_fault() -> int:
     bits = ctypes.c_uint(0)
     _check("luce_get_fault", lib().luce_get_fault(ctypes.byref(bits)))
@@ -242,5 +261,6 @@ __all__ = ["LuceError", "lib", "status_string", "luce_route_topk", "luce_quantiz
            "luce_moe_glu_pair", "luce_moe_prep", "luce_moe_layer", "luce_set_pdl",
            "luce_moe_down_combine", "luce_argmax", "luce_argmax_workspace_bytes", "luce_argmax_noalloc",
            "luce_argmax_shard", "luce_argmax_pick", "luce_rmsnorm_router", "luce_ep_mask", "luce_add_f32",
+           "luce_moe_glu_q4k", "luce_moe_down_combine_q4k",
            "luce_get_fault", "luce_version", "LUCE_OK", "LUCE_ERR_INVALID_ARG", "LUCE_ERR_UNSUPPORTED",
            "LUCE_ERR_CUDA", "LUCE_FAULT_BAD_ID", "LUCE_FAULT_TIMEOUT"]

@@ -1,0 +1,217 @@
+// q4k_ops.cu -- the gate/up pair with its SwiGLU and the down product with
+// the masked route-weighted combine for Q4_K expert weights, with their
+// C-ABI entry points.
+//
+// Pages cited by title: [PR826] = Lucebox PR #826 "feat(ds41): two-box
+// expert-parallel serving": commit "fused DS4.1 decode kernels" (wide Q4_K
+// products among the layer's matrix products), commit "RDNA4 Q8_0 gate/up
+// pair" (gate and up on one load of the activations, the GLU in the
+// epilogue), commit "fused routed combine and q8_1 inputs for the hybrid
+// owners" (masked combine, each product and sum rounded on its own).
+//
+// Format (the ggml K-quant the pages name): a super-block of 256 values in
+// 144 bytes -- fp16 d, fp16 dmin, 12 bytes packing eight 6-bit scales sc_j
+// and mins m_j, 128 bytes of 4-bit codes; sub-block j (32 values) takes the
+// low (j even) or high (j odd) nibbles of bytes 32 (j / 2) ...  Against a
+// q8_1 activation block (d8, s8 = d8 sum q8, codes) sub-block j contributes
+// d sc_j d8 isum_j - dmin m_j s8, isum_j the exact int32 sum of codes times
+// activation codes.
+//
+// First design (plain, not yet tuned): one warp per dot product row; a lane
+// takes a pair of sub-blocks (2c, 2c + 1) of a super-block, whose codes are
+// the same 32 bytes (low and high nibbles), with 16-byte loads of the
+// super-block header and codes; dp4a on nibble-masked words.
+#include <algorithm>
+#include <climits>
+#include <cmath>
+
+#include "common.cuh"
+
+LUCE_DEFINE_FAULT_WORD(luce_internal_fault_q4k)
+
+namespace {
+
+using namespace luce;
+
+constexpr int Q4K_BYTES = 144;
+constexpr int QKK = 256;
+constexpr int WARPS = 8;
+
+// (sc, m) of sub-blocks 2c and 2c + 1 from the 12 scale bytes held as three
+// little-endian words
+__device__ __forceinline__ void scale_min_pair(const uint32_t (&sw)[3], int c, int (&sc)[2], int (&m)[2])
+{
+    auto byte = [&](int i) -> int { return (int)((sw[i >> 2] >> (8 * (i & 3))) & 0xffu); };
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+        const int j = 2 * c + h;
+        if (j < 4) {
+            sc[h] = byte(j) & 63;
+            m[h] = byte(j + 4) & 63;
+        } else {
+            sc[h] = (byte(j + 4) & 15) | ((byte(j - 4) >> 6) << 4);
+            m[h] = (byte(j + 4) >> 4) | ((byte(j) >> 6) << 4);
+        }
+    }
+}
+
+// This lane's part of a Q4_K row (K values) times a q8_1 row: pairs
+// p = lane, lane + 32, ... of the row's K / 64 sub-block pairs.
+__device__ __forceinline__ float q4k_lane_dot(const uint8_t *__restrict__ w_row, const uint32_t *__restrict__ x_row,
+                                              int K, int lane)
+{
+    float acc = 0.0f;
+    const int P = K >> 6;
+    for (int p = lane; p < P; p += 32) {
+        const int sb = p >> 2, c = p & 3;
+        const uint4 hd = __ldg(reinterpret_cast<const uint4 *>(w_row + (size_t)sb * Q4K_BYTES));
+        const uint4 *qp = reinterpret_cast<const uint4 *>(w_row + (size_t)sb * Q4K_BYTES + 16 + 32 * c);
+        const uint4 q0 = __ldg(qp), q1 = __ldg(qp + 1);
+        const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
+        const uint32_t sw[3] = {hd.y, hd.z, hd.w};
+        int sc[2], m[2];
+        scale_min_pair(sw, c, sc, m);
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            const uint32_t *xb = x_row + (size_t)(8 * sb + 2 * c + h) * Q8_1_WORDS;
+            const uint32_t xd = __ldg(xb);
+            int isum = 0;
+#pragma unroll
+            for (int w = 0; w < 8; w++)
+                isum = __dp4a((int)((qw[w] >> (4 * h)) & 0x0F0F0F0Fu), (int)__ldg(xb + 1 + w), isum);
+            const float d8 = half_bits_to_float(xd), s8 = half_bits_to_float(xd >> 16);
+            acc = fmaf(d * (float)sc[h] * d8, (float)isum, acc);
+            acc = fmaf(-dmin * (float)m[h], s8, acc);
+        }
+    }
+    return acc;
+}
+
+// Gate/up rows -> h.  Block (i chunk of WARPS rows, route or shared row r);
+// warp w computes h[r][i] for i = blockIdx.x WARPS + w.
+__global__ void __launch_bounds__(WARPS * 32)
+    k_glu_q4k(const uint8_t *__restrict__ wg, const uint8_t *__restrict__ wu, const uint8_t *__restrict__ wsg,
+              const uint8_t *__restrict__ wsu, const uint32_t *__restrict__ xq, const int32_t *__restrict__ ids, int T,
+              int k, int E, int H, int I, float clamp, float *__restrict__ h)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.y, i = blockIdx.x * WARPS + warp;
+    if (i >= I)
+        return;
+    const size_t rowb = (size_t)(H / QKK) * Q4K_BYTES;
+    const uint8_t *G, *U;
+    int t;
+    if (r < T * k) {
+        const int e = ids[r];
+        if (e < 0)
+            return; // masked route
+        if (e >= E) {
+            if (lane == 0 && i == 0)
+                atomicOr(&g_fault_word, LUCE_FAULT_BAD_ID);
+            return;
+        }
+        t = r / k;
+        G = wg + ((size_t)e * I + i) * rowb;
+        U = wu + ((size_t)e * I + i) * rowb;
+    } else {
+        t = r - T * k;
+        G = wsg + (size_t)i * rowb;
+        U = wsu + (size_t)i * rowb;
+    }
+    const uint32_t *x = xq + (size_t)t * (H / QK) * Q8_1_WORDS;
+    const float g = warp_sum(q4k_lane_dot(G, x, H, lane));
+    const float u = warp_sum(q4k_lane_dot(U, x, H, lane));
+    if (lane == 0)
+        h[(size_t)r * I + i] = swiglu(g, u, clamp);
+}
+
+// Down rows and the combine.  Block (chunk of WARPS output rows, token t);
+// warp w: out[t][n] for n = blockIdx.x WARPS + w, the k route slots in slot
+// order with each product and sum rounded, then the shared expert.
+__global__ void __launch_bounds__(WARPS * 32)
+    k_down_combine_q4k(const uint8_t *__restrict__ wd, const uint8_t *__restrict__ wsd,
+                       const uint32_t *__restrict__ hq, const int32_t *__restrict__ ids,
+                       const float *__restrict__ weights, int T, int k, int E, int H, int I, float *__restrict__ out)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.y, n = blockIdx.x * WARPS + warp;
+    if (n >= H)
+        return;
+    const size_t rowb = (size_t)(I / QKK) * Q4K_BYTES;
+    const size_t hrow = (size_t)(I / QK) * Q8_1_WORDS;
+    float acc = 0.0f;
+    for (int j = 0; j < k; j++) {
+        const int r = t * k + j;
+        const int e = ids[r];
+        if (e < 0)
+            continue;
+        if (e >= E) {
+            if (lane == 0 && n == 0)
+                atomicOr(&g_fault_word, LUCE_FAULT_BAD_ID);
+            continue;
+        }
+        const float y = warp_sum(q4k_lane_dot(wd + ((size_t)e * H + n) * rowb, hq + (size_t)r * hrow, I, lane));
+        acc = __fadd_rn(acc, __fmul_rn(weights[r], y));
+    }
+    if (wsd) {
+        const float y = warp_sum(q4k_lane_dot(wsd + (size_t)n * rowb, hq + ((size_t)T * k + t) * hrow, I, lane));
+        acc = __fadd_rn(acc, y);
+    }
+    if (lane == 0)
+        out[(size_t)t * H + n] = acc;
+}
+
+} // namespace
+
+using namespace luce_host;
+
+extern "C" luce_status luce_moe_glu_q4k(const luce_block_q4_k *w_gate, const luce_block_q4_k *w_up,
+                                        const luce_block_q4_k *ws_gate, const luce_block_q4_k *ws_up,
+                                        const luce_block_q8_1 *xq, const int32_t *ids, int T, int k, int E, int H,
+                                        int I, float clamp, float *h, void *stream)
+{
+    if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E || k > 64 || H <= 0 || I <= 0 || H % QKK != 0 ||
+        I % QKK != 0 || !(clamp == clamp))
+        return LUCE_ERR_INVALID_ARG;
+    const bool has_ws = ws_gate != nullptr;
+    if ((ws_up != nullptr) != has_ws)
+        return LUCE_ERR_INVALID_ARG;
+    if (T == 0)
+        return LUCE_OK;
+    if (!w_gate || !w_up || !xq || !ids || !h || !aligned(w_gate, 16) || !aligned(w_up, 16) ||
+        (has_ws && (!aligned(ws_gate, 16) || !aligned(ws_up, 16))) || !aligned(xq, 4) || !aligned(ids, 4) ||
+        !aligned(h, 4))
+        return LUCE_ERR_INVALID_ARG;
+    const int rows = T * k + (has_ws ? T : 0);
+    if ((int64_t)T * k > (1 << 20) || rows > 65535)
+        return LUCE_ERR_INVALID_ARG;
+    return launch(k_glu_q4k, dim3((unsigned)((I + WARPS - 1) / WARPS), (unsigned)rows), dim3(WARPS * 32), 0,
+                  as_stream(stream), reinterpret_cast<const uint8_t *>(w_gate), reinterpret_cast<const uint8_t *>(w_up),
+                  reinterpret_cast<const uint8_t *>(ws_gate), reinterpret_cast<const uint8_t *>(ws_up),
+                  reinterpret_cast<const uint32_t *>(xq), ids, T, k, E, H, I, clamp, h);
+}
+
+extern "C" luce_status luce_moe_down_combine_q4k(const luce_block_q4_k *w_down, const luce_block_q4_k *ws_down,
+                                                 const luce_block_q8_1 *hq, const int32_t *ids, const float *weights,
+                                                 int T, int k, int E, int H, int I, float *out, void *stream)
+{
+    if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E || k > 64 || H <= 0 || I <= 0 || H % QKK != 0 ||
+        I % QKK != 0)
+        return LUCE_ERR_INVALID_ARG;
+    if (T == 0)
+        return LUCE_OK;
+    if (!w_down || !hq || !ids || !weights || !out || !aligned(w_down, 16) || (ws_down && !aligned(ws_down, 16)) ||
+        !aligned(hq, 4) || !aligned(ids, 4) || !aligned(weights, 4) || !aligned(out, 4))
+        return LUCE_ERR_INVALID_ARG;
+    if (T > 65535)
+        return LUCE_ERR_INVALID_ARG;
+    return launch(k_down_combine_q4k, dim3((unsigned)((H + WARPS - 1) / WARPS), (unsigned)T), dim3(WARPS * 32), 0,
+                  as_stream(stream), reinterpret_cast<const uint8_t *>(w_down),
+                  reinterpret_cast<const uint8_t *>(ws_down), reinterpret_cast<const uint32_t *>(hq), ids, weights, T,
+                  k, E, H, I, out);
+}

@@ -172,3 +172,20 @@ def test_edge_ops_validation(lib):
     a.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64, ctypes.c_void_p]
     assert a(G, _p(GOOD + 2), G, 8, None) == 1                     # misaligned b
     assert a(G, G, G, 0, None) == 0
+
+
+def test_q4k_validation(lib):
+    G = _p(GOOD)
+    g = lib.luce_moe_glu_q4k
+    g.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
+    assert g(G, G, G, G, G, G, 1, 2, 8, 2048 + 32, 1024, 0.0, G, None) == 1   # H % 256
+    assert g(G, G, G, G, G, G, 1, 2, 8, 2048, 1000, 0.0, G, None) == 1        # I % 256
+    assert g(G, G, G, None, G, G, 1, 2, 8, 2048, 1024, 0.0, G, None) == 1     # one shared matrix missing
+    assert g(_p(GOOD + 4), G, G, G, G, G, 1, 2, 8, 2048, 1024, 0.0, G, None) == 1  # 16-byte alignment
+    assert g(G, G, G, G, G, G, 1, 9, 8, 2048, 1024, 0.0, G, None) == 1        # k > E
+    assert g(G, G, G, G, G, G, 0, 2, 8, 2048, 1024, 0.0, G, None) == 0        # T = 0
+    d = lib.luce_moe_down_combine_q4k
+    d.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 + [ctypes.c_void_p] * 2
+    assert d(G, G, G, G, G, 1, 2, 8, 2048, 1000, G, None) == 1                # I % 256
+    assert d(G, None, G, G, None, 1, 2, 8, 2048, 1024, G, None) == 1          # weights missing
+    assert d(G, None, G, G, G, 0, 2, 8, 2048, 1024, G, None) == 0

@@ -1,0 +1,111 @@
+"""GPU: the Q4_K expert-weight path (luce_moe_glu_q4k, luce_quantize_q8_1 of
+h, luce_moe_down_combine_q4k) against the oracle: h within the float bound,
+hq exactly the q8_1 rule where the quantization is stable, out within the
+bound plus the allowance for q8_1 flips of h; masked routes untouched and
+skipped; the decode-layer shape and a verify-like shape."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_close, assert_hq_valid, chain_allowance, dev, host
+from quantized_moe_decode_luce_gb300 import binding as B
+from quantized_moe_decode_luce_gb300 import build as BLD
+from quantized_moe_decode_luce_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    BLD.build()
+    B.lib()
+    yield
+
+
+@pytest.fixture(autouse=True)
+def _no_device_faults():
+    yield
+    assert B.luce_get_fault() == 0
+
+
+# name, T, H, I, E, k, shared, clamp, masked route
+CASES = [
+    ("decode_shape", 1, 2048, 1024, 16, 6, True, 0.0, False),
+    ("verify_like", 5, 1024, 512, 12, 4, True, 10.0, False),
+    ("masked_no_shared", 3, 512, 256, 6, 2, False, 0.0, True),
+    ("wide_rows", 2, 4096, 256, 4, 2, True, 0.0, False),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_q4k_layer_matches_oracle(case):
+    name, T, H, I, E, k, shared, clamp, masked = case
+    wl = W.Workload(name, T=T, H=H, I=I, E=E, k=k, shared=shared, clamp=clamp, seed=800 + T * 10 + k, bias_std=0.1)
+    L = W.host_layer_q4k(wl)
+    ids, w = oracle.route_topk(L.logits, L.bias, k)
+    if masked:
+        ids[1, 0] = -1
+    w32 = w.astype(np.float32)
+    xq = oracle.quantize_q8_1(L.x)
+    rows = T * k + (T if shared else 0)
+    h_ref, h_terms = oracle.glu_q4k(L.wg, L.wu, L.wsg, L.wsu, xq, ids, E, H, I, clamp)
+
+    h = torch.full((rows, I), float("nan"), dtype=torch.float32, device="cuda")
+    B.luce_moe_glu_q4k(dev(L.wg), dev(L.wu), dev(L.wsg) if shared else None, dev(L.wsu) if shared else None, dev(xq),
+                       dev(ids), E, H, I, clamp, h)
+    hq = torch.zeros((rows, I // 32, 36), dtype=torch.uint8, device="cuda")
+    B.luce_quantize_q8_1(h.nan_to_num(0.0), hq)
+    torch.cuda.synchronize()
+    hg = host(h)
+    valid = ~np.isnan(h_ref[:, 0])
+    assert np.isnan(hg[~valid]).all(), "rows of masked routes must not be written"
+    assert_close(hg[valid], h_ref[valid], h_terms[valid], f"h ({name})")
+    h32 = np.nan_to_num(h_ref, nan=0.0).astype(np.float32)
+    allow = oracle.hq_flip_allowance(h32, oracle.tol(np.nan_to_num(h_terms, nan=0.0)))
+    hq_ref = oracle.quantize_q8_1(h32)
+    assert_hq_valid(host(hq)[valid], hq_ref[valid], allow[valid], f"hq ({name})")
+
+    # the down product and combine, fed the oracle's own hq (so the bound is the plain float rule)
+    out_ref, out_terms = oracle.down_combine_q4k(L.wd, L.wsd, hq_ref, ids, w32, E, H, I)
+    out = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+    B.luce_moe_down_combine_q4k(dev(L.wd), dev(L.wsd) if shared else None, dev(hq_ref), dev(ids), dev(w32), E, H, I,
+                                out)
+    torch.cuda.synchronize()
+    assert_close(host(out), out_ref, out_terms, f"out ({name})")
+
+    # and the whole chain on the GPU's own hq, with the allowance for flips of h
+    out2 = torch.empty_like(out)
+    B.luce_moe_down_combine_q4k(dev(L.wd), dev(L.wsd) if shared else None, hq, dev(ids), dev(w32), E, H, I, out2)
+    torch.cuda.synchronize()
+    allow_out = chain_allowance_q4k(L.wd, L.wsd, ids, w32, allow)
+    assert np.all(np.abs(host(out2) - out_ref) <= oracle.tol(out_terms) + allow_out)
+
+
+def chain_allowance_q4k(wd, wsd, ids, weights, h_allow):
+    """|out| change bound from flips of q8_1(h): sum_j |w_j| sum_i |Wd value| allow (values dequantized loosely:
+    |d sc q - dmin m| <= |d| 63 15 + |dmin| 63 per element)."""
+    T, k = ids.shape
+    H = wd.shape[1]
+
+    def bound_rows(W_rows):  # [H, I/256, 144] -> per-element magnitude bound [H, I]
+        d = np.abs(W_rows[..., 0:2].copy().view(np.float16).astype(np.float64))
+        dm = np.abs(W_rows[..., 2:4].copy().view(np.float16).astype(np.float64))
+        b = (d * 63 * 15 + dm * 63)[..., 0]
+        return np.repeat(b, 256, axis=-1)
+
+    out = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            e = ids[t, j]
+            if e < 0:
+                continue
+            a = h_allow[t * k + j]
+            if a.any():
+                out[t] += abs(float(weights[t, j])) * (bound_rows(wd[e]) @ a)
+        if wsd is not None:
+            a = h_allow[T * k + t]
+            if a.any():
+                out[t] += bound_rows(wsd) @ a
+    return out * 1.001
