@@ -346,6 +346,40 @@ def edge_ops_measure(dev, peak, stream):
                                                 "GBps": nbytes / (us * 1e-6) / 1e9,
                                                 "frac": nbytes / (us * 1e-6) / 1e9 / peak,
                                                 "bound": "hbm (latency-bound at this size)"}
+
+    # the Q4_K path at the decode shape: 64 routed experts + shared (230 MB,
+    # more than L2), six distinct routed experts drawn per step
+    E, H, I, k, N3 = 64, 2048, 1024, 6, 200
+
+    def q4k(rows, K):
+        b = torch.randint(0, 256, (rows, K // 256, 144), generator=g, device=dev, dtype=torch.uint8)
+        dd = (torch.rand((rows, K // 256, 2), generator=g, device=dev) * 1.9e-3 + 1e-4).half()
+        b[..., 0:4] = dd.view(torch.uint8).reshape(rows, K // 256, 4)
+        return b
+
+    wg, wu, wd = q4k(E * I, H), q4k(E * I, H), q4k(E * H, I)
+    wsg, wsu, wsd = q4k(I, H), q4k(I, H), q4k(H, I)
+    ids_all = torch.stack([torch.randperm(E, generator=g, device=dev)[:k] for _ in range(N3)]).int().view(N3, 1, k)
+    wts = torch.full((1, k), 1.0 / k, device=dev)
+    xq = torch.zeros((1, H // 32, 36), dtype=torch.uint8, device=dev)
+    Bd.luce_quantize_q8_1(torch.randn((1, H), generator=g, device=dev), xq)
+    hbuf = torch.zeros((k + 1, I), device=dev)
+    hq = torch.zeros((k + 1, I // 32, 36), dtype=torch.uint8, device=dev)
+    o = torch.empty((1, H), device=dev)
+    ids_v = [ids_all[i] for i in range(N3)]
+
+    def q4k_steps(a, b):
+        for i in range(a, b):
+            Bd.luce_moe_glu_q4k(wg, wu, wsg, wsu, xq, ids_v[i], E, H, I, 0.0, hbuf)
+            Bd.luce_quantize_q8_1(hbuf, hq)
+            Bd.luce_moe_down_combine_q4k(wd, wsd, hq, ids_v[i], wts, E, H, I, o)
+
+    us = timed_graph(q4k_steps, N3)
+    nbytes = (k + 1) * 3 * I * (H // 256) * 144 + H // 32 * 36 + (k + 1) * I * 4 + H * 4
+    out["Q4_K layer (k_glu_q4k + k_quantize_q8_1 + k_down_combine_q4k)"] = {
+        "workload": "T=1 H=2048 I=1024 E=64 k=6 + shared, Q4_K weights", "avg_step_us": us, "launches": 3,
+        "bytes_per_step": nbytes, "GBps": nbytes / (us * 1e-6) / 1e9, "frac": nbytes / (us * 1e-6) / 1e9 / peak,
+        "bound": "hbm"}
     return out
 
 
