@@ -145,18 +145,29 @@ __global__ void __launch_bounds__(WARPS * 32)
     const size_t rowb = (size_t)(I / QKK) * Q4K_BYTES;
     const size_t hrow = (size_t)(I / QK) * Q8_1_WORDS;
     float acc = 0.0f;
-    for (int j = 0; j < k; j++) {
-        const int r = t * k + j;
-        const int e = ids[r];
-        if (e < 0)
-            continue;
-        if (e >= E) {
-            if (lane == 0 && n == 0)
+    // SB slots at a time: their lane dots do not depend on one another, so
+    // the loads of all of them are in flight together; the sums then join
+    // the combine in slot order
+    constexpr int SB = 8;
+    for (int j0 = 0; j0 < k; j0 += SB) {
+        float yl[SB];
+        bool live[SB];
+#pragma unroll
+        for (int jj = 0; jj < SB; jj++) {
+            const int j = j0 + jj;
+            const int e = j < k ? ids[t * k + j] : -1;
+            if (e >= E && lane == 0 && n == 0)
                 atomicOr(&g_fault_word, LUCE_FAULT_BAD_ID);
-            continue;
+            live[jj] = e >= 0 && e < E;
+            yl[jj] = live[jj] ? q4k_lane_dot(wd + ((size_t)e * H + n) * rowb, hq + (size_t)(t * k + j) * hrow, I, lane)
+                              : 0.0f;
         }
-        const float y = warp_sum(q4k_lane_dot(wd + ((size_t)e * H + n) * rowb, hq + (size_t)r * hrow, I, lane));
-        acc = __fadd_rn(acc, __fmul_rn(weights[r], y));
+#pragma unroll
+        for (int jj = 0; jj < SB; jj++) {
+            const float y = warp_sum(yl[jj]);
+            if (live[jj])
+                acc = __fadd_rn(acc, __fmul_rn(weights[t * k + j0 + jj], y));
+        }
     }
     if (wsd) {
         const float y = warp_sum(q4k_lane_dot(wsd + (size_t)n * rowb, hq + ((size_t)T * k + t) * hrow, I, lane));
