@@ -393,7 +393,6 @@ def test_argmax_bit_exact(R, V, kind):
         torch.cuda.synchronize()
         assert np.array_equal(host(idx), ref_i)
         assert np.array_equal(host(val).view(np.uint32), ref_v.view(np.uint32))
-    assert int(am.workspace[-64:].sum()) == 0 or True
 
 
 # ----------------------------------------------------------------------------- fused prep
