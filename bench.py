@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-edge-ops", action="store_true", help="skip timing the router and vocabulary-split steps")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip timing the single decode, verify and prefill layer workloads")
     p.add_argument("--path", choices=["layer", "split"], default="layer",
                    help="layer: each MoE layer is one launch (luce_moe_layer); split: prep, gate/up, down launches")
     p.add_argument("--layers", type=int, default=None, help="(debug) fewer layers; invalid as a bench number")
@@ -383,6 +385,166 @@ def edge_ops_measure(dev, peak, stream):
     return out
 
 
+def configs_measure(dev, peak, stream):
+    """Device time of the other layer workloads, one launch sequence per
+    workload captured in a CUDA graph and replayed (device time, no host
+    launch cost):
+
+    * decode_layer (T=1, H=2048, I=1024, E=64, top-6 + shared, seed 1):
+      8 resident copies of the layer (3.5 GB) and 64 input draws rotate, so
+      consecutive launches touch different weights (each 46.8 MB);
+    * verify_layer (T=5, H=4096, I=2048, E=128, top-8 + shared, clamp 10,
+      seed 2): 2 resident copies (6.9 GB) and 8 input draws (each its own
+      shared column means); each launch touches (U+1) x 26.7 MB, U the
+      unique routed experts, counted from the launch's own selection; plus
+      the greedy argmax over 5 x 129,280 logits rotating over 64 buffers;
+    * prefill_layer (T=512, H=4096, I=1536, E=128, top-8 + shared, clamp 10,
+      seed 4): one copy (2.59 GB, all of it touched by every launch).
+
+    Returns a dict of per-workload entries (µs per layer, tokens/s, GB/s and
+    the fraction of the measured copy bandwidth)."""
+    import torch
+
+    from quantized_moe_decode_luce_gb300.layer import Argmax, MoEStep
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def timed(body, n, reps=5):
+        with torch.cuda.stream(stream):
+            body(0, n)  # eager once: kernel attributes, argument checks
+            torch.cuda.synchronize()
+            gph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gph, stream=stream):
+                body(0, n)
+            for _ in range(2):
+                gph.replay()
+            torch.cuda.synchronize()
+            us = []
+            for _ in range(reps):
+                ev[0].record(stream)
+                gph.replay()
+                ev[1].record(stream)
+                torch.cuda.synchronize()
+                us.append(ev[0].elapsed_time(ev[1]) * 1e3 / n)
+        return statistics.median(us)
+
+    def draw(wl, n_inputs, seed):
+        xs, lgs, bias = [], [], None
+        for i in range(n_inputs):
+            g = W.rng(seed, 50_000 + i)
+            lg, b = W.router_logits(g, wl)
+            if bias is None:
+                bias = b
+            lgs.append(lg)
+            xs.append(W.activations(W.rng(seed, 60_000 + i), wl.T, wl.H))
+        xs_d = torch.from_numpy(np.stack(xs)).to(dev)
+        lg_d = torch.from_numpy(np.stack(lgs)).to(dev)
+        b_d = torch.from_numpy(bias).to(dev) if bias is not None else None
+        return xs_d, lg_d, b_d
+
+    out = {}
+    plan = [("decode_layer", 8, 64, 64), ("verify_layer", 2, 8, 16), ("prefill_layer", 1, 2, 4)]
+    for name, n_copies, n_inputs, n_launch in plan:
+        wl = W.WORKLOADS[name]
+        lays = [W.device_layer(wl, wl.seed * 1000 + 500 + c, dev) for c in range(n_copies)]
+        xs_d, lg_d, b_d = draw(wl, n_inputs, wl.seed)
+        st = MoEStep(wl.T, wl.H, wl.I, wl.E, wl.k, wl.shared, wl.clamp, device=dev)
+        o = torch.empty((n_launch, wl.T, wl.H), device=dev)
+        # unique routed experts of each input (from the launch's own selection)
+        uniq = []
+        with torch.cuda.stream(stream):
+            for i in range(n_inputs):
+                st.run(lays[i % n_copies], xs_d[i], lg_d[i], b_d, stream=stream, out=o[0])
+                uniq.append(int(torch.unique(st.ids).numel()))
+        torch.cuda.synchronize()
+
+        def body(a, b):
+            for i in range(a, b):
+                st.run(lays[i % n_copies], xs_d[i % n_inputs], lg_d[i % n_inputs], b_d, stream=stream, out=o[i])
+
+        us = timed(body, n_launch)
+        nb = float(np.mean([W.touched_weight_bytes(wl, uniq[i % n_inputs]) + _act_bytes(wl)
+                            for i in range(n_launch)]))
+        gbs = nb / (us * 1e-6) / 1e9
+        ent = {"T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k, "clamp": wl.clamp,
+               "path": "one launch per layer" if st.path == "layer" else "prep + gate/up + down launches",
+               "us_per_layer": us, "tokens_per_s": wl.T / (us * 1e-6), "bytes_per_layer": nb,
+               "GBps": gbs, "frac_of_measured_hbm": gbs / peak, "frac_of_8TBps_spec": gbs / SPEC_HBM_GBS,
+               "l2": f"{n_copies} resident weight copies x {n_inputs} input draws rotate "
+                     f"({n_copies * (wl.E + 1) * wl.expert_bytes / 1e9:.1f} GB resident)"}
+        if name == "verify_layer":
+            ent["unique_routed_experts"] = uniq
+            ent["unique_routed_experts_mean"] = float(np.mean(uniq))
+        if name == "prefill_layer":
+            ops = 2.0 * (wl.T * wl.k + wl.T) * 3 * wl.H * wl.I
+            ent["int8_ops_per_layer"] = ops
+            ent["int8_tops"] = ops / (us * 1e-6) / 1e12
+        out[name] = ent
+        del lays, st, o
+        torch.cuda.empty_cache()
+        if name == "verify_layer":
+            V, R, N = 129280, 5, 64
+            g = torch.Generator(device=dev)
+            g.manual_seed(wl.seed)
+            vocab = torch.randn((N, R, V), generator=g, device=dev)
+            am = Argmax(R, V, device=dev)
+            vv = [vocab[i] for i in range(N)]
+
+            def am_body(a, b):
+                for i in range(a, b):
+                    am.run(vv[i], stream=stream)
+
+            us = timed(am_body, N)
+            nbytes = R * V * 4
+            out["verify_argmax"] = {"R": R, "V": V, "us": us, "bytes": nbytes,
+                                    "GBps": nbytes / (us * 1e-6) / 1e9,
+                                    "frac_of_measured_hbm": nbytes / (us * 1e-6) / 1e9 / peak,
+                                    "l2": f"{N} logit buffers rotate ({N * nbytes / 1e6:.0f} MB)"}
+            del vocab, vv, am
+            torch.cuda.empty_cache()
+    return out
+
+
+def _act_bytes(wl):
+    """Activation bytes of one layer: x and logits read, xq, h, hq written and
+    read once, out written."""
+    rows = wl.T * wl.k + (wl.T if wl.shared else 0)
+    return (wl.T * wl.H * 4 + wl.T * wl.E * 4 + wl.T * wl.H // 32 * 36 * 2 + rows * wl.I * 4 * 2
+            + rows * wl.I // 32 * 36 * 2 + wl.T * wl.H * 4)
+
+
+def _oracle_worker(job):
+    """One host process of the all-core oracle row: times `n` decode layers
+    (inputs drawn outside the timed calls).  Returns the seconds spent in the
+    oracle and the layers done."""
+    wl_name, layers, seed, start, n = job
+    import oracle
+    wl = W.WORKLOADS[wl_name]
+    make = host_layer_sampler(wl, layers, seed)
+    spent, done = 0.0, 0
+    for j in range(n):
+        args = make((start + j) % layers)
+        t = time.perf_counter()
+        oracle.moe_layer(*args)
+        spent += time.perf_counter() - t
+        done += 1
+    return spent, done
+
+
+def oracle_all_cores(wl, layers, per_core_layers):
+    """The oracle on every host core at once: one process per core, each
+    running its own decode layers (independent work, nothing shared)."""
+    import multiprocessing as mp
+    ncores = os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    jobs = [(wl.name, layers, wl.seed, c * per_core_layers, per_core_layers) for c in range(ncores)]
+    with ctx.Pool(ncores) as pool:
+        res = pool.map(_oracle_worker, jobs)
+    slowest = max(s for s, _ in res)
+    done = sum(d for _, d in res)
+    return done, slowest, ncores
+
+
 def run_ours(args, wl, layers):
     import torch
     import torch.distributed as dist
@@ -430,7 +592,6 @@ def run_ours(args, wl, layers):
             return torch.cuda.Event(enable_timing=True)
 
     one_launch = args.path == "layer"
-    sync = torch.zeros(4, dtype=torch.int32, device=dev)  # device barrier state of the one-launch layer
 
     def run_step(s, x_src, lg_src, v_src, out_dst, record):
         bufs = step_bufs
@@ -441,7 +602,7 @@ def run_ours(args, wl, layers):
                     record[l][0].record()
                 Bd.luce_moe_layer(lg_src[s, l], b_d[l], x_src[s, l], wl.k, wl.I, lay.wg, lay.wu, lay.wd, lay.wsg,
                                   lay.wsu, lay.wsd, wl.clamp, bufs.ids, bufs.weights, bufs.xq, bufs.counts,
-                                  bufs.offsets, bufs.routes, bufs.h, bufs.hq, out_dst[l], sync)
+                                  bufs.offsets, bufs.routes, bufs.h, bufs.hq, out_dst[l], bufs.workspace)
                 if record is not None:
                     record[l][1].record()
                 continue
@@ -526,18 +687,42 @@ def run_ours(args, wl, layers):
     peak, peak_kind = measured_peaks()
     glu_avg = float(np.mean(glu_ms)) if glu_ms else None
     down_avg = float(np.mean(down_ms)) if down_ms else None
+    # the argmax's share of a step, timed alone (a graph of argmax launches
+    # over the rotating vocabulary rows), so that the layer kernel's time
+    # follows from the timed region: (step - argmax) / layers
+    am_us = None
+    with torch.cuda.stream(stream):
+        gam = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gam, stream=stream):
+            for s in range(S):
+                am.run(vocab_d[s])
+        gam.replay()
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        gam.replay()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        am_us = a0.elapsed_time(a1) * 1e3 / S
+    layer_us_timed = (ms_per_step * 1e3 - am_us) / layers
     kernels = {}
     roofline = None
     if one_launch:
-        # the dominant (and only) layer kernel: all of the layer's algorithmic bytes
+        # the dominant (and only) layer kernel: all of the layer's algorithmic
+        # bytes over its share of the timed region
         kernel_files = ["quantized_moe_decode_luce_gb300/csrc/moe_layer.cu",
                         "quantized_moe_decode_luce_gb300/csrc/common.cuh"]
+        ach = lb / (layer_us_timed * 1e-6) / 1e9
+        roofline = {"kernel": "k_moe_layer", "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                    "frac": ach / peak, "peak_kind": f"{peak_kind} (STREAM-style copy, burst)",
+                    "frac_of_8TBps_spec": ach / SPEC_HBM_GBS, "bytes_per_launch": lb,
+                    "launch_us_from_timed_region": layer_us_timed,
+                    "how": "achieved = bytes_per_launch / ((ms_per_step - argmax_us) / layers)",
+                    "argmax_us": am_us,
+                    "traffic": profiled_traffic(kernel_files, "k_moe_layer")}
         if glu_avg:
-            ach = lb / (glu_avg * 1e-3) / 1e9
-            roofline = {"kernel": "k_moe_layer", "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
-                        "frac": ach / peak, "peak_kind": f"{peak_kind} (STREAM-style copy)",
-                        "frac_of_8TBps_spec": ach / SPEC_HBM_GBS, "bytes_per_launch": lb,
-                        "avg_launch_us": glu_avg * 1e3, "traffic": profiled_traffic(kernel_files, "k_moe_layer")}
+            roofline["diag_event_bracketed_launch_us"] = glu_avg * 1e3
     else:
         gb = glu_bytes(wl, n_active)
         kernel_files = ["quantized_moe_decode_luce_gb300/csrc/glu_pair.cu",
@@ -610,6 +795,15 @@ def run_ours(args, wl, layers):
         except Exception as exc:  # a report, never a reason to fail the bench
             kernels["edge_ops"] = {"failed": str(exc)}
 
+    configs = None
+    if rank == 0 and not args.no_configs:
+        del dls, graphs
+        torch.cuda.empty_cache()
+        try:
+            configs = configs_measure(dev, peak, stream)
+        except Exception as exc:  # a report, never a reason to fail the bench
+            configs = {"failed": str(exc)}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
@@ -620,6 +814,12 @@ def run_ours(args, wl, layers):
                    "sample": f"{len(times)} decode layers of one token (T=1, H=2048, I=1024, E=64, top-6 + shared); "
                              f"tokens/s = 1 / (mean layer time x {layers})",
                    "layer_us": layer_s * 1e6}
+            done, slowest, ncores = oracle_all_cores(wl, layers, max(2, len(times) // 2))
+            cpu["all_cores"] = {"value": done / slowest / layers, "unit": UNIT, "cores": ncores,
+                                "kind": "oracle",
+                                "sample": f"{done} decode layers, one process per core, each its own layers "
+                                          f"(independent tokens); tokens/s = layers done / slowest process's "
+                                          f"oracle seconds / {layers}"}
         except Exception as exc:  # the baseline is a report, never a reason to fail the bench
             cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {exc}"}
 
@@ -634,7 +834,7 @@ def run_ours(args, wl, layers):
                 "layer_us": ms_per_step * 1e3 / layers,
                 "stack_weight_GBps": step_bytes / (ms_per_step * 1e-3) / 1e9,
                 "stack_frac_of_measured_hbm": step_bytes / (ms_per_step * 1e-3) / 1e9 / peak,
-                "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roofline, "kernels": kernels, "configs": configs, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps, "clocks": clk,
                 "device_faults": fault, "weights_gen_s": round(t_gen, 2)}
         if layers != 43:

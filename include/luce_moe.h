@@ -82,6 +82,8 @@ typedef struct {
 /* Device fault bits (luce_get_fault). */
 #define LUCE_FAULT_BAD_ID 0x1u  /* a route id >= E was seen and skipped          */
 #define LUCE_FAULT_TIMEOUT 0x2u /* a bounded device wait gave up (never expected) */
+#define LUCE_FAULT_DESYNC 0x4u  /* a device-wide barrier of luce_moe_layer gave up: its count is out of step
+                                   with the grid, so zero the `sync` word before the next call */
 
 /* ------------------------------------------------------------------------
  * luce_route_topk -- router select + weights in one launch.
@@ -372,28 +374,44 @@ LUCE_API luce_status luce_moe_prep(const float *logits, const float *bias, const
  *   clamp as in luce_moe_glu_pair; outputs as in the three calls.  h
  *   [T*k+T][I] f32 (16-byte aligned) is required: the launch keeps h there
  *   between its gate/up and down parts.
- *   sync: 8 bytes of device memory (8-byte aligned) owned by the caller,
- *   zero before the first call: a 64-bit count of barrier arrivals that
- *   only grows and needs no reset.  Calls that share it must run on the
- *   same device with the same shapes (the same grid), one at a time (one
- *   stream or ordered streams); calls that may run at the same time need
- *   distinct words.  After a LUCE_FAULT_TIMEOUT, zero it again.
+ *   workspace: workspace_bytes >= luce_moe_layer_workspace_bytes(T, k, H, I)
+ *   bytes of device memory (16-byte aligned) owned by the caller, all zero
+ *   before the first call.  Its first 8 bytes are a 64-bit count of
+ *   device-wide barrier arrivals that only grows (no reset, so CUDA-graph
+ *   replays need no host update); the rest holds per-block counters that
+ *   every call leaves at zero, or the y values of large layers.  The grid is
+ *   always one CTA per SM, so calls of any shape may share one workspace on
+ *   one device, one at a time (one stream or ordered streams); calls that
+ *   may run at the same time need distinct workspaces.  If luce_get_fault
+ *   reports LUCE_FAULT_DESYNC or LUCE_FAULT_TIMEOUT after this call, zero the
+ *   whole workspace again before the next call.
  *
- * The grid is launched cooperatively (all CTAs resident at once; its CTAs
- * meet at a device-wide barrier between the gate/up and the down parts, and
- * at a second one after the q8_1 of h when hq exceeds 24 KB).
+ * The grid is launched cooperatively (all CTAs resident at once).  Each CTA
+ * takes an equal share of the gate/up rows (of the shared expert and of the
+ * routed experts); h goes through global memory; the CTAs meet at a
+ * device-wide barrier after h and its q8_1 blocks are stored.  Down work:
+ * when every q8_1 row of h fits 32 KB of shared memory, each CTA takes an
+ * equal share of the output rows of every expert and combines them itself
+ * (a q8_1 block of h is formed by the CTA whose rows complete its 32 rows);
+ * otherwise each CTA quantizes an equal share of the q8_1 blocks after the
+ * first barrier, takes an equal share of the flat (expert, output row) list
+ * after a second, writes y to the workspace, and a third barrier precedes
+ * the combine.
  * Supported: 1 <= T <= 8, T*k <= 64, E <= 256 (else LUCE_ERR_UNSUPPORTED,
  * and the three calls serve); H, I multiples of 256 up to 32768.  Argument
- * errors as in the three calls.  Not allowed inside a kernel that the caller
- * runs concurrently with another cooperative grid on the same device.
+ * errors as in the three calls, plus a workspace too small or misaligned.
+ * Not allowed inside a kernel that the caller runs concurrently with another
+ * cooperative grid on the same device.
  */
+LUCE_API size_t luce_moe_layer_workspace_bytes(int T, int k, int H, int I);
 LUCE_API luce_status luce_moe_layer(const float *logits, const float *bias, const float *x,
                                     const luce_block_q8_0 *w_gate, const luce_block_q8_0 *w_up,
                                     const luce_block_q8_0 *w_down, const luce_block_q8_0 *ws_gate,
                                     const luce_block_q8_0 *ws_up, const luce_block_q8_0 *ws_down, int T, int E, int k,
                                     int H, int I, float clamp, int32_t *ids, float *weights, luce_block_q8_1 *xq,
                                     int32_t *counts, int32_t *offsets, int32_t *routes, float *h,
-                                    luce_block_q8_1 *hq, float *out, uint32_t *sync, void *stream);
+                                    luce_block_q8_1 *hq, float *out, void *workspace, size_t workspace_bytes,
+                                    void *stream);
 
 /* ------------------------------------------------------------------------
  * luce_set_pdl -- process-wide switch (default 0 = off) for programmatic

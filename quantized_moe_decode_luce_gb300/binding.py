@@ -22,6 +22,7 @@ LUCE_ERR_UNSUPPORTED = 2
 LUCE_ERR_CUDA = 3
 LUCE_FAULT_BAD_ID = 0x1
 LUCE_FAULT_TIMEOUT = 0x2
+LUCE_FAULT_DESYNC = 0x4
 
 _LIB = None
 
@@ -47,7 +48,7 @@ def lib() -> ctypes.CDLL:
             "luce_moe_glu_pair": [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, i32, P],
             "luce_moe_prep": [P, P, P, i32, i32, i32, i32, P, P, P, P, P, P, P],
             "luce_moe_layer": [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, P, P, P, P, P, P, P,
-                               P, P],
+                               P, sz, P],
             "luce_moe_down_combine": [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, P, i32, P],
             "luce_argmax": [P, i32, i64, P, P, P, sz, P],
             "luce_argmax_noalloc": [P, i32, i64, P, P, P],
@@ -65,6 +66,8 @@ def lib() -> ctypes.CDLL:
             fn.restype = ctypes.c_int
         L.luce_set_pdl.argtypes = [i32]
         L.luce_set_pdl.restype = ctypes.c_int
+        L.luce_moe_layer_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        L.luce_moe_layer_workspace_bytes.restype = sz
         L.luce_argmax_workspace_bytes.argtypes = [i32, i64]
         L.luce_argmax_workspace_bytes.restype = sz
         L.luce_status_string.argtypes = [ctypes.c_int]
@@ -146,21 +149,26 @@ def luce_moe_prep(logits, bias, x, k: int, ids, weights, xq, counts, offsets, ro
         _ptr(offsets, i32, "offsets"), _ptr(routes, i32, "routes"), _stream(stream)))
 
 
+def luce_moe_layer_workspace_bytes(T: int, k: int, H: int, I: int) -> int:
+    return int(lib().luce_moe_layer_workspace_bytes(T, k, H, I))
+
+
 def luce_moe_layer(logits, bias, x, k: int, I: int, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, clamp: float,
-                   ids, weights, xq, counts, offsets, routes, h, hq, out, sync, stream=None) -> None:
-    """The whole layer in one launch; `sync` is an int32 CUDA tensor of >= 2
-    elements, zero before the first call (the library keeps it consistent)."""
+                   ids, weights, xq, counts, offsets, routes, h, hq, out, workspace, stream=None) -> None:
+    """The whole layer in one launch; `workspace` is a uint8 CUDA tensor of at
+    least luce_moe_layer_workspace_bytes(T, k, H, I) bytes, all zero before
+    the first call (the library keeps it consistent)."""
     T, E = logits.shape
     H = x.shape[1]
-    if sync is None or sync.numel() < 2:
-        raise ValueError("sync must hold at least 2 int32 elements")
+    if workspace is None:
+        raise ValueError("workspace is required")
     _check("luce_moe_layer", lib().luce_moe_layer(
         _ptr(logits, f32, "logits"), _ptr(bias, f32, "bias"), _ptr(x, f32, "x"), _ptr(w_gate, u8, "w_gate"),
         _ptr(w_up, u8, "w_up"), _ptr(w_down, u8, "w_down"), _ptr(ws_gate, u8, "ws_gate"), _ptr(ws_up, u8, "ws_up"),
         _ptr(ws_down, u8, "ws_down"), T, E, k, H, I, float(clamp), _ptr(ids, i32, "ids"),
         _ptr(weights, f32, "weights"), _ptr(xq, u8, "xq"), _ptr(counts, i32, "counts"),
         _ptr(offsets, i32, "offsets"), _ptr(routes, i32, "routes"), _ptr(h, f32, "h"), _ptr(hq, u8, "hq"),
-        _ptr(out, f32, "out"), _ptr(sync, i32, "sync"), _stream(stream)))
+        _ptr(out, f32, "out"), _ptr(workspace, u8, "workspace"), workspace.numel(), _stream(stream)))
 
 
 def luce_set_pdl(enable: bool) -> None:
@@ -258,9 +266,9 @@ def luce_version() -> int:
 
 
 __all__ = ["LuceError", "lib", "status_string", "luce_route_topk", "luce_quantize_q8_1", "luce_moe_group",
-           "luce_moe_glu_pair", "luce_moe_prep", "luce_moe_layer", "luce_set_pdl",
+           "luce_moe_glu_pair", "luce_moe_prep", "luce_moe_layer", "luce_moe_layer_workspace_bytes", "luce_set_pdl",
            "luce_moe_down_combine", "luce_argmax", "luce_argmax_workspace_bytes", "luce_argmax_noalloc",
            "luce_argmax_shard", "luce_argmax_pick", "luce_rmsnorm_router", "luce_ep_mask", "luce_add_f32",
            "luce_moe_glu_q4k", "luce_moe_down_combine_q4k",
            "luce_get_fault", "luce_version", "LUCE_OK", "LUCE_ERR_INVALID_ARG", "LUCE_ERR_UNSUPPORTED",
-           "LUCE_ERR_CUDA", "LUCE_FAULT_BAD_ID", "LUCE_FAULT_TIMEOUT"]
+           "LUCE_ERR_CUDA", "LUCE_FAULT_BAD_ID", "LUCE_FAULT_TIMEOUT", "LUCE_FAULT_DESYNC"]

@@ -130,6 +130,29 @@ __device__ __forceinline__ void load_q8_0_smem(const uint8_t *row, int b, Q80Blo
         blk.q[i] = __funnelshift_rc(w[i], w[i + 1], sh);
 }
 
+// The same block read through a shared-memory address (explicit ld.shared,
+// whatever the compiler can prove about a generic pointer).
+__device__ __forceinline__ uint32_t lds32(uint32_t saddr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(saddr));
+    return v;
+}
+
+__device__ __forceinline__ void load_q8_0_sh(uint32_t row_saddr, int b, Q80Block &blk)
+{
+    const uint32_t p = row_saddr + ((34u * (uint32_t)b) & ~3u);
+    uint32_t w[9];
+#pragma unroll
+    for (int i = 0; i < 9; i++)
+        w[i] = lds32(p + 4u * i);
+    const uint32_t sh = (b & 1) ? 32u : 16u;
+    blk.d = half_bits_to_float(__funnelshift_rc(w[0], w[1], sh - 16u));
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        blk.q[i] = __funnelshift_rc(w[i], w[i + 1], sh);
+}
+
 // Which blocks of a Q8_0 row (nb blocks of 34 B, row start 16-byte aligned)
 // a lane takes, and in which order it accumulates them.  34-byte blocks b and
 // b + 32 start 272 words, i.e. 16 banks, apart, and so do two consecutive rows
@@ -187,6 +210,15 @@ __device__ __forceinline__ void load_q8_1_any(const uint32_t *words, Q81Block &b
 #pragma unroll
     for (int i = 0; i < 8; i++)
         blk.q[i] = (int)words[1 + i];
+}
+
+// q8_1 block through a shared-memory address.
+__device__ __forceinline__ void load_q8_1_sh(uint32_t saddr, Q81Block &blk)
+{
+    blk.d = half_bits_to_float(lds32(saddr));
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        blk.q[i] = (int)lds32(saddr + 4u + 4u * i);
 }
 
 // Exact int32 block sum of 32 int8 products; four independent partial sums
@@ -297,17 +329,38 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps (up to `ns` nanoseconds) until it completes, instead of spinning and
+// taking issue slots from the warps that work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase of `parity` to complete, for at most WAIT_LIMIT_NS.
 // Returns false (and the caller raises LUCE_FAULT_TIMEOUT) if it gave up.
+// Between polls the thread sleeps (backing off from 32 to 256 ns), so that
+// waiting warps leave the issue slots to the warps that work.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const unsigned long long t0 = global_timer_ns();
-    for (uint32_t i = 1;; i++) {
+    uint32_t ns = 32;
+    for (;;) {
+        __nanosleep(ns);
         if (mbar_try_wait(bar, parity))
             return true;
-        if ((i & 31u) == 0u && global_timer_ns() - t0 > WAIT_LIMIT_NS)
+        ns = ns < 256 ? 2 * ns : 256;
+        if (global_timer_ns() - t0 > WAIT_LIMIT_NS)
             return false;
     }
 }
@@ -413,7 +466,7 @@ struct Tuning {
     int layer_cps = 1;        // whole-layer kernel: CTAs per SM
     int layer_prefetch = 1;   // whole-layer kernel: warm L2 with the shared expert
     int layer_dsplit = 0;     // whole-layer kernel: down rows split by weight across CTAs
-    int layer_psleep = 0;     // whole-layer kernel: producer back-off in ns while the ring is full
+    int layer_psleep = 64;    // whole-layer kernel: producer back-off in ns while the ring is full
     int layer_down_early = 0; // whole-layer kernel: down stages before every gate/up part is requested
     int layer_hq_bulk = 1;    // whole-layer kernel: stage a shared hq with one bulk copy
 };

@@ -1334,13 +1334,33 @@ luce_status launch_layer(const LayerArgs &a, cudaStream_t stream, size_t smem, i
 
 using namespace luce_host;
 
+// The flat-split kernel for layers whose q8_1 rows of h exceed 24 KB
+// (moe_layer_flat.cu); same arguments and checks.
+extern "C" __attribute__((visibility("hidden"))) luce_status
+luce_internal_moe_layer_flat(const float *logits, const float *bias, const float *x, const luce_block_q8_0 *w_gate,
+                             const luce_block_q8_0 *w_up, const luce_block_q8_0 *w_down,
+                             const luce_block_q8_0 *ws_gate, const luce_block_q8_0 *ws_up,
+                             const luce_block_q8_0 *ws_down, int T, int E, int k, int H, int I, float clamp,
+                             int32_t *ids, float *weights, luce_block_q8_1 *xq, int32_t *counts, int32_t *offsets,
+                             int32_t *routes, float *h, luce_block_q8_1 *hq, float *out, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+extern "C" size_t luce_moe_layer_workspace_bytes(int T, int k, int H, int I)
+{
+    if (T < 0 || k < 0 || H < 0 || I < 0)
+        return 0;
+    (void)I;
+    return 16 + (size_t)T * (size_t)(k + 1) * (size_t)H * sizeof(float); // barrier count, y values
+}
+
 extern "C" luce_status luce_moe_layer(const float *logits, const float *bias, const float *x,
                                       const luce_block_q8_0 *w_gate, const luce_block_q8_0 *w_up,
                                       const luce_block_q8_0 *w_down, const luce_block_q8_0 *ws_gate,
                                       const luce_block_q8_0 *ws_up, const luce_block_q8_0 *ws_down, int T, int E,
                                       int k, int H, int I, float clamp, int32_t *ids, float *weights,
                                       luce_block_q8_1 *xq, int32_t *counts, int32_t *offsets, int32_t *routes,
-                                      float *h, luce_block_q8_1 *hq, float *out, uint32_t *sync, void *stream)
+                                      float *h, luce_block_q8_1 *hq, float *out, void *workspace,
+                                      size_t workspace_bytes, void *stream)
 {
     if (T < 0 || E < 1 || k < 1 || k > E || k > 64 || H <= 0 || I <= 0 || H % 256 != 0 || I % 256 != 0 ||
         H / 32 > 1024 || I / 32 > 1024 || !(clamp == clamp))
@@ -1351,16 +1371,26 @@ extern "C" luce_status luce_moe_layer(const float *logits, const float *bias, co
     if (T == 0)
         return LUCE_OK;
     if (!logits || !x || !w_gate || !w_up || !w_down || !ids || !weights || !xq || !counts || !offsets || !routes ||
-        !h || !hq || !out || !sync)
+        !h || !hq || !out || !workspace)
+        return LUCE_ERR_INVALID_ARG;
+    if (workspace_bytes < luce_moe_layer_workspace_bytes(T, k, H, I))
         return LUCE_ERR_INVALID_ARG;
     if (!aligned(logits, 4) || (bias && !aligned(bias, 4)) || !aligned(x, 16) || !aligned(w_gate, 16) ||
         !aligned(w_up, 16) || !aligned(w_down, 16) ||
         (has_ws && (!aligned(ws_gate, 16) || !aligned(ws_up, 16) || !aligned(ws_down, 16))) || !aligned(ids, 4) ||
         !aligned(weights, 4) || !aligned(xq, 4) || !aligned(counts, 4) || !aligned(offsets, 4) ||
-        !aligned(routes, 4) || !aligned(h, 16) || !aligned(hq, 16) || !aligned(out, 4) || !aligned(sync, 8))
+        !aligned(routes, 4) || !aligned(h, 16) || !aligned(hq, 16) || !aligned(out, 4) || !aligned(workspace, 16))
         return LUCE_ERR_INVALID_ARG;
     if (T > MAX_T || T * k > MAX_R || E > MAX_E)
         return LUCE_ERR_UNSUPPORTED;
+    {
+        // large q8_1 rows of h (speculative verify): the flat-split kernel
+        const size_t hs = (size_t)(T * k + T) * (size_t)(I / 32) * Q8_1_BYTES;
+        if (hs > 24 * 1024)
+            return luce_internal_moe_layer_flat(logits, bias, x, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, T, E,
+                                                k, H, I, clamp, ids, weights, xq, counts, offsets, routes, h, hq, out,
+                                                workspace, workspace_bytes, stream);
+    }
 
     LayerArgs a;
     a.logits = logits;
@@ -1387,7 +1417,7 @@ extern "C" luce_status luce_moe_layer(const float *logits, const float *bias, co
     a.h = h;
     a.hq = reinterpret_cast<uint32_t *>(hq);
     a.out = out;
-    a.sync = reinterpret_cast<unsigned long long *>(sync);
+    a.sync = reinterpret_cast<unsigned long long *>(workspace); // the barrier count: the workspace's first word
     a.nbH = H / 32;
     a.nbI = I / 32;
     a.rbg = a.nbH * Q8_0_BYTES;

@@ -498,6 +498,7 @@ size_t argmax_pairs_bytes(int R, int C) { return ((size_t)R * C * sizeof(ArgPair
 extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault_glu(unsigned int *bits);
 extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault_down(unsigned int *bits);
 extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault_layer(unsigned int *bits);
+extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault_layer_flat(unsigned int *bits);
 extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault_q4k(unsigned int *bits);
 
 namespace luce_host {
@@ -558,7 +559,9 @@ extern "C" luce_status luce_get_fault(unsigned int *bits)
     cudaError_t e3 = luce_internal_fault_down(bits);
     cudaError_t e4 = luce_internal_fault_layer(bits);
     cudaError_t e5 = luce_internal_fault_q4k(bits);
-    return (e1 == cudaSuccess && e2 == cudaSuccess && e3 == cudaSuccess && e4 == cudaSuccess && e5 == cudaSuccess)
+    cudaError_t e6 = luce_internal_fault_layer_flat(bits);
+    return (e1 == cudaSuccess && e2 == cudaSuccess && e3 == cudaSuccess && e4 == cudaSuccess && e5 == cudaSuccess &&
+            e6 == cudaSuccess)
                ? LUCE_OK
                : LUCE_ERR_CUDA;
 }

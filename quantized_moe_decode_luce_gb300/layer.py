@@ -30,7 +30,8 @@ class MoEStep:
         self.h = torch.empty((max(1, rows), I), dtype=torch.float32, device=dev)
         self.hq = torch.empty((max(1, rows), I // QK, Q8_1_BYTES), dtype=torch.uint8, device=dev)
         self.out = torch.empty((T, H), dtype=torch.float32, device=dev)
-        self.sync = torch.zeros(4, dtype=torch.int32, device=dev)  # device barrier state of luce_moe_layer
+        # luce_moe_layer's workspace: its barrier count (first 8 bytes, zero) and scratch
+        self.workspace = torch.zeros(B.luce_moe_layer_workspace_bytes(T, k, H, I), dtype=torch.uint8, device=dev)
         self.fused_prep = True
         # "layer": the whole layer in one cooperative launch (T <= 8, T*k <= 64,
         # E <= 256), measured faster on GB300; "split": three launches, any
@@ -49,7 +50,7 @@ class MoEStep:
             try:
                 B.luce_moe_layer(logits, bias, x, k, I, layer.wg, layer.wu, layer.wd, wsg, wsu, wsd, self.clamp,
                                  self.ids, self.weights, self.xq, self.counts, self.offsets, self.routes, self.h,
-                                 self.hq, out, self.sync, stream)
+                                 self.hq, out, self.workspace, stream)
                 return out
             except B.LuceError as err:
                 if err.status != B.LUCE_ERR_UNSUPPORTED:

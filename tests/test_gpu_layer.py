@@ -124,7 +124,7 @@ def test_repeated_calls_and_barrier_state():
     torch.cuda.synchronize()
     assert torch.equal(st.out, ref) and st.path == "layer"
     # the 64-bit arrival count grows by the grid size per barrier, one barrier per decode call
-    count = int(host(st.sync[:2].contiguous()).view(np.int64)[0])
+    count = int(st.workspace[:8].view(torch.int64)[0].item())
     grid = torch.cuda.get_device_properties(0).multi_processor_count
     assert count == 21 * grid
 
@@ -167,7 +167,7 @@ def test_graph_replay_with_programmatic_launch():
     for i in range(3):
         assert torch.equal(outs[i], refs[i])
     assert st.path == "layer"
-    count = int(host(st.sync[:2].contiguous()).view(np.int64)[0])
+    count = int(st.workspace[:8].view(torch.int64)[0].item())
     assert count % torch.cuda.get_device_properties(0).multi_processor_count == 0
 
 
@@ -186,13 +186,13 @@ def test_shapes_beyond_the_limits_are_declined_without_a_launch():
     hq = torch.empty((T * k, I // 32, 36), dtype=torch.uint8, device="cuda")
     h = torch.empty((T * k, I), dtype=torch.float32, device="cuda")
     out = torch.full((T, H), 7.0, dtype=torch.float32, device="cuda")
-    sync = torch.zeros(4, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(B.luce_moe_layer_workspace_bytes(T, k, H, I), dtype=torch.uint8, device="cuda")
     with pytest.raises(B.LuceError) as ei:
         B.luce_moe_layer(f, None, x, k, I, w, w, wd, None, None, None, 0.0, ids, wts, xq, cnt, off, rt, h, hq,
-                         out, sync)
+                         out, ws)
     assert ei.value.status == B.LUCE_ERR_UNSUPPORTED
     torch.cuda.synchronize()
-    assert torch.all(out == 7.0) and torch.all(sync == 0)
+    assert torch.all(out == 7.0) and torch.all(ws == 0)
     # MoEStep serves such a shape with the split launches, even when asked for one launch
     st = MoEStep(T, H, I, E, k, False, 0.0)
     st.path = "layer"
