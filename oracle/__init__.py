@@ -399,14 +399,13 @@ def hq_flip_allowance(h32, h_tol):
     d = (amax32 / np.float32(127.0)).astype(np.float64)  # the fp32 d of the rule
     tmax = tb.max(axis=1)
     delta_d = tmax / 127.0 * 1.01 + 1e-30
-    d16 = d.astype(np.float16)
-    up = np.nextafter(d16, np.float16(np.inf)).astype(np.float64)
-    dn = np.nextafter(d16, np.float16(0)).astype(np.float64)
-    d16 = d16.astype(np.float64)
-    mid_hi = 0.5 * (d16 + up)
-    mid_lo = 0.5 * (d16 + dn)
-    d16_unstable = ((mid_hi - d) <= delta_d) | ((d - mid_lo) <= delta_d)
-    d16_change = np.where(d16_unstable, np.maximum(up - d16, d16 - dn), 0.0)
+    # the stored d16 of any amax within the bound lies between fp16(d - delta_d)
+    # and fp16(d + delta_d) (rounding is monotonic): several fp16 steps when
+    # delta_d spans more than one
+    d16 = d.astype(np.float16).astype(np.float64)
+    d16_hi = (d + delta_d).astype(np.float16).astype(np.float64)
+    d16_lo = np.maximum(d - delta_d, 0.0).astype(np.float16).astype(np.float64)
+    d16_change = np.maximum(d16_hi - d16, d16 - d16_lo)
     safe_d = np.where(d > 0, d, 1.0)
     ratio = np.abs(hb) / safe_d[:, None]
     eps = (tb + ratio * delta_d[:, None]) / safe_d[:, None] * 1.01 + 1e-6

@@ -2,12 +2,14 @@
 seeded inputs (GB300).  Integer outputs bit for bit; float outputs within
 1e-4 * terms + 1e-6; q8_1 blocks of GPU-computed values identical wherever
 the quantization is stable (see gpu_util)."""
+import os
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from gpu_util import assert_close, assert_hq_valid, chain_allowance, dev, host
+from gpu_util import assert_close, assert_hq_is_rule_of_h, assert_hq_valid, chain_allowance, dev, host
 from quantized_moe_decode_luce_gb300 import binding as B
 from quantized_moe_decode_luce_gb300 import build as BLD
 from quantized_moe_decode_luce_gb300 import workloads as W
@@ -178,7 +180,7 @@ def test_glu_pair(case):
     assert_close(hg[valid], h_ref[valid], h_terms[valid], f"h ({name})")
     h32 = h_ref[valid].astype(np.float32)
     allow = oracle.hq_flip_allowance(h32, oracle.tol(h_terms[valid]))
-    flips = assert_hq_valid(host(hq)[valid], oracle.quantize_q8_1(h32), allow, f"hq ({name})")
+    flips = assert_hq_valid(host(hq)[valid], oracle.quantize_q8_1(h32), allow, f"hq ({name})", h_gpu=hg[valid])
     assert flips <= max(2, h32.size // 1000)
     # hq is exactly the q8_1 rule applied to the h the kernel stored
     hq2 = torch.empty_like(hq)
@@ -242,7 +244,8 @@ def _check_chain(wl, L, step):
     assert np.array_equal(host(step.xq), ref["xq"])
     valid = ~np.isnan(ref["h"][:, 0])
     assert_close(host(step.h)[valid], ref["h"][valid], ref["h_terms"][valid], "h")
-    flips = assert_hq_valid(host(step.hq)[valid], ref["hq"][valid], ref["h_allow"][valid], "hq")
+    flips = assert_hq_valid(host(step.hq)[valid], ref["hq"][valid], ref["h_allow"][valid], "hq",
+                            h_gpu=host(step.h)[valid])
     allow = chain_allowance(L.wd, L.wsd, ref["ids"], ref["weights"], ref["h_allow"])
     gout = host(step.out)
     bound = oracle.tol(ref["out_terms"]) + allow
@@ -319,7 +322,7 @@ def test_verify_layer_full_size(path):
     h32 = h_ref.astype(np.float32)
     h_allow = oracle.hq_flip_allowance(h32, oracle.tol(h_terms))
     hq_ref = oracle.quantize_q8_1(h32)
-    assert_hq_valid(host(step.hq), hq_ref, h_allow, "hq (verify)")
+    assert_hq_valid(host(step.hq), hq_ref, h_allow, "hq (verify)", h_gpu=host(step.h))
     out_ref, out_terms = oracle.down_combine(wd, wsd, hq_ref, cids, w_ref.astype(np.float32), len(used),
                                              wl.H, wl.I)
     allow = chain_allowance(wd, wsd, cids, w_ref, h_allow)
@@ -328,39 +331,50 @@ def test_verify_layer_full_size(path):
     del ref
 
 
-def test_prefill_layer_full_size_sampled():
+def test_prefill_layer_full_size_every_token():
+    """The 512-token prefill layer against the oracle on every token: the
+    oracle's steps run on host threads over chunks of tokens (its C calls
+    release the interpreter lock), on host copies of all the experts."""
+    from concurrent.futures import ThreadPoolExecutor
     wl = W.WORKLOADS["prefill_layer"]
+    T, k, E, H, I = wl.T, wl.k, wl.E, wl.H, wl.I
     dl = W.device_layer(wl, wl.seed, "cuda")
-    x = W.activations(W.rng(wl.seed, 2), wl.T, wl.H)
+    x = W.activations(W.rng(wl.seed, 2), T, H)
     logits, bias = W.router_logits(W.rng(wl.seed, 3), wl)
-    step = MoEStep(wl.T, wl.H, wl.I, wl.E, wl.k, wl.shared, wl.clamp)
+    step = MoEStep(T, H, I, E, k, wl.shared, wl.clamp)
     step.run(dl, dev(x), dev(logits), None)
     torch.cuda.synchronize()
-    ids_ref, w_ref = oracle.route_topk(logits, bias, wl.k)
+    ids_ref, w_ref = oracle.route_topk(logits, bias, k)
     assert np.array_equal(host(step.ids), ids_ref)
-    c_ref, o_ref, r_ref = oracle.moe_group(ids_ref, wl.E)
+    c_ref, o_ref, r_ref = oracle.moe_group(ids_ref, E)
     assert np.array_equal(host(step.counts), c_ref)
-    assert np.array_equal(host(step.routes), r_ref)
+    assert np.array_equal(host(step.offsets), o_ref) and np.array_equal(host(step.routes), r_ref)
     xq = oracle.quantize_q8_1(x)
     assert np.array_equal(host(step.xq), xq)
     hg, hqg, og = host(step.h), host(step.hq), host(step.out)
-    for t in (0, 1, 255, 511):
-        used = sorted(set(ids_ref[t].tolist()))
-        remap = {e: i for i, e in enumerate(used)}
-        cids = np.array([[remap[e] for e in ids_ref[t]]], np.int32)
-        wg, wu, wd = _compact(wl, dl, used)
-        wsg, wsu, wsd = host(dl.wsg), host(dl.wsu), host(dl.wsd)
-        h_ref, h_terms = oracle.glu_pair(wg, wu, wsg, wsu, xq[t:t + 1], cids, len(used), wl.H, wl.I, wl.clamp)
-        rows = list(range(t * wl.k, (t + 1) * wl.k)) + [wl.T * wl.k + t]
-        assert_close(hg[rows], h_ref, h_terms, f"h (prefill t={t})")
+    assert_hq_is_rule_of_h(hqg, hg, "hq (prefill)")
+    wg, wu, wd = host(dl.wg), host(dl.wu), host(dl.wd)
+    wsg, wsu, wsd = host(dl.wsg), host(dl.wsu), host(dl.wsd)
+    w32 = w_ref.astype(np.float32)
+
+    def check(a, b):
+        rows = list(range(a * k, b * k)) + [T * k + t for t in range(a, b)]
+        h_ref, h_terms = oracle.glu_pair(wg, wu, wsg, wsu, xq[a:b], ids_ref[a:b], E, H, I, wl.clamp)
+        assert_close(hg[rows], h_ref, h_terms, f"h (prefill tokens {a}..{b})")
         h32 = h_ref.astype(np.float32)
         h_allow = oracle.hq_flip_allowance(h32, oracle.tol(h_terms))
         hq_ref = oracle.quantize_q8_1(h32)
-        assert_hq_valid(hqg[rows], hq_ref, h_allow, f"hq (prefill t={t})")
-        out_ref, out_terms = oracle.down_combine(wd, wsd, hq_ref, cids, w_ref[t:t + 1].astype(np.float32),
-                                                 len(used), wl.H, wl.I)
-        allow = chain_allowance(wd, wsd, cids, w_ref[t:t + 1], h_allow)
-        assert np.all(np.abs(og[t:t + 1] - out_ref) <= oracle.tol(out_terms) + allow)
+        assert_hq_valid(hqg[rows], hq_ref, h_allow, f"hq (prefill tokens {a}..{b})")
+        out_ref, out_terms = oracle.down_combine(wd, wsd, hq_ref, ids_ref[a:b], w32[a:b], E, H, I)
+        allow = chain_allowance(wd, wsd, ids_ref[a:b], w_ref[a:b], h_allow)
+        assert np.all(np.abs(og[a:b] - out_ref) <= oracle.tol(out_terms) + allow), \
+            f"out (prefill tokens {a}..{b}) outside tolerance"
+        return b - a
+
+    chunk = 16
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        done = sum(ex.map(lambda a: check(a, min(T, a + chunk)), range(0, T, chunk)))
+    assert done == T
 
 
 # ----------------------------------------------------------------------------- argmax

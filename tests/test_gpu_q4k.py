@@ -65,7 +65,7 @@ def test_q4k_layer_matches_oracle(case):
     h32 = np.nan_to_num(h_ref, nan=0.0).astype(np.float32)
     allow = oracle.hq_flip_allowance(h32, oracle.tol(np.nan_to_num(h_terms, nan=0.0)))
     hq_ref = oracle.quantize_q8_1(h32)
-    assert_hq_valid(host(hq)[valid], hq_ref[valid], allow[valid], f"hq ({name})")
+    assert_hq_valid(host(hq)[valid], hq_ref[valid], allow[valid], f"hq ({name})", h_gpu=hg[valid])
 
     # the down product and combine, fed the oracle's own hq (so the bound is the plain float rule)
     out_ref, out_terms = oracle.down_combine_q4k(L.wd, L.wsd, hq_ref, ids, w32, E, H, I)

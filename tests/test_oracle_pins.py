@@ -583,3 +583,134 @@ def test_q4k_layer_routes_and_masks_like_the_q8_0_layer():
     g0, _ = oracle.dot_q4_k_q8_1(L.wg[m[0, 0], 5], xq[0])
     u0, _ = oracle.dot_q4_k_q8_1(L.wu[m[0, 0], 5], xq[0])
     assert h[0, 5] == oracle.swiglu(g0, u0)
+
+
+def test_q4k_down_combine_matches_dequantized_dense_matmul():
+    """The Q4_K down product + combine against numpy float64 matmuls of the
+    values the packer was given (d sc_j q - dmin m_j per sub-block j; the dot
+    reads the mins against the q8_1 block's stored sum s8), combined in slot
+    order with each product and sum rounded to fp32, shared expert last."""
+    g = np.random.default_rng(34)
+    E, H, I, T, k = 3, 48, 512, 2, 2
+    nsb = I // 256
+
+    def expert_rows(nrows):
+        blocks, vals, mins = [], np.zeros((nrows, I)), np.zeros((nrows, I // 32))
+        for n in range(nrows):
+            row = []
+            for sb in range(nsb):
+                d = float(np.float16(g.uniform(1e-4, 2e-3)))
+                dmin = float(np.float16(g.uniform(1e-4, 2e-3)))
+                sc = g.integers(0, 64, 8).tolist()
+                m = g.integers(0, 64, 8).tolist()
+                q = g.integers(0, 16, (8, 32)).tolist()
+                row.append(_pack_q4k(d, dmin, sc, m, q))
+                for j in range(8):
+                    c0 = sb * 256 + 32 * j
+                    vals[n, c0:c0 + 32] = d * sc[j] * np.array(q[j], np.float64)
+                    mins[n, sb * 8 + j] = dmin * m[j]
+            blocks.append(np.frombuffer(b"".join(row), np.uint8).reshape(nsb, 144))
+        return np.stack(blocks), vals, mins
+
+    wd, vd, md = zip(*[expert_rows(H) for _ in range(E)])
+    wsd, vs, ms = expert_rows(H)
+    wd = np.stack(wd)
+    ids = np.array([[2, 0], [1, -1]], np.int32)
+    weights = g.uniform(0.05, 0.9, (T, k)).astype(np.float32)
+    hq = oracle.quantize_q8_1(g.standard_normal((T * k + T, I)).astype(np.float32))
+    out, ot = oracle.down_combine_q4k(wd, wsd, hq, ids, weights, E, H, I)
+    hd = oracle.dequant_q8_1(hq).astype(np.float64)
+    s8 = oracle.fp16_decode(hq[..., 2:4].copy().view(np.uint16)[..., 0]).astype(np.float64)  # [rows, I/32]
+
+    def y_of(vals, mins, r):
+        return vals @ hd[r] - mins @ s8[r]
+
+    for t in range(T):
+        acc = np.float32(0)
+        for j in range(k):
+            e = ids[t, j]
+            if e < 0:
+                continue
+            y = np.float32(y_of(vd[e], md[e], t * k + j))
+            acc = np.float32(acc + np.float32(weights[t, j] * y))
+        acc = np.float32(acc + np.float32(y_of(vs, ms, T * k + t)))
+        assert np.all(np.abs(out[t] - acc) <= 4 * np.spacing(np.abs(acc).astype(np.float32)) + 1e-12 * ot[t])
+    # a masked route and a missing shared expert: the combine of the remaining slots
+    out2, _ = oracle.down_combine_q4k(wd, None, hq[:T * k], np.array([[-1, -1], [1, -1]], np.int32), weights,
+                                      E, H, I)
+    assert np.all(out2[0] == 0.0)
+    y = np.float32(y_of(vd[1], md[1], 2))
+    assert np.all(np.abs(out2[1] - np.float32(weights[1, 0] * y)) <= 4 * np.spacing(np.abs(y)) + 1e-30)
+
+
+def _flip_setup():
+    """h of the decode layer through the oracle, and its float bound."""
+    wl = W.WORKLOADS["decode_layer"]
+    L = W.host_layer(wl)
+    ids, _ = oracle.route_topk(L.logits, L.bias, wl.k)
+    xq = oracle.quantize_q8_1(L.x)
+    h, ht = oracle.glu_pair(L.wg, L.wu, L.wsg, L.wsu, xq, ids, wl.E, wl.H, wl.I, wl.clamp)
+    return h.astype(np.float32), oracle.tol(ht)
+
+
+def test_hq_flip_allowance_covers_every_change_within_the_float_bound():
+    """Perturb h by anything the float rule admits and re-quantize: every
+    dequantized q8_1 value that changes does so where the allowance is
+    positive, and by no more than it."""
+    h32, htol = _flip_setup()
+    allow = oracle.hq_flip_allowance(h32, htol)
+    ref = oracle.dequant_q8_1(oracle.quantize_q8_1(h32)).astype(np.float64)
+    g = np.random.default_rng(40)
+    changed = 0
+    for trial in range(60):
+        if trial < 20:
+            delta = g.uniform(-1.0, 1.0, h32.shape) * htol
+        elif trial < 40:
+            delta = g.choice([-1.0, 1.0], h32.shape) * htol  # the bound's corners
+        else:
+            delta = g.choice([-1.0, 0.0, 1.0], h32.shape) * htol * 0.999
+        hp = (h32.astype(np.float64) + delta).astype(np.float32)
+        got = oracle.dequant_q8_1(oracle.quantize_q8_1(hp)).astype(np.float64)
+        diff = np.abs(got - ref)
+        moved = diff > 0
+        changed += int(moved.sum())
+        assert np.all(allow[moved] > 0), "a q8_1 value changed where the allowance says it is stable"
+        assert np.all(diff <= allow + 1e-30), "a q8_1 value moved by more than its allowance"
+    assert changed > 0  # the perturbations do reach unstable elements
+
+
+def test_hq_flip_allowance_is_sharp():
+    """Sharpness.  With a perturbation of a few fp32 ulps of h (the size of a
+    reordered fp32 sum) the allowance marks few elements at the decode shape;
+    under the float bound itself (1e-4 of the terms, large against |h| where
+    the gate and up sums cancel) d may cross an fp16 midpoint in nearly every
+    block, and the allowance says so.  Hand-made blocks: an element on a
+    rounding midpoint is marked, the block maximum and integers are not, and a
+    block of exact integer codes far from every midpoint stays all zero."""
+    h32, htol = _flip_setup()
+    ulps = np.abs(h32).astype(np.float64) * 2.0 ** -23 * 16
+    frac_ulps = float((oracle.hq_flip_allowance(h32, ulps) > 0).mean())
+    assert frac_ulps < 0.01, frac_ulps
+    frac_bound = float((oracle.hq_flip_allowance(h32, htol) > 0).mean())
+    assert frac_bound > 0.5, frac_bound
+    # zero perturbation: nothing can move
+    assert np.all(oracle.hq_flip_allowance(h32, np.zeros_like(ulps)) == 0.0)
+    # hand-made block: amax 127 gives d = 1 (exact); values k + 0.5 are on a
+    # rounding midpoint, integers are far from one
+    blk = np.zeros((1, 32), np.float32)
+    blk[0, 0] = 127.0
+    blk[0, 1] = 10.5
+    blk[0, 2] = 11.0
+    t = np.full((1, 32), 1e-4)
+    a = oracle.hq_flip_allowance(blk, t)
+    assert a[0, 1] > 0 and a[0, 2] == 0.0 and a[0, 0] == 0.0
+    far = ((np.arange(32) - 16) * 4).astype(np.float32).reshape(1, 32)  # integers; amax 127 gives d = 1
+    far[0, 0] = -127.0
+    a2 = oracle.hq_flip_allowance(far, np.full((1, 32), 1e-9))
+    assert np.all(a2 == 0.0)
+    # the same block scaled by 127/16: x/d = 7.9375 (i - 16) lands on a
+    # midpoint exactly for i - 16 = +-8 (63.5), and only there
+    mid = far * np.float32(1.0)
+    mid[0, :] = ((np.arange(32) - 16) * np.float32(127.0 / 16.0)).astype(np.float32)
+    a3 = oracle.hq_flip_allowance(mid, np.full((1, 32), 1e-9))
+    assert set(np.nonzero(a3[0])[0].tolist()) == {8, 24}
