@@ -378,25 +378,29 @@ LUCE_API luce_status luce_moe_prep(const float *logits, const float *bias, const
  *   bytes of device memory (16-byte aligned) owned by the caller, all zero
  *   before the first call.  Its first 8 bytes are a 64-bit count of
  *   device-wide barrier arrivals that only grows (no reset, so CUDA-graph
- *   replays need no host update); the rest holds per-block counters that
- *   every call leaves at zero, or the y values of large layers.  The grid is
- *   always one CTA per SM, so calls of any shape may share one workspace on
- *   one device, one at a time (one stream or ordered streams); calls that
- *   may run at the same time need distinct workspaces.  If luce_get_fault
- *   reports LUCE_FAULT_DESYNC or LUCE_FAULT_TIMEOUT after this call, zero the
- *   whole workspace again before the next call.
+ *   replays need no host update); from byte 16 on it holds the y values
+ *   [T*k+T][H] f32 of large layers between two barriers (contents need no
+ *   initialisation).  The grid is always one CTA per SM, so calls of any
+ *   shape may share one workspace on one device, one at a time (one stream
+ *   or ordered streams); calls that may run at the same time need distinct
+ *   workspaces.  If luce_get_fault reports LUCE_FAULT_DESYNC or
+ *   LUCE_FAULT_TIMEOUT after this call, zero the first 8 bytes again before
+ *   the next call.
  *
- * The grid is launched cooperatively (all CTAs resident at once).  Each CTA
- * takes an equal share of the gate/up rows (of the shared expert and of the
- * routed experts); h goes through global memory; the CTAs meet at a
- * device-wide barrier after h and its q8_1 blocks are stored.  Down work:
- * when every q8_1 row of h fits 32 KB of shared memory, each CTA takes an
- * equal share of the output rows of every expert and combines them itself
- * (a q8_1 block of h is formed by the CTA whose rows complete its 32 rows);
- * otherwise each CTA quantizes an equal share of the q8_1 blocks after the
- * first barrier, takes an equal share of the flat (expert, output row) list
- * after a second, writes y to the workspace, and a third barrier precedes
- * the combine.
+ * The grid is launched cooperatively (all CTAs resident at once) and every
+ * CTA routes the tokens itself.  Two structures, chosen by the size of hq
+ * ((T*k+T) * I/32 * 36 bytes):
+ *   hq <= 24 KB (decode): each CTA takes an equal share of the 32-row gate/up
+ *   groups (shared expert and routed experts) and quantizes the groups it
+ *   computes; one device-wide barrier; each CTA then copies all of hq into
+ *   shared memory, computes an equal share of the output rows of every
+ *   expert and combines them itself.
+ *   hq > 24 KB (verify, wide layers): each CTA takes a byte-balanced slice
+ *   of the gate/up rows and stores h; barrier; each CTA quantizes an equal
+ *   share of the q8_1 blocks of h; barrier; each CTA takes an equal share of
+ *   the flat (expert, output row) list and writes y to the workspace;
+ *   barrier; each CTA combines an equal share of the out elements.
+ * Every barrier wait is bounded (LUCE_FAULT_TIMEOUT, LUCE_FAULT_DESYNC).
  * Supported: 1 <= T <= 8, T*k <= 64, E <= 256 (else LUCE_ERR_UNSUPPORTED,
  * and the three calls serve); H, I multiples of 256 up to 32768.  Argument
  * errors as in the three calls, plus a workspace too small or misaligned.

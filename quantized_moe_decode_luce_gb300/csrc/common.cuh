@@ -8,6 +8,9 @@
 
 #include <math.h>
 
+#include <atomic>
+#include <mutex>
+
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -443,8 +446,43 @@ inline luce_status launch_status()
     return e == cudaSuccess ? LUCE_OK : LUCE_ERR_CUDA;
 }
 
-// Number of SMs of the current device (cached per device).
+// Number of SMs of the current device (cached per device, thread-safe).
 int sm_count();
+
+// The dynamic shared memory limit of ONE kernel (one object per kernel or
+// template instance), raised on the current device to at least `bytes` by
+// the first call that needs it; later calls make no attribute call.  Safe
+// from several host threads.  After a failed launch the caller calls forget()
+// so that the next call sets the attribute again (a reset context starts
+// from the default limit).
+struct SmemLimit {
+    std::atomic<size_t> set[64];
+    std::mutex mu;
+    template <class Kernel> cudaError_t raise(Kernel kern, size_t bytes)
+    {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess)
+            return e;
+        if (dev < 0 || dev >= 64)
+            return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (set[dev].load(std::memory_order_acquire) >= bytes)
+            return cudaSuccess;
+        std::lock_guard<std::mutex> lock(mu);
+        if (set[dev].load(std::memory_order_relaxed) >= bytes)
+            return cudaSuccess;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (e == cudaSuccess)
+            set[dev].store(bytes, std::memory_order_release);
+        return e;
+    }
+    void forget()
+    {
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64)
+            set[dev].store(0, std::memory_order_release);
+    }
+};
 
 // Launch-shape parameters of the streaming kernels.  The values here are the
 // library's choices; they are plain data so that a tuning build can sweep

@@ -423,17 +423,16 @@ __global__ void __launch_bounds__((CW + 1) * 32, 2) k_down_combine(const DownArg
 template <int NC, bool COOP>
 luce_status launch_down(const DownArgs &a, dim3 grid, size_t smem, cudaStream_t stream)
 {
-    static size_t smem_set[64] = {0}; // per device: the attribute value in force
+    static luce_host::SmemLimit limit;
     auto kern = k_down_combine<NC, COOP>;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    if (limit.raise(kern, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
         return LUCE_ERR_CUDA;
-    if (smem_set[dev] < smem) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return LUCE_ERR_CUDA;
-        smem_set[dev] = smem;
     }
-    return luce_host::launch(kern, grid, dim3((CW + 1) * 32), smem, stream, a);
+    const luce_status st = luce_host::launch(kern, grid, dim3((CW + 1) * 32), smem, stream, a);
+    if (st != LUCE_OK)
+        limit.forget();
+    return st;
 }
 
 template <int NC>

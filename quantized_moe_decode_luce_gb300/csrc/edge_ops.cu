@@ -203,20 +203,16 @@ extern "C" luce_status luce_rmsnorm_router(const float *x, const float *gamma, f
     if (tiles > 65535 || chunks > INT_MAX)
         return LUCE_ERR_INVALID_ARG;
     const size_t smem = (size_t)tpc * H * sizeof(float);
-    static bool smem_set[64] = {false};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    static SmemLimit limit;
+    if (limit.raise(k_rmsnorm_router, 64 * 1024) != cudaSuccess) {
+        (void)cudaGetLastError();
         return LUCE_ERR_CUDA;
-    if (!smem_set[dev]) {
-        if (cudaFuncSetAttribute(k_rmsnorm_router, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
-            cudaSuccess) {
-            (void)cudaGetLastError();
-            return LUCE_ERR_CUDA;
-        }
-        smem_set[dev] = true;
     }
-    return launch(k_rmsnorm_router, dim3((unsigned)chunks, (unsigned)tiles), dim3(RW * 32), smem, as_stream(stream), x,
-                  gamma, eps, w_router, T, E, H, tpc, xn, logits);
+    const luce_status st = launch(k_rmsnorm_router, dim3((unsigned)chunks, (unsigned)tiles), dim3(RW * 32), smem,
+                                  as_stream(stream), x, gamma, eps, w_router, T, E, H, tpc, xn, logits);
+    if (st != LUCE_OK)
+        limit.forget();
+    return st;
 }
 
 extern "C" luce_status luce_argmax_pick(const float *vals, const int32_t *idxs, int S, int R, int32_t *idx, float *val,

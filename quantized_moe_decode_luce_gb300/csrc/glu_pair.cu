@@ -339,17 +339,16 @@ __global__ void __launch_bounds__(THREADS) k_glu_pair(const GluArgs a)
 template <int NC>
 luce_status launch_glu(const GluArgs &a, cudaStream_t stream, size_t smem, int grid)
 {
-    static size_t smem_set[64] = {0};
+    static luce_host::SmemLimit limit;
     auto kern = k_glu_pair<NC>;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    if (limit.raise(kern, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
         return LUCE_ERR_CUDA;
-    if (smem_set[dev] < smem) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return LUCE_ERR_CUDA;
-        smem_set[dev] = smem;
     }
-    return luce_host::launch(kern, dim3(grid), dim3(THREADS), smem, stream, a);
+    const luce_status st = luce_host::launch(kern, dim3(grid), dim3(THREADS), smem, stream, a);
+    if (st != LUCE_OK)
+        limit.forget();
+    return st;
 }
 
 } // namespace

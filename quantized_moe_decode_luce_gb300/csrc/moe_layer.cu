@@ -1296,17 +1296,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
 template <int NC>
 luce_status launch_layer(const LayerArgs &a, cudaStream_t stream, size_t smem, int cps)
 {
-    static size_t smem_set[64] = {0};
+    static luce_host::SmemLimit limit;
     auto kern = k_moe_layer<NC>;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-        return LUCE_ERR_CUDA;
-    if (smem_set[dev] < smem) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return LUCE_ERR_UNSUPPORTED;
-        }
-        smem_set[dev] = smem;
+    if (limit.raise(kern, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return LUCE_ERR_UNSUPPORTED;
     }
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, THREADS, smem) != cudaSuccess) {
@@ -1325,6 +1319,7 @@ luce_status launch_layer(const LayerArgs &a, cudaStream_t stream, size_t smem, i
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
+        limit.forget();
         return LUCE_ERR_CUDA;
     }
     return LUCE_OK;

@@ -1067,21 +1067,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
 template <int TT, bool FLAT>
 luce_status launch_layer(const LayerArgs &a, cudaStream_t stream, size_t smem)
 {
-    static std::atomic<size_t> smem_set[64];
-    static std::mutex mu;
+    static luce_host::SmemLimit limit;
     auto kern = k_moe_layer<TT, FLAT>;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-        return LUCE_ERR_CUDA;
-    if (smem_set[dev].load(std::memory_order_acquire) < smem) {
-        std::lock_guard<std::mutex> lock(mu);
-        if (smem_set[dev].load(std::memory_order_relaxed) < smem) {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
-                (void)cudaGetLastError();
-                return LUCE_ERR_UNSUPPORTED;
-            }
-            smem_set[dev].store(smem, std::memory_order_release);
-        }
+    if (limit.raise(kern, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return LUCE_ERR_UNSUPPORTED;
     }
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, THREADS, smem) != cudaSuccess) {
@@ -1102,6 +1092,7 @@ luce_status launch_layer(const LayerArgs &a, cudaStream_t stream, size_t smem)
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
+        limit.forget();
         return LUCE_ERR_CUDA;
     }
     return LUCE_OK;

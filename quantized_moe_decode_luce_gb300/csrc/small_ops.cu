@@ -508,17 +508,19 @@ bool pdl_enabled() { return __atomic_load_n(&g_pdl, __ATOMIC_RELAXED) != 0; }
 
 int sm_count()
 {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return 148;
-    if (cached[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 148;
-        cached[dev] = n;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            (void)cudaGetLastError();
+            return 148;
+        }
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return n;
 }
 } // namespace luce_host
 
@@ -731,10 +733,6 @@ namespace {
 constexpr size_t kNoallocScratchBytes = 16384; // the fixed maximum
 constexpr int kNoallocMaxRows = 1024;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
-// Device address of g_noalloc_scratch per device, set once by the first call
-// made with that device current (in host code the array's name is only a
-// stand-in, not a device address).
-static void *g_noalloc_scratch_addr[64];
 } // namespace
 
 extern "C" luce_status luce_argmax_noalloc(const float *logits, int R, int64_t V, int32_t *idx, float *val,
@@ -749,16 +747,13 @@ extern "C" luce_status luce_argmax_noalloc(const float *logits, int R, int64_t V
     const size_t need = luce_argmax_workspace_bytes(R, V);
     if (R > kNoallocMaxRows || need > kNoallocScratchBytes)
         return LUCE_ERR_UNSUPPORTED; // beyond the fixed scratch: use luce_argmax with a workspace
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    // the array's device address in the current context, looked up on every
+    // call (in host code its name is only a stand-in, and a cached address
+    // would outlive a reset context or belong to another device)
+    void *base = nullptr;
+    if (cudaGetSymbolAddress(&base, g_noalloc_scratch) != cudaSuccess || base == nullptr) {
+        (void)cudaGetLastError();
         return LUCE_ERR_CUDA;
-    void *base = g_noalloc_scratch_addr[dev];
-    if (base == nullptr) {
-        if (cudaGetSymbolAddress(&base, g_noalloc_scratch) != cudaSuccess || base == nullptr) {
-            (void)cudaGetLastError();
-            return LUCE_ERR_CUDA;
-        }
-        g_noalloc_scratch_addr[dev] = base;
     }
     int64_t L;
     int C;

@@ -25,9 +25,10 @@ def _lib():
 
 
 @pytest.fixture(autouse=True)
-def _no_device_faults():
+def _no_device_faults(request):
     yield
-    assert B.luce_get_fault() == 0
+    if "allow_fault" not in request.keywords:
+        assert B.luce_get_fault() == 0
 
 
 # name, T, H, I, E, k, shared, clamp, masked route
@@ -109,3 +110,37 @@ def chain_allowance_q4k(wd, wsd, ids, weights, h_allow):
             if a.any():
                 out[t] += bound_rows(wsd) @ a
     return out * 1.001
+
+
+@pytest.mark.allow_fault
+def test_q4k_out_of_range_id_is_skipped_and_flagged():
+    """An id >= E in either Q4_K call: that route is skipped (its h row is not
+    written, the combine leaves it out) and LUCE_FAULT_BAD_ID is raised; the
+    results equal the oracle's with that route masked."""
+    assert B.luce_get_fault() == 0
+    T, H, I, E, k = 2, 512, 256, 4, 2
+    wl = W.Workload("q4k_bad_id", T=T, H=H, I=I, E=E, k=k, shared=True, clamp=0.0, seed=871, bias_std=0.0)
+    L = W.host_layer_q4k(wl)
+    ids_bad = np.array([[1, E], [3, 0]], np.int32)
+    ids_masked = np.array([[1, -1], [3, 0]], np.int32)
+    w32 = np.array([[0.6, 0.4], [0.7, 0.3]], np.float32)
+    xq = oracle.quantize_q8_1(L.x)
+    rows = T * k + T
+    h_ref, h_terms = oracle.glu_q4k(L.wg, L.wu, L.wsg, L.wsu, xq, ids_masked, E, H, I, 0.0)
+    h = torch.full((rows, I), float("nan"), dtype=torch.float32, device="cuda")
+    B.luce_moe_glu_q4k(dev(L.wg), dev(L.wu), dev(L.wsg), dev(L.wsu), dev(xq), dev(ids_bad), E, H, I, 0.0, h)
+    torch.cuda.synchronize()
+    assert B.luce_get_fault() == B.LUCE_FAULT_BAD_ID
+    hg = host(h)
+    assert np.isnan(hg[1]).all(), "the row of the out-of-range route must not be written"
+    valid = ~np.isnan(h_ref[:, 0])
+    assert_close(hg[valid], h_ref[valid], h_terms[valid], "h (bad id)")
+    # the down product on the oracle's hq: the bad route is left out of the combine
+    hq_ref = oracle.quantize_q8_1(np.nan_to_num(h_ref, nan=0.0).astype(np.float32))
+    out_ref, out_terms = oracle.down_combine_q4k(L.wd, L.wsd, hq_ref, ids_masked, w32, E, H, I)
+    out = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+    B.luce_moe_down_combine_q4k(dev(L.wd), dev(L.wsd), dev(hq_ref), dev(ids_bad), dev(w32), E, H, I, out)
+    torch.cuda.synchronize()
+    assert B.luce_get_fault() == B.LUCE_FAULT_BAD_ID
+    assert_close(host(out), out_ref, out_terms, "out (bad id)")
+    assert B.luce_get_fault() == 0  # reading clears
