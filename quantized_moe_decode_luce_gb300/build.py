@@ -19,7 +19,7 @@ LIBDIR = os.path.join(PKG, "lib")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(LIBDIR, "libluce_moe.so")
 SOURCES = ["small_ops.cu", "glu_pair.cu", "down_combine.cu", "moe_layer.cu", "moe_layer_flat.cu", "edge_ops.cu",
-           "q4k_ops.cu"]
+           "q4k_ops.cu", "moe_tc.cu"]
 HEADERS = ["common.cuh", os.path.join("..", "..", "include", "luce_moe.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden", "-Xptxas", "-warn-spills"]

@@ -88,7 +88,10 @@ __device__ __forceinline__ unsigned long long global_timer_ns()
 // d16 = fp16(d), s16 = fp16(d * sum(q)) (round to nearest even).  The block
 // is written as 9 little-endian 32-bit words: d16 | s16 << 16, then the
 // codes four to a word.
-__device__ __forceinline__ void quantize_q8_1_warp(float x, uint32_t *__restrict__ out_words, int lane)
+// The lane's code and the block's fp16 d bits are returned in q_out and
+// d16_out (every lane gets d16).
+__device__ __forceinline__ void quantize_q8_1_warp(float x, uint32_t *__restrict__ out_words, int lane, int &q_out,
+                                                   uint32_t &d16_out)
 {
     const float amax = warp_max(fabsf(x));
     const float d = __fdiv_rn(amax, 127.0f);
@@ -100,13 +103,22 @@ __device__ __forceinline__ void quantize_q8_1_warp(float x, uint32_t *__restrict
     w |= __shfl_down_sync(0xffffffffu, byte, 1) << 8;
     w |= __shfl_down_sync(0xffffffffu, byte, 2) << 16;
     w |= __shfl_down_sync(0xffffffffu, byte, 3) << 24;
+    const uint32_t d16 = __half_as_ushort(__float2half_rn(d));
     if (lane == 0) {
-        const uint32_t d16 = __half_as_ushort(__float2half_rn(d));
         const uint32_t s16 = __half_as_ushort(__float2half_rn(__fmul_rn(d, (float)sum)));
         out_words[0] = d16 | (s16 << 16);
     }
     if ((lane & 3) == 0)
         out_words[1 + (lane >> 2)] = w;
+    q_out = q;
+    d16_out = d16;
+}
+
+__device__ __forceinline__ void quantize_q8_1_warp(float x, uint32_t *__restrict__ out_words, int lane)
+{
+    int q;
+    uint32_t d16;
+    quantize_q8_1_warp(x, out_words, lane, q, d16);
 }
 
 // ---------------------------------------------------------------------------

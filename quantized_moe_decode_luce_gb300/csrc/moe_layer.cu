@@ -1340,11 +1340,26 @@ luce_internal_moe_layer_flat(const float *logits, const float *bias, const float
                              int32_t *routes, float *h, luce_block_q8_1 *hq, float *out, void *workspace,
                              size_t workspace_bytes, void *stream);
 
+// The grouped tensor-core path for many tokens (moe_tc.cu); same arguments.
+extern "C" __attribute__((visibility("hidden"))) luce_status
+luce_internal_moe_layer_tc(const float *logits, const float *bias, const float *x, const luce_block_q8_0 *w_gate,
+                           const luce_block_q8_0 *w_up, const luce_block_q8_0 *w_down, const luce_block_q8_0 *ws_gate,
+                           const luce_block_q8_0 *ws_up, const luce_block_q8_0 *ws_down, int T, int E, int k, int H,
+                           int I, float clamp, int32_t *ids, float *weights, luce_block_q8_1 *xq, int32_t *counts,
+                           int32_t *offsets, int32_t *routes, float *h, luce_block_q8_1 *hq, float *out,
+                           void *workspace, size_t workspace_bytes, void *stream);
+extern "C" __attribute__((visibility("hidden"))) size_t luce_internal_moe_layer_tc_bytes(int T, int k, int H, int I);
+
+// Whether a shape goes to the grouped tensor-core path: more tokens or routes
+// than the one-launch kernels take.
+static bool tc_shape(int T, int k) { return T > MAX_T || (long long)T * k > MAX_R; }
+
 extern "C" size_t luce_moe_layer_workspace_bytes(int T, int k, int H, int I)
 {
     if (T < 0 || k < 0 || H < 0 || I < 0)
         return 0;
-    (void)I;
+    if (T > 0 && k > 0 && tc_shape(T, k))
+        return luce_internal_moe_layer_tc_bytes(T, k, H, I);
     return 16 + (size_t)T * (size_t)(k + 1) * (size_t)H * sizeof(float); // barrier count, y values
 }
 
@@ -1376,7 +1391,11 @@ extern "C" luce_status luce_moe_layer(const float *logits, const float *bias, co
         !aligned(weights, 4) || !aligned(xq, 4) || !aligned(counts, 4) || !aligned(offsets, 4) ||
         !aligned(routes, 4) || !aligned(h, 16) || !aligned(hq, 16) || !aligned(out, 4) || !aligned(workspace, 16))
         return LUCE_ERR_INVALID_ARG;
-    if (T > MAX_T || T * k > MAX_R || E > MAX_E)
+    if (tc_shape(T, k))
+        return luce_internal_moe_layer_tc(logits, bias, x, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, T, E, k, H, I,
+                                          clamp, ids, weights, xq, counts, offsets, routes, h, hq, out, workspace,
+                                          workspace_bytes, stream);
+    if (E > MAX_E)
         return LUCE_ERR_UNSUPPORTED;
     {
         // large q8_1 rows of h (speculative verify): the flat-split kernel

@@ -499,6 +499,7 @@ extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault
 extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault_down(unsigned int *bits);
 extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault_layer(unsigned int *bits);
 extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault_layer_flat(unsigned int *bits);
+extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault_tc(unsigned int *bits);
 extern "C" __attribute__((visibility("hidden"))) cudaError_t luce_internal_fault_q4k(unsigned int *bits);
 
 namespace luce_host {
@@ -562,8 +563,9 @@ extern "C" luce_status luce_get_fault(unsigned int *bits)
     cudaError_t e4 = luce_internal_fault_layer(bits);
     cudaError_t e5 = luce_internal_fault_q4k(bits);
     cudaError_t e6 = luce_internal_fault_layer_flat(bits);
+    cudaError_t e7 = luce_internal_fault_tc(bits);
     return (e1 == cudaSuccess && e2 == cudaSuccess && e3 == cudaSuccess && e4 == cudaSuccess && e5 == cudaSuccess &&
-            e6 == cudaSuccess)
+            e6 == cudaSuccess && e7 == cudaSuccess)
                ? LUCE_OK
                : LUCE_ERR_CUDA;
 }

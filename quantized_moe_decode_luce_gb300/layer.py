@@ -33,10 +33,10 @@ class MoEStep:
         # luce_moe_layer's workspace: its barrier count (first 8 bytes, zero) and scratch
         self.workspace = torch.zeros(B.luce_moe_layer_workspace_bytes(T, k, H, I), dtype=torch.uint8, device=dev)
         self.fused_prep = True
-        # "layer": the whole layer in one cooperative launch (T <= 8, T*k <= 64,
-        # E <= 256), measured faster on GB300; "split": three launches, any
-        # shape.  Both give bitwise the same results.
-        self.path = "layer" if (T <= 8 and T * k <= 64 and E <= 256) else "split"
+        # "layer": luce_moe_layer -- one cooperative launch for T <= 8, T*k <= 64,
+        # E <= 256 (bitwise the results of the split launches), the grouped
+        # tensor-core path for more tokens; "split": the separate launches.
+        self.path = "split" if (T <= 8 and T * k <= 64 and E > 256) else "layer"
 
     def run(self, layer, x, logits, bias=None, stream=None, out=None) -> torch.Tensor:
         """layer: object with wg, wu, wd (+ wsg, wsu, wsd) uint8 CUDA tensors.

@@ -172,7 +172,9 @@ def test_graph_replay_with_programmatic_launch():
 
 
 def test_shapes_beyond_the_limits_are_declined_without_a_launch():
-    T, H, I, E, k = 9, 256, 256, 8, 2
+    # few tokens but more than 256 experts: beyond the one-launch kernels, and
+    # not a many-token shape for the grouped tensor-core path
+    T, H, I, E, k = 2, 256, 256, 300, 2
     f = torch.zeros((T, E), dtype=torch.float32, device="cuda")
     x = torch.zeros((T, H), dtype=torch.float32, device="cuda")
     w = torch.zeros((E, I, H // 32, 34), dtype=torch.uint8, device="cuda")
