@@ -385,6 +385,16 @@ def edge_ops_measure(dev, peak, stream):
     return out
 
 
+def _path_label(st):
+    """What luce_moe_layer (or the split launches) runs for this step's shape."""
+    if st.path != "layer":
+        return "prep + gate/up + down launches"
+    if st.T > 8 or st.T * st.k > 64:
+        return ("grouped tensor-core launches: route, quantize, group, work lists + gathered codes, "
+                "gate/up GEMM, down GEMM, combine")
+    return "one launch per layer"
+
+
 def configs_measure(dev, peak, stream):
     """Device time of the other layer workloads, one launch sequence per
     workload captured in a CUDA graph and replayed (device time, no host
@@ -467,7 +477,7 @@ def configs_measure(dev, peak, stream):
                             for i in range(n_launch)]))
         gbs = nb / (us * 1e-6) / 1e9
         ent = {"T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k, "clamp": wl.clamp,
-               "path": "one launch per layer" if st.path == "layer" else "prep + gate/up + down launches",
+               "path": _path_label(st),
                "us_per_layer": us, "tokens_per_s": wl.T / (us * 1e-6), "bytes_per_layer": nb,
                "GBps": gbs, "frac_of_measured_hbm": gbs / peak, "frac_of_8TBps_spec": gbs / SPEC_HBM_GBS,
                "l2": f"{n_copies} resident weight copies x {n_inputs} input draws rotate "
@@ -479,6 +489,12 @@ def configs_measure(dev, peak, stream):
             ops = 2.0 * (wl.T * wl.k + wl.T) * 3 * wl.H * wl.I
             ent["int8_ops_per_layer"] = ops
             ent["int8_tops"] = ops / (us * 1e-6) / 1e12
+            # the same layer on the dp4a launches (prep, gate/up pair, down + combine), for comparison
+            st.path = "split"
+            us_split = timed(body, n_launch)
+            ent["dp4a_split_path"] = {"us_per_layer": us_split, "int8_tops": ops / (us_split * 1e-6) / 1e12,
+                                      "GBps": nb / (us_split * 1e-6) / 1e9,
+                                      "tensor_core_speedup": us_split / us}
         out[name] = ent
         del lays, st, o
         torch.cuda.empty_cache()

@@ -53,6 +53,9 @@
 #include <algorithm>
 #include <climits>
 #include <cmath>
+#include <mutex>
+
+#include <cuda.h> // CUtensorMap and its enums (the encoder is reached through the runtime's entry-point query)
 
 #include "common.cuh"
 
@@ -65,12 +68,19 @@ using namespace luce;
 constexpr int TM = 128;       // weight rows of one item (MMA M)
 constexpr int TN = 64;        // tokens of one item at most
 constexpr int SKB = 8;        // 32-value blocks per stage
-constexpr int RA = 2;         // A slots in tensor memory
-constexpr int RD = 3;         // D slots in tensor memory
-constexpr int EPI_WARPS = 8;  // convert + epilogue warps (0 .. 7)
-constexpr int MMA_WARP = 9;
-constexpr int TC_THREADS = 384;
-constexpr int PROD_LANES = 96; // three producer warps
+constexpr int RA = 3;          // A slots in tensor memory
+constexpr int RD = 3;          // D slots in tensor memory
+constexpr int LAG = 2;         // a warp converts block b, then applies the scales of block b - LAG
+constexpr int EPI_WARPS = 8;   // convert + epilogue warps (0 .. 7): two per tensor-memory lane quarter
+constexpr int CPW = 2;         // 16-token chunks per epilogue warp
+constexpr int PROD_WARP0 = 8;  // producers: 8 (tensor-map tiles), 9 (activation block scales)
+constexpr int MMA_WARP = 10;
+constexpr int TC_THREADS = 11 * 32;
+constexpr int FULL_ARRIVALS = 33; // a stage is full: the tiles' arrival + bytes, 32 lanes of scale copies
+// A slot reuse needs no wait of its own: a warp converts block b after it applied the
+// scales of block b - LAG - 1 = b - RA, whose MMAs (the last readers of that slot) it
+// waited for then.
+static_assert(RA == LAG + 1 && LAG < RD, "slot reuse ordering");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int RAW_ROW = SKB * Q8_0_BYTES; // 272: one row's stage of raw Q8_0 blocks
 constexpr int RAW_MAT = TM * RAW_ROW;     // 34,816
@@ -87,10 +97,12 @@ template <int NMAT> struct Stage {
     static_assert(bytes % 1024 == 0, "stages keep the swizzle atoms 1024-byte aligned");
 };
 
-// Tensor memory columns: A slots first, then D slots.
-template <int NMAT> __device__ __forceinline__ uint32_t acol(int slot, int m) { return (uint32_t)(slot * 16 * NMAT + 16 * m); }
-__device__ __forceinline__ uint32_t dcol(int slot, int m) { return (uint32_t)(64 + slot * 128 + 64 * m); }
-static_assert(64 + RD * 128 <= (int)TMEM_COLS, "tensor memory budget");
+// Tensor memory columns: A slots first (16 columns = 32 fp16 codes of a row
+// per matrix), then D slots (64 columns = 64 tokens per matrix).
+constexpr int A_COLS = RA * 32;
+__device__ __forceinline__ uint32_t acol(int slot, int m) { return (uint32_t)(slot * 32 + 16 * m); }
+__device__ __forceinline__ uint32_t dcol(int slot, int m) { return (uint32_t)(A_COLS + slot * 128 + 64 * m); }
+static_assert(A_COLS + RD * 128 <= (int)TMEM_COLS, "tensor memory budget");
 
 struct TcItem {
     int e;  // expert, or -1: the shared expert
@@ -100,9 +112,11 @@ struct TcItem {
 };
 
 struct TcArgs {
-    const uint8_t *w[2];  // routed experts [E][M][nbK][34] (gate, up) or (down)
-    const uint8_t *ws[2]; // shared expert [M][nbK][34] or null
-    const uint16_t *b16;  // activation codes as fp16 [P][K]
+    // tensor maps (2D tiles, copied by the TMA unit):
+    //  tm_w[m] / tm_ws[m]: Q8_0 rows of matrix m (routed: E*M rows; shared: M rows) seen as
+    //    u16 elements, nbK*17 to a row; box = 136 elements (8 blocks, 272 bytes) x 128 rows
+    //  tm_b: activation codes fp16 [P][K]; box = 64 values (128 bytes) x 64 rows, 128-byte swizzle
+    CUtensorMap tm_w[2], tm_ws[2], tm_b;
     const float *bscale;  // activation block scales [P][nbK]
     const TcItem *items;
     const int *nitems;
@@ -121,10 +135,6 @@ struct TcArgs {
 
 // ---------------------------------------------------------------------------
 // tcgen05 / cp.async wrappers (sm_100 family PTX).
-__device__ __forceinline__ void cp_async16(void *dst, const void *src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
 __device__ __forceinline__ void cp_async4(void *dst, const void *src)
 {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
@@ -135,6 +145,14 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// One 2D tile of a tensor map into shared memory, completing its bytes on `bar`.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+                 : "memory");
+}
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -191,21 +209,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// acc[0..1] += d[0..1] * (w * x[0..1]): one packed multiply, one packed FMA.
-__device__ __forceinline__ void fma_pair(float &a0, float &a1, uint32_t d0, uint32_t d1, float w, float x0, float x1)
-{
-    asm("{\n\t.reg .b64 s, x, d, c;\n\t"
-        "mov.b64 x, {%2, %3};\n\t"
-        "mov.b64 s, {%4, %4};\n\t"
-        "mul.rn.f32x2 s, s, x;\n\t"
-        "mov.b64 d, {%5, %6};\n\t"
-        "mov.b64 c, {%0, %1};\n\t"
-        "fma.rn.f32x2 c, d, s, c;\n\t"
-        "mov.b64 {%0, %1}, c;\n\t}"
-        : "+f"(a0), "+f"(a1)
-        : "f"(x0), "f"(x1), "f"(w), "r"(d0), "r"(d1));
-}
-
 // Four int8 codes -> two fp16 pairs holding the same integers: bias to
 // unsigned (c + 128), place each byte under the exponent of 1024 (fp16
 // 0x64XX = 1024 + XX), subtract 1152.  Exact for every code.
@@ -229,10 +232,12 @@ __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile
 {
     if (mbar_try_wait(bar, parity))
         return true;
+    // each poll parks the thread in hardware until the phase completes (or a
+    // suspend-time hint of 10 us runs out), so a waiting thread takes no issue
+    // slots from the warps that work, and wakes at once
     const unsigned long long t0 = global_timer_ns();
     for (;;) {
-        __nanosleep(32);
-        if (mbar_try_wait(bar, parity))
+        if (mbar_try_wait_sleep(bar, parity, 10000))
             return true;
         if (*abort_flag)
             return false;
@@ -244,16 +249,15 @@ __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile
     }
 }
 
-// The same wait taken by lane 0 for the whole warp (the warp stays
-// converged for the .sync.aligned tensor-memory instructions that follow).
+// The same wait for a whole converged warp: every lane polls, and one poll
+// instruction gives every lane the same answer, so the warp stays converged
+// for the .sync.aligned tensor-memory instructions that follow.
 __device__ __forceinline__ bool tc_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int lane)
 {
-    int ok = 0;
-    if (lane == 0)
-        ok = tc_wait(bar, parity, abort_flag) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
+    (void)lane;
+    const bool ok = tc_wait(bar, parity, abort_flag);
     __syncwarp();
-    return ok != 0;
+    return ok;
 }
 
 // Block j of a row's stage sits at byte 34 j, inside the three 16-byte
@@ -292,35 +296,59 @@ template <int J> __device__ __forceinline__ void load_window(const uint8_t *row,
     }
 }
 
-// Apply the block scales of one finished block: acc += isum * (d_w * d_x) for
-// the 16-token chunks c = hh, hh + 2 of this warp, then release the D slot
-// (and the stage, after its last block).
+// A ring position: slot index and phase parity, advanced one block at a time
+// (no division by the ring size).
+template <int R> struct Ring {
+    uint32_t slot = 0, phase = 0;
+    __device__ __forceinline__ void next()
+    {
+        if (++slot == R) {
+            slot = 0;
+            phase ^= 1;
+        }
+    }
+};
+
+// Apply the block scales of one finished block to this warp's 16-token chunks
+// c = c0 + 2 cc (those below nch): acc[cc][m][i] += isum * (d_w[m] * d_x[i]),
+// pairs of tokens in packed fp32 arithmetic; then release the D slot (and the
+// stage, after its last block).
 template <int NMAT>
-__device__ __forceinline__ bool tc_epilogue(float (&acc)[2][NMAT][16], const float (&dw)[NMAT], uint32_t eb,
-                                            const float *dxs, bool stage_end, uint64_t *dfull, uint64_t *dfree,
-                                            uint64_t *sfree_s, uint32_t tl, int hh, int nch, int lane,
-                                            volatile int *abort_flag)
+__device__ __forceinline__ bool tc_epilogue(float2 (&acc)[CPW][NMAT][8], const uint8_t *stage, int rowoff, int j,
+                                            const Ring<RD> &dr, uint64_t *dfull, uint64_t *dfree, uint64_t *sfree_s,
+                                            uint32_t tl, int c0, int nch, int lane, volatile int *abort_flag)
 {
-    const int ds = (int)(eb % RD);
-    if (!tc_wait_warp(&dfull[ds], (eb / RD) & 1, abort_flag, lane))
+    using S = Stage<NMAT>;
+    if (!tc_wait_warp(&dfull[dr.slot], dr.phase, abort_flag, lane))
         return false;
     tc_fence_after();
+    float dw[NMAT]; // the weight scales of row r, block j (the stage is held until its last block is done)
 #pragma unroll
-    for (int cc = 0; cc < 2; cc++) {
-        const int c = hh + 2 * cc;
+    for (int m = 0; m < NMAT; m++)
+        dw[m] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(stage + rowoff + m * RAW_MAT + Q8_0_BYTES * j));
+    const float *dxj = reinterpret_cast<const float *>(stage + S::dx_off) + j * TN;
+#pragma unroll
+    for (int cc = 0; cc < CPW; cc++) {
+        const int c = c0 + 2 * cc;
         if (c < nch) {
-            const float4 *x4 = reinterpret_cast<const float4 *>(dxs + 16 * c);
+            const float4 *x4 = reinterpret_cast<const float4 *>(dxj + 16 * c);
 #pragma unroll
             for (int m = 0; m < NMAT; m++) {
+                const float2 w2 = make_float2(dw[m], dw[m]);
                 uint32_t dv[16];
-                tmem_ld16(tl + dcol(ds, m) + 16 * c, dv);
+                tmem_ld16(tl + dcol(dr.slot, m) + 16 * c, dv);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i4 = 0; i4 < 4; i4++) {
-                    const float4 xv = x4[i4];
-                    fma_pair(acc[cc][m][4 * i4], acc[cc][m][4 * i4 + 1], dv[4 * i4], dv[4 * i4 + 1], dw[m], xv.x, xv.y);
-                    fma_pair(acc[cc][m][4 * i4 + 2], acc[cc][m][4 * i4 + 3], dv[4 * i4 + 2], dv[4 * i4 + 3], dw[m],
-                             xv.z, xv.w);
+                    const float4 x = x4[i4];
+                    const float2 s0 = __fmul2_rn(w2, make_float2(x.x, x.y));
+                    const float2 s1 = __fmul2_rn(w2, make_float2(x.z, x.w));
+                    acc[cc][m][2 * i4] = __ffma2_rn(
+                        make_float2(__uint_as_float(dv[4 * i4]), __uint_as_float(dv[4 * i4 + 1])), s0,
+                        acc[cc][m][2 * i4]);
+                    acc[cc][m][2 * i4 + 1] = __ffma2_rn(
+                        make_float2(__uint_as_float(dv[4 * i4 + 2]), __uint_as_float(dv[4 * i4 + 3])), s1,
+                        acc[cc][m][2 * i4 + 1]);
                 }
             }
         }
@@ -328,8 +356,8 @@ __device__ __forceinline__ bool tc_epilogue(float (&acc)[2][NMAT][16], const flo
     tc_fence_before();
     __syncwarp();
     if (lane == 0) {
-        mbar_arrive(&dfree[ds]);
-        if (stage_end)
+        mbar_arrive(&dfree[dr.slot]);
+        if (j == SKB - 1)
             mbar_arrive(sfree_s);
     }
     return true;
@@ -337,12 +365,12 @@ __device__ __forceinline__ bool tc_epilogue(float (&acc)[2][NMAT][16], const flo
 
 // ---------------------------------------------------------------------------
 template <int NMAT>
-__global__ void __launch_bounds__(TC_THREADS, 1) k_moe_tc(const TcArgs a)
+__global__ void __launch_bounds__(TC_THREADS, 1) k_moe_tc(const __grid_constant__ TcArgs a)
 {
     using S = Stage<NMAT>;
     constexpr int NS = S::count;
     extern __shared__ uint8_t smraw[];
-    __shared__ uint64_t full[NS], sfree[NS], afull[RA], afree[RA], dfull[RD], dfree[RD], drain;
+    __shared__ uint64_t full[NS], sfree[NS], afull[RA], dfull[RD], dfree[RD], drain;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_word;
     volatile int *abort_flag = &abort_word;
@@ -351,13 +379,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_moe_tc(const TcArgs a)
 
     if (tid == 0) {
         for (int s = 0; s < NS; s++) {
-            mbar_init(&full[s], PROD_LANES);
+            mbar_init(&full[s], FULL_ARRIVALS);
             mbar_init(&sfree[s], 1 + EPI_WARPS);
         }
-        for (int i = 0; i < RA; i++) {
+        for (int i = 0; i < RA; i++)
             mbar_init(&afull[i], EPI_WARPS);
-            mbar_init(&afree[i], 1);
-        }
         for (int i = 0; i < RD; i++) {
             mbar_init(&dfull[i], 1);
             mbar_init(&dfree[i], EPI_WARPS);
@@ -378,12 +404,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_moe_tc(const TcArgs a)
     pdl_wait(); // items, activation codes and scales come from the previous launches
     const int nitems = *a.nitems;
     const int nst = a.nbK / SKB;
-    const size_t rowbytes = (size_t)a.nbK * Q8_0_BYTES;
-    const int K = a.nbK * QK;
 
-    if (warp == 8 || warp == 10 || warp == 11) {
+    if (warp == PROD_WARP0 || warp == PROD_WARP0 + 1) {
         // ------------------------------------------------------------ producers
-        const int pw = warp == 8 ? 0 : warp == 10 ? 1 : 2;
+        const int pw = warp - PROD_WARP0;
         uint32_t gs = 0;
         for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
             const TcItem item = a.items[it];
@@ -393,44 +417,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_moe_tc(const TcArgs a)
                 if (!tc_wait_warp(&sfree[s], ((gs / NS) & 1) ^ 1, abort_flag, lane))
                     goto out_prod;
                 uint8_t *stg = sm + s * S::bytes;
-                if (pw < 2) {
-                    // raw Q8_0 rows: warps 8 / 10 take matrix 0 / 1 (down: rows 0-63 / 64-127)
-                    const int m = NMAT == 2 ? pw : 0;
-                    const int r_lo = NMAT == 2 ? 0 : 64 * pw, r_hi = NMAT == 2 ? TM : r_lo + 64;
-                    // (selects, not a runtime index into the parameter block, which would copy it to the stack)
-                    const uint8_t *wr = m == 0 ? a.w[0] : a.w[1];
-                    const uint8_t *wsr = m == 0 ? a.ws[0] : a.ws[1];
-                    const uint8_t *wb = item.e >= 0 ? wr + ((size_t)item.e * a.M + item.m0) * rowbytes
-                                                    : wsr + (size_t)item.m0 * rowbytes;
-                    wb += (size_t)st * RAW_ROW;
-                    uint8_t *db = stg + S::raw_off + m * RAW_MAT;
-                    // 17 pieces of 16 bytes a row; lane i takes linear piece i, i + 32, ...
-                    int r = r_lo + lane / 17, pc = lane % 17;
-                    while (r < r_hi) {
-                        cp_async16(db + r * RAW_ROW + pc * 16, wb + (size_t)r * rowbytes + pc * 16);
-                        pc += 15; // + 32 pieces = one row and 15 pieces
-                        r += 1;
-                        if (pc >= 17) {
-                            pc -= 17;
-                            r += 1;
-                        }
+                if (pw == 0) {
+                    // the weight tiles of every matrix (128 rows x 8 blocks each) and the
+                    // activation tile (64 token rows x 256 codes, four swizzled 64-code columns)
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&full[s], (uint32_t)(NMAT * RAW_MAT + B_BYTES));
+                        const int wy = item.e >= 0 ? item.e * a.M + item.m0 : item.m0;
+#pragma unroll
+                        for (int m = 0; m < NMAT; m++)
+                            tma_load_2d(stg + S::raw_off + m * RAW_MAT, item.e >= 0 ? &a.tm_w[m] : &a.tm_ws[m],
+                                        st * (RAW_ROW / 2), wy, &full[s]);
+#pragma unroll
+                        for (int kc = 0; kc < 4; kc++)
+                            tma_load_2d(stg + S::b_off + kc * B_ATOM, &a.tm_b, st * (SKB * QK) + kc * 64, item.p0,
+                                        &full[s]);
                     }
                 } else {
-                    // activation codes: one token row (512 bytes) per warp instruction, swizzled
-                    const int kc = lane >> 3, cc = lane & 7;
-                    for (int row = 0; row < npad; row++) {
-                        const int src = item.p0 + min(row, item.n - 1);
-                        cp_async16(stg + S::b_off + kc * B_ATOM + row * 128 + ((cc ^ (row & 7)) << 4),
-                                   a.b16 + (size_t)src * K + (size_t)st * (SKB * QK) + lane * 8);
-                    }
                     // block scales, transposed to [block][token]
                     for (int i = lane; i < npad * SKB; i += 32) {
                         const int row = i >> 3, j = i & 7;
                         const int src = item.p0 + min(row, item.n - 1);
                         cp_async4(stg + S::dx_off + (j * TN + row) * 4, a.bscale + (size_t)src * a.nbK + st * SKB + j);
                     }
+                    cp_async_arrive(&full[s]);
                 }
-                cp_async_arrive(&full[s]);
             }
         }
     out_prod:
@@ -438,23 +448,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_moe_tc(const TcArgs a)
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
-            uint32_t gb = 0, gs = 0;
+            Ring<NS> sr;
+            Ring<RA> ar;
+            Ring<RD> dr;
             for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
                 const TcItem item = a.items[it];
                 const int npad = (item.n + 15) & ~15;
                 const uint32_t idesc = mma_idesc(npad);
-                for (int st = 0; st < nst; st++, gs++) {
-                    const int s = (int)(gs % NS);
-                    if (!tc_wait(&full[s], (gs / NS) & 1, abort_flag))
+                for (int st = 0; st < nst; st++, sr.next()) {
+                    if (!tc_wait(&full[sr.slot], sr.phase, abort_flag))
                         goto out_mma;
-                    // the copies landed through the generic proxy; the tensor core reads through the async proxy
+                    // the scale copies landed through the generic proxy; the tensor core reads through the async proxy
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    const uint32_t bbase = smem_addr(sm + s * S::bytes + S::b_off);
-                    for (int j = 0; j < SKB; j++, gb++) {
-                        const int as = (int)(gb % RA), ds = (int)(gb % RD);
-                        if (!tc_wait(&afull[as], (gb / RA) & 1, abort_flag))
+                    const uint32_t bbase = smem_addr(sm + sr.slot * S::bytes + S::b_off);
+                    for (int j = 0; j < SKB; j++, ar.next(), dr.next()) {
+                        if (!tc_wait(&afull[ar.slot], ar.phase, abort_flag))
                             goto out_mma;
-                        if (!tc_wait(&dfree[ds], ((gb / RD) & 1) ^ 1, abort_flag))
+                        if (!tc_wait(&dfree[dr.slot], dr.phase ^ 1, abort_flag))
                             goto out_mma;
                         tc_fence_after();
 #pragma unroll
@@ -462,12 +472,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_moe_tc(const TcArgs a)
                             const uint64_t bd = sw128_desc(bbase + (j >> 1) * B_ATOM + (j & 1) * 64 + sk * 32);
 #pragma unroll
                             for (int m = 0; m < NMAT; m++)
-                                mma_ts(tmem + dcol(ds, m), tmem + acol<NMAT>(as, m) + 8 * sk, bd, idesc, sk > 0);
+                                mma_ts(tmem + dcol(dr.slot, m), tmem + acol(ar.slot, m) + 8 * sk, bd, idesc, sk > 0);
                         }
-                        mma_commit(&afree[as]);
-                        mma_commit(&dfull[ds]);
+                        mma_commit(&dfull[dr.slot]);
                     }
-                    mma_commit(&sfree[s]);
+                    mma_commit(&sfree[sr.slot]);
                 }
             }
         out_mma:
@@ -478,108 +487,86 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_moe_tc(const TcArgs a)
         __syncwarp();
     } else if (warp < EPI_WARPS) {
         // ------------------------------------------------------------ convert + epilogue
-        const int q = warp & 3, hh = warp >> 2;
+        const int q = warp & 3, w2 = warp >> 2;
         const int r = 32 * q + lane;
         const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
-        const int mc = NMAT == 2 ? hh : 0; // the matrix this warp converts
-        uint32_t gb = 0, gs = 0;
+        // conversion: the gate pair -- matrix w2, every block; the down product --
+        // the blocks of parity w2.  Epilogue: token chunks w2 and w2 + 2.
+        const int mc = NMAT == 2 ? w2 : 0;
+        const int rowoff = S::raw_off + r * RAW_ROW; // this row in a stage's raw weights
+        Ring<NS> sr;                                 // stage being converted
+        Ring<RA> ar;                                 // A slot being written
+        Ring<RD> dr;                                 // D slot whose scales are applied next
         for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
             const TcItem item = a.items[it];
             const int nch = (item.n + 15) >> 4;
-            float acc[2][NMAT][16];
+            float2 acc[CPW][NMAT][8];
 #pragma unroll
-            for (int cc = 0; cc < 2; cc++)
+            for (int cc = 0; cc < CPW; cc++)
 #pragma unroll
                 for (int m = 0; m < NMAT; m++)
 #pragma unroll
-                    for (int i = 0; i < 16; i++)
-                        acc[cc][m][i] = 0.0f;
-            // the block whose sums are applied next: its stage, index and weight scales
-            bool pend = false;
-            uint32_t pgb = 0;
-            int ps = 0, pj = 0;
-            float pdw[NMAT];
+                    for (int i = 0; i < 8; i++)
+                        acc[cc][m][i] = make_float2(0.0f, 0.0f);
 
-            for (int st = 0; st < nst; st++, gs++) {
-                const int s = (int)(gs % NS);
-                if (!tc_wait_warp(&full[s], (gs / NS) & 1, abort_flag, lane))
+            for (int st = 0; st < nst; st++, sr.next()) {
+                const int s = (int)sr.slot;
+                const int sprev = s == 0 ? NS - 1 : s - 1;
+                if (!tc_wait_warp(&full[s], sr.phase, abort_flag, lane))
                     goto out_epi;
-                const uint8_t *raw = sm + s * S::bytes + S::raw_off;
-                const uint8_t *myrow = raw + mc * RAW_MAT + r * RAW_ROW;
-#pragma unroll
-                for (int j = 0; j < SKB; j++) {
-                    {
-                        float dwo = 0.0f; // this warp's matrix
-                        uint32_t cw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                        {
-                            uint32_t W[12];
-                            // (template arguments must be constants: dispatch on the unrolled index)
-#define LUCE_TC_BLOCK(J)                                                                                             \
-    if (j == J) {                                                                                                    \
-        load_window<J>(myrow, W);                                                                                    \
-        dwo = half_bits_to_float(win_d16<J>(W));                                                                     \
-        win_codes<J>(W, cw);                                                                                         \
+                const uint8_t *myrow = sm + s * S::bytes + rowoff + mc * RAW_MAT;
+                // one block: its conversion into A slot ar, then the scales of the
+                // block LAG back (same stage for J >= LAG, else the previous one);
+                // the template arguments need J as a constant, hence a macro
+#define LUCE_TC_STEP(J)                                                                                              \
+    {                                                                                                                \
+        if (NMAT == 2 || ((J) & 1) == w2) {                                                                          \
+            uint32_t W[12], cw[8], hv[16];                                                                           \
+            load_window<J>(myrow, W);                                                                                \
+            win_codes<J>(W, cw);                                                                                     \
+            _Pragma("unroll") for (int m = 0; m < 8; m++) codes_to_half2(cw[m], hv[2 * m], hv[2 * m + 1]);          \
+            tmem_st16(tl + acol(ar.slot, mc), hv);                                                                   \
+            tmem_wait_st();                                                                                          \
+        }                                                                                                            \
+        tc_fence_before();                                                                                           \
+        __syncwarp();                                                                                                \
+        if (lane == 0)                                                                                               \
+            mbar_arrive(&afull[ar.slot]);                                                                            \
+        ar.next();                                                                                                   \
+        if ((J) >= LAG || st > 0) {                                                                                  \
+            const int es = (J) >= LAG ? s : sprev;                                                                   \
+            if (!tc_epilogue<NMAT>(acc, sm + es * S::bytes, rowoff, ((J) + SKB - LAG) % SKB, dr, dfull, dfree,       \
+                                   &sfree[es], tl, w2, nch, lane, abort_flag))                                       \
+                goto out_epi;                                                                                        \
+            dr.next();                                                                                               \
+        }                                                                                                            \
     }
-                            LUCE_TC_BLOCK(0)
-                            LUCE_TC_BLOCK(1)
-                            LUCE_TC_BLOCK(2)
-                            LUCE_TC_BLOCK(3)
-                            LUCE_TC_BLOCK(4)
-                            LUCE_TC_BLOCK(5)
-                            LUCE_TC_BLOCK(6)
-                            LUCE_TC_BLOCK(7)
-#undef LUCE_TC_BLOCK
-                        }
-                        float dw[NMAT];
-                        if constexpr (NMAT == 2) {
-                            const uint8_t *other = raw + (1 - mc) * RAW_MAT + r * RAW_ROW + 34 * j;
-                            const float dwx = half_bits_to_float(*reinterpret_cast<const uint16_t *>(other));
-                            dw[0] = mc == 0 ? dwo : dwx;
-                            dw[1] = mc == 0 ? dwx : dwo;
-                        } else {
-                            dw[0] = dwo;
-                        }
-                        const int as = (int)(gb % RA);
-                        if (!tc_wait_warp(&afree[as], ((gb / RA) & 1) ^ 1, abort_flag, lane))
-                            goto out_epi;
-                        if (NMAT == 2 || (j & 1) == hh) {
-                            uint32_t hv[16];
+                LUCE_TC_STEP(0)
+                LUCE_TC_STEP(1)
+                LUCE_TC_STEP(2)
+                LUCE_TC_STEP(3)
+                LUCE_TC_STEP(4)
+                LUCE_TC_STEP(5)
+                LUCE_TC_STEP(6)
+                LUCE_TC_STEP(7)
+#undef LUCE_TC_STEP
+            }
+            {
+                // the item's last LAG blocks (indices SKB - LAG .. SKB - 1 of its last stage)
+                const int s = sr.slot == 0 ? NS - 1 : (int)sr.slot - 1;
 #pragma unroll
-                            for (int m = 0; m < 8; m++)
-                                codes_to_half2(cw[m], hv[2 * m], hv[2 * m + 1]);
-                            tmem_st16(tl + acol<NMAT>(as, mc), hv);
-                            tmem_wait_st();
-                        }
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive(&afull[as]);
-                        if (pend && !tc_epilogue<NMAT>(acc, pdw, pgb,
-                                                       reinterpret_cast<const float *>(sm + ps * S::bytes + S::dx_off) +
-                                                           pj * TN,
-                                                       pj == SKB - 1, dfull, dfree, &sfree[ps], tl, hh, nch, lane,
-                                                       abort_flag))
-                            goto out_epi;
-                        pend = true;
-                        pgb = gb;
-                        ps = s;
-                        pj = j;
-#pragma unroll
-                        for (int m = 0; m < NMAT; m++)
-                            pdw[m] = dw[m];
-                        gb++;
-                    }
+                for (int k2 = LAG; k2 >= 1; k2--) {
+                    if (!tc_epilogue<NMAT>(acc, sm + s * S::bytes, rowoff, SKB - k2, dr, dfull, dfree, &sfree[s], tl,
+                                           w2, nch, lane, abort_flag))
+                        goto out_epi;
+                    dr.next();
                 }
             }
-            if (pend && !tc_epilogue<NMAT>(acc, pdw, pgb,
-                                           reinterpret_cast<const float *>(sm + ps * S::bytes + S::dx_off) + pj * TN,
-                                           pj == SKB - 1, dfull, dfree, &sfree[ps], tl, hh, nch, lane, abort_flag))
-                goto out_epi;
 
-            // ---- the item's results
+            // ---- the item's results: chunks w2, w2 + 2 of the tokens, rows 32q .. 32q+31
 #pragma unroll
-            for (int cc = 0; cc < 2; cc++) {
-                const int c = hh + 2 * cc;
+            for (int cc = 0; cc < CPW; cc++) {
+                const int c = w2 + 2 * cc;
                 if (c >= nch)
                     continue;
 #pragma unroll
@@ -590,7 +577,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_moe_tc(const TcArgs a)
                     const int p = item.p0 + n;
                     const int col = item.m0 + r;
                     if constexpr (NMAT == 2) {
-                        const float hv = swiglu(acc[cc][0][i], acc[cc][1][i], a.clamp);
+                        const float g = (i & 1) ? acc[cc][0][i >> 1].y : acc[cc][0][i >> 1].x;
+                        const float u = (i & 1) ? acc[cc][1][i >> 1].y : acc[cc][1][i >> 1].x;
+                        const float hv = swiglu(g, u, a.clamp);
                         const int row = item.e >= 0 ? a.routes[p] : p;
                         a.h[(size_t)row * a.M + col] = hv;
                         const int blk = (item.m0 >> 5) + q;
@@ -601,7 +590,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_moe_tc(const TcArgs a)
                         if (lane == 0)
                             a.hscale[(size_t)p * (a.M / QK) + blk] = half_bits_to_float(d16);
                     } else {
-                        a.y[(size_t)p * a.M + col] = acc[cc][0][i];
+                        a.y[(size_t)p * a.M + col] = (i & 1) ? acc[cc][0][i >> 1].y : acc[cc][0][i >> 1].x;
                     }
                 }
             }
@@ -779,6 +768,59 @@ bool tc_layout(int T, int k, int H, int I, TcLayout &L)
     return true;
 }
 
+// cuTensorMapEncodeTiled, from the driver through the runtime's entry-point
+// query (no link against the driver library); looked up once.
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+// Q8_0 rows [rows][nbK][34] as u16 elements; box = 8 blocks x 128 rows, no swizzle.
+bool map_q8_0_rows(CUtensorMap *m, const void *base, long long rows, int nbK)
+{
+    EncodeTiledFn f = encode_tiled();
+    if (!f || !base)
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)nbK * (Q8_0_BYTES / 2), (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)nbK * Q8_0_BYTES};
+    const cuuint32_t box[2] = {RAW_ROW / 2, TM};
+    const cuuint32_t estr[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// fp16 codes [P][K]; box = 64 codes (128 bytes) x 64 rows, 128-byte swizzle (rows past P read as zero).
+bool map_codes(CUtensorMap *m, const void *base, long long rows, int K)
+{
+    EncodeTiledFn f = encode_tiled();
+    if (!f || !base)
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {64, TN};
+    const cuuint32_t estr[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int NMAT> luce_status launch_tc(const TcArgs &args, cudaStream_t stream)
 {
     static luce_host::SmemLimit limit;
@@ -836,26 +878,15 @@ extern "C" __attribute__((visibility("hidden"))) luce_status luce_internal_moe_l
     const int Tk = T * k;
     cudaStream_t st = as_stream(stream);
 
-    luce_status s = luce_route_topk(logits, bias, T, E, k, ids, weights, stream);
-    if (s == LUCE_OK)
-        s = luce_quantize_q8_1(x, T, H, xq, stream);
-    if (s == LUCE_OK)
-        s = luce_moe_group(ids, T, k, E, counts, offsets, routes, stream);
-    if (s == LUCE_OK)
-        s = launch(k_tc_items, dim3(1), dim3(ITEM_THREADS), 0, st, (const int32_t *)counts, (const int32_t *)offsets, E,
-                   T, k, (int)shared, I / TM, H / TM, glu_items, down_items, nitems);
-    if (s == LUCE_OK)
-        s = launch(k_tc_gather, dim3((unsigned)(Tk + (shared ? T : 0))), dim3(128), 0, st,
-                   reinterpret_cast<const uint32_t *>(xq), (const int32_t *)offsets, (const int32_t *)routes, E, T, k,
-                   H / QK, x16, xscale, inv);
-    if (s != LUCE_OK)
-        return s;
-    TcArgs g{};
-    g.w[0] = reinterpret_cast<const uint8_t *>(w_gate);
-    g.w[1] = reinterpret_cast<const uint8_t *>(w_up);
-    g.ws[0] = reinterpret_cast<const uint8_t *>(ws_gate);
-    g.ws[1] = reinterpret_cast<const uint8_t *>(ws_up);
-    g.b16 = x16;
+    // the tensor maps first: a failure launches nothing
+    const long long P = (long long)Tk + T;
+    TcArgs g{}, d{};
+    if (!map_q8_0_rows(&g.tm_w[0], w_gate, (long long)E * I, H / QK) ||
+        !map_q8_0_rows(&g.tm_w[1], w_up, (long long)E * I, H / QK) || !map_codes(&g.tm_b, x16, P, H) ||
+        !map_q8_0_rows(&d.tm_w[0], w_down, (long long)E * H, I / QK) || !map_codes(&d.tm_b, h16, P, I) ||
+        (shared && (!map_q8_0_rows(&g.tm_ws[0], ws_gate, I, H / QK) || !map_q8_0_rows(&g.tm_ws[1], ws_up, I, H / QK) ||
+                    !map_q8_0_rows(&d.tm_ws[0], ws_down, H, I / QK))))
+        return LUCE_ERR_CUDA;
     g.bscale = xscale;
     g.items = glu_items;
     g.nitems = nitems;
@@ -868,20 +899,29 @@ extern "C" __attribute__((visibility("hidden"))) luce_status luce_internal_moe_l
     g.hq = reinterpret_cast<uint32_t *>(hq);
     g.h16 = h16;
     g.hscale = hscale;
-    s = launch_tc<2>(g, st);
-    if (s != LUCE_OK)
-        return s;
-    TcArgs d{};
-    d.w[0] = reinterpret_cast<const uint8_t *>(w_down);
-    d.ws[0] = reinterpret_cast<const uint8_t *>(ws_down);
-    d.b16 = h16;
     d.bscale = hscale;
     d.items = down_items;
     d.nitems = nitems + 1;
     d.M = H;
     d.nbK = I / QK;
     d.y = y;
-    s = launch_tc<1>(d, st);
+
+    luce_status s = luce_route_topk(logits, bias, T, E, k, ids, weights, stream);
+    if (s == LUCE_OK)
+        s = luce_quantize_q8_1(x, T, H, xq, stream);
+    if (s == LUCE_OK)
+        s = luce_moe_group(ids, T, k, E, counts, offsets, routes, stream);
+    if (s == LUCE_OK)
+        s = launch(k_tc_items, dim3(1), dim3(ITEM_THREADS), 0, st, (const int32_t *)counts, (const int32_t *)offsets, E,
+                   T, k, (int)shared, I / TM, H / TM, glu_items, down_items, nitems);
+    if (s == LUCE_OK)
+        s = launch(k_tc_gather, dim3((unsigned)(Tk + (shared ? T : 0))), dim3(128), 0, st,
+                   reinterpret_cast<const uint32_t *>(xq), (const int32_t *)offsets, (const int32_t *)routes, E, T, k,
+                   H / QK, x16, xscale, inv);
+    if (s == LUCE_OK)
+        s = launch_tc<2>(g, st);
+    if (s == LUCE_OK)
+        s = launch_tc<1>(d, st);
     if (s != LUCE_OK)
         return s;
     return launch(k_tc_combine, dim3((unsigned)((H / 4 + 255) / 256), (unsigned)T), dim3(256), 0, st, (const float *)y,
