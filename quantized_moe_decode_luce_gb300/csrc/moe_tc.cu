@@ -26,13 +26,14 @@
 // CTA per SM) takes items round-robin; each item streams its 128 rows over
 // all K in stages of 8 blocks (272 bytes a row).
 //
-// CTA roles (12 warps):
-//  * warps 8, 10, 11 -- producers: cp.async 16-byte copies of the raw Q8_0
-//    rows (dense [128][272] per matrix and stage), of the activation codes
-//    (fp16, laid out in the tensor core's 128-byte swizzled K-major form) and
-//    of the activation block scales; completion reaches the stage's mbarrier
-//    through cp.async.mbarrier.arrive.
-//  * warp 9, one thread -- issues tcgen05.mma (A from tensor memory, B from
+// CTA roles (11 warps):
+//  * warp 8 -- TMA: per stage one 2D tile of each weight matrix (128 rows x
+//    272 bytes, the Q8_0 rows seen as u16 elements, landing dense) and four
+//    128-byte-swizzled tiles of the activation codes (fp16, the tensor core's
+//    K-major layout), all completing on the stage's mbarrier; and an L2
+//    prefetch of the weight tiles two stages ahead.
+//  * warp 9 -- cp.async copies of the activation block scales ([block][token]).
+//  * warp 10, one thread -- issues tcgen05.mma (A from tensor memory, B from
 //    shared memory) and the tcgen05.commit arrivals.
 //  * warps 0-7 -- lane quarter q = warp & 3 (rows 32q .. 32q+31, the tensor
 //    memory lanes this warp may access), half h = warp >> 2.  They turn the
@@ -41,15 +42,15 @@
 //    product: half h converts the blocks of parity h), then read each block's
 //    exact sums back (tcgen05.ld) and accumulate isum * (d_w * d_x) in
 //    registers with packed fp32x2 multiply/FMA (half h takes the 16-token
-//    chunks c = h, h + 2).  At the end of an item the gate pair forms
+//    chunks h and h + 2).  At the end of an item the gate pair forms
 //    h = SwiGLU(g, u), stores h, its q8_1 blocks (each 32-row lane quarter is
 //    one q8_1 block of h per token) and the fp16 codes and scales the down
 //    product reads; the down product stores y.
-// A thread converts block b, then finishes block b - 1, so the MMAs of block
-// b run while the scales of block b - 1 are applied.  Every wait is bounded:
-// on timeout the kernel raises LUCE_FAULT_TIMEOUT, the other roles leave at
-// their next wait, and the CTA drains its copies and MMAs and frees its
-// tensor memory before returning.
+// A warp converts block b while the sums of block b - 2 load from tensor
+// memory, then applies their scales; so the MMAs of two blocks are in flight
+// behind the scale work.  Every wait is bounded: on timeout the kernel raises
+// LUCE_FAULT_TIMEOUT, the other roles leave at their next wait, and the CTA
+// drains its copies and MMAs and frees its tensor memory before returning.
 #include <algorithm>
 #include <climits>
 #include <cmath>
@@ -66,7 +67,7 @@ namespace {
 using namespace luce;
 
 constexpr int TM = 128;       // weight rows of one item (MMA M)
-constexpr int TN = 64;        // tokens of one item at most
+constexpr int TN = 64;        // tokens of one item at most (four 16-token chunks)
 constexpr int SKB = 8;        // 32-value blocks per stage
 constexpr int RA = 3;          // A slots in tensor memory
 constexpr int RD = 3;          // D slots in tensor memory
@@ -84,9 +85,11 @@ static_assert(RA == LAG + 1 && LAG < RD, "slot reuse ordering");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int RAW_ROW = SKB * Q8_0_BYTES; // 272: one row's stage of raw Q8_0 blocks
 constexpr int RAW_MAT = TM * RAW_ROW;     // 34,816
-constexpr int B_ATOM = TN * 128;          // one 64-value K column of the activation tile
-constexpr int B_BYTES = 4 * B_ATOM;       // 256 K values of 64 tokens, fp16
-constexpr int DX_BYTES = SKB * TN * 4;    // activation block scales [block][token]
+constexpr int B_ATOM = TN * 128;          // one 64-value K column of the activation tile (1024-aligned)
+constexpr int B_BYTES = 4 * B_ATOM;       // 256 K values of TN tokens, fp16
+constexpr int DX_BYTES = 2048;            // activation block scales [block][token] (SKB * TN * 4, padded)
+constexpr int PF_STAGES = 2;              // weight tiles are prefetched into L2 this many stages ahead
+static_assert(B_ATOM % 1024 == 0 && SKB * TN * 4 <= DX_BYTES, "stage layout");
 
 template <int NMAT> struct Stage {
     static constexpr int b_off = 0; // 1024-aligned (swizzle atoms)
@@ -98,11 +101,11 @@ template <int NMAT> struct Stage {
 };
 
 // Tensor memory columns: A slots first (16 columns = 32 fp16 codes of a row
-// per matrix), then D slots (64 columns = 64 tokens per matrix).
+// per matrix), then D slots (TN columns = TN tokens per matrix).
 constexpr int A_COLS = RA * 32;
 __device__ __forceinline__ uint32_t acol(int slot, int m) { return (uint32_t)(slot * 32 + 16 * m); }
-__device__ __forceinline__ uint32_t dcol(int slot, int m) { return (uint32_t)(A_COLS + slot * 128 + 64 * m); }
-static_assert(A_COLS + RD * 128 <= (int)TMEM_COLS, "tensor memory budget");
+__device__ __forceinline__ uint32_t dcol(int slot, int m) { return (uint32_t)(A_COLS + slot * 2 * TN + TN * m); }
+static_assert(A_COLS + RD * 2 * TN <= (int)TMEM_COLS, "tensor memory budget");
 
 struct TcItem {
     int e;  // expert, or -1: the shared expert
@@ -145,6 +148,14 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Hint: bring one 2D tile of a tensor map into L2.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
 
 // One 2D tile of a tensor map into shared memory, completing its bytes on `bar`.
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar)
@@ -194,6 +205,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
                      taddr),
                  "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
                  "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                  : "memory");
 }
 
@@ -309,58 +327,84 @@ template <int R> struct Ring {
     }
 };
 
-// Apply the block scales of one finished block to this warp's 16-token chunks
-// c = c0 + 2 cc (those below nch): acc[cc][m][i] += isum * (d_w[m] * d_x[i]),
-// pairs of tokens in packed fp32 arithmetic; then release the D slot (and the
-// stage, after its last block).
+// The scales of one finished block, applied in two halves around the
+// conversion of a later block so that the tensor-memory loads overlap it.
+// begin: wait for the block's sums, start loading chunk c0 (matrix 0), read
+// the block's weight scales.  finish: acc[cc][m][i] += isum * (d_w[m] *
+// d_x[i]) for the chunks c = c0 + 2 cc below nch (pairs of tokens in packed
+// fp32 arithmetic; chunk c0 + 2 is loaded here).
+template <int NMAT> struct EpiBlock {
+    uint32_t dv[NMAT][16];
+    float dw[NMAT];
+    const float *dxj;
+    uint32_t dslot;
+};
+
 template <int NMAT>
-__device__ __forceinline__ bool tc_epilogue(float2 (&acc)[CPW][NMAT][8], const uint8_t *stage, int rowoff, int j,
-                                            const Ring<RD> &dr, uint64_t *dfull, uint64_t *dfree, uint64_t *sfree_s,
-                                            uint32_t tl, int c0, int nch, int lane, volatile int *abort_flag)
+__device__ __forceinline__ bool epi_begin(EpiBlock<NMAT> &eb, const uint8_t *stage, int rowoff, int j,
+                                          const Ring<RD> &dr, uint64_t *dfull, uint32_t tl, int c0, int nch,
+                                          volatile int *abort_flag)
 {
     using S = Stage<NMAT>;
-    if (!tc_wait_warp(&dfull[dr.slot], dr.phase, abort_flag, lane))
+    if (!tc_wait(&dfull[dr.slot], dr.phase, abort_flag))
         return false;
+    __syncwarp();
     tc_fence_after();
-    float dw[NMAT]; // the weight scales of row r, block j (the stage is held until its last block is done)
+    eb.dslot = dr.slot;
+    // (loaded whether or not chunk c0 holds tokens: no branch around the asm outputs, which
+    // keeps them in registers; matrix 1 is loaded in epi_finish, so fewer registers are held)
+    tmem_ld16(tl + dcol(dr.slot, 0) + 16 * c0, eb.dv[0]);
 #pragma unroll
     for (int m = 0; m < NMAT; m++)
-        dw[m] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(stage + rowoff + m * RAW_MAT + Q8_0_BYTES * j));
-    const float *dxj = reinterpret_cast<const float *>(stage + S::dx_off) + j * TN;
+        eb.dw[m] =
+            half_bits_to_float(*reinterpret_cast<const uint16_t *>(stage + rowoff + m * RAW_MAT + Q8_0_BYTES * j));
+    eb.dxj = reinterpret_cast<const float *>(stage + S::dx_off) + j * TN;
+    return true;
+}
+
+template <int NMAT>
+__device__ __forceinline__ void epi_fma(float2 (&acc)[NMAT][8], const uint32_t (&dv)[NMAT][16], const float (&dw)[NMAT],
+                                        const float *dx)
+{
+    const float4 *x4 = reinterpret_cast<const float4 *>(dx);
 #pragma unroll
-    for (int cc = 0; cc < CPW; cc++) {
-        const int c = c0 + 2 * cc;
-        if (c < nch) {
-            const float4 *x4 = reinterpret_cast<const float4 *>(dxj + 16 * c);
+    for (int i4 = 0; i4 < 4; i4++) {
+        const float4 x = x4[i4];
 #pragma unroll
-            for (int m = 0; m < NMAT; m++) {
-                const float2 w2 = make_float2(dw[m], dw[m]);
-                uint32_t dv[16];
-                tmem_ld16(tl + dcol(dr.slot, m) + 16 * c, dv);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i4 = 0; i4 < 4; i4++) {
-                    const float4 x = x4[i4];
-                    const float2 s0 = __fmul2_rn(w2, make_float2(x.x, x.y));
-                    const float2 s1 = __fmul2_rn(w2, make_float2(x.z, x.w));
-                    acc[cc][m][2 * i4] = __ffma2_rn(
-                        make_float2(__uint_as_float(dv[4 * i4]), __uint_as_float(dv[4 * i4 + 1])), s0,
-                        acc[cc][m][2 * i4]);
-                    acc[cc][m][2 * i4 + 1] = __ffma2_rn(
-                        make_float2(__uint_as_float(dv[4 * i4 + 2]), __uint_as_float(dv[4 * i4 + 3])), s1,
-                        acc[cc][m][2 * i4 + 1]);
-                }
-            }
+        for (int m = 0; m < NMAT; m++) {
+            const float2 w2 = make_float2(dw[m], dw[m]);
+            const float2 s0 = __fmul2_rn(w2, make_float2(x.x, x.y));
+            const float2 s1 = __fmul2_rn(w2, make_float2(x.z, x.w));
+            acc[m][2 * i4] = __ffma2_rn(make_float2(__uint_as_float(dv[m][4 * i4]), __uint_as_float(dv[m][4 * i4 + 1])),
+                                        s0, acc[m][2 * i4]);
+            acc[m][2 * i4 + 1] = __ffma2_rn(
+                make_float2(__uint_as_float(dv[m][4 * i4 + 2]), __uint_as_float(dv[m][4 * i4 + 3])), s1,
+                acc[m][2 * i4 + 1]);
         }
     }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) {
-        mbar_arrive(&dfree[dr.slot]);
-        if (j == SKB - 1)
-            mbar_arrive(sfree_s);
+}
+
+template <int NMAT>
+__device__ __forceinline__ void epi_finish(float2 (&acc)[CPW][NMAT][8], EpiBlock<NMAT> &eb, uint32_t tl, int c0,
+                                           int nch)
+{
+    if constexpr (NMAT == 2)
+        tmem_ld16(tl + dcol(eb.dslot, 1) + 16 * c0, eb.dv[1]);
+    tmem_wait_ld();
+    if (c0 < nch)
+        epi_fma<NMAT>(acc[0], eb.dv, eb.dw, eb.dxj + 16 * c0);
+#pragma unroll
+    for (int cc = 1; cc < CPW; cc++) {
+        const int c = c0 + 2 * cc;
+        if (c < nch) {
+            uint32_t dv[NMAT][16];
+#pragma unroll
+            for (int m = 0; m < NMAT; m++)
+                tmem_ld16(tl + dcol(eb.dslot, m) + 16 * c, dv[m]);
+            tmem_wait_ld();
+            epi_fma<NMAT>(acc[cc], dv, eb.dw, eb.dxj + 16 * c);
+        }
     }
-    return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -431,6 +475,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_moe_tc(const __grid_constant_
                         for (int kc = 0; kc < 4; kc++)
                             tma_load_2d(stg + S::b_off + kc * B_ATOM, &a.tm_b, st * (SKB * QK) + kc * 64, item.p0,
                                         &full[s]);
+                        // the weight tiles PF_STAGES ahead (this item's, else the CTA's next item's) into L2
+                        int pst = st + PF_STAGES, pit = it;
+                        if (pst >= nst) {
+                            pst -= nst;
+                            pit += gridDim.x;
+                        }
+                        if (pit < nitems) {
+                            const TcItem pi = pit == it ? item : a.items[pit];
+                            const int py = pi.e >= 0 ? pi.e * a.M + pi.m0 : pi.m0;
+#pragma unroll
+                            for (int m = 0; m < NMAT; m++)
+                                tma_prefetch_2d(pi.e >= 0 ? &a.tm_w[m] : &a.tm_ws[m], pst * (RAW_ROW / 2), py);
+                        }
                     }
                 } else {
                     // block scales, transposed to [block][token]
@@ -515,31 +572,47 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_moe_tc(const __grid_constant_
                 if (!tc_wait_warp(&full[s], sr.phase, abort_flag, lane))
                     goto out_epi;
                 const uint8_t *myrow = sm + s * S::bytes + rowoff + mc * RAW_MAT;
-                // one block: its conversion into A slot ar, then the scales of the
-                // block LAG back (same stage for J >= LAG, else the previous one);
-                // the template arguments need J as a constant, hence a macro
+                // one block J: start the scales of the block LAG back (same stage for
+                // J >= LAG, else the previous one), convert block J into A slot ar
+                // while those loads run, finish the scales, then one fence for both
+                // arrivals; the template arguments need J as a constant, hence a macro
 #define LUCE_TC_STEP(J)                                                                                              \
     {                                                                                                                \
-        if (NMAT == 2 || ((J) & 1) == w2) {                                                                          \
-            uint32_t W[12], cw[8], hv[16];                                                                           \
+        const bool has_epi = (J) >= LAG || st > 0;                                                                   \
+        const int es = (J) >= LAG ? s : sprev;                                                                       \
+        constexpr int ej = ((J) + SKB - LAG) % SKB;                                                                  \
+        EpiBlock<NMAT> eb;                                                                                           \
+        if (has_epi && !epi_begin<NMAT>(eb, sm + es * S::bytes, rowoff, ej, dr, dfull, tl, w2, nch, abort_flag))     \
+            goto out_epi;                                                                                            \
+        const bool conv = NMAT == 2 || ((J) & 1) == w2;                                                              \
+        if (conv) {                                                                                                  \
+            uint32_t W[12], cw[8];                                                                                   \
             load_window<J>(myrow, W);                                                                                \
             win_codes<J>(W, cw);                                                                                     \
-            _Pragma("unroll") for (int m = 0; m < 8; m++) codes_to_half2(cw[m], hv[2 * m], hv[2 * m + 1]);          \
-            tmem_st16(tl + acol(ar.slot, mc), hv);                                                                   \
-            tmem_wait_st();                                                                                          \
+            _Pragma("unroll") for (int hf = 0; hf < 2; hf++) {                                                      \
+                uint32_t hv[8];                                                                                      \
+                _Pragma("unroll") for (int m = 0; m < 4; m++)                                                       \
+                    codes_to_half2(cw[4 * hf + m], hv[2 * m], hv[2 * m + 1]);                                        \
+                tmem_st8(tl + acol(ar.slot, mc) + 8 * hf, hv);                                                       \
+            }                                                                                                        \
         }                                                                                                            \
+        if (has_epi)                                                                                                 \
+            epi_finish<NMAT>(acc, eb, tl, w2, nch);                                                                  \
+        if (conv)                                                                                                    \
+            tmem_wait_st();                                                                                          \
         tc_fence_before();                                                                                           \
         __syncwarp();                                                                                                \
-        if (lane == 0)                                                                                               \
+        if (lane == 0) {                                                                                             \
             mbar_arrive(&afull[ar.slot]);                                                                            \
-        ar.next();                                                                                                   \
-        if ((J) >= LAG || st > 0) {                                                                                  \
-            const int es = (J) >= LAG ? s : sprev;                                                                   \
-            if (!tc_epilogue<NMAT>(acc, sm + es * S::bytes, rowoff, ((J) + SKB - LAG) % SKB, dr, dfull, dfree,       \
-                                   &sfree[es], tl, w2, nch, lane, abort_flag))                                       \
-                goto out_epi;                                                                                        \
-            dr.next();                                                                                               \
+            if (has_epi) {                                                                                           \
+                mbar_arrive(&dfree[dr.slot]);                                                                        \
+                if (ej == SKB - 1)                                                                                   \
+                    mbar_arrive(&sfree[es]);                                                                         \
+            }                                                                                                        \
         }                                                                                                            \
+        ar.next();                                                                                                   \
+        if (has_epi)                                                                                                 \
+            dr.next();                                                                                               \
     }
                 LUCE_TC_STEP(0)
                 LUCE_TC_STEP(1)
@@ -556,9 +629,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_moe_tc(const __grid_constant_
                 const int s = sr.slot == 0 ? NS - 1 : (int)sr.slot - 1;
 #pragma unroll
                 for (int k2 = LAG; k2 >= 1; k2--) {
-                    if (!tc_epilogue<NMAT>(acc, sm + s * S::bytes, rowoff, SKB - k2, dr, dfull, dfree, &sfree[s], tl,
-                                           w2, nch, lane, abort_flag))
+                    EpiBlock<NMAT> eb;
+                    if (!epi_begin<NMAT>(eb, sm + s * S::bytes, rowoff, SKB - k2, dr, dfull, tl, w2, nch, abort_flag))
                         goto out_epi;
+                    epi_finish<NMAT>(acc, eb, tl, w2, nch);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&dfree[dr.slot]);
+                        if (k2 == 1)
+                            mbar_arrive(&sfree[s]);
+                    }
                     dr.next();
                 }
             }
