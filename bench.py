@@ -58,7 +58,42 @@ def parse():
     p.add_argument("--layers", type=int, default=None, help="(debug) fewer layers; invalid as a bench number")
     p.add_argument("--input-steps", type=int, default=None,
                    help="pre-drawn input steps to cycle (default 64; fewer keeps profiling runs short)")
+    p.add_argument("--layer-only", choices=["decode_layer", "verify_layer", "prefill_layer"], default=None,
+                   help="(profiling) run one layer workload --reps times through luce_moe_layer and print its "
+                        "event-timed µs per layer; no bench line")
+    p.add_argument("--reps", type=int, default=1)
     return p.parse_args()
+
+
+def layer_only(args):
+    """One layer workload (the parity-test inputs) through luce_moe_layer, `reps`
+    times after one untimed call: the short, self-contained command that the
+    ncu summaries in profiles/ are taken from."""
+    import torch
+
+    from quantized_moe_decode_luce_gb300 import binding as Bd
+    from quantized_moe_decode_luce_gb300 import build as Bl
+    from quantized_moe_decode_luce_gb300.layer import MoEStep
+    Bl.build()
+    Bd.lib()
+    wl = W.WORKLOADS[args.layer_only]
+    dl = W.device_layer(wl, wl.seed, "cuda")
+    x = torch.from_numpy(W.activations(W.rng(wl.seed, 2), wl.T, wl.H)).cuda()
+    lg, b = W.router_logits(W.rng(wl.seed, 3), wl)
+    lg = torch.from_numpy(lg).cuda()
+    b = torch.from_numpy(b).cuda() if b is not None else None
+    st = MoEStep(wl.T, wl.H, wl.I, wl.E, wl.k, wl.shared, wl.clamp)
+    st.run(dl, x, lg, b)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record()
+    for _ in range(args.reps):
+        st.run(dl, x, lg, b)
+    ev[1].record()
+    torch.cuda.synchronize()
+    print(json.dumps({"workload": wl.name, "path": _path_label(st), "reps": args.reps,
+                      "us_per_layer": ev[0].elapsed_time(ev[1]) * 1e3 / max(1, args.reps),
+                      "device_faults": Bd.luce_get_fault()}))
 
 
 def measured_peaks():
@@ -863,6 +898,9 @@ def run_ours(args, wl, layers):
 
 def main():
     args = parse()
+    if args.layer_only:
+        layer_only(args)
+        return
     wl = W.WORKLOADS["decode_stack43"]
     if args.input_steps:
         wl = W.Workload(**{**wl.__dict__, "steps": args.input_steps})
