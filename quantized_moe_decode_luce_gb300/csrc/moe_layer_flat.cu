@@ -213,7 +213,54 @@ struct LayerPlan {
     int SR;       // down items per stage (whole experts' row runs where they fit)
 };
 
-__device__ LayerPlan make_plan(const LayerArgs &a, int nvr, int bx, int nb)
+// The routed gate/up row where CTA b of nb starts: the rows of the nvr
+// virtual experts are laid end to end and split so that every CTA gets an
+// equal share of their cost, a row of an expert with c columns costing 4 + c
+// (streaming the row, measured at about four dots' time, plus one dot per column).  vcols == null:
+// every expert has one column (equal rows).  Monotone in b; b = nb gives the
+// end of the rows.
+__device__ int routed_row_at(const LayerArgs &a, int nvr, const int *vcols, int b, int nb)
+{
+    if (!vcols)
+        return (int)((unsigned)nvr * (unsigned)a.I * (unsigned)b / (unsigned)nb); // <= 2^21 * 152
+    unsigned long long tot = 0;
+    for (int v = 0; v < nvr; v++)
+        tot += (unsigned long long)(4 + vcols[v]) * (unsigned)a.I;
+    const unsigned long long target = tot * (unsigned)b / (unsigned)nb;
+    unsigned long long acc = 0;
+    for (int v = 0; v < nvr; v++) {
+        const unsigned long long c = (unsigned long long)(4 + vcols[v]) * (unsigned)a.I;
+        if (acc + c > target)
+            return v * a.I + (int)((target - acc) / (unsigned)(4 + vcols[v]));
+        acc += c;
+    }
+    return nvr * a.I;
+}
+
+// The flat down item (v, n) = v H + n where CTA b of nb starts: items of
+// virtual expert v (the shared expert last, with T columns) cost 2 + its
+// columns (a down row is half a gate/up row pair), and every CTA gets an
+// equal share of the cost.  vcols == null: equal items.
+__device__ int down_item_at(const LayerArgs &a, int nvr, int nv, const int *vcols, int b, int nb)
+{
+    auto cols = [&](int v) { return v < nvr ? vcols[v] : a.T; };
+    if (!vcols)
+        return (int)((unsigned)nv * (unsigned)a.H * (unsigned)b / (unsigned)nb); // <= 65 * 2^15 * 152
+    unsigned long long tot = 0;
+    for (int v = 0; v < nv; v++)
+        tot += (unsigned long long)(2 + cols(v)) * (unsigned)a.H;
+    const unsigned long long target = tot * (unsigned)b / (unsigned)nb;
+    unsigned long long acc = 0;
+    for (int v = 0; v < nv; v++) {
+        const unsigned long long c = (unsigned long long)(2 + cols(v)) * (unsigned)a.H;
+        if (acc + c > target)
+            return v * a.H + (int)((target - acc) / (unsigned)(2 + cols(v)));
+        acc += c;
+    }
+    return nv * a.H;
+}
+
+__device__ LayerPlan make_plan(const LayerArgs &a, int nvr, int bx, int nb, const int *vcols = nullptr)
 {
     LayerPlan q;
     const int RU = a.RU;
@@ -226,9 +273,8 @@ __device__ LayerPlan make_plan(const LayerArgs &a, int nvr, int bx, int nb)
         q.ps0 = q.s0 / RU;
         q.NPs = q.s1 > q.s0 ? (q.s1 + RU - 1) / RU - q.ps0 : 0;
     }
-    const unsigned Q = (unsigned)nvr * (unsigned)a.I; // <= 2^21: Q * bx fits 32 bits
-    q.q0 = (int)(Q * (unsigned)bx / (unsigned)nb);
-    q.q1 = (int)(Q * (unsigned)(bx + 1) / (unsigned)nb);
+    q.q0 = routed_row_at(a, nvr, vcols, bx, nb);
+    q.q1 = routed_row_at(a, nvr, vcols, bx + 1, nb);
     q.pr0 = q.q0 / RU;
     q.NPr = q.q1 > q.q0 ? (q.q1 + RU - 1) / RU - q.pr0 : 0;
     q.NPglu = q.NPs + q.NPr;
@@ -236,9 +282,8 @@ __device__ LayerPlan make_plan(const LayerArgs &a, int nvr, int bx, int nb)
     q.nrows = (int)((unsigned)a.H * (unsigned)(bx + 1) / (unsigned)nb) - q.n0;
     q.it0 = q.it1 = 0;
     if (a.flat) {
-        const unsigned NI = (unsigned)q.NV * (unsigned)a.H; // <= 65 * 2^15: NI * bx fits 32 bits
-        q.it0 = (int)(NI * (unsigned)bx / (unsigned)nb);
-        q.it1 = (int)(NI * (unsigned)(bx + 1) / (unsigned)nb);
+        q.it0 = down_item_at(a, nvr, q.NV, vcols, bx, nb);
+        q.it1 = down_item_at(a, nvr, q.NV, vcols, bx + 1, nb);
         q.nrb = q.rpb = q.rlast = q.spr = q.slast = 0;
         q.SR = a.SR;
         q.NPd = (q.it1 - q.it0 + q.SR - 1) / q.SR;
@@ -362,6 +407,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     __shared__ int v_e[MAX_V], v_first[MAX_V], v_ncols[MAX_V];
     __shared__ uint32_t sel_bits[MAX_T][MAX_E / 32]; // expert e selected by token t
     __shared__ int s_abort;
+    __shared__ int s_issued; // stages requested so far (written by the producer after each request)
     __shared__ int s_nvr;   // routed virtual experts
     __shared__ unsigned long long s_c0; // barrier count at the start
 
@@ -388,6 +434,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         }
         fence_mbar_init();
         s_abort = 0;
+        s_issued = 0;
     }
     __syncthreads(); // barriers initialized
     int issued = 0;  // producer lane 0: stages requested
@@ -395,8 +442,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         // the shared expert's parts do not depend on the previous kernel:
         // request them before waiting for it
         #pragma unroll 1
-        for (; issued < P1.NPs && issued < a.NS; issued++)
+        for (; issued < P1.NPs && issued < a.NS; issued++) {
             issue_stage(a, P1, issued, ring, full, pol, v_e);
+            __threadfence_block(); // the stage's expect_tx arrival before its count
+            *(volatile int *)&s_issued = issued + 1;
+        }
     }
     if (warp == CW) {
         // the inputs of the routing into L2 (a hint)
@@ -412,18 +462,32 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
 
     bool dead = false;
     // Waits for stage s (slot s % NS, use s / NS); false if this CTA gave up
-    // (warp-collective: every lane takes the same branch).  NS is a multiple
-    // of NG, so a slot's gate/up parts all belong to one consumer group,
-    // which consumes them in order; every consumer warp consumes the down
-    // stages in order, after every gate/up part.  So when a warp waits for
-    // use u of a slot, it has itself seen use u - 1 complete, and the parity
-    // of u is unambiguous.
+    // (warp-collective: every lane takes the same branch).  Consumer groups
+    // take the gate/up parts round-robin and share the ring's slots, so a
+    // group may reach part s while the slot still shows an older use of the
+    // same parity: it first waits until the producer has requested stage s
+    // (s_issued > s; the request arms the slot's phase for this use), and only
+    // then for the phase's parity.  Every consumer warp consumes the down
+    // stages in order, after every gate/up part.
     auto wait_stage = [&](int s) -> bool {
         if (__any_sync(FULL, *(volatile int *)&s_abort != 0))
             dead = true;
         if (dead)
             return false;
-        const bool got = __all_sync(FULL, mbar_wait_bounded(&full[s % a.NS], (uint32_t)(s / a.NS) & 1u));
+        bool req = *(volatile int *)&s_issued > s;
+        if (!__all_sync(FULL, req)) {
+            const unsigned long long t0 = global_timer_ns();
+            for (;;) {
+                __nanosleep(32);
+                req = *(volatile int *)&s_issued > s;
+                if (__all_sync(FULL, req) || __any_sync(FULL, *(volatile int *)&s_abort != 0) ||
+                    __any_sync(FULL, global_timer_ns() - t0 > WAIT_LIMIT_NS))
+                    break;
+            }
+        }
+        __threadfence_block(); // the request's arrival before the parity test
+        const bool got =
+            __all_sync(FULL, req) && __all_sync(FULL, mbar_wait_bounded(&full[s % a.NS], (uint32_t)(s / a.NS) & 1u));
         if (!got) {
             if (lane == 0) {
                 atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
@@ -657,7 +721,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         }
         __syncthreads(); // tables, weights and route list in shared memory
     }
-    const LayerPlan P = T == 1 ? P1 : make_plan(a, s_nvr, bx, nb);
+    const LayerPlan P = T == 1 ? P1 : make_plan(a, s_nvr, bx, nb, v_ncols);
 
     if (warp == CW) {
         // ---------------- the producer: every stage of this CTA ----------------
@@ -678,6 +742,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
             }
             issue_stage(a, P, issued, ring, full, pol, v_e);
             issued++;
+            __threadfence_block(); // the stage's expect_tx arrival before its count
+            *(volatile int *)&s_issued = issued;
         }
         // no bulk copy may still be writing shared memory when the CTA exits
         #pragma unroll 1
@@ -855,6 +921,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     const int v_lo = FLAT ? (int)(P.it0 / a.H) : 0;
     const int v_hi = FLAT ? (P.it1 > P.it0 ? (int)((P.it1 - 1) / a.H) : v_lo) : 0;
     const int nhrows = FLAT ? (v_hi - v_lo + 1) * T : nslots;
+    if (FLAT && nhrows > a.hq_rows && tid == 0 && !*(volatile int *)&s_abort) {
+        // (the host sizes hq_rows for every split; never expected)
+        atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
+        *(volatile int *)&s_abort = 1;
+    }
+    named_barrier(BAR_CONS, CTHREADS);
     // (16-byte loads by every consumer thread: a few KB, so one round trip
     // to L2 rather than many small bulk copies)
     if (!*(volatile int *)&s_abort) {
@@ -1042,11 +1114,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
             for (int d = da; d < db; d++)
                 mbar_arrive(&empty[(d0 + d) % a.NS]);
     };
-    // Down stages go in windows: all of them when they fit the ring at once,
-    // else half the ring at a time (the producer fills the other half).
+    // Down stages go one at a time: each warp releases a stage as soon as it
+    // has its rows of it, so the producer keeps the rest of the ring in flight.
     // flat items [it0, it1) of the list over (v, n), n < H; y to the workspace
     {
-        const int WD = P.NPd <= a.NS ? max(P.NPd, 1) : max(1, a.NS / 2);
+        const int WD = 1;
         const int it0 = (int)P.it0, ni = (int)(P.it1 - P.it0);
         #pragma unroll 1
         for (int w = 0; w < P.NPd; w += WD) {
@@ -1176,8 +1248,9 @@ extern "C" __attribute__((visibility("hidden"))) luce_status luce_internal_moe_l
     // the workspace.
     a.flat = 1;
     {
+        // a CTA's cost share over the cheapest items (cost 3 each, of at most 2 + T)
         const long long nv_max = std::min(E, T * k) + (has_ws ? 1 : 0);
-        const long long items_max = (nv_max * H + nb - 1) / nb;
+        const long long items_max = ((2LL + T) * nv_max * H + 3LL * nb - 1) / (3LL * nb) + 1;
         const int span = (int)((items_max + H - 1) / H) + 1; // experts a range of items_max can touch
         a.hq_rows = span * T;
     }
@@ -1193,8 +1266,8 @@ extern "C" __attribute__((visibility("hidden"))) luce_status luce_internal_moe_l
     // about four bulk copies in flight (measured on GB300: four 16 KB copies
     // per SM reach ~7 TB/s, four 4 KB copies ~2.3 TB/s), so a copy should be
     // at least 16 KB: the smallest RU <= 16 with RU rbg >= 16 KB, halved while
-    // the ring holds fewer than two stages.  Then CW / RU consumer groups if
-    // the ring gives each a slot, else as many groups as slots.
+    // the ring holds fewer than two stages.  CW / RU consumer groups take the
+    // parts round-robin and share every slot of the ring.
     if (budget < fixed + 2 * ((size_t)std::max(2 * a.rbg, a.rbd) + 16))
         return LUCE_ERR_UNSUPPORTED;
     const size_t ring = budget - fixed;
@@ -1206,10 +1279,10 @@ extern "C" __attribute__((visibility("hidden"))) luce_status luce_internal_moe_l
     a.RU = RU;
     a.stage_bytes = std::max(2 * RU * a.rbg, a.rbd);
     const int ns = (int)std::min<size_t>(32, ring / ((size_t)a.stage_bytes + 16));
-    a.NG = ns >= CW / RU ? CW / RU : std::max(1, ns);
+    a.NG = CW / RU; // consumer groups share the slots (ordered by the producer's request count)
     a.SR = a.stage_bytes / a.rbd;
-    a.NS = ns - ns % a.NG; // a multiple of NG: each slot's gate/up parts belong to one consumer group
-    if (a.NS < a.NG)
+    a.NS = ns;
+    if (a.NS < 2)
         return LUCE_ERR_UNSUPPORTED;
     const size_t smem = (size_t)a.NS * a.stage_bytes + (size_t)2 * a.NS * sizeof(uint64_t) + fixed;
     cudaStream_t st = as_stream(stream);
