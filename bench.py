@@ -83,6 +83,8 @@ def layer_only(args):
     lg = torch.from_numpy(lg).cuda()
     b = torch.from_numpy(b).cuda() if b is not None else None
     st = MoEStep(wl.T, wl.H, wl.I, wl.E, wl.k, wl.shared, wl.clamp)
+    if args.path == "split":
+        st.path = "split"
     st.run(dl, x, lg, b)
     torch.cuda.synchronize()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
