@@ -219,6 +219,22 @@ struct LayerPlan {
 // (streaming the row, measured at about four dots' time, plus one dot per column).  vcols == null:
 // every expert has one column (equal rows).  Monotone in b; b = nb gives the
 // end of the rows.
+// Bounded wait that parks the thread in hardware until the phase completes
+// (or a 10 us suspend hint runs out), so a waiter wakes as soon as its data
+// or slot is there instead of after a back-off sleep.
+__device__ __forceinline__ bool mbar_wait_parked(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const unsigned long long t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 10000))
+            return true;
+        if (global_timer_ns() - t0 > WAIT_LIMIT_NS)
+            return false;
+    }
+}
+
 __device__ int routed_row_at(const LayerArgs &a, int nvr, const int *vcols, int b, int nb)
 {
     if (!vcols)
@@ -487,7 +503,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         }
         __threadfence_block(); // the request's arrival before the parity test
         const bool got =
-            __all_sync(FULL, req) && __all_sync(FULL, mbar_wait_bounded(&full[s % a.NS], (uint32_t)(s / a.NS) & 1u));
+            __all_sync(FULL, req) && __all_sync(FULL, mbar_wait_parked(&full[s % a.NS], (uint32_t)(s / a.NS) & 1u));
         if (!got) {
             if (lane == 0) {
                 atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
@@ -735,7 +751,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
             const int slot = issued % a.NS, use = issued / a.NS;
             // the slot's previous stage released by its consumers (the wait
             // sleeps rather than spins)
-            if (use > 0 && !mbar_wait_bounded(&empty[slot], (uint32_t)(use - 1) & 1u)) {
+            if (use > 0 && !mbar_wait_parked(&empty[slot], (uint32_t)(use - 1) & 1u)) {
                 atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
                 *(volatile int *)&s_abort = 1;
                 break;
