@@ -1069,6 +1069,85 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                 return;
             }
         }
+        if (!two) {
+            // Two items at a time (their dot chains interleave; each item's
+            // arithmetic and order are those of the one-item loop below).  Two
+            // items of the same expert share their hq blocks.
+            #pragma unroll 1
+            for (int q = c0i; q < c1i; q += 2) { // warp-uniform
+                const bool live1 = q + 1 < c1i;
+                int v1 = v, m1 = m + 1;
+                if (m1 >= rows) {
+                    m1 -= rows;
+                    v1++;
+                }
+                int first0 = 0, nc0 = 0, first1 = 0, nc1 = 0;
+                item_cols(v, first0, nc0);
+                if (live1)
+                    item_cols(v1, first1, nc1);
+                const int r0 = i - ib0, d0s = r0 / P.SR;
+                const uint8_t *wr0 =
+                    ring + (size_t)((d0 + sd0 + d0s) % a.NS) * a.stage_bytes + (size_t)(r0 - d0s * P.SR) * a.rbd;
+                const int r1 = r0 + 1, d1s = r1 / P.SR;
+                const uint8_t *wr1 =
+                    ring + (size_t)((d0 + sd0 + d1s) % a.NS) * a.stage_bytes + (size_t)(r1 - d1s * P.SR) * a.rbd;
+                const bool same = live1 && v1 == v;
+                const int ncm = max(nc0, nc1);
+                #pragma unroll 1
+                for (int cb = 0; cb < ncm; cb += TT) {
+                    float acc0[TT], acc1[TT];
+                    uint32_t xs0[TT], xs1[TT];
+#pragma unroll
+                    for (int c = 0; c < TT; c++) {
+                        acc0[c] = acc1[c] = 0.0f;
+                        xs0[c] = smem_addr(cb + c < nc0 ? hrow(v, first0, cb + c) : act);
+                        xs1[c] = smem_addr(live1 && cb + c < nc1 ? hrow(v1, first1, cb + c) : act);
+                    }
+                    const uint32_t wsa0 = smem_addr(wr0), wsa1 = smem_addr(live1 ? wr1 : wr0);
+                    for (int jb = 0; jb < nbl; jb++) {
+                        const int b = rowmap_block(dmap, lane, jb);
+                        Q80Block wb0, wb1;
+                        load_q8_0_sh(wsa0, b, wb0);
+                        load_q8_0_sh(wsa1, b, wb1);
+#pragma unroll
+                        for (int c = 0; c < TT; c++) {
+                            if (cb + c < nc0) {
+                                Q81Block xb;
+                                load_q8_1_sh(xs0[c] + 4u * (uint32_t)xblock_word(b, hpad), xb);
+                                acc0[c] = fmaf(wb0.d * xb.d, (float)dot_q8_block(wb0.q, xb.q), acc0[c]);
+                                if (same)
+                                    acc1[c] = fmaf(wb1.d * xb.d, (float)dot_q8_block(wb1.q, xb.q), acc1[c]);
+                            }
+                            if (live1 && !same && cb + c < nc1) {
+                                Q81Block xb;
+                                load_q8_1_sh(xs1[c] + 4u * (uint32_t)xblock_word(b, hpad), xb);
+                                acc1[c] = fmaf(wb1.d * xb.d, (float)dot_q8_block(wb1.q, xb.q), acc1[c]);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int c = 0; c < TT; c++) {
+                        if (cb + c < nc0) {
+                            const float y = warp_sum(acc0[c]);
+                            if (lane == 0)
+                                put(col_slot(v, first0, cb + c), v, m, y);
+                        }
+                        if (live1 && cb + c < nc1) {
+                            const float y = warp_sum(acc1[c]);
+                            if (lane == 0)
+                                put(col_slot(v1, first1, cb + c), v1, m1, y);
+                        }
+                    }
+                }
+                i += 2;
+                m += 2;
+                while (m >= rows) {
+                    m -= rows;
+                    v++;
+                }
+            }
+            return;
+        }
         // warp-uniform trip count: the chunk's item pairs (or items)
         #pragma unroll 1
         for (int q = c0i; q < c1i; q += step) {
@@ -1130,11 +1209,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
             for (int d = da; d < db; d++)
                 mbar_arrive(&empty[(d0 + d) % a.NS]);
     };
-    // Down stages go one at a time: each warp releases a stage as soon as it
-    // has its rows of it, so the producer keeps the rest of the ring in flight.
+    // Down stages go two at a time (one when rows go two to a warp): each warp
+    // takes two items of the window, then releases its stages, so the
+    // producer keeps the rest of the ring in flight.
     // flat items [it0, it1) of the list over (v, n), n < H; y to the workspace
     {
-        const int WD = 1;
+        const int WD = two ? 1 : 2; // two items per warp and window (one each when rows go two to a warp)
         const int it0 = (int)P.it0, ni = (int)(P.it1 - P.it0);
         #pragma unroll 1
         for (int w = 0; w < P.NPd; w += WD) {
