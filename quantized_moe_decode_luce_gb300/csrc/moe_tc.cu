@@ -72,11 +72,13 @@ constexpr int SKB = 8;        // 32-value blocks per stage
 constexpr int RA = 3;          // A slots in tensor memory
 constexpr int RD = 3;          // D slots in tensor memory
 constexpr int LAG = 2;         // a warp converts block b, then applies the scales of block b - LAG
-constexpr int EPI_WARPS = 8;   // convert + epilogue warps (0 .. 7): two per tensor-memory lane quarter
-constexpr int CPW = 2;         // 16-token chunks per epilogue warp
-constexpr int PROD_WARP0 = 8;  // producers: 8 (tensor-map tiles), 9 (activation block scales)
-constexpr int MMA_WARP = 10;
-constexpr int TC_THREADS = 11 * 32;
+constexpr int EPQ = 2;                   // convert + epilogue warps per tensor-memory lane quarter
+constexpr int EPI_WARPS = 4 * EPQ;       // warps 0 .. EPI_WARPS-1
+constexpr int CPW = 4 / EPQ;             // 16-token chunks per epilogue warp
+constexpr int PROD_WARP0 = EPI_WARPS;    // producers: tensor-map tiles, activation block scales
+constexpr int MMA_WARP = EPI_WARPS + 2;
+constexpr int TC_THREADS = (EPI_WARPS + 3) * 32;
+static_assert(EPQ == 2 || EPQ == 4, "chunk and conversion split");
 constexpr int FULL_ARRIVALS = 33; // a stage is full: the tiles' arrival + bytes, 32 lanes of scale copies
 // A slot reuse needs no wait of its own: a warp converts block b after it applied the
 // scales of block b - LAG - 1 = b - RA, whose MMAs (the last readers of that slot) it
@@ -331,8 +333,8 @@ template <int R> struct Ring {
 // conversion of a later block so that the tensor-memory loads overlap it.
 // begin: wait for the block's sums, start loading chunk c0 (matrix 0), read
 // the block's weight scales.  finish: acc[cc][m][i] += isum * (d_w[m] *
-// d_x[i]) for the chunks c = c0 + 2 cc below nch (pairs of tokens in packed
-// fp32 arithmetic; chunk c0 + 2 is loaded here).
+// d_x[i]) for the chunks c = c0 + EPQ cc below nch (pairs of tokens in packed
+// fp32 arithmetic; the chunks after the first are loaded here).
 template <int NMAT> struct EpiBlock {
     uint32_t dv[NMAT][16];
     float dw[NMAT];
@@ -395,7 +397,7 @@ __device__ __forceinline__ void epi_finish(float2 (&acc)[CPW][NMAT][8], EpiBlock
         epi_fma<NMAT>(acc[0], eb.dv, eb.dw, eb.dxj + 16 * c0);
 #pragma unroll
     for (int cc = 1; cc < CPW; cc++) {
-        const int c = c0 + 2 * cc;
+        const int c = c0 + EPQ * cc;
         if (c < nch) {
             uint32_t dv[NMAT][16];
 #pragma unroll
@@ -547,9 +549,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_moe_tc(const __grid_constant_
         const int q = warp & 3, w2 = warp >> 2;
         const int r = 32 * q + lane;
         const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
-        // conversion: the gate pair -- matrix w2, every block; the down product --
-        // the blocks of parity w2.  Epilogue: token chunks w2 and w2 + 2.
-        const int mc = NMAT == 2 ? w2 : 0;
+        // conversion: the gate pair -- matrix w2 & 1, the blocks j with
+        // j mod (EPQ / 2) = w2 >> 1; the down product -- the blocks j with
+        // j mod EPQ = w2.  Epilogue: token chunks w2 + EPQ cc.
+        const int mc = NMAT == 2 ? (w2 & 1) : 0;
         const int rowoff = S::raw_off + r * RAW_ROW; // this row in a stage's raw weights
         Ring<NS> sr;                                 // stage being converted
         Ring<RA> ar;                                 // A slot being written
@@ -584,7 +587,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_moe_tc(const __grid_constant_
         EpiBlock<NMAT> eb;                                                                                           \
         if (has_epi && !epi_begin<NMAT>(eb, sm + es * S::bytes, rowoff, ej, dr, dfull, tl, w2, nch, abort_flag))     \
             goto out_epi;                                                                                            \
-        const bool conv = NMAT == 2 || ((J) & 1) == w2;                                                              \
+        const bool conv = NMAT == 2 ? (((J) & (EPQ / 2 - 1)) == (w2 >> 1)) : (((J) % EPQ) == w2);                  \
         if (conv) {                                                                                                  \
             uint32_t W[12], cw[8];                                                                                   \
             load_window<J>(myrow, W);                                                                                \
@@ -644,10 +647,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_moe_tc(const __grid_constant_
                 }
             }
 
-            // ---- the item's results: chunks w2, w2 + 2 of the tokens, rows 32q .. 32q+31
+            // ---- the item's results: chunks w2 + EPQ cc of the tokens, rows 32q .. 32q+31
 #pragma unroll
             for (int cc = 0; cc < CPW; cc++) {
-                const int c = w2 + 2 * cc;
+                const int c = w2 + EPQ * cc;
                 if (c >= nch)
                     continue;
 #pragma unroll
