@@ -41,6 +41,7 @@
 #include <climits>
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -840,18 +841,17 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                 }
             } else {
                 const int first = routed ? v_first[v] : 0, ncols = routed ? v_ncols[v] : T;
-                #pragma unroll 1
-                for (int c0 = 0; c0 < ncols; c0 += TT) {
-                    const int nc = min(TT, ncols - c0);
-                    const uint32_t *xc[TT];
+                // NC columns at a time, NC a constant: no column slot of the
+                // unrolled loops is predicated off
+                auto cols = [&](int c0, auto ncc) {
+                    constexpr int NC = decltype(ncc)::value;
+                    uint32_t xsa[NC];
 #pragma unroll
-                    for (int c = 0; c < TT; c++) {
-                        const int cc = c0 + (c < nc ? c : 0);
-                        xc[c] = act + (size_t)(routed ? routes_s[first + cc] / k : cc) * a.xstride;
-                    }
-                    float ag[TT], au[TT];
+                    for (int c = 0; c < NC; c++)
+                        xsa[c] = smem_addr(act + (size_t)(routed ? routes_s[first + c0 + c] / k : c0 + c) * a.xstride);
+                    float ag[NC], au[NC];
 #pragma unroll
-                    for (int c = 0; c < TT; c++)
+                    for (int c = 0; c < NC; c++)
                         ag[c] = au[c] = 0.0f;
                     for (int jj = 0; jj < nblg; jj++) {
                         const int b = rowmap_block(gmap, lane, jj);
@@ -859,28 +859,36 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                         load_q8_0_sh(gsa, b, gbk);
                         load_q8_0_sh(usa, b, ubk);
 #pragma unroll
-                        for (int c = 0; c < TT; c++) {
-                            if (c < nc) {
-                                Q81Block xb;
-                                load_q8_1_sh(smem_addr(xc[c]) + 4u * (uint32_t)xblock_word(b, xpad), xb);
-                                const int sg = dot_q8_block(gbk.q, xb.q);
-                                const int su = dot_q8_block(ubk.q, xb.q);
-                                ag[c] = fmaf(gbk.d * xb.d, (float)sg, ag[c]);
-                                au[c] = fmaf(ubk.d * xb.d, (float)su, au[c]);
-                            }
+                        for (int c = 0; c < NC; c++) {
+                            Q81Block xb;
+                            load_q8_1_sh(xsa[c] + 4u * (uint32_t)xblock_word(b, xpad), xb);
+                            const int sg = dot_q8_block(gbk.q, xb.q);
+                            const int su = dot_q8_block(ubk.q, xb.q);
+                            ag[c] = fmaf(gbk.d * xb.d, (float)sg, ag[c]);
+                            au[c] = fmaf(ubk.d * xb.d, (float)su, au[c]);
                         }
                     }
 #pragma unroll
-                    for (int c = 0; c < TT; c++) {
-                        if (c < nc) {
-                            const float sm = reduce2(ag[c], au[c], lane);
-                            const float u = __shfl_sync(FULL, sm, 16);
-                            if (lane == 0) {
-                                const int slot = routed ? routes_s[first + c0 + c] : R + c0 + c;
-                                a.h[(size_t)slot * a.I + i] = swiglu(sm, u, a.clamp);
-                            }
+                    for (int c = 0; c < NC; c++) {
+                        const float sm = reduce2(ag[c], au[c], lane);
+                        const float u = __shfl_sync(FULL, sm, 16);
+                        if (lane == 0) {
+                            const int slot = routed ? routes_s[first + c0 + c] : R + c0 + c;
+                            a.h[(size_t)slot * a.I + i] = swiglu(sm, u, a.clamp);
                         }
                     }
+                };
+                #pragma unroll 1
+                for (int c0 = 0; c0 < ncols; c0 += TT) {
+                    const int nc = min(TT, ncols - c0);
+                    if (TT >= 4 && nc >= 4)
+                        cols(c0, std::integral_constant<int, (TT >= 4 ? 4 : 1)>{});
+                    else if (TT >= 3 && nc == 3)
+                        cols(c0, std::integral_constant<int, (TT >= 3 ? 3 : 1)>{});
+                    else if (TT >= 2 && nc == 2)
+                        cols(c0, std::integral_constant<int, (TT >= 2 ? 2 : 1)>{});
+                    else
+                        cols(c0, std::integral_constant<int, 1>{});
                 }
             }
         }
@@ -1002,6 +1010,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         const int c0i = ia + ni * warp / CW, c1i = ia + ni * (warp + 1) / CW;
         if (c1i > c0i) {
             const int dn = sd0 + (c1i - 1 - ib0) / P.SR; // the chunk's last stage
+            const int da = sd0 + (c0i - ib0) / P.SR;     // and its first
+            if (dw < da - 1)
+                dw = da - 1; // (stages before the chunk's first: not read by this warp)
             while (dw < dn && !dead) {
                 ++dw;
                 wait_stage(d0 + dw);
@@ -1093,15 +1104,19 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                     ring + (size_t)((d0 + sd0 + d1s) % a.NS) * a.stage_bytes + (size_t)(r1 - d1s * P.SR) * a.rbd;
                 const bool same = live1 && v1 == v;
                 const int ncm = max(nc0, nc1);
-                #pragma unroll 1
-                for (int cb = 0; cb < ncm; cb += TT) {
-                    float acc0[TT], acc1[TT];
-                    uint32_t xs0[TT], xs1[TT];
+                // NC columns at a time, NC a constant, and the common case of
+                // two items of one expert (same column count, shared hq
+                // blocks) apart: no slot of the unrolled loops is predicated off
+                auto pass = [&](int cb, auto ncc, auto samec) {
+                    constexpr int NC = decltype(ncc)::value;
+                    constexpr bool SAME = decltype(samec)::value;
+                    float acc0[NC], acc1[NC];
+                    uint32_t xs0[NC], xs1[NC];
 #pragma unroll
-                    for (int c = 0; c < TT; c++) {
+                    for (int c = 0; c < NC; c++) {
                         acc0[c] = acc1[c] = 0.0f;
-                        xs0[c] = smem_addr(cb + c < nc0 ? hrow(v, first0, cb + c) : act);
-                        xs1[c] = smem_addr(live1 && cb + c < nc1 ? hrow(v1, first1, cb + c) : act);
+                        xs0[c] = smem_addr(SAME || cb + c < nc0 ? hrow(v, first0, cb + c) : act);
+                        xs1[c] = SAME ? 0u : smem_addr(live1 && cb + c < nc1 ? hrow(v1, first1, cb + c) : act);
                     }
                     const uint32_t wsa0 = smem_addr(wr0), wsa1 = smem_addr(live1 ? wr1 : wr0);
                     for (int jb = 0; jb < nbl; jb++) {
@@ -1110,15 +1125,15 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                         load_q8_0_sh(wsa0, b, wb0);
                         load_q8_0_sh(wsa1, b, wb1);
 #pragma unroll
-                        for (int c = 0; c < TT; c++) {
-                            if (cb + c < nc0) {
+                        for (int c = 0; c < NC; c++) {
+                            if (SAME || cb + c < nc0) {
                                 Q81Block xb;
                                 load_q8_1_sh(xs0[c] + 4u * (uint32_t)xblock_word(b, hpad), xb);
                                 acc0[c] = fmaf(wb0.d * xb.d, (float)dot_q8_block(wb0.q, xb.q), acc0[c]);
-                                if (same)
+                                if (SAME)
                                     acc1[c] = fmaf(wb1.d * xb.d, (float)dot_q8_block(wb1.q, xb.q), acc1[c]);
                             }
-                            if (live1 && !same && cb + c < nc1) {
+                            if (!SAME && live1 && cb + c < nc1) {
                                 Q81Block xb;
                                 load_q8_1_sh(xs1[c] + 4u * (uint32_t)xblock_word(b, hpad), xb);
                                 acc1[c] = fmaf(wb1.d * xb.d, (float)dot_q8_block(wb1.q, xb.q), acc1[c]);
@@ -1126,18 +1141,36 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                         }
                     }
 #pragma unroll
-                    for (int c = 0; c < TT; c++) {
-                        if (cb + c < nc0) {
+                    for (int c = 0; c < NC; c++) {
+                        if (SAME || cb + c < nc0) {
                             const float y = warp_sum(acc0[c]);
                             if (lane == 0)
                                 put(col_slot(v, first0, cb + c), v, m, y);
                         }
-                        if (live1 && cb + c < nc1) {
+                        if (SAME || (live1 && cb + c < nc1)) {
                             const float y = warp_sum(acc1[c]);
                             if (lane == 0)
                                 put(col_slot(v1, first1, cb + c), v1, m1, y);
                         }
                     }
+                };
+                auto pass_n = [&](int cb, auto samec) {
+                    const int nc = min(TT, ncm - cb);
+                    if (TT >= 4 && nc >= 4)
+                        pass(cb, std::integral_constant<int, (TT >= 4 ? 4 : 1)>{}, samec);
+                    else if (TT >= 3 && nc == 3)
+                        pass(cb, std::integral_constant<int, (TT >= 3 ? 3 : 1)>{}, samec);
+                    else if (TT >= 2 && nc == 2)
+                        pass(cb, std::integral_constant<int, (TT >= 2 ? 2 : 1)>{}, samec);
+                    else
+                        pass(cb, std::integral_constant<int, 1>{}, samec);
+                };
+                #pragma unroll 1
+                for (int cb = 0; cb < ncm; cb += TT) {
+                    if (same)
+                        pass_n(cb, std::true_type{});
+                    else
+                        pass_n(cb, std::false_type{});
                 }
                 i += 2;
                 m += 2;
@@ -1206,8 +1239,20 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         __syncwarp();
         if (lane == 0 && !dead)
             #pragma unroll 1
-            for (int d = da; d < db; d++)
+            for (int d = da; d < db; d++) {
+                if (d > dw) {
+                    // a stage this warp did not wait for: its slot's previous use
+                    // is released by every warp once the stage is requested
+                    const unsigned long long t0 = global_timer_ns();
+                    while (*(volatile int *)&s_issued <= d0 + d) {
+                        if (*(volatile int *)&s_abort || global_timer_ns() - t0 > WAIT_LIMIT_NS)
+                            break;
+                        __nanosleep(64);
+                    }
+                    __threadfence_block();
+                }
                 mbar_arrive(&empty[(d0 + d) % a.NS]);
+            }
     };
     // Down stages go two at a time (one when rows go two to a warp): each warp
     // takes two items of the window, then releases its stages, so the
