@@ -236,48 +236,81 @@ __device__ __forceinline__ bool mbar_wait_parked(uint64_t *bar, uint32_t parity)
     }
 }
 
-__device__ int routed_row_at(const LayerArgs &a, int nvr, const int *vcols, int b, int nb)
+// The item where CTA b of nb starts in a list of nv runs of M items, an item
+// of run v costing w(v) > 0: the first item of the first run whose cost
+// prefix exceeds b / nb of the total cost, offset into that run by the
+// rest of that share over the run's item cost.  Warp-collective (every lane
+// gets the result): the run costs are summed and scanned across the lanes,
+// in exact 64-bit integers, so the result is the one the plain sequential
+// walk over the runs gives.
+template <typename Wf>
+__device__ int split_at_warp(int nv, unsigned M, Wf w, int b, int nb, int lane)
+{
+    unsigned long long tot = 0;
+    #pragma unroll 1
+    for (int v0 = 0; v0 < nv; v0 += 32) {
+        const int v = v0 + lane;
+        unsigned long long c = v < nv ? (unsigned long long)w(v) * M : 0ull;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            c += __shfl_xor_sync(FULL, c, o);
+        tot += c;
+    }
+    const unsigned long long target = tot * (unsigned)b / (unsigned)nb;
+    unsigned long long base = 0;
+    #pragma unroll 1
+    for (int v0 = 0; v0 < nv; v0 += 32) {
+        const int v = v0 + lane;
+        const int wv = v < nv ? w(v) : 1;
+        const unsigned long long c = v < nv ? (unsigned long long)wv * M : 0ull;
+        unsigned long long incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(FULL, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        incl += base;
+        const unsigned bal = __ballot_sync(FULL, v < nv && incl > target);
+        if (bal) {
+            const int L = __ffs(bal) - 1;
+            const unsigned long long acc = __shfl_sync(FULL, incl - c, L);
+            const int wl = __shfl_sync(FULL, wv, L);
+            return (v0 + L) * (int)M + (int)((target - acc) / (unsigned)wl);
+        }
+        base = __shfl_sync(FULL, incl, 31);
+    }
+    return nv * (int)M;
+}
+
+// The routed gate/up row where CTA b of nb starts: the rows of the nvr
+// virtual experts are laid end to end and split so that every CTA gets an
+// equal share of their cost, a row of an expert with c columns costing 4 + c
+// (streaming the row, measured at about four dots' time, plus one dot per
+// column).  vcols == null: every expert has one column (equal rows; any
+// thread).  Otherwise warp-collective.  Monotone in b; b = nb gives the end
+// of the rows.
+__device__ int routed_row_at(const LayerArgs &a, int nvr, const int *vcols, int b, int nb, int lane)
 {
     if (!vcols)
         return (int)((unsigned)nvr * (unsigned)a.I * (unsigned)b / (unsigned)nb); // <= 2^21 * 152
-    unsigned long long tot = 0;
-    for (int v = 0; v < nvr; v++)
-        tot += (unsigned long long)(4 + vcols[v]) * (unsigned)a.I;
-    const unsigned long long target = tot * (unsigned)b / (unsigned)nb;
-    unsigned long long acc = 0;
-    for (int v = 0; v < nvr; v++) {
-        const unsigned long long c = (unsigned long long)(4 + vcols[v]) * (unsigned)a.I;
-        if (acc + c > target)
-            return v * a.I + (int)((target - acc) / (unsigned)(4 + vcols[v]));
-        acc += c;
-    }
-    return nvr * a.I;
+    return split_at_warp(nvr, (unsigned)a.I, [&](int v) { return 4 + vcols[v]; }, b, nb, lane);
 }
 
 // The flat down item (v, n) = v H + n where CTA b of nb starts: items of
 // virtual expert v (the shared expert last, with T columns) cost 2 + its
 // columns (a down row is half a gate/up row pair), and every CTA gets an
-// equal share of the cost.  vcols == null: equal items.
-__device__ int down_item_at(const LayerArgs &a, int nvr, int nv, const int *vcols, int b, int nb)
+// equal share of the cost.  vcols == null: equal items (any thread);
+// otherwise warp-collective.
+__device__ int down_item_at(const LayerArgs &a, int nvr, int nv, const int *vcols, int b, int nb, int lane)
 {
-    auto cols = [&](int v) { return v < nvr ? vcols[v] : a.T; };
     if (!vcols)
         return (int)((unsigned)nv * (unsigned)a.H * (unsigned)b / (unsigned)nb); // <= 65 * 2^15 * 152
-    unsigned long long tot = 0;
-    for (int v = 0; v < nv; v++)
-        tot += (unsigned long long)(2 + cols(v)) * (unsigned)a.H;
-    const unsigned long long target = tot * (unsigned)b / (unsigned)nb;
-    unsigned long long acc = 0;
-    for (int v = 0; v < nv; v++) {
-        const unsigned long long c = (unsigned long long)(2 + cols(v)) * (unsigned)a.H;
-        if (acc + c > target)
-            return v * a.H + (int)((target - acc) / (unsigned)(2 + cols(v)));
-        acc += c;
-    }
-    return nv * a.H;
+    return split_at_warp(nv, (unsigned)a.H, [&](int v) { return 2 + (v < nvr ? vcols[v] : a.T); }, b, nb, lane);
 }
 
-__device__ LayerPlan make_plan(const LayerArgs &a, int nvr, int bx, int nb, const int *vcols = nullptr)
+// (vcols != null: warp-collective)
+__device__ LayerPlan make_plan(const LayerArgs &a, int nvr, int bx, int nb, const int *vcols = nullptr, int lane = 0)
 {
     LayerPlan q;
     const int RU = a.RU;
@@ -290,8 +323,8 @@ __device__ LayerPlan make_plan(const LayerArgs &a, int nvr, int bx, int nb, cons
         q.ps0 = q.s0 / RU;
         q.NPs = q.s1 > q.s0 ? (q.s1 + RU - 1) / RU - q.ps0 : 0;
     }
-    q.q0 = routed_row_at(a, nvr, vcols, bx, nb);
-    q.q1 = routed_row_at(a, nvr, vcols, bx + 1, nb);
+    q.q0 = routed_row_at(a, nvr, vcols, bx, nb, lane);
+    q.q1 = routed_row_at(a, nvr, vcols, bx + 1, nb, lane);
     q.pr0 = q.q0 / RU;
     q.NPr = q.q1 > q.q0 ? (q.q1 + RU - 1) / RU - q.pr0 : 0;
     q.NPglu = q.NPs + q.NPr;
@@ -299,8 +332,8 @@ __device__ LayerPlan make_plan(const LayerArgs &a, int nvr, int bx, int nb, cons
     q.nrows = (int)((unsigned)a.H * (unsigned)(bx + 1) / (unsigned)nb) - q.n0;
     q.it0 = q.it1 = 0;
     if (a.flat) {
-        q.it0 = down_item_at(a, nvr, q.NV, vcols, bx, nb);
-        q.it1 = down_item_at(a, nvr, q.NV, vcols, bx + 1, nb);
+        q.it0 = down_item_at(a, nvr, q.NV, vcols, bx, nb, lane);
+        q.it1 = down_item_at(a, nvr, q.NV, vcols, bx + 1, nb, lane);
         q.nrb = q.rpb = q.rlast = q.spr = q.slast = 0;
         q.SR = a.SR;
         q.NPd = (q.it1 - q.it0 + q.SR - 1) / q.SR;
@@ -426,6 +459,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     __shared__ int s_abort;
     __shared__ int s_issued; // stages requested so far (written by the producer after each request)
     __shared__ int s_nvr;   // routed virtual experts
+    __shared__ LayerPlan s_plan; // several tokens: the plan, made by the tables warp
     __shared__ unsigned long long s_c0; // barrier count at the start
 
 
@@ -584,7 +618,6 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         named_barrier(bar, nthr);
         const int npair = T * E;
         const int qj = lane & 7; // eight threads per pair
-        const int qE = (E + 7) >> 3;
         #pragma unroll 1
         for (int base = 0; base < npair; base += nthr / 8) { // warp-uniform trip count
             const int p = base + (rt >> 3);
@@ -594,9 +627,10 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                 e = p - t * E;
                 const float *sc = scores + (size_t)t * E;
                 const float v = sc[e];
-                const int e_end = min(E, (qj + 1) * qE);
+                // thread qj takes experts qj, qj + 8, ...: the eight threads of a
+                // pair read eight neighbouring words (no bank conflict)
 #pragma unroll 4
-                for (int e2 = qj * qE; e2 < e_end; e2++) {
+                for (int e2 = qj; e2 < E; e2 += 8) {
                     const float o = sc[e2];
                     rank += (o > v || (o == v && e2 < e)) ? 1 : 0;
                 }
@@ -666,15 +700,16 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
             const float sel1 = lane + 32 < k ? lsm[t * E + ids_s[t * k + lane + 32]] : 0.0f;
             route_softmax_warp(sel0, sel1, k, w_s + t * k, lane);
         }
+        // the routes ahead of r = t k + j: every route of a lower expert
+        // (off_s[e]) and the routes of expert e from earlier tokens (a
+        // token selects k distinct experts)
         #pragma unroll 1
         for (int r = lane; r < R; r += 32) {
-            const int e = ids_s[r];
-            int pos = 0;
+            const int e = ids_s[r], t = r / k;
+            int pos = off_s[e];
             #pragma unroll 1
-            for (int r2 = 0; r2 < R; r2++) {
-                const int e2 = ids_s[r2];
-                pos += (e2 < e || (e2 == e && r2 < r)) ? 1 : 0;
-            }
+            for (int t2 = 0; t2 < t; t2++)
+                pos += (int)((sel_bits[t2][e >> 5] >> (e & 31)) & 1u);
             routes_s[pos] = r;
         }
     };
@@ -695,17 +730,18 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
             a.offsets[E] = off_s[E];
     };
 
-    // Every warp ranks the experts.  Then the first half of the consumer warps
-    // quantizes x.  With one token the producer derives the routed virtual
+    // Every warp ranks the experts.  With one token the first half of the
+    // consumer warps then quantizes x, the producer derives the routed virtual
     // experts (the selected experts in index order) and starts requesting
     // their rows at once, while warp RT0 / 32 builds the tables the consumers
     // need (expert columns, route list, weights, CTA 0's copy); the consumers
     // meet it at BAR_TABLES before their first routed part.  With more tokens
-    // the producer warp builds the tables and every warp waits for them.
+    // every consumer warp quantizes x, then the producer warp builds the
+    // tables and this CTA's plan, and every warp waits for them.
     route_rank(0, THREADS, BAR_SEL); // every warp
     const int wsel = RT0 / 32; // the tables warp (one token)
-    if (tid < RT0)
-        quantize_x(0, RT0 / 32);
+    if (T == 1 ? tid < RT0 : tid < CTHREADS)
+        quantize_x(0, T == 1 ? RT0 / 32 : CW);
     if (T == 1) {
         if (warp == CW) {
             // virtual expert v = the v-th selected expert in index order
@@ -731,14 +767,17 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         if (warp == CW) {
             build_tables();
             __syncwarp();
+            const LayerPlan q = make_plan(a, s_nvr, bx, nb, v_ncols, lane);
+            if (lane == 0)
+                s_plan = q;
             weights_routes();
             __syncwarp();
             if (cta0)
                 store_tables();
         }
-        __syncthreads(); // tables, weights and route list in shared memory
+        __syncthreads(); // tables, weights, route list and plan in shared memory
     }
-    const LayerPlan P = T == 1 ? P1 : make_plan(a, s_nvr, bx, nb, v_ncols);
+    const LayerPlan P = T == 1 ? P1 : s_plan;
 
     if (warp == CW) {
         // ---------------- the producer: every stage of this CTA ----------------
