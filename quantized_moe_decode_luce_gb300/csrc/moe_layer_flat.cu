@@ -14,11 +14,11 @@
 // those of luce_moe_glu_pair + luce_moe_down_combine bit for bit.  The launch
 // structure is our own:
 //
-//  * Byte balance.  Every CTA takes the same number of gate/up rows: an equal
-//    slice of the shared expert's I rows (requested before the launch waits
-//    for its inputs) and an equal slice of the flat list of the routed
-//    experts' rows; and the same number of down items from the flat list of
-//    (virtual expert, output row).
+//  * Cost balance.  Every CTA takes an equal slice of the shared expert's I
+//    rows and an equal cost share of the flat list of the routed experts'
+//    rows (a row of an expert with c columns costs GU_ROW_COST + c); and an
+//    equal cost share of the down items of the flat list of (virtual expert,
+//    output row) (DN_ROW_COST + c each).
 //  * One producer warp streams the CTA's stages in order through a ring of
 //    shared-memory slots with cp.async.bulk (evict-first L2 policy).  The copy
 //    engine of an SM keeps about four bulk copies in flight (measured on
@@ -63,6 +63,12 @@ constexpr int MAX_R = 64;  // T * k
 constexpr int MAX_E = 256; // experts (selection bit masks of MAX_E / 32 words)
 constexpr int MAX_V = MAX_R + 1;
 constexpr int RB_MAX = 64; // down rows per row block (y buffer rows)
+// Cost of a gate/up row pair and of a down row with c columns, in units of
+// one column's dot products: streaming the row through the ring costs
+// about as much as that many dots (measured on the verify layer: the time
+// per CTA follows these weights).
+constexpr int GU_ROW_COST = 6;
+constexpr int DN_ROW_COST = 4;
 constexpr unsigned FULL = 0xffffffffu;
 
 struct LayerArgs {
@@ -214,12 +220,6 @@ struct LayerPlan {
     int SR;       // down items per stage (whole experts' row runs where they fit)
 };
 
-// The routed gate/up row where CTA b of nb starts: the rows of the nvr
-// virtual experts are laid end to end and split so that every CTA gets an
-// equal share of their cost, a row of an expert with c columns costing 4 + c
-// (streaming the row, measured at about four dots' time, plus one dot per column).  vcols == null:
-// every expert has one column (equal rows).  Monotone in b; b = nb gives the
-// end of the rows.
 // Bounded wait that parks the thread in hardware until the phase completes
 // (or a 10 us suspend hint runs out), so a waiter wakes as soon as its data
 // or slot is there instead of after a back-off sleep.
@@ -285,28 +285,27 @@ __device__ int split_at_warp(int nv, unsigned M, Wf w, int b, int nb, int lane)
 
 // The routed gate/up row where CTA b of nb starts: the rows of the nvr
 // virtual experts are laid end to end and split so that every CTA gets an
-// equal share of their cost, a row of an expert with c columns costing 4 + c
-// (streaming the row, measured at about four dots' time, plus one dot per
-// column).  vcols == null: every expert has one column (equal rows; any
-// thread).  Otherwise warp-collective.  Monotone in b; b = nb gives the end
-// of the rows.
+// equal share of their cost, a row of an expert with c columns costing
+// GU_ROW_COST + c.  vcols == null: every expert has one column (equal rows;
+// any thread).  Otherwise warp-collective.  Monotone in b; b = nb gives the
+// end of the rows.
 __device__ int routed_row_at(const LayerArgs &a, int nvr, const int *vcols, int b, int nb, int lane)
 {
     if (!vcols)
         return (int)((unsigned)nvr * (unsigned)a.I * (unsigned)b / (unsigned)nb); // <= 2^21 * 152
-    return split_at_warp(nvr, (unsigned)a.I, [&](int v) { return 4 + vcols[v]; }, b, nb, lane);
+    return split_at_warp(nvr, (unsigned)a.I, [&](int v) { return GU_ROW_COST + vcols[v]; }, b, nb, lane);
 }
 
 // The flat down item (v, n) = v H + n where CTA b of nb starts: items of
-// virtual expert v (the shared expert last, with T columns) cost 2 + its
-// columns (a down row is half a gate/up row pair), and every CTA gets an
-// equal share of the cost.  vcols == null: equal items (any thread);
-// otherwise warp-collective.
+// virtual expert v (the shared expert last, with T columns) cost DN_ROW_COST
+// + its columns, and every CTA gets an equal share of the cost.  vcols ==
+// null: equal items (any thread); otherwise warp-collective.
 __device__ int down_item_at(const LayerArgs &a, int nvr, int nv, const int *vcols, int b, int nb, int lane)
 {
     if (!vcols)
         return (int)((unsigned)nv * (unsigned)a.H * (unsigned)b / (unsigned)nb); // <= 65 * 2^15 * 152
-    return split_at_warp(nv, (unsigned)a.H, [&](int v) { return 2 + (v < nvr ? vcols[v] : a.T); }, b, nb, lane);
+    return split_at_warp(
+        nv, (unsigned)a.H, [&](int v) { return DN_ROW_COST + (v < nvr ? vcols[v] : a.T); }, b, nb, lane);
 }
 
 // (vcols != null: warp-collective)
@@ -474,8 +473,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     const int dmap = a.nbI == 32 ? ROWMAP_TWO_ROWS : (a.nbI % 64 == 0) ? ROWMAP_PAIRS : ROWMAP_PLAIN;
     const int hpad = dmap == ROWMAP_PAIRS ? 16 : 0;
 
-    // With one token the router selects k experts, so the shared parts (and
-    // their place in the stage order) are known before the routing.
+    // With one token the router selects k experts, so the plan is known
+    // before the routing.
     const LayerPlan P1 = make_plan(a, T == 1 ? k : 0, bx, nb);
     if (tid == CTHREADS) {
         #pragma unroll 1
@@ -488,17 +487,10 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         s_issued = 0;
     }
     __syncthreads(); // barriers initialized
-    int issued = 0;  // producer lane 0: stages requested
-    if (tid == CTHREADS) {
-        // the shared expert's parts do not depend on the previous kernel:
-        // request them before waiting for it
-        #pragma unroll 1
-        for (; issued < P1.NPs && issued < a.NS; issued++) {
-            issue_stage(a, P1, issued, ring, full, pol, v_e);
-            __threadfence_block(); // the stage's expect_tx arrival before its count
-            *(volatile int *)&s_issued = issued + 1;
-        }
-    }
+    // (The producer requests every stage after the routing: requesting the
+    // shared expert's first stages before it, while the routing runs, measured
+    // slower on the verify layer.)
+    int issued = 0; // producer lane 0: stages requested
     if (warp == CW) {
         // the inputs of the routing into L2 (a hint)
         for (int i = lane; i < (T * E + 31) / 32; i += 32)
@@ -1428,9 +1420,12 @@ extern "C" __attribute__((visibility("hidden"))) luce_status luce_internal_moe_l
     // the workspace.
     a.flat = 1;
     {
-        // a CTA's cost share over the cheapest items (cost 3 each, of at most 2 + T)
+        // a CTA's cost share over the cheapest items (cost DN_ROW_COST + 1
+        // each, of at most DN_ROW_COST + T)
         const long long nv_max = std::min(E, T * k) + (has_ws ? 1 : 0);
-        const long long items_max = ((2LL + T) * nv_max * H + 3LL * nb - 1) / (3LL * nb) + 1;
+        const long long items_max =
+            ((long long)(DN_ROW_COST + T) * nv_max * H + (DN_ROW_COST + 1LL) * nb - 1) / ((DN_ROW_COST + 1LL) * nb) +
+            1;
         const int span = (int)((items_max + H - 1) / H) + 1; // experts a range of items_max can touch
         a.hq_rows = span * T;
     }
