@@ -296,22 +296,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     // This CTA's gate/up groups: [g0, g1) of all NV * G32 groups (virtual expert
     // major, the shared expert last), taken shared ones first; the j-th group
     // it takes goes to consumer group j % 2, each with its own half of the
-    // ring.  With one token the routing always yields k experts, so NV = k + 1
-    // and the ranges are known before the routing: the first shared group's
-    // parts are then requested at once and (one pass of x) computed while the
-    // other warps route.
-    const bool predict = a.wsg && T == 1;
-    const int NVp = k + 1;
-    int pg0 = 0, pg1 = 0, psh = 0; // predicted range and its shared groups
-    if (predict) {
-        const int NGp = NVp * G32;
-        pg0 = (int)((unsigned)(NGp * bx) / (unsigned)nb);
-        pg1 = (int)((unsigned)(NGp * (bx + 1)) / (unsigned)nb);
-        psh = max(0, pg1 - max(pg0, k * G32));
-    }
+    // ring.  No weight is requested before the routing: bulk copies in flight
+    // hold back this SM's other memory accesses (the routing's loads of the
+    // logits and of x among them), and requesting the shared expert's first
+    // parts before the routing measured slower (20.9 vs 20.3 us per decode
+    // layer).
     const int nbx = T * a.nbH; // x blocks
-    const int NPe = psh > 0 ? min(PPG, HALF) : 0; // parts of the first (shared) group requested at once
-    const bool early = NPe > 0 && nbx <= GTHREADS / 4;
     // part p of a group: RU gate rows then RU up rows into half c, sequence n
     auto issue_part = [&](int c, int n, int gi, int p, const uint8_t *wg_e, const uint8_t *wu_e) {
         const uint32_t slot = (uint32_t)(c * HALF + n % HALF);
@@ -334,11 +324,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     }
     __syncthreads(); // barriers initialized
     if (tid == CTHREADS) {
-        // weights do not depend on the previous kernel: request them before waiting for it
-        for (int p = 0; p < NPe; p++)
-            issue_part(0, p, pg1 - psh, p, a.wsg, a.wsu);
         if (a.wsd && a.prefetch) {
-            // and warm L2 with this CTA's slice of the shared expert's down rows
+            // warm L2 with this CTA's slice of the shared expert's down rows (a
+            // hint: no bulk copy, so the routing's loads are not held back)
             const size_t tot_d = (size_t)a.H * a.rbd; // a multiple of 16
             const size_t cd = ((tot_d / nb) + 15) & ~size_t(15);
             const size_t od = cd * bx;
@@ -365,7 +353,6 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     // ---------------- helpers ----------------
     // ---------------- consumer helpers ----------------
     const int grp = warp / GW, wl = warp - grp * GW; // consumer group, warp within it
-    const int gtid = tid - grp * GTHREADS;
     bool dead = false;
     // waits for the stage in `slot`, use `use`; false if this CTA gave up
     auto wait_slot = [&](int slot, int use) -> bool {
@@ -740,7 +727,6 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     };
 
     LayerPlan P;
-    int eg_parts = 0; // parts of the first shared group that group 0 took before the routing
     if (warp == CW) {
         // ---------------- the producer: every stage of this CTA ----------------
         // With one token the plan is known at once (k experts); the producer
@@ -770,7 +756,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
             return E; // not reached: a token selects k experts
         };
         auto group_of = [&](int j) { return j < P.nsh ? P.g1 - P.nsh + j : P.g0 + (j - P.nsh); };
-        int n[2] = {NPe, 0};  // stages requested per half
+        int n[2] = {0, 0};    // stages requested per half
         int dq[2] = {0, 0};   // down stages requested per half
         const int nglu[2] = {P.nglu0, P.nglu1};
         unsigned long long t_idle = 0;
@@ -854,14 +840,6 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     }
     if (warp < GW) {
         quantize_x();
-        if (early) {
-            named_barrier(1, GTHREADS); // all of x is quantized (one pass, by this group)
-            load_xregs();
-            float *hb = hbuf; // group 0, buffer 0
-            for (int p = 0; p < NPe; p++)
-                glu_part(p % HALF, p / HALF, p, false, 0, T, hb);
-            eg_parts = NPe;
-        }
     } else {
         route_rank();
         if (T == 1) {
@@ -874,8 +852,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         } else {
             weights_routes(0, 0, RTHREADS - 32);
         }
-        if (!early)
-            quantize_x(); // what is left of x (with the early stage, group 0 alone quantizes all of it)
+        quantize_x(); // what is left of x
     }
     // tables, weights, route list and x are in shared memory
     named_barrier(BAR_TABLES, T == 1 ? CTHREADS : THREADS);
@@ -898,8 +875,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     auto down_slot = [&](int d, int &hh, int &n) { down_slot_of(P, d, hh, n); };
 
     // ---------------- 4. gate/up groups -> h, hq (consumer group grp takes j = grp, grp + 2, ...) ----------------
-    if (!(early && grp == 0))
-        load_xregs();
+    load_xregs();
     {
         int n = 0;  // stages of this group's half
         int lb = 0; // h buffer
@@ -910,8 +886,6 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
             const int first = routed ? v_first[v] : 0, ncols = routed ? v_ncols[v] : T;
             float *hb = hbuf + (size_t)(grp * 2 + lb) * 32 * HB_STRIDE;
             for (int p = 0; p < PPG; p++, n++) {
-                if (j == 0 && p < eg_parts)
-                    continue; // taken before the routing
                 glu_part(grp * HALF + n % HALF, n / HALF, p, routed, first, ncols, hb);
             }
             if (defer)
