@@ -81,6 +81,10 @@ SHAPES = [
     ("wide_h", 4, 8192, 256, 64, 8, True, 0.0, "shared_col", 0.0),
     ("wide_i", 1, 256, 8192, 64, 6, True, 10.0, "zipf", 0.1),
     ("all_experts", 2, 256, 256, 4, 4, True, 0.0, "normal", 0.0),
+    # flat-split kernel (hq > 24 KB) with more than 32 routed virtual experts:
+    # the plan's lane scans take several 32-expert chunks
+    ("flat_t6_e64", 6, 512, 512, 64, 8, True, 10.0, "normal", 0.0),
+    ("flat_t8_e128", 8, 512, 512, 128, 8, True, 0.0, "normal", 0.1),
 ]
 
 
