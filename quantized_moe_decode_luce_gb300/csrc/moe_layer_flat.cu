@@ -68,7 +68,7 @@ constexpr int RB_MAX = 64; // down rows per row block (y buffer rows)
 // about as much as that many dots (measured on the verify layer: the time
 // per CTA follows these weights).
 constexpr int GU_ROW_COST = 6;
-constexpr int DN_ROW_COST = 4;
+constexpr int DN_ROW_COST = 3;
 constexpr unsigned FULL = 0xffffffffu;
 
 struct LayerArgs {
@@ -1036,9 +1036,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     const int nbl = rowmap_blocks(dmap, a.nbI, lane);
     int dw = -1; // the last down stage this warp waited for (stage number - d0)
     const int d0 = P.NPglu;
-    auto down_items = [&](int ia, int ib, int ib0, int sd0, int rows, auto hrow, auto put) {
+    auto down_items = [&](int ia, int ib, int ib0, int sd0, int rows, auto hrow, auto put, int wi, int nwc) {
         const int ni = ib - ia;
-        const int c0i = ia + ni * warp / CW, c1i = ia + ni * (warp + 1) / CW;
+        const int c0i = ia + ni * wi / nwc, c1i = ia + ni * (wi + 1) / nwc;
         if (c1i > c0i) {
             const int dn = sd0 + (c1i - 1 - ib0) / P.SR; // the chunk's last stage
             const int da = sd0 + (c0i - ib0) / P.SR;     // and its first
@@ -1266,7 +1266,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
             }
         }
     };
-    auto release = [&](int da, int db) {
+    auto release = [&](int da, int db, uint32_t cnt) {
         __syncwarp();
         if (lane == 0 && !dead)
             #pragma unroll 1
@@ -1282,24 +1282,37 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                     }
                     __threadfence_block();
                 }
-                mbar_arrive(&empty[(d0 + d) % a.NS]);
+                mbar_arrive_count(&empty[(d0 + d) % a.NS], cnt);
             }
     };
-    // Down stages go two at a time (one when rows go two to a warp): each warp
-    // takes two items of the window, then releases its stages, so the
-    // producer keeps the rest of the ring in flight.
     // flat items [it0, it1) of the list over (v, n), n < H; y to the workspace
     {
-        const int WD = two ? 1 : 2; // two items per warp and window (one each when rows go two to a warp)
         const int it0 = (int)P.it0, ni = (int)(P.it1 - P.it0);
-        #pragma unroll 1
-        for (int w = 0; w < P.NPd; w += WD) {
-            const int we = min(P.NPd, w + WD);
-            down_items(
-                it0 + w * P.SR, it0 + min(ni, we * P.SR), it0, 0, a.H,
-                [&](int v, int, int c) -> const uint32_t * { return act + (size_t)((v - v_lo) * T + c) * a.hstride; },
-                [&](int slot, int, int n, float y) { a.ws_y[(size_t)slot * a.H + n] = y; });
-            release(w, we);
+        auto hrow = [&](int v, int, int c) -> const uint32_t * {
+            return act + (size_t)((v - v_lo) * T + c) * a.hstride;
+        };
+        auto put = [&](int slot, int, int n, float y) { a.ws_y[(size_t)slot * a.H + n] = y; };
+        if (!two) {
+            // As the gate/up parts: down stage d goes to consumer group d mod
+            // NG, whose RU warps each take a contiguous quarter (1 / RU) of its
+            // items and release the stage with CW / RU arrivals each, so the
+            // groups run on their own and the producer refills a slot as soon
+            // as its group is done with it.
+            const int grp = warp / a.RU, wl = warp - grp * a.RU;
+            #pragma unroll 1
+            for (int d = grp; d < P.NPd; d += a.NG) {
+                down_items(it0 + d * P.SR, it0 + min(ni, (d + 1) * P.SR), it0, 0, a.H, hrow, put, wl, a.RU);
+                release(d, d + 1, (uint32_t)(CW / a.RU));
+            }
+        } else {
+            // Rows go two to a warp: stages one at a time, each warp taking
+            // its share of the stage's items, then releasing it, so the
+            // producer keeps the rest of the ring in flight.
+            #pragma unroll 1
+            for (int w = 0; w < P.NPd; w++) {
+                down_items(it0 + w * P.SR, it0 + min(ni, (w + 1) * P.SR), it0, 0, a.H, hrow, put, warp, CW);
+                release(w, w + 1, 1u);
+            }
         }
     }
     barrier(3); // every y value is stored
