@@ -57,6 +57,7 @@ constexpr int THREADS = CTHREADS + 32; // + the producer warp
 constexpr int BAR_CONS = 1;          // named barrier of the consumer threads
 constexpr int BAR_SEL = 2;           // the ranking (every thread)
 constexpr int BAR_TABLES = 3;        // one token: the tables, tables warp -> consumers
+constexpr int BAR_PLAN = 4;          // several tokens: the tables, producer warp -> warps 0 and 1
 constexpr int RT0 = CTHREADS / 2;    // threads below quantize x; warp RT0 / 32 builds the tables
 constexpr int MAX_T = 8;
 constexpr int MAX_R = 64;  // T * k
@@ -236,16 +237,17 @@ __device__ __forceinline__ bool mbar_wait_parked(uint64_t *bar, uint32_t parity)
     }
 }
 
-// The item where CTA b of nb starts in a list of nv runs of M items, an item
-// of run v costing w(v) > 0: the first item of the first run whose cost
-// prefix exceeds b / nb of the total cost, offset into that run by the
-// rest of that share over the run's item cost.  Warp-collective (every lane
-// gets the result): the run costs are summed and scanned across the lanes,
-// in exact 64-bit integers, so the result is the one the plain sequential
-// walk over the runs gives.
+// The items where CTAs b and b + 1 of nb start in a list of nv runs of M
+// items, an item of run v costing w(v) > 0: the first item of the first run
+// whose cost prefix exceeds b / nb of the total cost, offset into that run
+// by the rest of that share over the run's item cost.  Warp-collective
+// (every lane gets the results): the run costs are summed and scanned across
+// the lanes, in exact 64-bit integers, so the results are the ones the plain
+// sequential walk over the runs gives.
 template <typename Wf>
-__device__ int split_at_warp(int nv, unsigned M, Wf w, int b, int nb, int lane)
+__device__ void split_at_warp(int nv, unsigned M, Wf w, int b, int nb, int lane, int &r0, int &r1)
 {
+    // r0 for CTA b, r1 for CTA b + 1 (the same walk, two targets)
     unsigned long long tot = 0;
     #pragma unroll 1
     for (int v0 = 0; v0 < nv; v0 += 32) {
@@ -256,10 +258,12 @@ __device__ int split_at_warp(int nv, unsigned M, Wf w, int b, int nb, int lane)
             c += __shfl_xor_sync(FULL, c, o);
         tot += c;
     }
-    const unsigned long long target = tot * (unsigned)b / (unsigned)nb;
+    const unsigned long long t0 = tot * (unsigned)b / (unsigned)nb, t1 = tot * (unsigned)(b + 1) / (unsigned)nb;
+    r0 = r1 = nv * (int)M;
+    bool f0 = false, f1 = false;
     unsigned long long base = 0;
     #pragma unroll 1
-    for (int v0 = 0; v0 < nv; v0 += 32) {
+    for (int v0 = 0; v0 < nv && !f1; v0 += 32) {
         const int v = v0 + lane;
         const int wv = v < nv ? w(v) : 1;
         const unsigned long long c = v < nv ? (unsigned long long)wv * M : 0ull;
@@ -271,45 +275,63 @@ __device__ int split_at_warp(int nv, unsigned M, Wf w, int b, int nb, int lane)
                 incl += y;
         }
         incl += base;
-        const unsigned bal = __ballot_sync(FULL, v < nv && incl > target);
-        if (bal) {
-            const int L = __ffs(bal) - 1;
+        const unsigned b0 = __ballot_sync(FULL, v < nv && incl > t0);
+        const unsigned b1 = __ballot_sync(FULL, v < nv && incl > t1);
+        if (!f0 && b0) {
+            const int L = __ffs(b0) - 1;
             const unsigned long long acc = __shfl_sync(FULL, incl - c, L);
             const int wl = __shfl_sync(FULL, wv, L);
-            return (v0 + L) * (int)M + (int)((target - acc) / (unsigned)wl);
+            r0 = (v0 + L) * (int)M + (int)((t0 - acc) / (unsigned)wl);
+            f0 = true;
+        }
+        if (b1) {
+            const int L = __ffs(b1) - 1;
+            const unsigned long long acc = __shfl_sync(FULL, incl - c, L);
+            const int wl = __shfl_sync(FULL, wv, L);
+            r1 = (v0 + L) * (int)M + (int)((t1 - acc) / (unsigned)wl);
+            f1 = true;
         }
         base = __shfl_sync(FULL, incl, 31);
     }
-    return nv * (int)M;
 }
 
-// The routed gate/up row where CTA b of nb starts: the rows of the nvr
+// The routed gate/up rows where CTAs b and b + 1 of nb start: the rows of the nvr
 // virtual experts are laid end to end and split so that every CTA gets an
 // equal share of their cost, a row of an expert with c columns costing
 // GU_ROW_COST + c.  vcols == null: every expert has one column (equal rows;
 // any thread).  Otherwise warp-collective.  Monotone in b; b = nb gives the
 // end of the rows.
-__device__ int routed_row_at(const LayerArgs &a, int nvr, const int *vcols, int b, int nb, int lane)
+__device__ void routed_rows_at(const LayerArgs &a, int nvr, const int *vcols, int b, int nb, int lane, int &r0,
+                               int &r1)
 {
-    if (!vcols)
-        return (int)((unsigned)nvr * (unsigned)a.I * (unsigned)b / (unsigned)nb); // <= 2^21 * 152
-    return split_at_warp(nvr, (unsigned)a.I, [&](int v) { return GU_ROW_COST + vcols[v]; }, b, nb, lane);
+    if (!vcols) {
+        r0 = (int)((unsigned)nvr * (unsigned)a.I * (unsigned)b / (unsigned)nb); // <= 2^21 * 152
+        r1 = (int)((unsigned)nvr * (unsigned)a.I * (unsigned)(b + 1) / (unsigned)nb);
+        return;
+    }
+    split_at_warp(nvr, (unsigned)a.I, [&](int v) { return GU_ROW_COST + vcols[v]; }, b, nb, lane, r0, r1);
 }
 
-// The flat down item (v, n) = v H + n where CTA b of nb starts: items of
+// The flat down items (v, n) = v H + n where CTAs b and b + 1 of nb start: items of
 // virtual expert v (the shared expert last, with T columns) cost DN_ROW_COST
 // + its columns, and every CTA gets an equal share of the cost.  vcols ==
 // null: equal items (any thread); otherwise warp-collective.
-__device__ int down_item_at(const LayerArgs &a, int nvr, int nv, const int *vcols, int b, int nb, int lane)
+__device__ void down_items_at(const LayerArgs &a, int nvr, int nv, const int *vcols, int b, int nb, int lane, int &r0,
+                              int &r1)
 {
-    if (!vcols)
-        return (int)((unsigned)nv * (unsigned)a.H * (unsigned)b / (unsigned)nb); // <= 65 * 2^15 * 152
-    return split_at_warp(
-        nv, (unsigned)a.H, [&](int v) { return DN_ROW_COST + (v < nvr ? vcols[v] : a.T); }, b, nb, lane);
+    if (!vcols) {
+        r0 = (int)((unsigned)nv * (unsigned)a.H * (unsigned)b / (unsigned)nb); // <= 65 * 2^15 * 152
+        r1 = (int)((unsigned)nv * (unsigned)a.H * (unsigned)(b + 1) / (unsigned)nb);
+        return;
+    }
+    split_at_warp(nv, (unsigned)a.H, [&](int v) { return DN_ROW_COST + (v < nvr ? vcols[v] : a.T); }, b, nb, lane,
+                  r0, r1);
 }
 
-// (vcols != null: warp-collective)
-__device__ LayerPlan make_plan(const LayerArgs &a, int nvr, int bx, int nb, const int *vcols = nullptr, int lane = 0)
+// (vcols != null: warp-collective.  with_down == false: the flat down split
+// is left to the caller, it0 = it1 = NPd = 0.)
+__device__ LayerPlan make_plan(const LayerArgs &a, int nvr, int bx, int nb, const int *vcols = nullptr, int lane = 0,
+                               bool with_down = true)
 {
     LayerPlan q;
     const int RU = a.RU;
@@ -322,8 +344,7 @@ __device__ LayerPlan make_plan(const LayerArgs &a, int nvr, int bx, int nb, cons
         q.ps0 = q.s0 / RU;
         q.NPs = q.s1 > q.s0 ? (q.s1 + RU - 1) / RU - q.ps0 : 0;
     }
-    q.q0 = routed_row_at(a, nvr, vcols, bx, nb, lane);
-    q.q1 = routed_row_at(a, nvr, vcols, bx + 1, nb, lane);
+    routed_rows_at(a, nvr, vcols, bx, nb, lane, q.q0, q.q1);
     q.pr0 = q.q0 / RU;
     q.NPr = q.q1 > q.q0 ? (q.q1 + RU - 1) / RU - q.pr0 : 0;
     q.NPglu = q.NPs + q.NPr;
@@ -331,8 +352,8 @@ __device__ LayerPlan make_plan(const LayerArgs &a, int nvr, int bx, int nb, cons
     q.nrows = (int)((unsigned)a.H * (unsigned)(bx + 1) / (unsigned)nb) - q.n0;
     q.it0 = q.it1 = 0;
     if (a.flat) {
-        q.it0 = down_item_at(a, nvr, q.NV, vcols, bx, nb, lane);
-        q.it1 = down_item_at(a, nvr, q.NV, vcols, bx + 1, nb, lane);
+        if (with_down)
+            down_items_at(a, nvr, q.NV, vcols, bx, nb, lane, q.it0, q.it1);
         q.nrb = q.rpb = q.rlast = q.spr = q.slast = 0;
         q.SR = a.SR;
         q.NPd = (q.it1 - q.it0 + q.SR - 1) / q.SR;
@@ -458,7 +479,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     __shared__ int s_abort;
     __shared__ int s_issued; // stages requested so far (written by the producer after each request)
     __shared__ int s_nvr;   // routed virtual experts
-    __shared__ LayerPlan s_plan; // several tokens: the plan, made by the tables warp
+    __shared__ LayerPlan s_plan; // several tokens: the plan (warp 0) ...
+    __shared__ int s_it[2];      // ... and its down split (warp 1)
     __shared__ unsigned long long s_c0; // barrier count at the start
 
 
@@ -705,6 +727,43 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
             routes_s[pos] = r;
         }
     };
+    // Several tokens: the route weights of token t (one warp; CTA 0 also
+    // stores them), the route list (one warp) and CTA 0's copy of the rest of
+    // the tables (one warp)
+    auto token_weights = [&](int t) {
+        const float sel0 = lane < k ? lsm[t * E + ids_s[t * k + lane]] : 0.0f;
+        const float sel1 = lane + 32 < k ? lsm[t * E + ids_s[t * k + lane + 32]] : 0.0f;
+        route_softmax_warp(sel0, sel1, k, w_s + t * k, lane);
+        __syncwarp();
+        if (cta0)
+            for (int j = lane; j < k; j += 32)
+                a.weights[t * k + j] = w_s[t * k + j];
+    };
+    auto route_positions = [&]() {
+        #pragma unroll 1
+        for (int r = lane; r < R; r += 32) {
+            const int e = ids_s[r], t = r / k;
+            int pos = off_s[e];
+            #pragma unroll 1
+            for (int t2 = 0; t2 < t; t2++)
+                pos += (int)((sel_bits[t2][e >> 5] >> (e & 31)) & 1u);
+            routes_s[pos] = r;
+        }
+    };
+    auto store_rest = [&]() {
+        #pragma unroll 1
+        for (int i = lane; i < R; i += 32) {
+            a.ids[i] = ids_s[i];
+            a.routes[i] = routes_s[i];
+        }
+        #pragma unroll 1
+        for (int e = lane; e < E; e += 32) {
+            a.counts[e] = cnt_s[e];
+            a.offsets[e] = off_s[e];
+        }
+        if (lane == 0)
+            a.offsets[E] = off_s[E];
+    };
     // CTA 0 stores the routing tables (one warp)
     auto store_tables = [&]() {
         #pragma unroll 1
@@ -728,8 +787,10 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     // their rows at once, while warp RT0 / 32 builds the tables the consumers
     // need (expert columns, route list, weights, CTA 0's copy); the consumers
     // meet it at BAR_TABLES before their first routed part.  With more tokens
-    // every consumer warp quantizes x, then the producer warp builds the
-    // tables and this CTA's plan, and every warp waits for them.
+    // every consumer warp quantizes x; then the producer warp builds the
+    // tables and the route list, warps 0 and 1 make this CTA's plan from the
+    // tables, warps 2 .. T + 1 weigh one token's routes each, and every warp
+    // waits for all of it.
     route_rank(0, THREADS, BAR_SEL); // every warp
     const int wsel = RT0 / 32; // the tables warp (one token)
     if (T == 1 ? tid < RT0 : tid < CTHREADS)
@@ -759,17 +820,41 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         if (warp == CW) {
             build_tables();
             __syncwarp();
-            const LayerPlan q = make_plan(a, s_nvr, bx, nb, v_ncols, lane);
-            if (lane == 0)
-                s_plan = q;
-            weights_routes();
+            named_barrier_arrive(BAR_PLAN, 3 * 32); // the tables for warps 0 and 1
+            route_positions();
             __syncwarp();
             if (cta0)
-                store_tables();
+                store_rest();
+        } else if (warp >= 2 && warp < 2 + T) {
+            token_weights(warp - 2); // (T <= 8: warps 2 .. 9)
+        } else if (warp < 2) {
+            named_barrier(BAR_PLAN, 3 * 32);
+            if (warp == 0) {
+                const LayerPlan q = make_plan(a, s_nvr, bx, nb, v_ncols, lane, false);
+                if (lane == 0)
+                    s_plan = q;
+            } else {
+                int i0, i1;
+                down_items_at(a, s_nvr, s_nvr + (a.wsg ? 1 : 0), v_ncols, bx, nb, lane, i0, i1);
+                if (lane == 0) {
+                    s_it[0] = i0;
+                    s_it[1] = i1;
+                }
+            }
         }
         __syncthreads(); // tables, weights, route list and plan in shared memory
     }
-    const LayerPlan P = T == 1 ? P1 : s_plan;
+    const LayerPlan P = [&]() {
+        if (T == 1)
+            return P1;
+        LayerPlan q = s_plan;
+        if (a.flat) {
+            q.it0 = s_it[0];
+            q.it1 = s_it[1];
+            q.NPd = (q.it1 - q.it0 + q.SR - 1) / q.SR;
+        }
+        return q;
+    }();
 
     if (warp == CW) {
         // ---------------- the producer: every stage of this CTA ----------------
