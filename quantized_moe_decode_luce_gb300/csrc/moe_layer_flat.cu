@@ -601,7 +601,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
 
     // ---------------- routing ----------------
     // Scores (a NaN ranks below every number) and the rank of every (token,
-    // expert) pair by `nthr` threads starting at thread `t0` (eight threads per
+    // expert) pair by `nthr` threads starting at thread `t0` (four threads per
     // pair): expert e of token t takes slot #{e' ranked before e} when that is
     // below k, the (score descending, index ascending) order of the
     // sequential selection.  Named barrier `bar` among the nthr threads.
@@ -631,27 +631,26 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
             (&sel_bits[0][0])[i] = 0u;
         named_barrier(bar, nthr);
         const int npair = T * E;
-        const int qj = lane & 7; // eight threads per pair
+        const int qj = lane & 3; // four threads per pair
         #pragma unroll 1
-        for (int base = 0; base < npair; base += nthr / 8) { // warp-uniform trip count
-            const int p = base + (rt >> 3);
+        for (int base = 0; base < npair; base += nthr / 4) { // warp-uniform trip count
+            const int p = base + (rt >> 2);
             int rank = 0, t = 0, e = 0;
             if (p < npair) {
                 t = p / E;
                 e = p - t * E;
                 const float *sc = scores + (size_t)t * E;
                 const float v = sc[e];
-                // thread qj takes experts qj, qj + 8, ...: the eight threads of a
-                // pair read eight neighbouring words (no bank conflict)
-#pragma unroll 4
-                for (int e2 = qj; e2 < E; e2 += 8) {
+                // thread qj takes experts qj, qj + 4, ...: the four threads of a
+                // pair read four neighbouring words (no bank conflict)
+#pragma unroll 8
+                for (int e2 = qj; e2 < E; e2 += 4) {
                     const float o = sc[e2];
                     rank += (o > v || (o == v && e2 < e)) ? 1 : 0;
                 }
             }
             rank += __shfl_xor_sync(FULL, rank, 1);
             rank += __shfl_xor_sync(FULL, rank, 2);
-            rank += __shfl_xor_sync(FULL, rank, 4);
             if (p < npair && qj == 0 && rank < k) {
                 ids_s[t * k + rank] = e;
                 atomicOr(&sel_bits[t][e >> 5], 1u << (e & 31));
