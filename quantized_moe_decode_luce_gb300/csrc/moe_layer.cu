@@ -905,9 +905,19 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
     uint2 *units = reinterpret_cast<uint2 *>(hbuf);
     named_barrier(BAR_ALL, CTHREADS); // this CTA's h and hq are stored
     if (warp == 0) {
-        if (lane == 0 && !grid_barrier(a.sync, gridDim.x, s_c0)) {
-            atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
-            *(volatile int *)&s_abort = 1;
+        if (lane == 0) {
+            if (!grid_barrier(a.sync, gridDim.x, s_c0)) {
+                atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
+                *(volatile int *)&s_abort = 1;
+            } else if (a.hs_on && a.hq_bulk) {
+                // all of hq into shared memory with one bulk copy, requested as
+                // soon as the barrier ends (the proxy fence orders the other
+                // CTAs' stores, seen through the barrier, before it)
+                const uint32_t bytes = (uint32_t)((R + (a.wsd ? T : 0)) * a.nbI * Q8_1_WORDS * 4);
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                mbar_arrive_expect_tx(&hq_bar, bytes);
+                bulk_copy_g2s(hs, a.hq, bytes, &hq_bar, l2_evict_normal_policy());
+            }
         }
         __syncwarp();
     } else if (by_units) {
@@ -935,15 +945,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
         const int nlive = R + (a.wsd ? T : 0);
         if (a.hs_on && !*(volatile int *)&s_abort) {
                 if (a.hq_bulk) {
-                    // all of hq into shared memory with one bulk copy (the rows
-                    // are multiples of 16 bytes); the proxy fence orders the
-                    // other CTAs' stores, seen through the barrier, before it
-                    const uint32_t bytes = (uint32_t)(nlive * ibytes_w * 4);
-                    if (tid == 0) {
-                        asm volatile("fence.proxy.async.global;" ::: "memory");
-                        mbar_arrive_expect_tx(&hq_bar, bytes);
-                        bulk_copy_g2s(hs, a.hq, bytes, &hq_bar, l2_evict_normal_policy());
-                    }
+                    // all of hq in shared memory: the bulk copy thread 0
+                    // requested as soon as the device-wide barrier ended
                     if (!__all_sync(FULL, mbar_wait_bounded(&hq_bar, 0))) {
                         if (lane == 0) {
                             atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
