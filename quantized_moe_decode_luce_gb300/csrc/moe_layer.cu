@@ -125,6 +125,22 @@ __device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned 
     return v;
 }
 
+// Bounded wait that parks the thread in hardware until the phase completes
+// (or a 10 us suspend hint runs out), so a waiter wakes as soon as its data
+// is there instead of after a back-off sleep.
+__device__ __forceinline__ bool mbar_wait_parked(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const unsigned long long t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 10000))
+            return true;
+        if (global_timer_ns() - t0 > WAIT_LIMIT_NS)
+            return false;
+    }
+}
+
 __device__ bool grid_barrier(unsigned long long *count, unsigned n, unsigned long long c0)
 {
     const unsigned long long target = (c0 / n + 1ull) * n;
@@ -361,7 +377,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
             dead = true;
         if (dead)
             return false;
-        const bool got = __all_sync(FULL, mbar_wait_bounded(&full[slot], (uint32_t)use & 1u));
+        const bool got = __all_sync(FULL, mbar_wait_parked(&full[slot], (uint32_t)use & 1u));
         if (!got) {
             if (lane == 0) {
                 atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
@@ -947,7 +963,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_moe_layer(const LayerArgs a)
                 if (a.hq_bulk) {
                     // all of hq in shared memory: the bulk copy thread 0
                     // requested as soon as the device-wide barrier ended
-                    if (!__all_sync(FULL, mbar_wait_bounded(&hq_bar, 0))) {
+                    if (!__all_sync(FULL, mbar_wait_parked(&hq_bar, 0))) {
                         if (lane == 0) {
                             atomicOr(&g_fault_word, LUCE_FAULT_TIMEOUT);
                             *(volatile int *)&s_abort = 1;
