@@ -55,14 +55,12 @@ __device__ __forceinline__ void scale_min_pair(const uint32_t (&sw)[3], int c, i
     }
 }
 
-// This lane's part of a Q4_K row (K values) times a q8_1 row: pairs
-// p = lane, lane + 32, ... of the row's K / 64 sub-block pairs.
-__device__ __forceinline__ float q4k_lane_dot(const uint8_t *__restrict__ w_row, const uint32_t *__restrict__ x_row,
-                                              int K, int lane)
+// Sub-block pair p (sub-blocks 2c and 2c + 1 of super-block p / 4) of a
+// Q4_K row times a q8_1 row, added to acc.
+__device__ __forceinline__ float q4k_pair_dot(const uint8_t *__restrict__ w_row, const uint32_t *__restrict__ x_row,
+                                              int p, float acc)
 {
-    float acc = 0.0f;
-    const int P = K >> 6;
-    for (int p = lane; p < P; p += 32) {
+    {
         const int sb = p >> 2, c = p & 3;
         const uint4 hd = __ldg(reinterpret_cast<const uint4 *>(w_row + (size_t)sb * Q4K_BYTES));
         const uint4 *qp = reinterpret_cast<const uint4 *>(w_row + (size_t)sb * Q4K_BYTES + 16 + 32 * c);
@@ -85,6 +83,18 @@ __device__ __forceinline__ float q4k_lane_dot(const uint8_t *__restrict__ w_row,
             acc = fmaf(-dmin * (float)m[h], s8, acc);
         }
     }
+    return acc;
+}
+
+// This lane's part of a Q4_K row (K values) times a q8_1 row: pairs
+// p = lane, lane + 32, ... of the row's K / 64 sub-block pairs.
+__device__ __forceinline__ float q4k_lane_dot(const uint8_t *__restrict__ w_row, const uint32_t *__restrict__ x_row,
+                                              int K, int lane)
+{
+    float acc = 0.0f;
+    const int P = K >> 6;
+    for (int p = lane; p < P; p += 32)
+        acc = q4k_pair_dot(w_row, x_row, p, acc);
     return acc;
 }
 
@@ -145,6 +155,50 @@ __global__ void __launch_bounds__(WARPS * 32)
     const size_t rowb = (size_t)(I / QKK) * Q4K_BYTES;
     const size_t hrow = (size_t)(I / QK) * Q8_1_WORDS;
     float acc = 0.0f;
+    if ((I >> 6) <= 16) {
+        // A row has at most 16 sub-block pairs: each half-warp takes a slot
+        // (half 0 the even ones, half 1 the odd ones), one pair per lane, four
+        // slots per half in flight at once.  The half-warp butterfly adds the
+        // same values in the same order as the warp butterfly over a warp whose
+        // upper 16 lanes hold zeros, so every y is the one-slot-per-warp y.
+        const int P = I >> 6, hh = lane >> 4, pl = lane & 15;
+        constexpr int SJ = 8; // slots per pass (four per half)
+        for (int j0 = 0; j0 < k; j0 += SJ) {
+            float part[SJ / 2];
+            bool live[SJ / 2];
+#pragma unroll
+            for (int q = 0; q < SJ / 2; q++) {
+                const int j = j0 + 2 * q + hh;
+                const int e = j < k ? ids[t * k + j] : -1;
+                if (e >= E && pl == 0 && n == 0)
+                    atomicOr(&g_fault_word, LUCE_FAULT_BAD_ID);
+                live[q] = e >= 0 && e < E;
+                part[q] = live[q] && pl < P
+                              ? q4k_pair_dot(wd + ((size_t)e * H + n) * rowb, hq + (size_t)(t * k + j) * hrow, pl, 0.0f)
+                              : 0.0f;
+            }
+#pragma unroll
+            for (int q = 0; q < SJ / 2; q++) {
+                const float y = half_warp_sum(part[q]);
+                const float y0 = __shfl_sync(0xffffffffu, y, 0), y1 = __shfl_sync(0xffffffffu, y, 16);
+                const bool l0 = __shfl_sync(0xffffffffu, live[q], 0), l1 = __shfl_sync(0xffffffffu, live[q], 16);
+                if (l0)
+                    acc = __fadd_rn(acc, __fmul_rn(weights[t * k + j0 + 2 * q], y0));
+                if (l1)
+                    acc = __fadd_rn(acc, __fmul_rn(weights[t * k + j0 + 2 * q + 1], y1));
+            }
+        }
+        if (wsd) {
+            const float y =
+                half_warp_sum(pl < P && hh == 0
+                                  ? q4k_pair_dot(wsd + (size_t)n * rowb, hq + ((size_t)T * k + t) * hrow, pl, 0.0f)
+                                  : 0.0f);
+            acc = __fadd_rn(acc, __shfl_sync(0xffffffffu, y, 0));
+        }
+        if (lane == 0)
+            out[(size_t)t * H + n] = acc;
+        return;
+    }
     // SB slots at a time: their lane dots do not depend on one another, so
     // the loads of all of them are in flight together; the sums then join
     // the combine in slot order
