@@ -17,10 +17,13 @@
 // d sc_j d8 isum_j - dmin m_j s8, isum_j the exact int32 sum of codes times
 // activation codes.
 //
-// First design (plain, not yet tuned): one warp per dot product row; a lane
-// takes a pair of sub-blocks (2c, 2c + 1) of a super-block, whose codes are
-// the same 32 bytes (low and high nibbles), with 16-byte loads of the
-// super-block header and codes; dp4a on nibble-masked words.
+// Design: one warp per dot product row; a lane takes a pair of sub-blocks
+// (2c, 2c + 1) of a super-block, whose codes are the same 32 bytes (low and
+// high nibbles), with 16-byte loads of the super-block header and codes;
+// dp4a on nibble-masked words.  The gate/up blocks stage the token's q8_1
+// row in shared memory once; the down/combine warps take one route slot per
+// half-warp when a row has at most 16 sub-block pairs (four slots per half
+// in flight).
 #include <algorithm>
 #include <climits>
 #include <cmath>
@@ -57,6 +60,7 @@ __device__ __forceinline__ void scale_min_pair(const uint32_t (&sw)[3], int c, i
 
 // Sub-block pair p (sub-blocks 2c and 2c + 1 of super-block p / 4) of a
 // Q4_K row times a q8_1 row, added to acc.
+template <bool XS = false>
 __device__ __forceinline__ float q4k_pair_dot(const uint8_t *__restrict__ w_row, const uint32_t *__restrict__ x_row,
                                               int p, float acc)
 {
@@ -73,11 +77,11 @@ __device__ __forceinline__ float q4k_pair_dot(const uint8_t *__restrict__ w_row,
 #pragma unroll
         for (int h = 0; h < 2; h++) {
             const uint32_t *xb = x_row + (size_t)(8 * sb + 2 * c + h) * Q8_1_WORDS;
-            const uint32_t xd = __ldg(xb);
+            const uint32_t xd = XS ? xb[0] : __ldg(xb);
             int isum = 0;
 #pragma unroll
             for (int w = 0; w < 8; w++)
-                isum = __dp4a((int)((qw[w] >> (4 * h)) & 0x0F0F0F0Fu), (int)__ldg(xb + 1 + w), isum);
+                isum = __dp4a((int)((qw[w] >> (4 * h)) & 0x0F0F0F0Fu), (int)(XS ? xb[1 + w] : __ldg(xb + 1 + w)), isum);
             const float d8 = half_bits_to_float(xd), s8 = half_bits_to_float(xd >> 16);
             acc = fmaf(d * (float)sc[h] * d8, (float)isum, acc);
             acc = fmaf(-dmin * (float)m[h], s8, acc);
@@ -109,6 +113,14 @@ __global__ void __launch_bounds__(WARPS * 32)
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.y, i = blockIdx.x * WARPS + warp;
+    extern __shared__ uint32_t xs[]; // the token's q8_1 row
+    {
+        const int tt = r < T * k ? r / k : r - T * k;
+        const uint32_t *xr = xq + (size_t)tt * (H / QK) * Q8_1_WORDS;
+        for (int w = threadIdx.x; w < (H / QK) * Q8_1_WORDS; w += WARPS * 32)
+            xs[w] = __ldg(xr + w);
+        __syncthreads();
+    }
     if (i >= I)
         return;
     const size_t rowb = (size_t)(H / QKK) * Q4K_BYTES;
@@ -132,8 +144,13 @@ __global__ void __launch_bounds__(WARPS * 32)
         U = wsu + (size_t)i * rowb;
     }
     const uint32_t *x = xq + (size_t)t * (H / QK) * Q8_1_WORDS;
-    const float g = warp_sum(q4k_lane_dot(G, x, H, lane));
-    const float u = warp_sum(q4k_lane_dot(U, x, H, lane));
+    float gl = 0.0f, ul = 0.0f;
+    for (int p = lane; p < (H >> 6); p += 32) {
+        gl = q4k_pair_dot<true>(G, xs, p, gl);
+        ul = q4k_pair_dot<true>(U, xs, p, ul);
+    }
+    const float g = warp_sum(gl);
+    const float u = warp_sum(ul);
     if (lane == 0)
         h[(size_t)r * I + i] = swiglu(g, u, clamp);
 }
@@ -255,7 +272,8 @@ extern "C" luce_status luce_moe_glu_q4k(const luce_block_q4_k *w_gate, const luc
     const int rows = T * k + (has_ws ? T : 0);
     if ((int64_t)T * k > (1 << 20) || rows > 65535)
         return LUCE_ERR_INVALID_ARG;
-    return launch(k_glu_q4k, dim3((unsigned)((I + WARPS - 1) / WARPS), (unsigned)rows), dim3(WARPS * 32), 0,
+    return launch(k_glu_q4k, dim3((unsigned)((I + WARPS - 1) / WARPS), (unsigned)rows), dim3(WARPS * 32),
+                  (size_t)(H / QK) * Q8_1_WORDS * 4,
                   as_stream(stream), reinterpret_cast<const uint8_t *>(w_gate), reinterpret_cast<const uint8_t *>(w_up),
                   reinterpret_cast<const uint8_t *>(ws_gate), reinterpret_cast<const uint8_t *>(ws_up),
                   reinterpret_cast<const uint32_t *>(xq), ids, T, k, E, H, I, clamp, h);
