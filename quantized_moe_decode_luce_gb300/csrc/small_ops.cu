@@ -9,6 +9,8 @@
 
 #include "common.cuh"
 
+#include <cooperative_groups.h>
+
 LUCE_DEFINE_FAULT_WORD(luce_internal_fault_small_ops)
 
 namespace {
@@ -480,6 +482,120 @@ __global__ void __launch_bounds__(ARGMAX_THREADS)
 
 // Chunking of an argmax row: a pure function of (R, V), so the workspace size
 // does not depend on the device.
+// Rows of at least ARGMAX_CLUSTER_MIN values: one cluster of AC = 16 CTAs
+// per row (a non-portable cluster size, allowed per device), each CTA an
+// equal slice of it (all its loads in flight: ~8 float4 a thread at V =
+// 129,280), the CTAs' pairs joined through distributed shared memory by rank
+// 0; no second pass through global memory and no atomics.  Measured 1.3 us
+// faster than the two-pass kernel at 5 x 129,280 (8-CTA clusters: 0.2 us).
+constexpr int AC = 16;
+constexpr int64_t ARGMAX_CLUSTER_MIN = 8 * 2048;
+
+__global__ void __cluster_dims__(AC, 1, 1) __launch_bounds__(ARGMAX_THREADS)
+    k_argmax_cluster(const float *__restrict__ logits, int64_t V, int64_t L, bool vec4, int32_t *__restrict__ idx,
+                     float *__restrict__ val)
+{
+    namespace cg = cooperative_groups;
+    pdl_wait();
+    pdl_trigger();
+    cg::cluster_group cl = cg::this_cluster();
+    const int c = (int)cl.block_rank(), r = blockIdx.y;
+    const int64_t lo = (int64_t)c * L, hi = min(V, lo + L);
+    const float *row = logits + (int64_t)r * V;
+    float bv = 0.0f;
+    int bi = INT_MAX;
+    if (lo < hi) {
+        if (vec4) {
+            const float4 *p = reinterpret_cast<const float4 *>(row + lo);
+            const int n4 = (int)((hi - lo) >> 2);
+            // every load of the slice in flight before the first comparison
+            constexpr int U = 8;
+            for (int i0 = threadIdx.x; i0 < n4; i0 += U * ARGMAX_THREADS) {
+                float4 q[U];
+#pragma unroll
+                for (int u = 0; u < U; u++) {
+                    const int i = i0 + u * ARGMAX_THREADS;
+                    q[u] = i < n4 ? __ldcs(p + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                }
+#pragma unroll
+                for (int u = 0; u < U; u++) {
+                    const int i = i0 + u * ARGMAX_THREADS;
+                    if (i < n4) {
+                        const int base = (int)(lo + 4 * (int64_t)i);
+                        better(bv, bi, q[u].x, base);
+                        better(bv, bi, q[u].y, base + 1);
+                        better(bv, bi, q[u].z, base + 2);
+                        better(bv, bi, q[u].w, base + 3);
+                    }
+                }
+            }
+            for (int64_t i = lo + 4 * (int64_t)n4 + threadIdx.x; i < hi; i += ARGMAX_THREADS)
+                better(bv, bi, row[i], (int)i);
+        } else {
+#pragma unroll 4
+            for (int64_t i = lo + threadIdx.x; i < hi; i += ARGMAX_THREADS)
+                better(bv, bi, __ldcs(row + i), (int)i);
+        }
+    }
+    block_argmax(bv, bi);
+    __shared__ float s_v;
+    __shared__ int s_i;
+    if (threadIdx.x == 0) {
+        s_v = bv;
+        s_i = bi;
+    }
+    cl.sync(); // every CTA's pair is in its shared memory
+    if (c == 0 && threadIdx.x < 32) {
+        float ov = 0.0f;
+        int oi = INT_MAX;
+        if (threadIdx.x < AC) {
+            ov = *cl.map_shared_rank(&s_v, (unsigned)threadIdx.x);
+            oi = *cl.map_shared_rank(&s_i, (unsigned)threadIdx.x);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float pv = __shfl_xor_sync(0xffffffffu, ov, o);
+            const int pi = __shfl_xor_sync(0xffffffffu, oi, o);
+            better(ov, oi, pv, pi);
+        }
+        if (threadIdx.x == 0) {
+            idx[r] = (int32_t)oi;
+            if (val)
+                val[r] = ov;
+        }
+    }
+    cl.sync(); // rank 0 has read every CTA's pair before any CTA exits
+}
+
+// Whether 16-CTA clusters are allowed for k_argmax_cluster on this device
+// (the attribute is set once per device; a refusal or a failed launch turns
+// the path off for the device).
+std::atomic<int> g_argmax_cluster[64];
+bool argmax_cluster_ok()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    int st = g_argmax_cluster[dev].load(std::memory_order_acquire);
+    if (st == 0) {
+        st = cudaFuncSetAttribute(k_argmax_cluster, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess
+                 ? 1
+                 : -1;
+        if (st < 0)
+            (void)cudaGetLastError();
+        g_argmax_cluster[dev].store(st, std::memory_order_release);
+    }
+    return st > 0;
+}
+void argmax_cluster_off()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64)
+        g_argmax_cluster[dev].store(-1, std::memory_order_release);
+}
+
 void argmax_chunks(int R, int64_t V, int64_t &L, int &C)
 {
     const int64_t want = R > 0 ? std::max<int64_t>(1, 320 / R) : 1;
@@ -647,6 +763,15 @@ extern "C" luce_status luce_argmax(const float *logits, int R, int64_t V, int32_
     unsigned int *counters =
         reinterpret_cast<unsigned int *>(reinterpret_cast<uint8_t *>(workspace) + argmax_pairs_bytes(R, C));
     const bool vec4 = (V % 4 == 0) && aligned(logits, 16);
+    if (V >= ARGMAX_CLUSTER_MIN && argmax_cluster_ok()) {
+        // (the workspace is not used on this path; the two-pass kernel below
+        // remains for short rows and for a device without 16-CTA clusters)
+        const int64_t Lc = (((V + AC - 1) / AC) + 3) & ~int64_t(3);
+        if (launch(k_argmax_cluster, dim3((unsigned)AC, (unsigned)R), dim3(ARGMAX_THREADS), 0, as_stream(stream),
+                   logits, V, Lc, vec4, idx, val) == LUCE_OK)
+            return LUCE_OK;
+        argmax_cluster_off();
+    }
     dim3 grid((unsigned)C, (unsigned)R);
     return launch(k_argmax, grid, dim3(ARGMAX_THREADS), 0, as_stream(stream), logits, V, L, C, vec4, pairs, counters,
                   idx, val, (int64_t)0);
