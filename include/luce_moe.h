@@ -196,9 +196,12 @@ LUCE_API luce_status luce_moe_down_combine(const luce_block_q8_0 *w_down, const 
 
 /* ------------------------------------------------------------------------
  * luce_argmax -- exact greedy argmax per row, as a "pair/pick": each CTA
- * reduces a chunk of a row to a (value, index) pair; the last CTA of the
- * row picks among the pairs.  [PR826], commit "fused DS4.1 decode kernels":
- * the greedy token comes from an exact argmax done as pairs and a pick.
+ * reduces a chunk of a row to a (value, index) pair and one CTA picks among
+ * the row's pairs (rows of 16,384 values or more: one cluster of CTAs per
+ * row, the pairs joined in distributed shared memory; shorter rows: the
+ * last CTA of the row to finish picks from pairs in the workspace).
+ * [PR826], commit "fused DS4.1 decode kernels": the greedy token comes from
+ * an exact argmax done as pairs and a pick.
  *
  * idx[r] = the lowest index of the maximum of logits[r][0..V) (float
  * comparison: -0 == +0 is a tie; inputs must hold no NaN); val[r] = that
