@@ -493,7 +493,7 @@ constexpr int64_t ARGMAX_CLUSTER_MIN = 8 * 2048;
 
 __global__ void __cluster_dims__(AC, 1, 1) __launch_bounds__(ARGMAX_THREADS)
     k_argmax_cluster(const float *__restrict__ logits, int64_t V, int64_t L, bool vec4, int32_t *__restrict__ idx,
-                     float *__restrict__ val)
+                     float *__restrict__ val, int64_t v0)
 {
     namespace cg = cooperative_groups;
     pdl_wait();
@@ -559,7 +559,7 @@ __global__ void __cluster_dims__(AC, 1, 1) __launch_bounds__(ARGMAX_THREADS)
             better(ov, oi, pv, pi);
         }
         if (threadIdx.x == 0) {
-            idx[r] = (int32_t)oi;
+            idx[r] = (int32_t)(oi + v0); // the shard's first column is column v0 of the vocabulary
             if (val)
                 val[r] = ov;
         }
@@ -768,7 +768,7 @@ extern "C" luce_status luce_argmax(const float *logits, int R, int64_t V, int32_
         // remains for short rows and for a device without 16-CTA clusters)
         const int64_t Lc = (((V + AC - 1) / AC) + 3) & ~int64_t(3);
         if (launch(k_argmax_cluster, dim3((unsigned)AC, (unsigned)R), dim3(ARGMAX_THREADS), 0, as_stream(stream),
-                   logits, V, Lc, vec4, idx, val) == LUCE_OK)
+                   logits, V, Lc, vec4, idx, val, (int64_t)0) == LUCE_OK)
             return LUCE_OK;
         argmax_cluster_off();
     }
@@ -796,6 +796,13 @@ extern "C" luce_status luce_argmax_shard(const float *logits, int R, int64_t Vs,
     unsigned int *counters =
         reinterpret_cast<unsigned int *>(reinterpret_cast<uint8_t *>(workspace) + argmax_pairs_bytes(R, C));
     const bool vec4 = (Vs % 4 == 0) && aligned(logits, 16);
+    if (Vs >= ARGMAX_CLUSTER_MIN && argmax_cluster_ok()) {
+        const int64_t Lc = (((Vs + AC - 1) / AC) + 3) & ~int64_t(3);
+        if (launch(k_argmax_cluster, dim3((unsigned)AC, (unsigned)R), dim3(ARGMAX_THREADS), 0, as_stream(stream),
+                   logits, Vs, Lc, vec4, idx, val, v0) == LUCE_OK)
+            return LUCE_OK;
+        argmax_cluster_off();
+    }
     dim3 grid((unsigned)C, (unsigned)R);
     return launch(k_argmax, grid, dim3(ARGMAX_THREADS), 0, as_stream(stream), logits, Vs, L, C, vec4, pairs, counters,
                   idx, val, v0);
