@@ -422,6 +422,74 @@ def edge_ops_measure(dev, peak, stream):
     return out
 
 
+def chain_measure(dev, peak, stream, wl, layers, dls, b_d, xs_d, vocab_d, bufs, am, lb):
+    """The decode stack with the step before each layer in the chain: per
+    layer the RMS norm + router logits of the residual stream (F32 router
+    matrix [E][H]), the one-launch MoE layer on the normed row, and the
+    residual add that makes the next layer's input; then the greedy token.
+    Each layer's routing therefore depends on the previous layer's output, as
+    in a real decode (attention is not part of this path and is left out).
+    Launches chain through programmatic launch; 8 input slots are captured
+    as graphs and replayed in turn.  Returns a kernels-dict entry."""
+    import torch
+    from quantized_moe_decode_luce_gb300 import binding as Bd
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(91)
+    T, H, E = wl.T, wl.H, wl.E
+    wr = torch.randn((layers, E, H), generator=g, device=dev) * 0.02
+    gamma = 1.0 + 0.1 * torch.randn((layers, H), generator=g, device=dev)
+    xres = torch.empty((layers + 1, T, H), device=dev)
+    xn = torch.empty((T, H), device=dev)
+    lg = torch.empty((T, E), device=dev)
+    outc = torch.empty((T, H), device=dev)
+    S = min(8, xs_d.shape[0])
+
+    def chain_step(s):
+        x = xs_d[s, 0]
+        for l in range(layers):
+            lay = dls[l]
+            Bd.luce_rmsnorm_router(x, gamma[l], 1e-6, wr[l], xn, lg)
+            Bd.luce_moe_layer(lg, b_d[l], xn, wl.k, wl.I, lay.wg, lay.wu, lay.wd, lay.wsg, lay.wsu, lay.wsd,
+                              wl.clamp, bufs.ids, bufs.weights, bufs.xq, bufs.counts, bufs.offsets, bufs.routes,
+                              bufs.h, bufs.hq, outc, bufs.workspace)
+            Bd.luce_add_f32(x, outc, xres[l + 1])
+            x = xres[l + 1]
+        am.run(vocab_d[s])
+
+    gs = []
+    with torch.cuda.stream(stream):
+        for s in range(S):  # eager once: every call checked
+            chain_step(s)
+        torch.cuda.synchronize()
+        for s in range(S):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                chain_step(s)
+            gs.append(gr)
+        for i in range(3 * S):
+            gs[i % S].replay()
+        torch.cuda.synchronize()
+        n = 400
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            gs[i % S].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / n
+    finite = bool(torch.isfinite(xres[layers]).all().item())
+    router_b = E * H * 4 + 2 * T * H * 4 + H * 4 + T * E * 4
+    step_b = layers * (lb + router_b + 3 * T * H * 4) + VOCAB * 4 * T
+    return {"workload": f"{layers} x (RMS norm + router [E={E}][H={H}] fp32, MoE layer, residual add) "
+                        f"+ {VOCAB}-entry argmax, T={T}, layer l+1 routed on layer l's output",
+            "tokens_per_s": T / (us * 1e-6), "us_per_step": us, "us_per_layer": us / layers,
+            "launches_per_step": 3 * layers + 1, "bytes_per_step": step_b,
+            "GBps": step_b / (us * 1e-6) / 1e9, "frac": step_b / (us * 1e-6) / 1e9 / peak,
+            "input_slots": S, "steps": n, "residual_finite": finite}
+
+
 def _path_label(st):
     """What luce_moe_layer (or the split launches) runs for this step's shape."""
     if st.path != "layer":
@@ -841,6 +909,13 @@ def run_ours(args, wl, layers):
         e2e = {"value": e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": K2,
                "path": "pinned host x/logits/vocab -> device copies -> C-ABI step -> outputs + token to pinned host"}
+
+    if rank == 0 and not args.no_edge_ops and one_launch:
+        try:
+            kernels["decode_stack43_chain"] = chain_measure(dev, peak, stream, wl, layers, dls, b_d, xs_d, vocab_d,
+                                                            step_bufs, am, lb)
+        except Exception as exc:  # a report, never a reason to fail the bench
+            kernels["decode_stack43_chain"] = {"failed": str(exc)}
 
     if rank == 0 and not args.no_edge_ops:
         try:

@@ -325,8 +325,9 @@ LUCE_API luce_status luce_argmax_pick(const float *vals, const int32_t *idxs, in
  *   xn [T][H] fp32 out or NULL (not stored); must not overlap x
  *   logits [T][E] fp32 out (the input of luce_route_topk / luce_moe_layer)
  * Requires H % 4 == 0, 4 <= H <= 12288, E >= 1, T >= 0.  Under programmatic
- * launch (luce_set_pdl) the kernel reads w_router before it waits for the
- * previous kernel, so that kernel must not write w_router.
+ * launch (luce_set_pdl) the kernel reads w_router (and, for one token with
+ * H <= 2048 and a 16-byte aligned gamma, gamma) before it waits for the
+ * previous kernel, so that kernel must write neither.
  */
 LUCE_API luce_status luce_rmsnorm_router(const float *x, const float *gamma, float eps, const float *w_router, int T,
                                          int E, int H, float *xn, float *logits, void *stream);

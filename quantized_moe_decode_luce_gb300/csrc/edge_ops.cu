@@ -28,9 +28,19 @@ using namespace luce;
 // its tile's tokens into shared memory (warp t sums token t's squares), then
 // warp w streams router row e = blockIdx.x RW + w once for all the tile's
 // tokens.  CTAs of the first expert chunk also store xn.
+//
+// ROW (one token, H <= 4 x 32 x WP, gamma 16-byte aligned): every warp holds
+// the whole row in registers instead -- its lane's slice of x, of gamma
+// (requested before the programmatic-launch wait, like the router row) and of
+// its router row -- and sums the squares itself, so the token's path after
+// the wait has no shared memory and no block barrier.  The lane slices, the
+// order of every sum and every rounding are the tiled path's, so both give
+// the same bits.
 constexpr int RW = 8;   // warps (router rows) per CTA
 constexpr int TPC = 8;  // most tokens per tile
+constexpr int WP = 16;  // router-row float4 per lane requested before the wait
 
+template <bool ROW>
 __global__ void __launch_bounds__(RW * 32)
     k_rmsnorm_router(const float *__restrict__ x, const float *__restrict__ gamma, float eps,
                      const float *__restrict__ w_router, int T, int E, int H, int tpc, float *__restrict__ xn,
@@ -43,14 +53,66 @@ __global__ void __launch_bounds__(RW * 32)
     const int H4 = H >> 2;
     const int e = blockIdx.x * RW + warp;
     const float4 *wr = reinterpret_cast<const float4 *>(w_router + (size_t)min(e, E - 1) * H);
+    const float4 zero4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     // the router row does not depend on the previous kernel: its first
     // WP float4 per lane are requested before waiting for that kernel
-    constexpr int WP = 16;
     float4 wpre[WP];
 #pragma unroll
     for (int u = 0; u < WP; u++) {
         const int i = lane + 32 * u;
-        wpre[u] = (e < E && i < H4) ? __ldg(wr + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        wpre[u] = (e < E && i < H4) ? __ldg(wr + i) : zero4;
+    }
+    if constexpr (ROW) {
+        float4 gv[WP], xv[WP];
+#pragma unroll
+        for (int u = 0; u < WP; u++) {
+            const int i = lane + 32 * u;
+            gv[u] = i < H4 ? __ldg(reinterpret_cast<const float4 *>(gamma) + i) : zero4;
+        }
+        pdl_wait();
+        pdl_trigger();
+        const float4 *xr = reinterpret_cast<const float4 *>(x + (size_t)t0 * H);
+#pragma unroll
+        for (int u = 0; u < WP; u++) {
+            const int i = lane + 32 * u;
+            xv[u] = i < H4 ? xr[i] : zero4;
+        }
+        float ss = 0.0f;
+#pragma unroll
+        for (int u = 0; u < WP; u++) {
+            if (lane + 32 * u < H4) {
+                ss = fmaf(xv[u].x, xv[u].x, ss);
+                ss = fmaf(xv[u].y, xv[u].y, ss);
+                ss = fmaf(xv[u].z, xv[u].z, ss);
+                ss = fmaf(xv[u].w, xv[u].w, ss);
+            }
+        }
+        ss = warp_sum(ss);
+        const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)H), eps)));
+        const bool store = xn != nullptr && blockIdx.x == 0 && warp == 0;
+        float4 *xo = reinterpret_cast<float4 *>(xn + (size_t)t0 * H);
+        float acc = 0.0f;
+#pragma unroll
+        for (int u = 0; u < WP; u++) {
+            const int i = lane + 32 * u;
+            if (i < H4) {
+                float4 v;
+                v.x = __fmul_rn(__fmul_rn(xv[u].x, r), gv[u].x);
+                v.y = __fmul_rn(__fmul_rn(xv[u].y, r), gv[u].y);
+                v.z = __fmul_rn(__fmul_rn(xv[u].z, r), gv[u].z);
+                v.w = __fmul_rn(__fmul_rn(xv[u].w, r), gv[u].w);
+                if (store)
+                    xo[i] = v;
+                acc = fmaf(wpre[u].x, v.x, acc);
+                acc = fmaf(wpre[u].y, v.y, acc);
+                acc = fmaf(wpre[u].z, v.z, acc);
+                acc = fmaf(wpre[u].w, v.w, acc);
+            }
+        }
+        acc = warp_sum(acc);
+        if (e < E && lane == 0)
+            logits[(size_t)t0 * E + e] = acc;
+        return;
     }
     pdl_wait();
     pdl_trigger();
@@ -202,14 +264,19 @@ extern "C" luce_status luce_rmsnorm_router(const float *x, const float *gamma, f
     const int64_t chunks = ((int64_t)E + RW - 1) / RW;
     if (tiles > 65535 || chunks > INT_MAX)
         return LUCE_ERR_INVALID_ARG;
+    // one token whose row fits the registers: the row path (xn then needs
+    // 16-byte alignment too, as its stores are float4)
+    if (T == 1 && H <= 4 * 32 * WP && aligned(gamma, 16) && (!xn || aligned(xn, 16)))
+        return launch(k_rmsnorm_router<true>, dim3((unsigned)chunks, 1u), dim3(RW * 32), 0, as_stream(stream), x,
+                      gamma, eps, w_router, T, E, H, 1, xn, logits);
     const size_t smem = (size_t)tpc * H * sizeof(float);
     static SmemLimit limit;
-    if (limit.raise(k_rmsnorm_router, 64 * 1024) != cudaSuccess) {
+    if (limit.raise(k_rmsnorm_router<false>, 64 * 1024) != cudaSuccess) {
         (void)cudaGetLastError();
         return LUCE_ERR_CUDA;
     }
-    const luce_status st = launch(k_rmsnorm_router, dim3((unsigned)chunks, (unsigned)tiles), dim3(RW * 32), smem,
-                                  as_stream(stream), x, gamma, eps, w_router, T, E, H, tpc, xn, logits);
+    const luce_status st = launch(k_rmsnorm_router<false>, dim3((unsigned)chunks, (unsigned)tiles), dim3(RW * 32),
+                                  smem, as_stream(stream), x, gamma, eps, w_router, T, E, H, tpc, xn, logits);
     if (st != LUCE_OK)
         limit.forget();
     return st;

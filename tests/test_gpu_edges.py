@@ -39,7 +39,8 @@ def _no_device_faults():
 # ----------------------------------------------------------------------------- RMS norm + router
 # T, E, H: decode and verify hidden sizes, several token tiles with a ragged
 # last one, a ragged last expert chunk, the largest H (one token per tile)
-NORM_CASES = [(1, 64, 2048), (5, 128, 4096), (13, 40, 512), (3, 9, 12288), (64, 256, 1024)]
+NORM_CASES = [(1, 64, 2048), (5, 128, 4096), (13, 40, 512), (3, 9, 12288), (64, 256, 1024), (1, 9, 516),
+              (1, 64, 4096)]
 
 
 @pytest.mark.parametrize("T,E,H", NORM_CASES)
@@ -82,6 +83,31 @@ def test_rmsnorm_of_zero_rows_is_zero():
     B.luce_rmsnorm_router(dev(x), dev(gamma), 1e-6, dev(w), xn, logits)
     torch.cuda.synchronize()
     assert torch.all(xn == 0.0) and torch.all(logits == 0.0)
+
+
+@pytest.mark.parametrize("H", [2048, 516])
+def test_rmsnorm_router_one_token_path_is_the_tiled_path(H):
+    # one token takes the register path, a batch (or an unaligned gamma) the
+    # tiled path: the same lane slices and sum orders give the same bits
+    E = 40
+    g = W.rng(720, H)
+    x = g.standard_normal((3, H)).astype(np.float32)
+    gamma = g.uniform(0.5, 1.5, H + 1).astype(np.float32)
+    w = (g.standard_normal((E, H)) * 0.02).astype(np.float32)
+    gam_d = dev(gamma)
+    wd = dev(w)
+    x1, lg1 = torch.empty((1, H), device="cuda"), torch.empty((1, E), device="cuda")
+    x3, lg3 = torch.empty((3, H), device="cuda"), torch.empty((3, E), device="cuda")
+    xu, lgu = torch.empty((1, H), device="cuda"), torch.empty((1, E), device="cuda")
+    B.luce_rmsnorm_router(dev(x[:1]), gam_d[:H], 1e-6, wd, x1, lg1)
+    B.luce_rmsnorm_router(dev(x), gam_d[:H], 1e-6, wd, x3, lg3)
+    gam_u = dev(np.concatenate([[0.0], gamma[:H]]).astype(np.float32))[1:]  # 4-byte aligned only
+    B.luce_rmsnorm_router(dev(x[:1]), gam_u, 1e-6, wd, xu, lgu)
+    torch.cuda.synchronize()
+    assert torch.equal(x1[0], x3[0]) and torch.equal(lg1[0], lg3[0])
+    assert torch.equal(x1, xu) and torch.equal(lg1, lgu)
+    xn_ref, lg_ref, terms = oracle.rmsnorm_router(x[:1], gamma[:H], 1e-6, w)
+    assert_close(host(lg1), lg_ref, terms, "logits")
 
 
 # ----------------------------------------------------------------------------- vocabulary split
