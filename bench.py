@@ -424,11 +424,12 @@ def edge_ops_measure(dev, peak, stream):
 
 def chain_measure(dev, peak, stream, wl, layers, dls, b_d, xs_d, vocab_d, bufs, am, lb):
     """The decode stack with the step before each layer in the chain: per
-    layer the RMS norm + router logits of the residual stream (F32 router
-    matrix [E][H]), the one-launch MoE layer on the normed row, and the
-    residual add that makes the next layer's input; then the greedy token.
-    Each layer's routing therefore depends on the previous layer's output, as
-    in a real decode (attention is not part of this path and is left out).
+    layer the residual add that makes the layer's input (the previous layer's
+    input + output), its RMS norm and the router logits (F32 router matrix
+    [E][H]) in one launch, then the one-launch MoE layer on the normed row;
+    after the last layer its residual add, then the greedy token.  Each
+    layer's routing therefore depends on the previous layer's output, as in a
+    real decode (attention is not part of this path and is left out).
     Launches chain through programmatic launch; 8 input slots are captured
     as graphs and replayed in turn.  Returns a kernels-dict entry."""
     import torch
@@ -442,19 +443,22 @@ def chain_measure(dev, peak, stream, wl, layers, dls, b_d, xs_d, vocab_d, bufs, 
     xres = torch.empty((layers + 1, T, H), device=dev)
     xn = torch.empty((T, H), device=dev)
     lg = torch.empty((T, E), device=dev)
-    outc = torch.empty((T, H), device=dev)
+    outc = torch.empty((2, T, H), device=dev)
     S = min(8, xs_d.shape[0])
 
     def chain_step(s):
         x = xs_d[s, 0]
         for l in range(layers):
             lay = dls[l]
-            Bd.luce_rmsnorm_router(x, gamma[l], 1e-6, wr[l], xn, lg)
+            if l == 0:
+                Bd.luce_rmsnorm_router(x, gamma[l], 1e-6, wr[l], xn, lg)
+            else:
+                Bd.luce_add_rmsnorm_router(x, outc[(l - 1) % 2], xres[l], gamma[l], 1e-6, wr[l], xn, lg)
+                x = xres[l]
             Bd.luce_moe_layer(lg, b_d[l], xn, wl.k, wl.I, lay.wg, lay.wu, lay.wd, lay.wsg, lay.wsu, lay.wsd,
                               wl.clamp, bufs.ids, bufs.weights, bufs.xq, bufs.counts, bufs.offsets, bufs.routes,
-                              bufs.h, bufs.hq, outc, bufs.workspace)
-            Bd.luce_add_f32(x, outc, xres[l + 1])
-            x = xres[l + 1]
+                              bufs.h, bufs.hq, outc[l % 2], bufs.workspace)
+        Bd.luce_add_f32(x, outc[(layers - 1) % 2], xres[layers])
         am.run(vocab_d[s])
 
     gs = []
@@ -482,10 +486,11 @@ def chain_measure(dev, peak, stream, wl, layers, dls, b_d, xs_d, vocab_d, bufs, 
     finite = bool(torch.isfinite(xres[layers]).all().item())
     router_b = E * H * 4 + 2 * T * H * 4 + H * 4 + T * E * 4
     step_b = layers * (lb + router_b + 3 * T * H * 4) + VOCAB * 4 * T
-    return {"workload": f"{layers} x (RMS norm + router [E={E}][H={H}] fp32, MoE layer, residual add) "
-                        f"+ {VOCAB}-entry argmax, T={T}, layer l+1 routed on layer l's output",
+    return {"workload": f"{layers} x (residual add + RMS norm + router [E={E}][H={H}] fp32 in one launch, "
+                        f"MoE layer) + final residual add + {VOCAB}-entry argmax, T={T}, layer l+1 routed on "
+                        f"layer l's output",
             "tokens_per_s": T / (us * 1e-6), "us_per_step": us, "us_per_layer": us / layers,
-            "launches_per_step": 3 * layers + 1, "bytes_per_step": step_b,
+            "launches_per_step": 2 * layers + 2, "bytes_per_step": step_b,
             "GBps": step_b / (us * 1e-6) / 1e9, "frac": step_b / (us * 1e-6) / 1e9 / peak,
             "input_slots": S, "steps": n, "residual_finite": finite}
 

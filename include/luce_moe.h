@@ -333,6 +333,27 @@ LUCE_API luce_status luce_rmsnorm_router(const float *x, const float *gamma, flo
                                          int E, int H, float *xn, float *logits, void *stream);
 
 /* ------------------------------------------------------------------------
+ * luce_add_rmsnorm_router -- luce_rmsnorm_router of the residual sum: the
+ * residual add that makes a layer's input (the previous layer's input plus
+ * its output) folded into the same launch as the norm and the router logits.
+ * The pages list the RMS norm among the launches that the decode path fuses
+ * ([PR826], commit "fused DS4.1 decode kernels"); the add is one fp32
+ * addition per value:
+ *   s[t][i] = x[t][i] + residual[t][i]     (fp32, round to nearest)
+ * and then xn and logits exactly as luce_rmsnorm_router computes them from s
+ * (the same bits as luce_add_f32 followed by luce_rmsnorm_router).
+ *
+ *   x, residual [T][H] fp32, both 16-byte aligned
+ *   x_sum [T][H] fp32 out or NULL (not stored); must not overlap x or residual
+ *   gamma, eps, w_router, xn, logits, T, E, H as for luce_rmsnorm_router
+ * residual may be NULL only when T == 0.  Under programmatic launch the
+ * previous kernel may write x and residual but neither w_router nor gamma.
+ */
+LUCE_API luce_status luce_add_rmsnorm_router(const float *x, const float *residual, float *x_sum,
+                                             const float *gamma, float eps, const float *w_router, int T, int E,
+                                             int H, float *xn, float *logits, void *stream);
+
+/* ------------------------------------------------------------------------
  * luce_ep_mask / luce_add_f32 -- the two pieces of an expert-parallel split
  * of the step.  [PR826], the cluster runtime commit (each rank holds a share
  * of the routed experts, and the ranks sum their outputs every MoE layer) and

@@ -55,6 +55,7 @@ def lib() -> ctypes.CDLL:
             "luce_argmax_shard": [P, i32, i64, i64, P, P, P, sz, P],
             "luce_argmax_pick": [P, P, i32, i32, P, P, P],
             "luce_rmsnorm_router": [P, P, f32, P, i32, i32, i32, P, P, P],
+            "luce_add_rmsnorm_router": [P, P, P, P, f32, P, i32, i32, i32, P, P, P],
             "luce_ep_mask": [P, i64, i32, i32, P, P],
             "luce_add_f32": [P, P, P, i64, P],
             "luce_moe_glu_q4k": [P, P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P],
@@ -226,6 +227,18 @@ def luce_rmsnorm_router(x, gamma, eps: float, w_router, xn, logits, stream=None)
         _ptr(xn, f32, "xn"), _ptr(logits, f32, "logits"), _stream(stream)))
 
 
+def luce_add_rmsnorm_router(x, residual, x_sum, gamma, eps: float, w_router, xn, logits, stream=None) -> None:
+    """x, residual [T, H] -> x_sum = x + residual (or None), then luce_rmsnorm_router of the sum."""
+    T, H = x.shape
+    if tuple(residual.shape) != (T, H):
+        raise ValueError("residual must have x's shape")
+    E = w_router.shape[0]
+    _check("luce_add_rmsnorm_router", lib().luce_add_rmsnorm_router(
+        _ptr(x, f32, "x"), _ptr(residual, f32, "residual"), _ptr(x_sum, f32, "x_sum"), _ptr(gamma, f32, "gamma"),
+        float(eps), _ptr(w_router, f32, "w_router"), T, E, H, _ptr(xn, f32, "xn"), _ptr(logits, f32, "logits"),
+        _stream(stream)))
+
+
 def luce_ep_mask(ids, e0: int, e1: int, ids_out, stream=None) -> None:
     _check("luce_ep_mask", lib().luce_ep_mask(
         _ptr(ids, i32, "ids"), ids.numel(), int(e0), int(e1), _ptr(ids_out, i32, "ids_out"), _stream(stream)))
@@ -268,7 +281,7 @@ def luce_version() -> int:
 __all__ = ["LuceError", "lib", "status_string", "luce_route_topk", "luce_quantize_q8_1", "luce_moe_group",
            "luce_moe_glu_pair", "luce_moe_prep", "luce_moe_layer", "luce_moe_layer_workspace_bytes", "luce_set_pdl",
            "luce_moe_down_combine", "luce_argmax", "luce_argmax_workspace_bytes", "luce_argmax_noalloc",
-           "luce_argmax_shard", "luce_argmax_pick", "luce_rmsnorm_router", "luce_ep_mask", "luce_add_f32",
+           "luce_argmax_shard", "luce_argmax_pick", "luce_rmsnorm_router", "luce_add_rmsnorm_router", "luce_ep_mask", "luce_add_f32",
            "luce_moe_glu_q4k", "luce_moe_down_combine_q4k",
            "luce_get_fault", "luce_version", "LUCE_OK", "LUCE_ERR_INVALID_ARG", "LUCE_ERR_UNSUPPORTED",
            "LUCE_ERR_CUDA", "LUCE_FAULT_BAD_ID", "LUCE_FAULT_TIMEOUT", "LUCE_FAULT_DESYNC"]

@@ -29,6 +29,10 @@ using namespace luce;
 // warp w streams router row e = blockIdx.x RW + w once for all the tile's
 // tokens.  CTAs of the first expert chunk also store xn.
 //
+// With a residual r the normed row is that of x + r (one fp32 add per value,
+// the sum stored by the first expert chunk): the residual add before the norm
+// in the same launch.
+//
 // ROW (one token, H <= 4 x 32 x WP, gamma 16-byte aligned): every warp holds
 // the whole row in registers instead -- its lane's slice of x, of gamma
 // (requested before the programmatic-launch wait, like the router row) and of
@@ -42,9 +46,9 @@ constexpr int WP = 16;  // router-row float4 per lane requested before the wait
 
 template <bool ROW>
 __global__ void __launch_bounds__(RW * 32)
-    k_rmsnorm_router(const float *__restrict__ x, const float *__restrict__ gamma, float eps,
-                     const float *__restrict__ w_router, int T, int E, int H, int tpc, float *__restrict__ xn,
-                     float *__restrict__ logits)
+    k_rmsnorm_router(const float *__restrict__ x, const float *__restrict__ res, float *__restrict__ xsum,
+                     const float *__restrict__ gamma, float eps, const float *__restrict__ w_router, int T, int E,
+                     int H, int tpc, float *__restrict__ xn, float *__restrict__ logits)
 {
     extern __shared__ __align__(16) float xs[]; // [tpc][H] normed rows
     __shared__ float rs[TPC];
@@ -76,6 +80,29 @@ __global__ void __launch_bounds__(RW * 32)
         for (int u = 0; u < WP; u++) {
             const int i = lane + 32 * u;
             xv[u] = i < H4 ? xr[i] : zero4;
+        }
+        if (res != nullptr) {
+            const float4 *rr = reinterpret_cast<const float4 *>(res + (size_t)t0 * H);
+            float4 rv[WP];
+#pragma unroll
+            for (int u = 0; u < WP; u++) {
+                const int i = lane + 32 * u;
+                rv[u] = i < H4 ? rr[i] : zero4;
+            }
+#pragma unroll
+            for (int u = 0; u < WP; u++) {
+                xv[u].x = __fadd_rn(xv[u].x, rv[u].x);
+                xv[u].y = __fadd_rn(xv[u].y, rv[u].y);
+                xv[u].z = __fadd_rn(xv[u].z, rv[u].z);
+                xv[u].w = __fadd_rn(xv[u].w, rv[u].w);
+            }
+            if (xsum != nullptr && blockIdx.x == 0 && warp == 1) {
+                float4 *so = reinterpret_cast<float4 *>(xsum + (size_t)t0 * H);
+#pragma unroll
+                for (int u = 0; u < WP; u++)
+                    if (lane + 32 * u < H4)
+                        so[lane + 32 * u] = xv[u];
+            }
         }
         float ss = 0.0f;
 #pragma unroll
@@ -118,10 +145,18 @@ __global__ void __launch_bounds__(RW * 32)
     pdl_trigger();
     if (warp < nt) {
         const float4 *xr = reinterpret_cast<const float4 *>(x + (size_t)(t0 + warp) * H);
+        const float4 *rr = res ? reinterpret_cast<const float4 *>(res + (size_t)(t0 + warp) * H) : nullptr;
         float ss = 0.0f;
 #pragma unroll 8
         for (int i = lane; i < H4; i += 32) {
-            const float4 v = xr[i];
+            float4 v = xr[i];
+            if (rr != nullptr) {
+                const float4 q = rr[i];
+                v.x = __fadd_rn(v.x, q.x);
+                v.y = __fadd_rn(v.y, q.y);
+                v.z = __fadd_rn(v.z, q.z);
+                v.w = __fadd_rn(v.w, q.w);
+            }
             ss = fmaf(v.x, v.x, ss);
             ss = fmaf(v.y, v.y, ss);
             ss = fmaf(v.z, v.z, ss);
@@ -133,9 +168,16 @@ __global__ void __launch_bounds__(RW * 32)
     }
     __syncthreads();
     const bool store = xn != nullptr && blockIdx.x == 0;
+    const bool store_sum = res != nullptr && xsum != nullptr && blockIdx.x == 0;
     for (int j = threadIdx.x; j < nt * H; j += RW * 32) {
         const int t = j / H, i = j - t * H;
-        const float v = __fmul_rn(__fmul_rn(x[(size_t)(t0 + t) * H + i], rs[t]), gamma[i]);
+        float xi = x[(size_t)(t0 + t) * H + i];
+        if (res != nullptr) {
+            xi = __fadd_rn(xi, res[(size_t)(t0 + t) * H + i]);
+            if (store_sum)
+                xsum[(size_t)(t0 + t) * H + i] = xi;
+        }
+        const float v = __fmul_rn(__fmul_rn(xi, rs[t]), gamma[i]);
         xs[j] = v;
         if (store)
             xn[(size_t)(t0 + t) * H + i] = v;
@@ -247,16 +289,27 @@ unsigned grid_for(int64_t n)
 
 using namespace luce_host;
 
-extern "C" luce_status luce_rmsnorm_router(const float *x, const float *gamma, float eps, const float *w_router, int T,
-                                           int E, int H, float *xn, float *logits, void *stream)
+// both entry points: res / xsum are NULL for the plain norm
+static luce_status rmsnorm_router(const float *x, const float *res, float *xsum, const float *gamma, float eps,
+                           const float *w_router, int T, int E, int H, float *xn, float *logits, void *stream)
 {
     if (T < 0 || E < 1 || H < 4 || H % 4 != 0 || H > 12288 || !(eps >= 0.0f) || !std::isfinite(eps))
         return LUCE_ERR_INVALID_ARG;
     if (T == 0)
         return LUCE_OK;
     if (!x || !gamma || !w_router || !logits || !aligned(x, 16) || !aligned(gamma, 4) || !aligned(w_router, 16) ||
-        !aligned(logits, 4) || (xn && !aligned(xn, 4)))
+        !aligned(logits, 4) || (xn && !aligned(xn, 4)) || (res && !aligned(res, 16)) || (xsum && !aligned(xsum, 4)))
         return LUCE_ERR_INVALID_ARG;
+    if (xsum) {
+        // the sum is stored while other CTAs still read x and r
+        const size_t n = (size_t)T * H * sizeof(float);
+        auto overlaps = [n](const void *a, const void *b) {
+            const uintptr_t p = reinterpret_cast<uintptr_t>(a), q = reinterpret_cast<uintptr_t>(b);
+            return p < q + n && q < p + n;
+        };
+        if (overlaps(xsum, x) || overlaps(xsum, res))
+            return LUCE_ERR_INVALID_ARG;
+    }
     // a tile's normed rows stay within 64 KB of shared memory (the kernel's
     // dynamic shared memory limit is raised to that once per device)
     const int tpc = std::max(1, std::min(TPC, 16384 / H));
@@ -264,11 +317,11 @@ extern "C" luce_status luce_rmsnorm_router(const float *x, const float *gamma, f
     const int64_t chunks = ((int64_t)E + RW - 1) / RW;
     if (tiles > 65535 || chunks > INT_MAX)
         return LUCE_ERR_INVALID_ARG;
-    // one token whose row fits the registers: the row path (xn then needs
-    // 16-byte alignment too, as its stores are float4)
-    if (T == 1 && H <= 4 * 32 * WP && aligned(gamma, 16) && (!xn || aligned(xn, 16)))
+    // one token whose row fits the registers: the row path (xn and the sum
+    // then need 16-byte alignment too, as their stores are float4)
+    if (T == 1 && H <= 4 * 32 * WP && aligned(gamma, 16) && (!xn || aligned(xn, 16)) && (!xsum || aligned(xsum, 16)))
         return launch(k_rmsnorm_router<true>, dim3((unsigned)chunks, 1u), dim3(RW * 32), 0, as_stream(stream), x,
-                      gamma, eps, w_router, T, E, H, 1, xn, logits);
+                      res, xsum, gamma, eps, w_router, T, E, H, 1, xn, logits);
     const size_t smem = (size_t)tpc * H * sizeof(float);
     static SmemLimit limit;
     if (limit.raise(k_rmsnorm_router<false>, 64 * 1024) != cudaSuccess) {
@@ -276,10 +329,26 @@ extern "C" luce_status luce_rmsnorm_router(const float *x, const float *gamma, f
         return LUCE_ERR_CUDA;
     }
     const luce_status st = launch(k_rmsnorm_router<false>, dim3((unsigned)chunks, (unsigned)tiles), dim3(RW * 32),
-                                  smem, as_stream(stream), x, gamma, eps, w_router, T, E, H, tpc, xn, logits);
+                                  smem, as_stream(stream), x, res, xsum, gamma, eps, w_router, T, E, H, tpc, xn,
+                                  logits);
     if (st != LUCE_OK)
         limit.forget();
     return st;
+}
+
+extern "C" luce_status luce_rmsnorm_router(const float *x, const float *gamma, float eps, const float *w_router, int T,
+                                           int E, int H, float *xn, float *logits, void *stream)
+{
+    return rmsnorm_router(x, nullptr, nullptr, gamma, eps, w_router, T, E, H, xn, logits, stream);
+}
+
+extern "C" luce_status luce_add_rmsnorm_router(const float *x, const float *residual, float *x_sum,
+                                               const float *gamma, float eps, const float *w_router, int T, int E,
+                                               int H, float *xn, float *logits, void *stream)
+{
+    if (!residual && T > 0)
+        return LUCE_ERR_INVALID_ARG;
+    return rmsnorm_router(x, residual, x_sum, gamma, eps, w_router, T, E, H, xn, logits, stream);
 }
 
 extern "C" luce_status luce_argmax_pick(const float *vals, const int32_t *idxs, int S, int R, int32_t *idx, float *val,

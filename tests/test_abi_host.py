@@ -151,6 +151,16 @@ def test_edge_ops_validation(lib):
     assert f(G, G, 1e-6, G, 1, 0, 2048, G, G, None) == 1           # E < 1
     assert f(G, G, 1e-6, G, 1, 64, 2048, G, None, None) == 1       # logits missing
     assert f(G, G, 1e-6, G, 0, 64, 2048, None, G, None) == 0       # T = 0
+    r = lib.luce_add_rmsnorm_router
+    r.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_float, ctypes.c_void_p] + [ctypes.c_int] * 3 + \
+        [ctypes.c_void_p] * 3
+    S = _p(GOOD + (1 << 20))
+    assert r(G, None, S, G, 1e-6, G, 1, 64, 2048, G, G, None) == 1          # residual missing
+    assert r(G, _p(GOOD + 4), S, G, 1e-6, G, 1, 64, 2048, G, G, None) == 1  # residual not 16-byte aligned
+    assert r(G, _p(GOOD + 8192), _p(GOOD + 4096), G, 1e-6, G, 1, 64, 2048, G, G, None) == 1  # x_sum overlaps x
+    assert r(G, _p(GOOD + 8192), _p(GOOD + 12288), G, 1e-6, G, 1, 64, 2048, G, G, None) == 1  # ... or residual
+    assert r(G, G, S, G, 1e-6, G, 1, 64, 2046, G, G, None) == 1             # H % 4, as the plain norm
+    assert r(G, None, None, G, 1e-6, G, 0, 64, 2048, None, G, None) == 0    # T = 0
     s = lib.luce_argmax_shard
     s.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]

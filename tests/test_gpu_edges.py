@@ -110,6 +110,35 @@ def test_rmsnorm_router_one_token_path_is_the_tiled_path(H):
     assert_close(host(lg1), lg_ref, terms, "logits")
 
 
+@pytest.mark.parametrize("T,E,H", [(1, 64, 2048), (5, 128, 4096), (1, 9, 516), (3, 9, 12288)])
+def test_add_rmsnorm_router_is_the_add_then_the_norm(T, E, H):
+    # the residual sum is one fp32 add (numpy's float32 addition, exactly);
+    # xn and the logits are the oracle's of that sum, and the same bits as
+    # luce_add_f32 followed by luce_rmsnorm_router
+    g = W.rng(730, T * 1000 + H)
+    x = g.standard_normal((T, H)).astype(np.float32)
+    r = (g.standard_normal((T, H)) * 3.0).astype(np.float32)
+    gamma = g.uniform(0.5, 1.5, H).astype(np.float32)
+    w = (g.standard_normal((E, H)) * 0.02).astype(np.float32)
+    s_ref = x + r
+    xn_ref, lg_ref, terms = oracle.rmsnorm_router(s_ref, gamma, 1e-6, w)
+    xd, rd, gd, wd = dev(x), dev(r), dev(gamma), dev(w)
+    s_out = torch.full((T, H), float("nan"), device="cuda")
+    xn = torch.full((T, H), float("nan"), device="cuda")
+    lg = torch.full((T, E), float("nan"), device="cuda")
+    B.luce_add_rmsnorm_router(xd, rd, s_out, gd, 1e-6, wd, xn, lg)
+    s2, xn2, lg2 = torch.empty_like(s_out), torch.empty_like(xn), torch.empty_like(lg)
+    B.luce_add_f32(xd, rd, s2)
+    B.luce_rmsnorm_router(s2, gd, 1e-6, wd, xn2, lg2)
+    lg3 = torch.empty_like(lg)
+    B.luce_add_rmsnorm_router(xd, rd, None, gd, 1e-6, wd, None, lg3)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(s_out).view(np.uint32), s_ref.view(np.uint32))
+    assert_close(host(xn), xn_ref, np.abs(xn_ref), "xn")
+    assert_close(host(lg), lg_ref, terms, "logits")
+    assert torch.equal(s_out, s2) and torch.equal(xn, xn2) and torch.equal(lg, lg2) and torch.equal(lg, lg3)
+
+
 # ----------------------------------------------------------------------------- vocabulary split
 @pytest.mark.parametrize("cuts", [[0, 64640, 129280], [0, 1, 70000, 129280], [0, 43093, 86186, 129280],
                                   [0, 129280]])
