@@ -267,20 +267,22 @@ LUCE_API luce_status luce_argmax_noalloc(const float *logits, int R, int64_t V, 
  *   ws_gate, ws_up [I][H/256] or both NULL; xq [T][H/32] q8_1; ids [T][k]
  *   (id < 0: masked, its h row untouched; id >= E: skipped and
  *   LUCE_FAULT_BAD_ID).  h [T*k (+T)][I] fp32 out: h = silu(g) u, or the
- *   clamped form when clamp > 0 (as luce_moe_glu_pair).  hq is not written:
- *   quantize h with luce_quantize_q8_1 (rows of masked routes: any values).
+ *   clamped form when clamp > 0 (as luce_moe_glu_pair).  hq [T*k (+T)][I/32]
+ *   q8_1 out or NULL: h quantized by the rule of luce_quantize_q8_1 (the same
+ *   bits) in the same launch; rows of masked or skipped routes are left
+ *   untouched in both.  With hq NULL, quantize h with luce_quantize_q8_1.
  * luce_moe_down_combine_q4k: w_down [E][H][I/256] (16-byte aligned), ws_down
  *   [H][I/256] or NULL, hq [T*k (+T)][I/32] q8_1, ids [T][k], weights [T][k]
  *   fp32 -> out [T][H] fp32, the combine of luce_moe_down_combine (slot
  *   order, each product and sum rounded, shared expert last).
- * Requires H % 256 == 0, I % 256 == 0, 1 <= k <= min(E, 64), E <= 1024.  A
- * first design (one warp per output value); every weight row is read once
- * per column that needs it.
+ * Requires H % 256 == 0, I % 256 == 0, 1 <= k <= min(E, 64), E <= 1024.
+ * Gate/up: one block per 32 values of h (two rows per warp); down: one warp
+ * per output value.  Every weight row is read once per column that needs it.
  */
 LUCE_API luce_status luce_moe_glu_q4k(const luce_block_q4_k *w_gate, const luce_block_q4_k *w_up,
                                       const luce_block_q4_k *ws_gate, const luce_block_q4_k *ws_up,
                                       const luce_block_q8_1 *xq, const int32_t *ids, int T, int k, int E, int H,
-                                      int I, float clamp, float *h, void *stream);
+                                      int I, float clamp, float *h, luce_block_q8_1 *hq, void *stream);
 LUCE_API luce_status luce_moe_down_combine_q4k(const luce_block_q4_k *w_down, const luce_block_q4_k *ws_down,
                                                const luce_block_q8_1 *hq, const int32_t *ids, const float *weights,
                                                int T, int k, int E, int H, int I, float *out, void *stream);

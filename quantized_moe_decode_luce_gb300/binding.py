@@ -58,7 +58,7 @@ def lib() -> ctypes.CDLL:
             "luce_add_rmsnorm_router": [P, P, P, P, f32, P, i32, i32, i32, P, P, P],
             "luce_ep_mask": [P, i64, i32, i32, P, P],
             "luce_add_f32": [P, P, P, i64, P],
-            "luce_moe_glu_q4k": [P, P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P],
+            "luce_moe_glu_q4k": [P, P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, P],
             "luce_moe_down_combine_q4k": [P, P, P, P, P, i32, i32, i32, i32, i32, P, P],
         }
         for name, args in sigs.items():
@@ -251,13 +251,14 @@ def luce_add_f32(a, b, out, stream=None) -> None:
         _ptr(a, f32, "a"), _ptr(b, f32, "b"), _ptr(out, f32, "out"), a.numel(), _stream(stream)))
 
 
-def luce_moe_glu_q4k(w_gate, w_up, ws_gate, ws_up, xq, ids, E: int, H: int, I: int, clamp: float, h,
+def luce_moe_glu_q4k(w_gate, w_up, ws_gate, ws_up, xq, ids, E: int, H: int, I: int, clamp: float, h, hq=None,
                      stream=None) -> None:
-    """Q4_K gate/up pair + SwiGLU -> h (quantize h with luce_quantize_q8_1)."""
+    """Q4_K gate/up pair + SwiGLU -> h, and its q8_1 blocks -> hq when given."""
     T, k = ids.shape
     _check("luce_moe_glu_q4k", lib().luce_moe_glu_q4k(
         _ptr(w_gate, u8, "w_gate"), _ptr(w_up, u8, "w_up"), _ptr(ws_gate, u8, "ws_gate"), _ptr(ws_up, u8, "ws_up"),
-        _ptr(xq, u8, "xq"), _ptr(ids, i32, "ids"), T, k, E, H, I, float(clamp), _ptr(h, f32, "h"), _stream(stream)))
+        _ptr(xq, u8, "xq"), _ptr(ids, i32, "ids"), T, k, E, H, I, float(clamp), _ptr(h, f32, "h"),
+        _ptr(hq, u8, "hq"), _stream(stream)))
 
 
 def luce_moe_down_combine_q4k(w_down, ws_down, hq, ids, weights, E: int, H: int, I: int, out, stream=None) -> None:

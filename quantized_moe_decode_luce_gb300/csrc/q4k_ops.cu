@@ -20,10 +20,12 @@
 // Design: one warp per dot product row; a lane takes a pair of sub-blocks
 // (2c, 2c + 1) of a super-block, whose codes are the same 32 bytes (low and
 // high nibbles), with 16-byte loads of the super-block header and codes;
-// dp4a on nibble-masked words.  The gate/up blocks stage the token's q8_1
-// row in shared memory once; the down/combine warps take one route slot per
-// half-warp when a row has at most 16 sub-block pairs (four slots per half
-// in flight).
+// dp4a on nibble-masked words.  A gate/up block stages the token's q8_1 row
+// in shared memory once and owns 32 consecutive h values (two rows per warp),
+// one q8_1 block of h, which it quantizes itself when asked (no separate
+// quantization launch).  The down/combine warps take one route slot per
+// half-warp when a row has at most 16 sub-block pairs (four slots per half in
+// flight), the shared expert as the last slot of the same pass.
 #include <algorithm>
 #include <climits>
 #include <cmath>
@@ -38,7 +40,9 @@ using namespace luce;
 
 constexpr int Q4K_BYTES = 144;
 constexpr int QKK = 256;
-constexpr int WARPS = 8;
+constexpr int WARPS = 8;           // warps per down/combine block
+constexpr int GW = 16;             // warps per gate/up block
+constexpr int GR = QK / GW;        // h rows per gate/up warp: a block's GW x GR rows are one q8_1 block
 
 // (sc, m) of sub-blocks 2c and 2c + 1 from the 12 scale bytes held as three
 // little-endian words
@@ -102,69 +106,90 @@ __device__ __forceinline__ float q4k_lane_dot(const uint8_t *__restrict__ w_row,
     return acc;
 }
 
-// Gate/up rows -> h.  Block (i chunk of WARPS rows, route or shared row r);
-// warp w computes h[r][i] for i = blockIdx.x WARPS + w.
-__global__ void __launch_bounds__(WARPS * 32)
+// Gate/up rows -> h (and its q8_1 block).  Block (32-row block b of h,
+// route or shared row r); warp w computes h[r][i] for i = 32 b + GR w + j,
+// j < GR, with the loads of its GR gate and GR up rows in flight together.
+// With hq the block's 32 values are then quantized by warp 0 into
+// hq[r][b] (the q8_1 rule of luce_quantize_q8_1, the same bits).  Under
+// programmatic launch a CTA releases the next kernel only once its stores are
+// issued: released at the start, the next kernel's CTAs became resident and
+// waited beside this kernel's, which made the pair slower than with a third
+// launch between them.
+__global__ void __launch_bounds__(GW * 32)
     k_glu_q4k(const uint8_t *__restrict__ wg, const uint8_t *__restrict__ wu, const uint8_t *__restrict__ wsg,
               const uint8_t *__restrict__ wsu, const uint32_t *__restrict__ xq, const int32_t *__restrict__ ids, int T,
-              int k, int E, int H, int I, float clamp, float *__restrict__ h)
+              int k, int E, int H, int I, float clamp, float *__restrict__ h, uint32_t *__restrict__ hq)
 {
     pdl_wait();
-    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = blockIdx.y, i = blockIdx.x * WARPS + warp;
+    const int r = blockIdx.y, i0 = blockIdx.x * QK + warp * GR;
     extern __shared__ uint32_t xs[]; // the token's q8_1 row
-    {
-        const int tt = r < T * k ? r / k : r - T * k;
-        const uint32_t *xr = xq + (size_t)tt * (H / QK) * Q8_1_WORDS;
-        for (int w = threadIdx.x; w < (H / QK) * Q8_1_WORDS; w += WARPS * 32)
-            xs[w] = __ldg(xr + w);
-        __syncthreads();
-    }
-    if (i >= I)
-        return;
-    const size_t rowb = (size_t)(H / QKK) * Q4K_BYTES;
+    __shared__ float hs[QK];
     const uint8_t *G, *U;
-    int t;
+    const size_t rowb = (size_t)(H / QKK) * Q4K_BYTES;
     if (r < T * k) {
         const int e = ids[r];
         if (e < 0)
-            return; // masked route
+            return; // masked route (the whole block: r is the block's)
         if (e >= E) {
-            if (lane == 0 && i == 0)
+            if (threadIdx.x == 0 && blockIdx.x == 0)
                 atomicOr(&g_fault_word, LUCE_FAULT_BAD_ID);
             return;
         }
-        t = r / k;
-        G = wg + ((size_t)e * I + i) * rowb;
-        U = wu + ((size_t)e * I + i) * rowb;
+        G = wg + ((size_t)e * I + i0) * rowb;
+        U = wu + ((size_t)e * I + i0) * rowb;
     } else {
-        t = r - T * k;
-        G = wsg + (size_t)i * rowb;
-        U = wsu + (size_t)i * rowb;
+        G = wsg + (size_t)i0 * rowb;
+        U = wsu + (size_t)i0 * rowb;
     }
-    const uint32_t *x = xq + (size_t)t * (H / QK) * Q8_1_WORDS;
-    float gl = 0.0f, ul = 0.0f;
+    {
+        const int tt = r < T * k ? r / k : r - T * k;
+        const uint32_t *xr = xq + (size_t)tt * (H / QK) * Q8_1_WORDS;
+        for (int w = threadIdx.x; w < (H / QK) * Q8_1_WORDS; w += GW * 32)
+            xs[w] = __ldg(xr + w);
+        __syncthreads();
+    }
+    float gl[GR], ul[GR];
+#pragma unroll
+    for (int j = 0; j < GR; j++)
+        gl[j] = ul[j] = 0.0f;
     for (int p = lane; p < (H >> 6); p += 32) {
-        gl = q4k_pair_dot<true>(G, xs, p, gl);
-        ul = q4k_pair_dot<true>(U, xs, p, ul);
+#pragma unroll
+        for (int j = 0; j < GR; j++) {
+            gl[j] = q4k_pair_dot<true>(G + (size_t)j * rowb, xs, p, gl[j]);
+            ul[j] = q4k_pair_dot<true>(U + (size_t)j * rowb, xs, p, ul[j]);
+        }
     }
-    const float g = warp_sum(gl);
-    const float u = warp_sum(ul);
-    if (lane == 0)
-        h[(size_t)r * I + i] = swiglu(g, u, clamp);
+#pragma unroll
+    for (int j = 0; j < GR; j++) {
+        const float g = warp_sum(gl[j]);
+        const float u = warp_sum(ul[j]);
+        const float v = swiglu(g, u, clamp);
+        if (lane == 0) {
+            h[(size_t)r * I + i0 + j] = v;
+            hs[warp * GR + j] = v;
+        }
+    }
+    if (hq == nullptr) {
+        pdl_trigger();
+        return;
+    }
+    __syncthreads();
+    if (warp == 0)
+        quantize_q8_1_warp(hs[lane], hq + ((size_t)r * (I / QK) + blockIdx.x) * Q8_1_WORDS, lane);
+    pdl_trigger();
 }
 
 // Down rows and the combine.  Block (chunk of WARPS output rows, token t);
 // warp w: out[t][n] for n = blockIdx.x WARPS + w, the k route slots in slot
-// order with each product and sum rounded, then the shared expert.
+// order with each product and sum rounded, then the shared expert.  The next
+// kernel is released once the out values are stored (as in k_glu_q4k).
 __global__ void __launch_bounds__(WARPS * 32)
     k_down_combine_q4k(const uint8_t *__restrict__ wd, const uint8_t *__restrict__ wsd,
                        const uint32_t *__restrict__ hq, const int32_t *__restrict__ ids,
                        const float *__restrict__ weights, int T, int k, int E, int H, int I, float *__restrict__ out)
 {
     pdl_wait();
-    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.y, n = blockIdx.x * WARPS + warp;
     if (n >= H)
@@ -175,12 +200,16 @@ __global__ void __launch_bounds__(WARPS * 32)
     if ((I >> 6) <= 16) {
         // A row has at most 16 sub-block pairs: each half-warp takes a slot
         // (half 0 the even ones, half 1 the odd ones), one pair per lane, four
-        // slots per half in flight at once.  The half-warp butterfly adds the
-        // same values in the same order as the warp butterfly over a warp whose
-        // upper 16 lanes hold zeros, so every y is the one-slot-per-warp y.
+        // slots per half in flight at once; slot k is the shared expert, so
+        // its row is read in the same pass as the routed ones and still joins
+        // the combine last, unweighted.  The half-warp butterfly adds the same
+        // values in the same order as the warp butterfly over a warp whose
+        // upper 16 lanes hold zeros (and the two halves reduce alike), so
+        // every y is the one-slot-per-warp y.
         const int P = I >> 6, hh = lane >> 4, pl = lane & 15;
+        const int ns = k + (wsd ? 1 : 0);
         constexpr int SJ = 8; // slots per pass (four per half)
-        for (int j0 = 0; j0 < k; j0 += SJ) {
+        for (int j0 = 0; j0 < ns; j0 += SJ) {
             float part[SJ / 2];
             bool live[SJ / 2];
 #pragma unroll
@@ -189,31 +218,27 @@ __global__ void __launch_bounds__(WARPS * 32)
                 const int e = j < k ? ids[t * k + j] : -1;
                 if (e >= E && pl == 0 && n == 0)
                     atomicOr(&g_fault_word, LUCE_FAULT_BAD_ID);
-                live[q] = e >= 0 && e < E;
-                part[q] = live[q] && pl < P
-                              ? q4k_pair_dot(wd + ((size_t)e * H + n) * rowb, hq + (size_t)(t * k + j) * hrow, pl, 0.0f)
-                              : 0.0f;
+                const bool sh = j == k && wsd != nullptr;
+                live[q] = sh || (e >= 0 && e < E);
+                const uint8_t *wrow = sh ? wsd + (size_t)n * rowb : wd + ((size_t)e * H + n) * rowb;
+                const uint32_t *hr = hq + (size_t)(sh ? T * k + t : t * k + j) * hrow;
+                part[q] = live[q] && pl < P ? q4k_pair_dot(wrow, hr, pl, 0.0f) : 0.0f;
             }
 #pragma unroll
             for (int q = 0; q < SJ / 2; q++) {
                 const float y = half_warp_sum(part[q]);
                 const float y0 = __shfl_sync(0xffffffffu, y, 0), y1 = __shfl_sync(0xffffffffu, y, 16);
                 const bool l0 = __shfl_sync(0xffffffffu, live[q], 0), l1 = __shfl_sync(0xffffffffu, live[q], 16);
+                const int j = j0 + 2 * q;
                 if (l0)
-                    acc = __fadd_rn(acc, __fmul_rn(weights[t * k + j0 + 2 * q], y0));
+                    acc = __fadd_rn(acc, j == k ? y0 : __fmul_rn(weights[t * k + j], y0));
                 if (l1)
-                    acc = __fadd_rn(acc, __fmul_rn(weights[t * k + j0 + 2 * q + 1], y1));
+                    acc = __fadd_rn(acc, j + 1 == k ? y1 : __fmul_rn(weights[t * k + j + 1], y1));
             }
-        }
-        if (wsd) {
-            const float y =
-                half_warp_sum(pl < P && hh == 0
-                                  ? q4k_pair_dot(wsd + (size_t)n * rowb, hq + ((size_t)T * k + t) * hrow, pl, 0.0f)
-                                  : 0.0f);
-            acc = __fadd_rn(acc, __shfl_sync(0xffffffffu, y, 0));
         }
         if (lane == 0)
             out[(size_t)t * H + n] = acc;
+        pdl_trigger();
         return;
     }
     // SB slots at a time: their lane dots do not depend on one another, so
@@ -246,6 +271,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
     if (lane == 0)
         out[(size_t)t * H + n] = acc;
+    pdl_trigger();
 }
 
 } // namespace
@@ -255,7 +281,7 @@ using namespace luce_host;
 extern "C" luce_status luce_moe_glu_q4k(const luce_block_q4_k *w_gate, const luce_block_q4_k *w_up,
                                         const luce_block_q4_k *ws_gate, const luce_block_q4_k *ws_up,
                                         const luce_block_q8_1 *xq, const int32_t *ids, int T, int k, int E, int H,
-                                        int I, float clamp, float *h, void *stream)
+                                        int I, float clamp, float *h, luce_block_q8_1 *hq, void *stream)
 {
     if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E || k > 64 || H <= 0 || I <= 0 || H % QKK != 0 ||
         I % QKK != 0 || !(clamp == clamp))
@@ -267,16 +293,18 @@ extern "C" luce_status luce_moe_glu_q4k(const luce_block_q4_k *w_gate, const luc
         return LUCE_OK;
     if (!w_gate || !w_up || !xq || !ids || !h || !aligned(w_gate, 16) || !aligned(w_up, 16) ||
         (has_ws && (!aligned(ws_gate, 16) || !aligned(ws_up, 16))) || !aligned(xq, 4) || !aligned(ids, 4) ||
-        !aligned(h, 4))
+        !aligned(h, 4) || (hq && !aligned(hq, 4)))
         return LUCE_ERR_INVALID_ARG;
     const int rows = T * k + (has_ws ? T : 0);
     if ((int64_t)T * k > (1 << 20) || rows > 65535)
         return LUCE_ERR_INVALID_ARG;
-    return launch(k_glu_q4k, dim3((unsigned)((I + WARPS - 1) / WARPS), (unsigned)rows), dim3(WARPS * 32),
+    // one block per 32 h values (I % 256 == 0, so no partial block)
+    return launch(k_glu_q4k, dim3((unsigned)(I / QK), (unsigned)rows), dim3(GW * 32),
                   (size_t)(H / QK) * Q8_1_WORDS * 4,
                   as_stream(stream), reinterpret_cast<const uint8_t *>(w_gate), reinterpret_cast<const uint8_t *>(w_up),
                   reinterpret_cast<const uint8_t *>(ws_gate), reinterpret_cast<const uint8_t *>(ws_up),
-                  reinterpret_cast<const uint32_t *>(xq), ids, T, k, E, H, I, clamp, h);
+                  reinterpret_cast<const uint32_t *>(xq), ids, T, k, E, H, I, clamp, h,
+                  reinterpret_cast<uint32_t *>(hq));
 }
 
 extern "C" luce_status luce_moe_down_combine_q4k(const luce_block_q4_k *w_down, const luce_block_q4_k *ws_down,

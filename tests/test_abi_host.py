@@ -187,13 +187,14 @@ def test_edge_ops_validation(lib):
 def test_q4k_validation(lib):
     G = _p(GOOD)
     g = lib.luce_moe_glu_q4k
-    g.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
-    assert g(G, G, G, G, G, G, 1, 2, 8, 2048 + 32, 1024, 0.0, G, None) == 1   # H % 256
-    assert g(G, G, G, G, G, G, 1, 2, 8, 2048, 1000, 0.0, G, None) == 1        # I % 256
-    assert g(G, G, G, None, G, G, 1, 2, 8, 2048, 1024, 0.0, G, None) == 1     # one shared matrix missing
-    assert g(_p(GOOD + 4), G, G, G, G, G, 1, 2, 8, 2048, 1024, 0.0, G, None) == 1  # 16-byte alignment
-    assert g(G, G, G, G, G, G, 1, 9, 8, 2048, 1024, 0.0, G, None) == 1        # k > E
-    assert g(G, G, G, G, G, G, 0, 2, 8, 2048, 1024, 0.0, G, None) == 0        # T = 0
+    g.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_int] * 5 + [ctypes.c_float] + [ctypes.c_void_p] * 3
+    assert g(G, G, G, G, G, G, 1, 2, 8, 2048 + 32, 1024, 0.0, G, None, None) == 1   # H % 256
+    assert g(G, G, G, G, G, G, 1, 2, 8, 2048, 1000, 0.0, G, None, None) == 1        # I % 256
+    assert g(G, G, G, None, G, G, 1, 2, 8, 2048, 1024, 0.0, G, None, None) == 1     # one shared matrix missing
+    assert g(_p(GOOD + 4), G, G, G, G, G, 1, 2, 8, 2048, 1024, 0.0, G, None, None) == 1  # 16-byte alignment
+    assert g(G, G, G, G, G, G, 1, 9, 8, 2048, 1024, 0.0, G, None, None) == 1        # k > E
+    assert g(G, G, G, G, G, G, 1, 2, 8, 2048, 1024, 0.0, G, _p(GOOD + 2), None) == 1  # hq alignment
+    assert g(G, G, G, G, G, G, 0, 2, 8, 2048, 1024, 0.0, G, None, None) == 0        # T = 0
     d = lib.luce_moe_down_combine_q4k
     d.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 + [ctypes.c_void_p] * 2
     assert d(G, G, G, G, G, 1, 2, 8, 2048, 1000, G, None) == 1                # I % 256

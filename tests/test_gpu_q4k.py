@@ -37,6 +37,9 @@ CASES = [
     ("verify_like", 5, 1024, 512, 12, 4, True, 10.0, False),
     ("masked_no_shared", 3, 512, 256, 6, 2, False, 0.0, True),
     ("wide_rows", 2, 4096, 256, 4, 2, True, 0.0, False),
+    ("odd_k_shared", 2, 512, 256, 8, 3, True, 0.0, False),     # the shared slot in the upper half-warp
+    ("two_passes", 2, 512, 512, 10, 8, True, 0.0, True),       # k + 1 slots over two passes
+    ("long_down_rows", 1, 256, 2048, 4, 2, True, 0.0, False),  # 32 sub-block pairs: one slot per warp
 ]
 
 
@@ -54,14 +57,23 @@ def test_q4k_layer_matches_oracle(case):
     h_ref, h_terms = oracle.glu_q4k(L.wg, L.wu, L.wsg, L.wsu, xq, ids, E, H, I, clamp)
 
     h = torch.full((rows, I), float("nan"), dtype=torch.float32, device="cuda")
+    hq = torch.full((rows, I // 32, 36), 0xAB, dtype=torch.uint8, device="cuda")
     B.luce_moe_glu_q4k(dev(L.wg), dev(L.wu), dev(L.wsg) if shared else None, dev(L.wsu) if shared else None, dev(xq),
-                       dev(ids), E, H, I, clamp, h)
-    hq = torch.zeros((rows, I // 32, 36), dtype=torch.uint8, device="cuda")
-    B.luce_quantize_q8_1(h.nan_to_num(0.0), hq)
+                       dev(ids), E, H, I, clamp, h, hq)
+    # the q8_1 blocks written in the gate/up launch are luce_quantize_q8_1 of h, bit for bit
+    hq_sep = torch.zeros_like(hq)
+    B.luce_quantize_q8_1(h.nan_to_num(0.0), hq_sep)
+    # and h without hq is the same h
+    h_only = torch.full_like(h, float("nan"))
+    B.luce_moe_glu_q4k(dev(L.wg), dev(L.wu), dev(L.wsg) if shared else None, dev(L.wsu) if shared else None, dev(xq),
+                       dev(ids), E, H, I, clamp, h_only)
     torch.cuda.synchronize()
     hg = host(h)
     valid = ~np.isnan(h_ref[:, 0])
     assert np.isnan(hg[~valid]).all(), "rows of masked routes must not be written"
+    assert np.array_equal(host(hq)[valid], host(hq_sep)[valid])
+    assert (host(hq)[~valid] == 0xAB).all(), "q8_1 rows of masked routes must not be written"
+    assert torch.equal(h.nan_to_num(0.0), h_only.nan_to_num(0.0))
     assert_close(hg[valid], h_ref[valid], h_terms[valid], f"h ({name})")
     h32 = np.nan_to_num(h_ref, nan=0.0).astype(np.float32)
     allow = oracle.hq_flip_allowance(h32, oracle.tol(np.nan_to_num(h_terms, nan=0.0)))
@@ -128,11 +140,13 @@ def test_q4k_out_of_range_id_is_skipped_and_flagged():
     rows = T * k + T
     h_ref, h_terms = oracle.glu_q4k(L.wg, L.wu, L.wsg, L.wsu, xq, ids_masked, E, H, I, 0.0)
     h = torch.full((rows, I), float("nan"), dtype=torch.float32, device="cuda")
-    B.luce_moe_glu_q4k(dev(L.wg), dev(L.wu), dev(L.wsg), dev(L.wsu), dev(xq), dev(ids_bad), E, H, I, 0.0, h)
+    hq = torch.full((rows, I // 32, 36), 0xAB, dtype=torch.uint8, device="cuda")
+    B.luce_moe_glu_q4k(dev(L.wg), dev(L.wu), dev(L.wsg), dev(L.wsu), dev(xq), dev(ids_bad), E, H, I, 0.0, h, hq)
     torch.cuda.synchronize()
     assert B.luce_get_fault() == B.LUCE_FAULT_BAD_ID
     hg = host(h)
     assert np.isnan(hg[1]).all(), "the row of the out-of-range route must not be written"
+    assert (host(hq)[1] == 0xAB).all(), "nor its q8_1 row"
     valid = ~np.isnan(h_ref[:, 0])
     assert_close(hg[valid], h_ref[valid], h_terms[valid], "h (bad id)")
     # the down product on the oracle's hq: the bad route is left out of the combine
