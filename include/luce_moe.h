@@ -452,8 +452,10 @@ LUCE_API luce_status luce_moe_layer(const float *logits, const float *bias, cons
  * early (they do not signal), so expert weights written by any earlier
  * kernel are safe.  One extra rule holds while it is on:
  * luce_moe_down_combine reads ids, weights, offsets and routes before it
- * waits, so the call that produced them must not be the launch immediately
- * before it (in the order prep/group, glu_pair, down_combine it never is).
+ * waits, and luce_moe_down_combine_q4k ids, weights and its weight rows, so
+ * the call that produced them must not be the launch immediately before it
+ * (in the order prep/group, glu_pair, down_combine, or route, glu_q4k,
+ * down_combine_q4k, it never is).
  */
 LUCE_API luce_status luce_set_pdl(int enable);
 

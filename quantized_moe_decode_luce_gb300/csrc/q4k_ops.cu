@@ -62,17 +62,27 @@ __device__ __forceinline__ void scale_min_pair(const uint32_t (&sw)[3], int c, i
     }
 }
 
-// Sub-block pair p (sub-blocks 2c and 2c + 1 of super-block p / 4) of a
-// Q4_K row times a q8_1 row, added to acc.
+// The weight bytes of sub-block pair p (sub-blocks 2c and 2c + 1 of
+// super-block p / 4) of a Q4_K row: the super-block header and the pair's 32
+// code bytes.
+struct Q4Pair {
+    uint4 hd, q0, q1;
+};
+
+__device__ __forceinline__ Q4Pair q4k_pair_load(const uint8_t *__restrict__ w_row, int p)
+{
+    const int sb = p >> 2, c = p & 3;
+    const uint4 *qp = reinterpret_cast<const uint4 *>(w_row + (size_t)sb * Q4K_BYTES + 16 + 32 * c);
+    return {__ldg(reinterpret_cast<const uint4 *>(w_row + (size_t)sb * Q4K_BYTES)), __ldg(qp), __ldg(qp + 1)};
+}
+
+// Loaded sub-block pair p of a Q4_K row times a q8_1 row, added to acc.
 template <bool XS = false>
-__device__ __forceinline__ float q4k_pair_dot(const uint8_t *__restrict__ w_row, const uint32_t *__restrict__ x_row,
-                                              int p, float acc)
+__device__ __forceinline__ float q4k_pair_fma(const Q4Pair &wp, const uint32_t *__restrict__ x_row, int p, float acc)
 {
     {
         const int sb = p >> 2, c = p & 3;
-        const uint4 hd = __ldg(reinterpret_cast<const uint4 *>(w_row + (size_t)sb * Q4K_BYTES));
-        const uint4 *qp = reinterpret_cast<const uint4 *>(w_row + (size_t)sb * Q4K_BYTES + 16 + 32 * c);
-        const uint4 q0 = __ldg(qp), q1 = __ldg(qp + 1);
+        const uint4 hd = wp.hd, q0 = wp.q0, q1 = wp.q1;
         const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
         const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
         const uint32_t sw[3] = {hd.y, hd.z, hd.w};
@@ -92,6 +102,14 @@ __device__ __forceinline__ float q4k_pair_dot(const uint8_t *__restrict__ w_row,
         }
     }
     return acc;
+}
+
+// Sub-block pair p of a Q4_K row times a q8_1 row, added to acc.
+template <bool XS = false>
+__device__ __forceinline__ float q4k_pair_dot(const uint8_t *__restrict__ w_row, const uint32_t *__restrict__ x_row,
+                                              int p, float acc)
+{
+    return q4k_pair_fma<XS>(q4k_pair_load(w_row, p), x_row, p, acc);
 }
 
 // This lane's part of a Q4_K row (K values) times a q8_1 row: pairs
@@ -183,17 +201,18 @@ __global__ void __launch_bounds__(GW * 32)
 // Down rows and the combine.  Block (chunk of WARPS output rows, token t);
 // warp w: out[t][n] for n = blockIdx.x WARPS + w, the k route slots in slot
 // order with each product and sum rounded, then the shared expert.  The next
-// kernel is released once the out values are stored (as in k_glu_q4k).
+// kernel is released once the out values are stored (as in k_glu_q4k).  On
+// rows of at most 16 sub-block pairs the route ids and weights and the first
+// pass's weight bytes are read before the wait for the previous kernel (the
+// gate/up launch, which writes only h and hq): the weight stream starts while
+// that kernel drains.
 __global__ void __launch_bounds__(WARPS * 32)
     k_down_combine_q4k(const uint8_t *__restrict__ wd, const uint8_t *__restrict__ wsd,
                        const uint32_t *__restrict__ hq, const int32_t *__restrict__ ids,
                        const float *__restrict__ weights, int T, int k, int E, int H, int I, float *__restrict__ out)
 {
-    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.y, n = blockIdx.x * WARPS + warp;
-    if (n >= H)
-        return;
     const size_t rowb = (size_t)(I / QKK) * Q4K_BYTES;
     const size_t hrow = (size_t)(I / QK) * Q8_1_WORDS;
     float acc = 0.0f;
@@ -212,6 +231,7 @@ __global__ void __launch_bounds__(WARPS * 32)
         for (int j0 = 0; j0 < ns; j0 += SJ) {
             float part[SJ / 2];
             bool live[SJ / 2];
+            Q4Pair wp[SJ / 2];
 #pragma unroll
             for (int q = 0; q < SJ / 2; q++) {
                 const int j = j0 + 2 * q + hh;
@@ -221,8 +241,17 @@ __global__ void __launch_bounds__(WARPS * 32)
                 const bool sh = j == k && wsd != nullptr;
                 live[q] = sh || (e >= 0 && e < E);
                 const uint8_t *wrow = sh ? wsd + (size_t)n * rowb : wd + ((size_t)e * H + n) * rowb;
+                if (live[q] && pl < P)
+                    wp[q] = q4k_pair_load(wrow, pl);
+            }
+            if (j0 == 0)
+                pdl_wait(); // hq is the previous kernel's
+#pragma unroll
+            for (int q = 0; q < SJ / 2; q++) {
+                const int j = j0 + 2 * q + hh;
+                const bool sh = j == k && wsd != nullptr;
                 const uint32_t *hr = hq + (size_t)(sh ? T * k + t : t * k + j) * hrow;
-                part[q] = live[q] && pl < P ? q4k_pair_dot(wrow, hr, pl, 0.0f) : 0.0f;
+                part[q] = live[q] && pl < P ? q4k_pair_fma(wp[q], hr, pl, 0.0f) : 0.0f;
             }
 #pragma unroll
             for (int q = 0; q < SJ / 2; q++) {
@@ -241,6 +270,7 @@ __global__ void __launch_bounds__(WARPS * 32)
         pdl_trigger();
         return;
     }
+    pdl_wait();
     // SB slots at a time: their lane dots do not depend on one another, so
     // the loads of all of them are in flight together; the sums then join
     // the combine in slot order
