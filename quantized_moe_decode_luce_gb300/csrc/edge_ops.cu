@@ -43,6 +43,11 @@ using namespace luce;
 constexpr int RW = 8;   // warps (router rows) per CTA
 constexpr int TPC = 8;  // most tokens per tile
 constexpr int WP = 16;  // router-row float4 per lane requested before the wait
+// warps (router rows) per CTA on the register path: its threads hold ~200
+// registers, and small CTAs leave room on their SMs for the next kernel's
+// CTAs (the one-launch layer, whose CTAs must all be resident) to be placed
+// while the router runs
+constexpr int RW_ROW = 2;
 
 template <bool ROW>
 __global__ void __launch_bounds__(RW * 32)
@@ -55,7 +60,7 @@ __global__ void __launch_bounds__(RW * 32)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.y * tpc, nt = min(tpc, T - t0);
     const int H4 = H >> 2;
-    const int e = blockIdx.x * RW + warp;
+    const int e = blockIdx.x * (ROW ? RW_ROW : RW) + warp;
     const float4 *wr = reinterpret_cast<const float4 *>(w_router + (size_t)min(e, E - 1) * H);
     const float4 zero4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     // the router row does not depend on the previous kernel: its first
@@ -320,8 +325,8 @@ static luce_status rmsnorm_router(const float *x, const float *res, float *xsum,
     // one token whose row fits the registers: the row path (xn and the sum
     // then need 16-byte alignment too, as their stores are float4)
     if (T == 1 && H <= 4 * 32 * WP && aligned(gamma, 16) && (!xn || aligned(xn, 16)) && (!xsum || aligned(xsum, 16)))
-        return launch(k_rmsnorm_router<true>, dim3((unsigned)chunks, 1u), dim3(RW * 32), 0, as_stream(stream), x,
-                      res, xsum, gamma, eps, w_router, T, E, H, 1, xn, logits);
+        return launch(k_rmsnorm_router<true>, dim3((unsigned)((E + RW_ROW - 1) / RW_ROW), 1u), dim3(RW_ROW * 32), 0,
+                      as_stream(stream), x, res, xsum, gamma, eps, w_router, T, E, H, 1, xn, logits);
     const size_t smem = (size_t)tpc * H * sizeof(float);
     static SmemLimit limit;
     if (limit.raise(k_rmsnorm_router<false>, 64 * 1024) != cudaSuccess) {
