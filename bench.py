@@ -58,11 +58,63 @@ def parse():
     p.add_argument("--layers", type=int, default=None, help="(debug) fewer layers; invalid as a bench number")
     p.add_argument("--input-steps", type=int, default=None,
                    help="pre-drawn input steps to cycle (default 64; fewer keeps profiling runs short)")
-    p.add_argument("--layer-only", choices=["decode_layer", "verify_layer", "prefill_layer"], default=None,
-                   help="(profiling) run one layer workload --reps times through luce_moe_layer and print its "
-                        "event-timed µs per layer; no bench line")
+    p.add_argument("--layer-only", choices=["decode_layer", "verify_layer", "prefill_layer", "q4k_decode_layer"],
+                   default=None,
+                   help="(profiling) run one layer workload --reps times through luce_moe_layer (or, for "
+                        "q4k_decode_layer, the two Q4_K launches) and print its event-timed µs per layer; no "
+                        "bench line")
     p.add_argument("--reps", type=int, default=1)
     return p.parse_args()
+
+
+def q4k_layer_only(args):
+    """The Q4_K decode-shape layer (T=1, H=2048, I=1024, 64 experts + shared,
+    230 MB of Q4_K weights, six distinct experts drawn per rep): gate/up with
+    its q8_1 blocks of h, then down + combine, `reps` times after one untimed
+    call; for the ncu summary of those two kernels."""
+    import torch
+
+    from quantized_moe_decode_luce_gb300 import binding as Bd
+    from quantized_moe_decode_luce_gb300 import build as Bl
+    Bl.build()
+    Bd.lib()
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    E, H, I, k = 64, 2048, 1024, 6
+
+    def q4k(rows, K):
+        b = torch.randint(0, 256, (rows, K // 256, 144), generator=g, device=dev, dtype=torch.uint8)
+        dd = (torch.rand((rows, K // 256, 2), generator=g, device=dev) * 1.9e-3 + 1e-4).half()
+        b[..., 0:4] = dd.view(torch.uint8).reshape(rows, K // 256, 4)
+        return b
+
+    wg, wu, wd = q4k(E * I, H), q4k(E * I, H), q4k(E * H, I)
+    wsg, wsu, wsd = q4k(I, H), q4k(I, H), q4k(H, I)
+    n = args.reps + 1
+    ids = torch.stack([torch.randperm(E, generator=g, device=dev)[:k] for _ in range(n)]).int().view(n, 1, k)
+    wts = torch.full((1, k), 1.0 / k, device=dev)
+    xq = torch.zeros((1, H // 32, 36), dtype=torch.uint8, device=dev)
+    Bd.luce_quantize_q8_1(torch.randn((1, H), generator=g, device=dev), xq)
+    h = torch.zeros((k + 1, I), device=dev)
+    hq = torch.zeros((k + 1, I // 32, 36), dtype=torch.uint8, device=dev)
+    out = torch.empty((1, H), device=dev)
+
+    def one(i):
+        Bd.luce_moe_glu_q4k(wg, wu, wsg, wsu, xq, ids[i], E, H, I, 0.0, h, hq)
+        Bd.luce_moe_down_combine_q4k(wd, wsd, hq, ids[i], wts, E, H, I, out)
+
+    one(0)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record()
+    for i in range(1, n):
+        one(i)
+    ev[1].record()
+    torch.cuda.synchronize()
+    print(json.dumps({"workload": "q4k_decode_layer", "path": "k_glu_q4k (with hq) + k_down_combine_q4k",
+                      "reps": args.reps, "us_per_layer": ev[0].elapsed_time(ev[1]) * 1e3 / max(1, args.reps),
+                      "device_faults": Bd.luce_get_fault()}))
 
 
 def layer_only(args):
@@ -979,6 +1031,9 @@ def run_ours(args, wl, layers):
 
 def main():
     args = parse()
+    if args.layer_only == "q4k_decode_layer":
+        q4k_layer_only(args)
+        return
     if args.layer_only:
         layer_only(args)
         return
