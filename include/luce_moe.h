@@ -18,7 +18,7 @@
  *     the stream reaches that point.
  *   - Arguments are validated on the host before anything is launched; a
  *     bad argument returns LUCE_ERR_INVALID_ARG (or LUCE_ERR_UNSUPPORTED for
- *     a valid shape this build has no kernel for) with nothing enqueued.
+ *     a valid shape this library has no kernel for) with nothing enqueued.
  *     A launch failure returns LUCE_ERR_CUDA.  No C++ exception crosses the
  *     ABI.  T == 0 (or R == 0) is a valid empty call that enqueues nothing.
  *   - Route ids < 0 are masked routes ([PR826], review "moe_combine_masked_
@@ -57,7 +57,7 @@ extern "C" {
 typedef enum {
     LUCE_OK = 0,
     LUCE_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or shape     */
-    LUCE_ERR_UNSUPPORTED = 2, /* valid but not supported by this build     */
+    LUCE_ERR_UNSUPPORTED = 2, /* valid but not supported by this library   */
     LUCE_ERR_CUDA = 3         /* a CUDA runtime call or launch failed      */
 } luce_status;
 
@@ -157,7 +157,7 @@ LUCE_API luce_status luce_moe_group(const int32_t *ids, int T, int k, int E, int
  *   w_gate, w_up   [E][I][H/32] Q8_0        ws_gate, ws_up [I][H/32] or NULL
  *   xq             [T][H/32] q8_1           offsets [E+1], routes [T*k]
  *   h              [T*k + T][I] fp32 out    hq [T*k + T][I/32] q8_1 out
- *   variant        0 = automatic (only one kernel exists in this build)
+ *   variant        0 = automatic (only one kernel exists in this library)
  * Requires H % 256 == 0, I % 256 == 0, H/32 <= 1024; w_*, xq, hq 16-byte
  * aligned; ws_gate and ws_up both given or both NULL.
  */
