@@ -58,13 +58,43 @@ def parse():
     p.add_argument("--layers", type=int, default=None, help="(debug) fewer layers; invalid as a bench number")
     p.add_argument("--input-steps", type=int, default=None,
                    help="pre-drawn input steps to cycle (default 64; fewer keeps profiling runs short)")
-    p.add_argument("--layer-only", choices=["decode_layer", "verify_layer", "prefill_layer", "q4k_decode_layer"],
+    p.add_argument("--layer-only", choices=["decode_layer", "verify_layer", "prefill_layer", "q4k_decode_layer",
+                                             "decode_chain"],
                    default=None,
                    help="(profiling) run one layer workload --reps times through luce_moe_layer (or, for "
                         "q4k_decode_layer, the two Q4_K launches) and print its event-timed µs per layer; no "
                         "bench line")
     p.add_argument("--reps", type=int, default=1)
     return p.parse_args()
+
+
+def chain_only(args):
+    """(profiling) The chained 43-layer decode stack (router + layer per layer,
+    final add, argmax), `reps` steps launched eagerly after one untimed step:
+    the command of the chained stack's launch list."""
+    import torch
+
+    from quantized_moe_decode_luce_gb300 import binding as Bd
+    from quantized_moe_decode_luce_gb300 import build as Bl
+    from quantized_moe_decode_luce_gb300.layer import Argmax, MoEStep
+    Bl.build()
+    Bd.lib()
+    Bd.luce_set_pdl(not args.no_pdl)
+    dev = torch.device("cuda")
+    wl = W.Workload(**{**W.WORKLOADS["decode_stack43"].__dict__, "steps": 8})
+    layers = args.layers or wl.layers
+    wls = W.Workload(**{**wl.__dict__, "layers": 1})
+    dls = [W.device_layer(wls, wl.seed * 1000 + l, dev) for l in range(layers)]
+    xs, lg, biases, vocab = draw_inputs(wl, layers, 0)
+    xs_d, b_d, vocab_d = (torch.from_numpy(a).to(dev) for a in (xs, biases, vocab))
+    bufs = MoEStep(wl.T, wl.H, wl.I, wl.E, wl.k, wl.shared, wl.clamp, device=dev)
+    am = Argmax(1, VOCAB, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    chain_measure(dev, 1.0, stream, wl, layers, dls, b_d, xs_d, vocab_d, bufs, am, 0, eager_steps=1)
+    r = chain_measure(dev, 1.0, stream, wl, layers, dls, b_d, xs_d, vocab_d, bufs, am, 0,
+                      eager_steps=max(1, args.reps))
+    print(json.dumps({"workload": "decode_chain", "layers": layers, "launches_per_step": 2 * layers + 2, **r,
+                      "device_faults": Bd.luce_get_fault()}))
 
 
 def q4k_layer_only(args):
@@ -473,7 +503,7 @@ def edge_ops_measure(dev, peak, stream):
     return out
 
 
-def chain_measure(dev, peak, stream, wl, layers, dls, b_d, xs_d, vocab_d, bufs, am, lb):
+def chain_measure(dev, peak, stream, wl, layers, dls, b_d, xs_d, vocab_d, bufs, am, lb, eager_steps=0):
     """The decode stack with the step before each layer in the chain: per
     layer the residual add that makes the layer's input (the previous layer's
     input + output), its RMS norm and the router logits (F32 router matrix
@@ -512,6 +542,16 @@ def chain_measure(dev, peak, stream, wl, layers, dls, b_d, xs_d, vocab_d, bufs, 
         Bd.luce_add_f32(x, outc[(layers - 1) % 2], xres[layers])
         am.run(vocab_d[s])
 
+    if eager_steps:  # (profiling) launches only, no graphs
+        with torch.cuda.stream(stream):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for s in range(eager_steps):
+                chain_step(s % S)
+            e1.record(stream)
+            torch.cuda.synchronize()
+        return {"eager_steps": eager_steps, "us_per_step": e0.elapsed_time(e1) * 1e3 / eager_steps}
     gs = []
     with torch.cuda.stream(stream):
         for s in range(S):  # eager once: every call checked
@@ -1063,6 +1103,9 @@ def main():
     args = parse()
     if args.layer_only == "q4k_decode_layer":
         q4k_layer_only(args)
+        return
+    if args.layer_only == "decode_chain":
+        chain_only(args)
         return
     if args.layer_only:
         layer_only(args)
